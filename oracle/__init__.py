@@ -1,0 +1,12 @@
+"""fp64 CPU oracle (test infrastructure; see ``oracle.attention``)."""
+
+from .attention import (  # noqa: F401
+    attention_backward,
+    attention_forward,
+    head_dkdv,
+    head_dq,
+    head_forward,
+    head_row_stats,
+    tile_grid,
+    valid_matrix,
+)

@@ -1,0 +1,279 @@
+"""fp64 CPU oracle for exact (masked) scaled-dot-product attention and its gradients.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline and
+reference legs of ``bench.py`` may import this module. The CUDA library never calls it, and it
+shares no code with the CUDA library (only the seeded input generators are common to both).
+
+What it computes
+----------------
+The plain definition. The FlashAttention plate ("FlashAttention.", Vol. XVI Kernels and Efficiency,
+plate 4, section "Never write the scores") says the fused, tiled kernel returns softmax(Q K^T / sqrt d) V,
+the same as standard attention apart from floating-point rounding; page 1 ("FlashAttention: Fast and
+Memory-Efficient Exact Attention with IO-Awareness", abstract) calls the method exact. So the oracle
+is standard, materialised attention, in float64, on the bf16 inputs upcast exactly:
+
+  1. s_ij = c * sum_k q_ik k_jk                                  (c = softmax scale, normally 1/sqrt d)
+  2. s_ij = -inf where key j is not valid for query i (see ``valid_matrix``)
+  3. m_i = max_j s_ij,  l_i = sum_j exp(s_ij - m_i),  P_ij = exp(s_ij - m_i) / l_i
+  4. O_i = sum_j P_ij v_j,  LSE_i = m_i + ln l_i   (natural log of the scaled scores)
+     A row with no valid key has O_i = 0, LSE_i = -inf and contributes no gradient.
+  5. Gradients of L = sum(dO * O) (the pages print none; textbook softmax calculus):
+     dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij;  dS = P * (dP - D);
+     dQ = c dS K;  dK = c dS^T Q.
+
+The backward pass of the method recomputes the scores from Q, K and the saved log-sum-exp rather
+than storing P (plate, "Never write the scores"); the oracle has no such constraint and simply
+evaluates the formulas above.
+
+Readings where the pages are silent (all are the plainest reading):
+  * causal: key j is visible to query i iff j <= i (square, top-left aligned);
+  * key padding: keys j >= L_b are masked for every query row of sequence b; query rows are not
+    masked;
+  * block mask: a uint8 [ceil(N/128), ceil(N/128)] grid shared by all (b, h); entry (I, J) != 0
+    keeps the 128 x 128 block of queries I*128.. and keys J*128..; it is ANDed with the other two.
+    Block-sparse attention is exact for the masked problem (the abstract calls it approximate only
+    relative to dense attention; the essay "Flash Attention: IO-Aware Attention Computation",
+    paragraph 5, describes it as skipping zero or irrelevant blocks).
+
+Memory
+------
+Every output row depends only on its own row of S, so forward rows and dQ rows are evaluated in
+independent chunks of rows (no sum is split). dK and dV for a set of key columns J are sums over all
+query rows i; they are computed from the full column block P[:, J] in one matrix product each, so
+no sum is split there either. Tests at large N evaluate a sample of rows and columns this way.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py`` (row sums, Q = 0,
+one-hot keys, mask equivalence, N = 1, finite differences, gradient identities, a library
+cross-check and planted mistakes). No function is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+TILE = 128  # granularity of the block mask (128 x 128 blocks)
+
+
+# ----------------------------------------------------------------------------- masks
+
+
+def valid_matrix(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=TILE):
+    """Boolean validity of (query row, key) pairs for one (b, h).
+
+    rows: 1-D int array of query indices; returns bool [len(rows), n_keys].
+    valid(i, j) = [not causal or j <= i] and [j < key_len] and [block_mask[i // tile, j // tile] != 0]
+    """
+    i = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.arange(n_keys, dtype=np.int64)[None, :]
+    ok = np.ones((i.shape[0], n_keys), dtype=bool)
+    if causal:
+        ok &= j <= i
+    if key_len is not None:
+        ok &= j < int(key_len)
+    if block_mask is not None:
+        bm = np.asarray(block_mask)
+        ok &= bm[i // tile, j // tile] != 0
+    return ok
+
+
+def valid_cols(cols, n_rows, causal=False, block_mask=None, key_len=None, tile=TILE):
+    """Validity for all query rows against a set of key columns: bool [n_rows, len(cols)]."""
+    i = np.arange(n_rows, dtype=np.int64)[:, None]
+    j = np.asarray(cols, dtype=np.int64)[None, :]
+    ok = np.ones((n_rows, j.shape[1]), dtype=bool)
+    if causal:
+        ok &= j <= i
+    if key_len is not None:
+        ok &= j < int(key_len)
+    if block_mask is not None:
+        bm = np.asarray(block_mask)
+        ok &= bm[i // tile, j // tile] != 0
+    return ok
+
+
+# ----------------------------------------------------------------------------- one head
+
+
+def scores(q_rows, k_cols, scale):
+    """Step 1: s = c * Q K^T (fp64)."""
+    return scale * (q_rows @ k_cols.T)
+
+
+def row_softmax(s, valid):
+    """Steps 2-3 for whole rows: returns P (0 where invalid), row max m and row sum l.
+
+    For a row with no valid key, P is all zero and m = -inf, l = 0.
+    """
+    s = np.where(valid, s, -np.inf)
+    m = s.max(axis=1)
+    empty = ~valid.any(axis=1)
+    m_fin = np.where(empty, 0.0, m)
+    e = np.where(valid, np.exp(s - m_fin[:, None]), 0.0)
+    l = e.sum(axis=1)
+    p = e / np.where(empty, 1.0, l)[:, None]
+    return p, m, l
+
+
+def lse_from_stats(m, l):
+    """Step 4: LSE_i = m_i + ln l_i, and -inf for a row with no valid key."""
+    empty = ~(l > 0)
+    return np.where(empty, -np.inf, m + np.log(np.where(empty, 1.0, l)))
+
+
+def probs_from_stats(s, valid, m, l):
+    """P_ij = exp(s_ij - m_i) / l_i for an arbitrary block of (i, j), given the row statistics
+    of step 3 computed over the full rows. Zero where invalid or where row i is empty."""
+    empty = ~(l > 0)
+    m_fin = np.where(empty, 0.0, m)
+    e = np.where(valid, np.exp(np.where(valid, s, 0.0) - m_fin[:, None]), 0.0)
+    return e / np.where(empty, 1.0, l)[:, None]
+
+
+def _row_chunks(rows, chunk):
+    rows = np.asarray(rows, dtype=np.int64)
+    for a in range(0, rows.shape[0], chunk):
+        yield rows[a : a + chunk]
+
+
+def head_forward(q, k, v, scale, causal=False, block_mask=None, key_len=None, rows=None, chunk=1024):
+    """O and LSE of one (b, h) head for the query rows ``rows`` (default all)."""
+    n = q.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    o = np.empty((rows.shape[0], v.shape[1]))
+    lse = np.empty(rows.shape[0])
+    at = 0
+    for r in _row_chunks(rows, chunk):
+        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len)
+        p, m, l = row_softmax(scores(q[r], k, scale), valid)
+        o[at : at + r.shape[0]] = p @ v
+        lse[at : at + r.shape[0]] = lse_from_stats(m, l)
+        at += r.shape[0]
+    return o, lse
+
+
+def head_row_stats(q, k, v, do, scale, causal=False, block_mask=None, key_len=None, chunk=1024):
+    """Row statistics m, l and D_i = sum_j P_ij dP_ij for every query row of one head."""
+    n = q.shape[0]
+    m_all = np.empty(n)
+    l_all = np.empty(n)
+    d_all = np.empty(n)
+    for r in _row_chunks(np.arange(n), chunk):
+        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len)
+        p, m, l = row_softmax(scores(q[r], k, scale), valid)
+        dp = do[r] @ v.T
+        m_all[r] = m
+        l_all[r] = l
+        d_all[r] = (p * dp).sum(axis=1)
+    return m_all, l_all, d_all
+
+
+def head_dq(q, k, v, do, scale, causal=False, block_mask=None, key_len=None, rows=None, chunk=1024):
+    """dQ rows of one head: dQ_i = c * sum_j P_ij (dP_ij - D_i) k_j."""
+    n = q.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    dq = np.empty((rows.shape[0], q.shape[1]))
+    at = 0
+    for r in _row_chunks(rows, chunk):
+        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len)
+        p, _, _ = row_softmax(scores(q[r], k, scale), valid)
+        dp = do[r] @ v.T
+        dd = (p * dp).sum(axis=1)
+        ds = p * (dp - dd[:, None])
+        dq[at : at + r.shape[0]] = scale * (ds @ k)
+        at += r.shape[0]
+    return dq
+
+
+def head_dkdv(q, k, v, do, scale, causal=False, block_mask=None, key_len=None, cols=None, stats=None):
+    """dK and dV for key columns ``cols`` of one head (default all):
+    dV_j = sum_i P_ij dO_i,  dK_j = c * sum_i P_ij (dP_ij - D_i) q_i.
+
+    ``stats`` = (m, l, D) over all rows from ``head_row_stats`` (computed here when None).
+    """
+    n = q.shape[0]
+    cols = np.arange(k.shape[0]) if cols is None else np.asarray(cols)
+    if stats is None:
+        stats = head_row_stats(q, k, v, do, scale, causal, block_mask, key_len)
+    m, l, dd = stats
+    valid = valid_cols(cols, n, causal, block_mask, key_len)
+    p = probs_from_stats(scores(q, k[cols], scale), valid, m, l)  # [n, |cols|]
+    dp = do @ v[cols].T
+    ds = p * (dp - dd[:, None])
+    dv = p.T @ do
+    dk = scale * (ds.T @ q)
+    return dk, dv
+
+
+# ----------------------------------------------------------------------------- [B, H, N, d]
+
+
+def _as64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _key_len(seqlens_k, b):
+    return None if seqlens_k is None else int(np.asarray(seqlens_k)[b])
+
+
+def _map_heads(fn, B, H, workers):
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    if workers is None:
+        workers = min(len(heads), len(os.sched_getaffinity(0)))
+    if workers <= 1:
+        return [fn(bh) for bh in heads]
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, heads))
+
+
+def attention_forward(q, k, v, scale, causal=False, block_mask=None, seqlens_k=None, workers=None):
+    """O [B,H,N,d] and LSE [B,H,N] in float64 for inputs laid out [B, H, N, d]."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, H, N, d = q.shape
+    o = np.empty((B, H, N, v.shape[3]))
+    lse = np.empty((B, H, N))
+
+    def one(bh):
+        b, h = bh
+        o[b, h], lse[b, h] = head_forward(q[b, h], k[b, h], v[b, h], scale, causal, block_mask, _key_len(seqlens_k, b))
+
+    _map_heads(one, B, H, workers)
+    return o, lse
+
+
+def attention_backward(q, k, v, do, scale, causal=False, block_mask=None, seqlens_k=None, workers=None):
+    """dQ, dK, dV [B,H,N,d] in float64 (the full gradient; N x N fp64 per head in memory)."""
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    B, H, N, d = q.shape
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+
+    def one(bh):
+        b, h = bh
+        L = _key_len(seqlens_k, b)
+        args = (q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, block_mask, L)
+        dq[b, h] = head_dq(*args)
+        dk[b, h], dv[b, h] = head_dkdv(*args)
+
+    _map_heads(one, B, H, workers)
+    return dq, dk, dv
+
+
+def tile_grid(N, causal=False, block_mask=None, key_len=None, tile=TILE):
+    """bool [nb, nb]: (query tile I, key tile J) holds at least one valid (i, j) pair, for one head.
+
+    A fused kernel that skips exactly the blocks with no valid pair visits the True entries:
+    row sums are the key tiles a query tile visits (forward), column sums the query tiles a key
+    tile visits (backward).
+    """
+    nb = (N + tile - 1) // tile
+    grid = np.zeros((nb, nb), dtype=bool)
+    for it in range(nb):
+        r = np.arange(it * tile, min(N, (it + 1) * tile))
+        cols_any = valid_matrix(r, N, causal, block_mask, key_len, tile).any(axis=0)
+        for jt in range(nb):
+            grid[it, jt] = cols_any[jt * tile : (jt + 1) * tile].any()
+    return grid

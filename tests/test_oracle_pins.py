@@ -1,0 +1,328 @@
+"""Pins for the fp64 oracle, from what the pages and the mathematics fix (CPU only).
+
+* Every softmax row sums to 1; Q = 0 gives the mean of the valid values with LSE = ln(count);
+  one-hot keys give one-hot attention (closed form for any scale); masked attention equals
+  attention over only the unmasked keys; N = 1; brute-force central finite differences of
+  L = sum(dO * O); exact gradient identities; shift invariance.
+* A library cross-check: torch.nn.functional.scaled_dot_product_attention in float64 (and its
+  autograd) for the same textbook definition.
+* Planted mistakes: each plausible slip in the oracle (dropped scale, reversed causal mask, a
+  transposed block mask, log2 for ln, a dropped D term, a missing gradient scale) is planted with
+  monkeypatch and must make at least one pin fail.
+
+Sources: the FlashAttention plate ("FlashAttention.", Kernels and Efficiency plate 4, 'Never write
+the scores') fixes the result as softmax(QK^T/sqrt d)V up to rounding; the essay ("Flash Attention:
+IO-Aware Attention Computation", paragraph 4) describes the running max and sum; paragraph 5 the
+skipping of masked blocks.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.attention as OA
+
+RNG = np.random.default_rng(1234)
+
+
+def brute_valid(i, j, causal, bm, L, tile=128):
+    """Brute-force mask predicate for tiny inputs (pure Python)."""
+    if causal and j > i:
+        return False
+    if L is not None and j >= L:
+        return False
+    if bm is not None and bm[i // tile][j // tile] == 0:
+        return False
+    return True
+
+
+MASKS = [
+    dict(causal=False, L=None, bm=None),
+    dict(causal=True, L=None, bm=None),
+    dict(causal=False, L=200, bm=None),
+    dict(causal=True, L=170, bm=None),
+    dict(causal=False, L=None, bm=np.array([[1, 0, 1], [0, 1, 0], [1, 1, 1]], dtype=np.uint8)),
+    dict(causal=True, L=281, bm=np.array([[1, 0, 0], [1, 0, 0], [0, 1, 1]], dtype=np.uint8)),
+]
+
+
+def _fwd1(q, k, v, c, m):
+    o, lse = oracle.attention_forward(q[None, None], k[None, None], v[None, None], c, m["causal"], m["bm"],
+                                      None if m["L"] is None else np.array([m["L"]]), workers=1)
+    return o[0, 0], lse[0, 0]
+
+
+def _bwd1(q, k, v, do, c, m):
+    g = oracle.attention_backward(q[None, None], k[None, None], v[None, None], do[None, None], c, m["causal"],
+                                  m["bm"], None if m["L"] is None else np.array([m["L"]]), workers=1)
+    return [x[0, 0] for x in g]
+
+
+# --------------------------------------------------------------------------- pins
+
+
+def pin_row_sums():
+    N, d = 300, 16
+    q, k = RNG.standard_normal((N, d)), RNG.standard_normal((N, d))
+    for m in MASKS:
+        valid = OA.valid_matrix(np.arange(N), N, m["causal"], m["bm"], m["L"])
+        p, _, _ = OA.row_softmax(OA.scores(q, k, 0.25), valid)
+        rs = p.sum(axis=1)
+        nonempty = valid.any(axis=1)
+        assert np.abs(rs[nonempty] - 1.0).max() <= 1e-14
+        assert (rs[~nonempty] == 0).all()
+        assert (p[~valid] == 0).all()
+
+
+def pin_q_zero():
+    """Q = 0: P uniform over valid keys, O_i = their mean, LSE_i = ln(count_i) exactly."""
+    N, d = 300, 8
+    q = np.zeros((N, d))
+    k, v = RNG.standard_normal((N, d)), RNG.standard_normal((N, d))
+    for m in MASKS:
+        o, lse = _fwd1(q, k, v, 0.3, m)
+        for i in range(N):
+            js = [j for j in range(N) if brute_valid(i, j, m["causal"], m["bm"], m["L"])]
+            if not js:
+                assert lse[i] == -np.inf and (o[i] == 0).all()
+                continue
+            assert abs(lse[i] - math.log(len(js))) <= 1e-13
+            assert np.abs(o[i] - v[js].mean(axis=0)).max() <= 1e-13
+    # closed form of the causal count: row i sees i + 1 keys
+    o, lse = _fwd1(q, k, v, 0.3, dict(causal=True, L=None, bm=None))
+    assert np.abs(lse - np.log(np.arange(1, N + 1))).max() <= 1e-13
+
+
+def pin_one_hot():
+    """q_i = k_i = a e_i (N <= d): s_ii = c a^2, s_ij = 0. Closed forms for P, LSE and O,
+    non-causal and causal; at c a^2 = 60 attention is one-hot (O_i = v_i)."""
+    N, d = 12, 16
+    v = RNG.standard_normal((N, d))
+    for a, c in ((1.3, 0.25), (2.0, 1.0 / math.sqrt(d)), (math.sqrt(60 / 0.125), 0.125)):
+        q = np.zeros((N, d))
+        q[np.arange(N), np.arange(N)] = a
+        k = q.copy()
+        e = math.exp(c * a * a)
+        o, lse = _fwd1(q, k, v, c, dict(causal=False, L=None, bm=None))
+        pii = e / (e + N - 1)
+        for i in range(N):
+            assert abs(lse[i] - math.log(e + N - 1)) <= 1e-13 * max(1.0, abs(lse[i]))
+            others = (v.sum(axis=0) - v[i]) / (N - 1)
+            assert np.abs(o[i] - (pii * v[i] + (1 - pii) * others)).max() <= 1e-13
+        o, lse = _fwd1(q, k, v, c, dict(causal=True, L=None, bm=None))
+        for i in range(N):
+            assert abs(lse[i] - math.log(e + i)) <= 1e-13 * max(1.0, abs(lse[i]))
+            pii = e / (e + i)
+            rest = v[:i].mean(axis=0) if i else 0.0
+            assert np.abs(o[i] - (pii * v[i] + (1 - pii) * rest)).max() <= 1e-13
+        if c * a * a >= 60:
+            assert np.abs(o - v).max() <= 1e-12
+
+
+def pin_mask_equivalence():
+    """Masked attention of row i == unmasked attention over the gathered valid keys of row i."""
+    N, d = 300, 8
+    q, k, v = (RNG.standard_normal((N, d)) for _ in range(3))
+    for m in MASKS:
+        o, lse = _fwd1(q, k, v, 0.4, m)
+        for i in range(0, N, 7):
+            js = [j for j in range(N) if brute_valid(i, j, m["causal"], m["bm"], m["L"])]
+            if not js:
+                assert lse[i] == -np.inf
+                continue
+            oi, li = oracle.head_forward(q[i : i + 1], k[js], v[js], 0.4)
+            assert np.abs(o[i] - oi[0]).max() <= 1e-13
+            assert abs(lse[i] - li[0]) <= 1e-13
+
+
+def pin_n1():
+    d = 8
+    q, k, v = (RNG.standard_normal((1, d)) for _ in range(3))
+    o, lse = _fwd1(q, k, v, 0.7, dict(causal=True, L=None, bm=None))
+    assert np.abs(o[0] - v[0]).max() == 0
+    assert abs(lse[0] - 0.7 * float(q[0] @ k[0])) <= 1e-15
+
+
+def _loss(q, k, v, do, c, m):
+    o, _ = _fwd1(q, k, v, c, m)
+    return float((o * do).sum())
+
+
+def pin_finite_differences():
+    """Central differences of L = sum(dO * O), step 1e-6, relative error <= 1e-6.
+
+    Tiny shapes; N = 136 with d = 2 spans two 128-blocks (ragged tail) so a block mask bites."""
+    cases = [
+        (6, 3, dict(causal=False, L=None, bm=None)),
+        (7, 4, dict(causal=True, L=None, bm=None)),
+        (8, 3, dict(causal=False, L=5, bm=None)),
+        (8, 2, dict(causal=True, L=6, bm=None)),
+        (136, 2, dict(causal=False, L=None, bm=np.array([[1, 0], [1, 1]], dtype=np.uint8))),
+        (136, 2, dict(causal=True, L=133, bm=np.array([[1, 1], [0, 1]], dtype=np.uint8))),
+    ]
+    h = 1e-6
+    for N, d, m in cases:
+        q, k, v, do = (RNG.standard_normal((N, d)) for _ in range(4))
+        c = 0.6
+        dq, dk, dv = _bwd1(q, k, v, do, c, m)
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            flat = list(np.ndindex(x.shape))
+            if len(flat) > 24:
+                flat = [flat[t] for t in RNG.choice(len(flat), 24, replace=False)]
+            num = np.empty(len(flat))
+            ana = np.empty(len(flat))
+            for t, idx in enumerate(flat):
+                x0 = x[idx]
+                x[idx] = x0 + h
+                lp = _loss(q, k, v, do, c, m)
+                x[idx] = x0 - h
+                lm = _loss(q, k, v, do, c, m)
+                x[idx] = x0
+                num[t] = (lp - lm) / (2 * h)
+                ana[t] = g[idx]
+            err = np.abs(num - ana).max() / max(1e-3, np.abs(ana).max())
+            assert err <= 1e-6, (N, d, m, name, err)
+
+
+def pin_grad_identities():
+    """sum_j dK_j = 0; sum_j dV_j = sum over non-empty rows of dO_i; shift invariance of O in K."""
+    N, d = 260, 8
+    q, k, v, do = (RNG.standard_normal((N, d)) for _ in range(4))
+    for m in MASKS:
+        dq, dk, dv = _bwd1(q, k, v, do, 0.35, m)
+        valid = OA.valid_matrix(np.arange(N), N, m["causal"], m["bm"], m["L"])
+        nonempty = valid.any(axis=1)
+        assert np.abs(dk.sum(axis=0)).max() <= 1e-12
+        assert np.abs(dv.sum(axis=0) - do[nonempty].sum(axis=0)).max() <= 1e-11
+        assert (dq[~nonempty] == 0).all()
+        u = RNG.standard_normal(d)
+        o1, _ = _fwd1(q, k, v, 0.35, m)
+        o2, _ = _fwd1(q, k + u, v, 0.35, m)
+        assert np.abs(o1 - o2).max() <= 1e-12
+
+
+def pin_library_crosscheck():
+    """torch SDPA in float64 (CPU) with its own causal flag / boolean mask, and autograd."""
+    for N, d, m in ((130, 16, dict(causal=False, L=None, bm=None)), (200, 8, dict(causal=True, L=None, bm=None)),
+                    (256, 8, dict(causal=False, L=190, bm=None))):
+        q, k, v, do = (RNG.standard_normal((N, d)) for _ in range(4))
+        c = 1 / math.sqrt(d)
+        tq, tk, tv = (torch.tensor(x[None, None], requires_grad=True) for x in (q, k, v))
+        mask = None
+        if m["L"] is not None:
+            mask = (torch.arange(N) < m["L"])[None, :].expand(N, N)[None, None]
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, is_causal=m["causal"], scale=c)
+        to.backward(torch.tensor(do[None, None]))
+        o, _ = _fwd1(q, k, v, c, m)
+        dq, dk, dv = _bwd1(q, k, v, do, c, m)
+        assert np.abs(o - to.detach().numpy()[0, 0]).max() <= 1e-12
+        for a, b in ((dq, tq), (dk, tk), (dv, tv)):
+            assert np.abs(a - b.grad.numpy()[0, 0]).max() <= 1e-11
+
+
+PINS = [pin_row_sums, pin_q_zero, pin_one_hot, pin_mask_equivalence, pin_n1, pin_finite_differences,
+        pin_grad_identities, pin_library_crosscheck]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+def test_sampled_rows_and_cols_match_full():
+    """The sampled-row / sampled-column entry points used at large N equal the full oracle."""
+    N, d = 300, 8
+    q, k, v, do = (RNG.standard_normal((N, d)) for _ in range(4))
+    for m in MASKS:
+        dq, dk, dv = _bwd1(q, k, v, do, 0.3, m)
+        rows = np.array([0, 5, 127, 128, 299])
+        cols = np.array([1, 64, 200, 256, 299])
+        sq = oracle.head_dq(q, k, v, do, 0.3, m["causal"], m["bm"], m["L"], rows=rows, chunk=2)
+        sk, sv = oracle.head_dkdv(q, k, v, do, 0.3, m["causal"], m["bm"], m["L"], cols=cols)
+        assert np.abs(sq - dq[rows]).max() <= 1e-13
+        assert np.abs(sk - dk[cols]).max() <= 1e-13
+        assert np.abs(sv - dv[cols]).max() <= 1e-13
+
+
+# --------------------------------------------------------------------------- planted mistakes
+
+
+def _mut_scores_no_scale(q_rows, k_cols, scale):
+    return q_rows @ k_cols.T
+
+
+def _mut_valid_reversed_causal(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=128):
+    i = np.asarray(rows)[:, None]
+    j = np.arange(n_keys)[None, :]
+    ok = np.ones((i.shape[0], n_keys), dtype=bool)
+    if causal:
+        ok &= j >= i
+    if key_len is not None:
+        ok &= j < key_len
+    if block_mask is not None:
+        ok &= np.asarray(block_mask)[i // tile, j // tile] != 0
+    return ok
+
+
+def _mut_valid_transposed_blocks(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=128):
+    i = np.asarray(rows)[:, None]
+    j = np.arange(n_keys)[None, :]
+    ok = np.ones((i.shape[0], n_keys), dtype=bool)
+    if causal:
+        ok &= j <= i
+    if key_len is not None:
+        ok &= j < key_len
+    if block_mask is not None:
+        ok &= np.asarray(block_mask)[j // tile, i // tile] != 0
+    return ok
+
+
+def _mut_lse_log2(m, l):
+    empty = ~(l > 0)
+    return np.where(empty, -np.inf, m + np.log2(np.where(empty, 1.0, l)))
+
+
+_real_dkdv = OA.head_dkdv
+
+
+def _mut_dkdv_no_scale(q, k, v, do, scale, causal=False, block_mask=None, key_len=None, cols=None, stats=None):
+    dk, dv = _real_dkdv(q, k, v, do, scale, causal, block_mask, key_len, cols, stats)
+    return dk / scale, dv
+
+
+def _mut_row_stats_no_D(q, k, v, do, scale, causal=False, block_mask=None, key_len=None, chunk=1024):
+    n = q.shape[0]
+    m_all, l_all = np.empty(n), np.empty(n)
+    for a in range(0, n, chunk):
+        r = np.arange(a, min(n, a + chunk))
+        valid = OA.valid_matrix(r, k.shape[0], causal, block_mask, key_len)
+        _, m, l = OA.row_softmax(OA.scores(q[r], k, scale), valid)
+        m_all[r], l_all[r] = m, l
+    return m_all, l_all, np.zeros(n)
+
+
+MUTANTS = [
+    ("scores", _mut_scores_no_scale),
+    ("valid_matrix", _mut_valid_reversed_causal),
+    ("valid_matrix", _mut_valid_transposed_blocks),
+    ("lse_from_stats", _mut_lse_log2),
+    ("head_dkdv", _mut_dkdv_no_scale),
+    ("head_row_stats", _mut_row_stats_no_D),
+]
+
+
+@pytest.mark.parametrize("attr,mutant", MUTANTS, ids=lambda x: getattr(x, "__name__", str(x)))
+def test_planted_mistake_is_caught(monkeypatch, attr, mutant):
+    monkeypatch.setattr(OA, attr, mutant)
+    failed = []
+    for pin in PINS:
+        if pin is pin_finite_differences and attr in ("lse_from_stats",):
+            continue
+        try:
+            pin()
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake in {attr}"
