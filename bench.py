@@ -1,0 +1,316 @@
+"""Benchmark: fused attention forward + backward on the long-context causal workload
+(B=1, H=32, N=8192, d=128, bf16 inputs, fp32 LSE), one step = fa_fwd + fa_bwd over one batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference] [--workload c4]
+
+Prints ONE JSON line (rank 0). ``value`` is whole-job attention TFLOP/s (forward 4 B H N^2 d,
+backward 2.5x, halved for causal) with inputs resident in HBM; ``e2e`` is the same metric with
+pinned-host inputs copied in and results copied out inside the timed region. Multi-GPU runs
+(torchrun) are weak-scaled replicas: every rank runs its own batch; there is no collective on the
+data path (only the max-over-ranks timing reduction).
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this method has) on a bounded
+sample of the same workload: one head per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_io_aware_38_gb300 import roofline as rl  # noqa: E402
+from exact_io_aware_38_gb300 import workloads  # noqa: E402
+
+METRIC = "attention TFLOP/s fwd+bwd (bf16, causal N=8192 d=128) and % of BF16 tensor peak"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="fa", choices=["fa", "reference"])
+    p.add_argument("--workload", default="c4", choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"bf16_tflops": d.get("bf16_tflops"), "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d.get("hbm_gbs"), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_step(inp, head):
+    """The fp64 oracle on one (b, h) head of the workload: forward and full backward."""
+    import oracle
+
+    b, h = head
+    q, k, v, do = (inp[n][b, h].double().numpy() for n in ("q", "k", "v", "do"))
+    bm = None if inp["block_mask"] is None else inp["block_mask"].numpy()
+    L = None if inp["seqlens_k"] is None else int(inp["seqlens_k"][b])
+    c, causal = inp["scale"], inp["causal"]
+    oracle.head_forward(q, k, v, c, causal, bm, L)
+    oracle.head_dq(q, k, v, do, c, causal, bm, L)
+    N = q.shape[0]
+    stats = oracle.head_row_stats(q, k, v, do, c, causal, bm, L)
+    for a in range(0, N, 2048):
+        oracle.head_dkdv(q, k, v, do, c, causal, bm, L, cols=np.arange(a, min(N, a + 2048)), stats=stats)
+
+
+def sample_flops(w, inp):
+    f = rl.attention_flops(1, 1, w.N, w.d, causal=w.causal,
+                           block_mask=None if inp["block_mask"] is None else inp["block_mask"].numpy())
+    return f["total"]
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(w, H=1)
+    fl = sample_flops(w, inp)
+    for _ in range(args.warmup):
+        cpu_oracle_step(inp, (0, 0))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_oracle_step(inp, (0, 0))
+    dt = (time.perf_counter() - t0) / args.steps
+    val = fl / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": {"workload": f"{w.name}: B{w.B} H{w.H} N{w.N} d{w.d}{' causal' if w.causal else ''}",
+                   "sample": f"one head of {w.B * w.H} per step (forward + full backward)"},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "one (b, h) head of the workload per step, fp64 numpy oracle"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import exact_io_aware_38_gb300 as fa
+    from exact_io_aware_38_gb300 import build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    build.build()
+    fa.lib()
+
+    inp = workloads.make_inputs(w, seed=w.seed + rank)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    bm = None if inp["block_mask"] is None else inp["block_mask"].to(dev)
+    sl = None if inp["seqlens_k"] is None else inp["seqlens_k"].to(dev)
+    kw = dict(causal=w.causal, block_mask=bm, seqlens_k=sl, scale=w.scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 4  # fwd kernel; bwd pre, main, post
+
+    def step():
+        fa.fwd(q, k, v, out=o, lse=lse, status=status, **kw)
+        fa.bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, status=status, **kw)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+
+    # ---- timed region (device-resident inputs; inputs 4 x 64 MiB > L2, so no flush between steps)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fa.fwd(q, k, v, out=o, lse=lse, status=status, **kw)
+        ev[i][1].record(stream)
+        fa.bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, status=status, **kw)
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms = start.elapsed_time(end) / args.steps
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+
+    flops = rl.attention_flops(B, H, N, d, causal=w.causal,
+                               block_mask=None if inp["block_mask"] is None else inp["block_mask"].numpy())
+    value = flops["total"] * world / (ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with pinned host buffers
+    hq, hk, hv, hdo = (inp[n].pin_memory() for n in ("q", "k", "v", "do"))
+    ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s2.elapsed_time(e2) / args.steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = flops["total"] * world / (e2e_ms * 1e-3) / 1e12
+
+    peaks = load_peaks()
+    # Dominant launch group: the backward call (pre + main + post in one event span).
+    bwd_tflops = flops["bwd"] / (bwd_ms * 1e-3) / 1e12
+    fwd_tflops = flops["fwd"] / (fwd_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    result = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": {"workload": f"{w.name}: B{B} H{H} N{N} d{d}{' causal' if w.causal else ''} fwd+bwd",
+                   "parallelism": f"replicas x{world}", "l2": "inputs 4 x 64 MiB > 129 MB L2; no flush"},
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops},
+        "roofline": {"bound": "tensor", "kernel": "fa_bwd (pre + main + post, one event span)", "achieved": bwd_tflops,
+                     "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak, "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)"},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        cpu_oracle_step(inp, (0, 0))
+        dt = time.perf_counter() - t0
+        fl = sample_flops(w, inp)
+        result["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+                                  "kind": "oracle", "sample": f"one (b, h) head of {B * H}, forward + full backward, "
+                                  f"fp64 numpy ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,148 @@
+"""Fused exact attention for GB300 (sm_103a): thin Python binding of ``libfa.so``.
+
+The binding only marshals arguments: every step of the forward and backward pass runs in the
+library's CUDA kernels. PyTorch provides device memory and the current stream. There is no CPU
+fallback: if the library is missing, every call raises.
+
+Raw C-ABI names (same signatures as ``include/fa.h``, pointers as ints):
+    fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_status_string
+Tensor helpers:
+    fwd(q, k, v, ...) -> (o, lse);  bwd(q, k, v, o, lse, do, ...) -> (dq, dk, dv)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P]),
+    "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P,
+                    ctypes.c_size_t, _P, _P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, rc: int):
+        super().__init__(fa_status_string(rc))
+        self.rc = rc
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so (built by ``exact_io_aware_38_gb300.build``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run exact_io_aware_38_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------------------------- raw ABI
+
+
+def fa_status_string(rc: int) -> str:
+    return lib().fa_status_string(int(rc)).decode()
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, causal, block_mask, seqlens_k, scale, tile_visits, dev_status, stream) -> int:
+    return int(lib().fa_fwd(q, k, v, o, lse, B, H, N, d, causal, block_mask, seqlens_k, scale, tile_visits, dev_status,
+                            stream))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, seqlens_k, scale, workspace,
+           workspace_bytes, dev_status, stream) -> int:
+    return int(lib().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, seqlens_k, scale,
+                            workspace, workspace_bytes, dev_status, stream))
+
+
+# ----------------------------------------------------------------------------- tensor helpers
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_qkv(*ts):
+    ref = ts[0]
+    for t in ts:
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape == ref.shape):
+            raise ValueError("q, k, v, o, dO must be contiguous bf16 CUDA tensors of one shape [B, H, N, d]")
+    if ref.dim() != 4:
+        raise ValueError("expected [B, H, N, d]")
+
+
+def _masks(block_mask, seqlens_k, N, B, dev):
+    nb = (N + 127) // 128
+    if block_mask is not None:
+        if not (block_mask.dtype == torch.uint8 and block_mask.is_contiguous() and block_mask.numel() == nb * nb
+                and block_mask.device == dev):
+            raise ValueError(f"block_mask must be a contiguous uint8 [{nb}, {nb}] tensor on {dev}")
+    if seqlens_k is not None:
+        if not (seqlens_k.dtype == torch.int32 and seqlens_k.is_contiguous() and seqlens_k.numel() == B
+                and seqlens_k.device == dev):
+            raise ValueError(f"seqlens_k must be a contiguous int32 [{B}] tensor on {dev}")
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def fwd(q, k, v, *, causal=False, block_mask=None, seqlens_k=None, scale=None, out=None, lse=None,
+        tile_visits=None, status=None, stream=None):
+    """O, LSE = attention(q, k, v) on the current CUDA stream. Outputs are allocated unless given."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    _masks(block_mask, seqlens_k, N, B, q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    _check_qkv(q, o)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, int(causal),
+                _ptr(block_mask), _ptr(seqlens_k), scale, _ptr(tile_visits), _ptr(status), _stream(stream))
+    if rc != 0:
+        raise FaError(rc)
+    return o, lse
+
+
+def bwd(q, k, v, o, lse, do, *, causal=False, block_mask=None, seqlens_k=None, scale=None, dq=None, dk=None, dv=None,
+        workspace=None, status=None, stream=None):
+    """dQ, dK, dV of attention on the current CUDA stream (outputs/workspace allocated unless given)."""
+    _check_qkv(q, k, v, o, do)
+    B, H, N, d = q.shape
+    _masks(block_mask, seqlens_k, N, B, q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    nbytes = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(causal), _ptr(block_mask), _ptr(seqlens_k), scale,
+                workspace.data_ptr(), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    if rc != 0:
+        raise FaError(rc)
+    return dq, dk, dv

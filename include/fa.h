@@ -1,0 +1,110 @@
+/*
+ * fa.h -- C ABI of the fused exact-attention library (libfa.so), sm_103a.
+ *
+ * Operation. Exact scaled-dot-product attention O = softmax(c * Q K^T [masked]) V computed as one
+ * fused, tiled kernel whose N x N score matrix never reaches global memory, plus its backward
+ * pass, which recomputes the score tiles from Q, K and the saved per-row log-sum-exp.
+ *   - "FlashAttention." (Vol. XVI Kernels and Efficiency, plate 4): intro (tiles of Q, K, V loaded
+ *     on chip, a score tile folded into a running output by the online softmax), "Never write the
+ *     scores" (same softmax(QK^T/sqrt d)V up to rounding; scores recomputed in the backward pass).
+ *   - "Flash Attention: IO-Aware Attention Computation", paragraph 4 (fused QK^T, softmax and
+ *     value sum; running max and sum), paragraph 5 (block-sparse: skip zero blocks).
+ *   - "FlashAttention: Fast and Memory-Efficient Exact Attention with IO-Awareness", abstract
+ *     (exact attention; block-sparse extension).
+ * The pages fix no interface, no mask format and no backward formulas; this header states the
+ * readings adopted:
+ *   masked score  : key j is valid for query i iff (!causal || j <= i) && (j < L_b) &&
+ *                   (block_mask == NULL || block_mask[(i/128)*nb + j/128] != 0), nb = ceil(N/128).
+ *   LSE           : natural-log log-sum-exp of the scaled, valid scores of each row (fp32);
+ *                   a row with no valid key gets O = 0 and LSE = -inf.
+ *   gradients     : of L = sum(dO * O): dV = P^T dO, dP = dO V^T, D_i = rowsum(dO * O)_i,
+ *                   dS = P * (dP - D), dQ = c dS K, dK = c dS^T Q.
+ *
+ * Layout. Q, K, V, O, dO, dQ, dK, dV are bf16, contiguous [B, H, N, d] (d innermost); LSE is fp32
+ * [B, H, N]. All tensor pointers are device pointers, 16-byte aligned. Supported: d in {64, 128},
+ * N >= 1 (any N; tails are masked), B, H >= 1, B*H*N*d < 2^31 elements per tensor.
+ *
+ * Ownership. The caller owns every buffer and keeps it alive until the work on `stream` has
+ * finished. The library allocates nothing on the device and keeps no per-call state.
+ *
+ * Errors. Every entry point validates its arguments on the host and returns a negative
+ * fa_status_t before launching anything; a launch failure returns FA_ERR_CUDA. Work is
+ * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream). Every wait inside a
+ * kernel is bounded; a wait that runs out, or (in builds with FA_DEBUG_BOUNDS) an index check
+ * that fails, writes its code into *dev_status (a caller-owned device int, nullable) and the
+ * kernel returns early with undefined outputs; the caller reads *dev_status after synchronising.
+ * Nothing is thrown across the ABI and there is no CPU fallback.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1,    /* null pointer, bad size, bad scale, ... */
+  FA_ERR_UNSUPPORTED = -2,    /* d not in {64, 128}, tensor too large */
+  FA_ERR_MISALIGNED = -3,     /* a tensor pointer is not 16-byte aligned */
+  FA_ERR_CUDA = -4,           /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_DEVICE_TIMEOUT = -5, /* written to *dev_status: a bounded in-kernel wait ran out */
+  FA_ERR_BOUNDS = -6          /* written to *dev_status: an in-kernel index check failed */
+} fa_status_t;
+
+/*
+ * Forward pass: O and LSE.
+ *   q, k, v     in : bf16 [B, H, N, d] device
+ *   o           out: bf16 [B, H, N, d] device
+ *   lse         out: fp32 [B, H, N] device (natural log)
+ *   causal      0 or 1 (top-left aligned: key j visible to query i iff j <= i)
+ *   block_mask  nullable, device uint8 [nb * nb], row-major (query tile, key tile), nonzero = keep
+ *   seqlens_k   nullable, device int32 [B], each in [0, N]; keys j >= seqlens_k[b] are masked for
+ *               every query row of sequence b (a value outside [0, N] is clamped into it)
+ *   scale       softmax scale c, finite and > 0 (callers normally pass 1/sqrt(d))
+ *   tile_visits nullable, device int32 [B * H * nb]: receives, per (b, h, query tile), the number
+ *               of 128 x 128 key tiles the kernel visited (tiles with no valid pair are skipped)
+ *   dev_status  nullable, device int (see Errors); left untouched on success
+ *   stream      cudaStream_t
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, int causal,
+           const uint8_t* block_mask, const int32_t* seqlens_k, float scale,
+           int32_t* tile_visits, int* dev_status, void* stream);
+
+/* Bytes of device workspace fa_bwd needs: D (fp32 [B,H,N]) and the fp32 dQ accumulator
+ * ([B,H,N,d]), each rounded up to 256 bytes. Returns 0 for invalid sizes. */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass: dQ, dK, dV from Q, K, V, the forward outputs O and LSE, and dO.
+ *   q, k, v, o, dout  in : bf16 [B, H, N, d] device (o and lse exactly as fa_fwd wrote them
+ *                          for the same q, k, v, mask and scale)
+ *   lse               in : fp32 [B, H, N] device
+ *   dq, dk, dv        out: bf16 [B, H, N, d] device
+ *   causal, block_mask, seqlens_k, scale: as for fa_fwd (must match the forward call)
+ *   workspace         device, >= fa_bwd_workspace_bytes(B, H, N, d) bytes, 256-byte aligned;
+ *                     scratch only (its contents on entry are ignored and on exit undefined)
+ *   dev_status, stream: as for fa_fwd
+ * Launches, in order on `stream`: a pre-pass (D = rowsum(dO * O), dQ accumulator cleared), the main
+ * pass (one CTA per key tile, looping over the query tiles it is visible to) and a post-pass
+ * (dQ fp32 -> bf16). dQ is accumulated with fp32 atomics, so its bits may differ between runs by
+ * the order of additions; dK, dV, O and LSE are run-to-run identical.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv,
+           int B, int H, int N, int d, int causal,
+           const uint8_t* block_mask, const int32_t* seqlens_k, float scale,
+           void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

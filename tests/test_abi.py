@@ -1,0 +1,96 @@
+"""C-ABI tests that need no GPU: the library builds, loads and exports every function declared in
+include/fa.h, and host-side validation rejects bad arguments before any CUDA call."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import exact_io_aware_38_gb300 as fa
+from exact_io_aware_38_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return fa.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for rc in (0, -1, -2, -3, -4, -5, -6, 7):
+        s = fa.fa_status_string(rc)
+        assert isinstance(s, str) and s
+
+
+def test_workspace_bytes(L):
+    B, H, N, d = 2, 3, 130, 64
+    rows = B * H * N
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == r256(rows * 4) + r256(rows * d * 4)
+    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
+    assert fa.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
+
+
+# Fake, never-dereferenced device addresses: validation must fail before any launch.
+A = 0x10000
+
+
+def fwd_rc(**kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=128, d=64, causal=0, block_mask=None, seqlens_k=None, scale=0.125,
+                tile_visits=None, dev_status=None, stream=None)
+    args.update(kw)
+    return fa.fa_fwd(**args)
+
+
+def bwd_rc(**kw):
+    args = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, B=1, H=1, N=128, d=64, causal=0, block_mask=None,
+                seqlens_k=None, scale=0.125, workspace=A, workspace_bytes=1 << 30, dev_status=None, stream=None)
+    args.update(kw)
+    return fa.fa_bwd(**args)
+
+
+@pytest.mark.parametrize("kw,rc", [
+    (dict(q=None), -1), (dict(lse=None), -1), (dict(B=0), -1), (dict(N=0), -1), (dict(H=-1), -1),
+    (dict(causal=2), -1), (dict(scale=0.0), -1), (dict(scale=-1.0), -1), (dict(scale=float("nan")), -1),
+    (dict(scale=float("inf")), -1), (dict(d=96), -2), (dict(d=256), -2), (dict(B=1 << 14, H=1 << 10, N=1 << 10), -2),
+    (dict(q=A + 8), -3), (dict(o=A + 2), -3), (dict(lse=A + 2), -3), (dict(seqlens_k=A + 1), -3),
+])
+def test_fwd_validation(L, kw, rc):
+    assert fwd_rc(**kw) == rc
+
+
+@pytest.mark.parametrize("kw,rc", [
+    (dict(dout=None), -1), (dict(workspace=None), -1), (dict(workspace_bytes=16), -1), (dict(d=32), -2),
+    (dict(dq=A + 8), -3), (dict(workspace=A + 16), -3), (dict(scale=float("nan")), -1),
+])
+def test_bwd_validation(L, kw, rc):
+    assert bwd_rc(**kw) == rc
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd(q, q, q)
