@@ -5,7 +5,7 @@ library's CUDA kernels. PyTorch provides device memory and the current stream. T
 fallback: if the library is missing, every call raises.
 
 Raw C-ABI names (same signatures as ``include/fa.h``, pointers as ints):
-    fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_status_string
+    fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_status_string, fa_bwd_noalloc
 Tensor helpers:
     fwd(q, k, v, ...) -> (o, lse);  bwd(q, k, v, o, lse, do, ...) -> (dq, dk, dv)
 """
@@ -30,7 +30,11 @@ _SIGS = {
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P,
                     ctypes.c_size_t, _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P]),
 }
+
+# Size of the fixed device scratch fa_bwd_noalloc uses instead of a workspace (FA_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class FaError(RuntimeError):
@@ -74,6 +78,13 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, se
            workspace_bytes, dev_status, stream) -> int:
     return int(lib().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, seqlens_k, scale,
                             workspace, workspace_bytes, dev_status, stream))
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, seqlens_k, scale, dev_status,
+                   stream) -> int:
+    """fa_bwd without a workspace: for callers that cannot allocate device memory (see fa.h)."""
+    return int(lib().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, seqlens_k,
+                                    scale, dev_status, stream))
 
 
 # ----------------------------------------------------------------------------- tensor helpers

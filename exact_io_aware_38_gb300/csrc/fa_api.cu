@@ -47,6 +47,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call or kernel launch failed";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a bounded in-kernel wait ran out";
     case FA_ERR_BOUNDS: return "FA_ERR_BOUNDS: an in-kernel index check failed";
+    case FA_ERR_SCRATCH_LIMIT: return "FA_ERR_SCRATCH_LIMIT: problem exceeds the fixed scratch of fa_bwd_noalloc";
     default: return "unknown fa status";
   }
 }

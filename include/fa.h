@@ -52,7 +52,8 @@ typedef enum {
   FA_ERR_MISALIGNED = -3,     /* a tensor pointer is not 16-byte aligned */
   FA_ERR_CUDA = -4,           /* a CUDA runtime/driver call or launch failed */
   FA_ERR_DEVICE_TIMEOUT = -5, /* written to *dev_status: a bounded in-kernel wait ran out */
-  FA_ERR_BOUNDS = -6          /* written to *dev_status: an in-kernel index check failed */
+  FA_ERR_BOUNDS = -6,         /* written to *dev_status: an in-kernel index check failed */
+  FA_ERR_SCRATCH_LIMIT = -7   /* fa_bwd_noalloc: the problem needs more than FA_NOALLOC_SCRATCH_BYTES */
 } fa_status_t;
 
 /*
@@ -99,6 +100,29 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int B, int H, int N, int d, int causal,
            const uint8_t* block_mask, const int32_t* seqlens_k, float scale,
            void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
+/*
+ * Backward pass that allocates nothing, for callers that cannot allocate device memory (a plugin
+ * or custom operator inside another framework receives only its input and output buffers; the
+ * host framework owns the memory pool, and a cudaMalloc of its own would bypass that pool's
+ * accounting, fail when the pool holds the device, or synchronise the device mid-stream).
+ * The method's sources have no counterpart to this entry point.
+ *
+ * Same arguments and results as fa_bwd, without the workspace: the library uses a fixed
+ * FA_NOALLOC_SCRATCH_BYTES array of its own device image instead (held on every GPU where the
+ * library is loaded, until the process exits). Problems whose fa_bwd_workspace_bytes exceed it
+ * return FA_ERR_SCRATCH_LIMIT before anything is launched; e.g. d = 128 fits up to about 65 000
+ * rows B*H*N. The first call on a device looks up the array's device address (call it once
+ * before any stream capture). Calls share the array: two calls whose work overlaps on the GPU
+ * (e.g. on different streams) race. Calls in sequence are safe; every call re-initialises what
+ * it reads.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   int B, int H, int N, int d, int causal,
+                   const uint8_t* block_mask, const int32_t* seqlens_k, float scale,
+                   int* dev_status, void* stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(int status);
