@@ -1,0 +1,413 @@
+// Forward attention on the 5th-generation tensor cores (sm_103a): TMA + mbarrier pipeline,
+// tcgen05 MMAs accumulating in tensor memory, warp-specialised roles.
+//
+// What it computes ("FlashAttention." plate, intro and "Never write the scores"; essay "Flash
+// Attention: IO-Aware Attention Computation", paragraphs 3-5): for each 128-row query tile, the
+// key/value tiles it can see are streamed through shared memory; each score tile S = Q K^T is
+// folded into a running output with the online softmax (running row max m and row sum l; the
+// partial output is rescaled when m grows), and O = acc / l and LSE = m + ln l are written at
+// the end. Scores never leave the chip. Tiles with no valid (query, key) pair are skipped whole.
+//
+// CTA layout (320 threads, one CTA per SM): two 128-row query tiles Q0, Q1 share every K/V tile.
+//   warp 0      TMA producer: Q0, Q1 once, then K_j, V_j through an NS-slot ring of 128-key tiles.
+//   warp 1      MMA issuer (one thread) and tensor-memory owner: S_x = Q_x K_j^T (both operands
+//               K-major in smem) and O_x += P_x V_j (P_x from tensor memory, V_j MN-major in smem).
+//   warps 2-5   softmax for Q0; warps 6-9 softmax for Q1. Thread t of a warpgroup owns one query
+//               row (its tensor-memory lane), so row max and row sum are thread-local (the row is
+//               never split across threads in the 32x32b tensor-memory access shape).
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
+// P_x is written as bf16 over the first 64 columns of S_x.
+// MMA issue order per key tile j: PV0(j), S0(j+1), PV1(j), S1(j+1), so the tensor core computes
+// one tile's products while the other tile's softmax runs.
+// The partial output is rescaled only when a row max grows by more than 2^8 (lazy rescaling;
+// exact, since l and O always share the same reference max).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 320;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kBoxes = D / 64;                 // 64-column (128-byte) TMA boxes per row
+  static constexpr int kTileBytes = 128 * D * 2;        // one 128-row bf16 tile
+  static constexpr int kSlots = D == 128 ? 4 : 8;       // K/V ring depth
+  static constexpr int kSmem = (2 + kSlots) * kTileBytes + 1024;
+  static constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+  static constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+  static constexpr uint32_t kTmemS0 = 0, kTmemO0 = 256;
+};
+
+struct FwdSmemCtl {
+  uint64_t q_full;
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FaFwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ FwdSmemCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem);                       // Q0, Q1 (later O staging)
+  const uint32_t sKV = sQ + 2 * C::kTileBytes;              // ring slots
+  volatile int* abort_flag = &ctl.abort_flag;
+
+  const AttnShape& s = a.s;
+  const int BH = s.B * s.H;
+  const int npairs = (s.nb + 1) >> 1;
+  const int pidx = blockIdx.x / BH;
+  const int bh = blockIdx.x % BH;
+  const int pair = s.causal ? (npairs - 1 - pidx) : pidx;  // longest causal work first
+  const int b = bh / s.H;
+  const int L = key_len(s, b);
+  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+  const bool has1 = qt1 < s.nb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  auto vis = [&](int x, int kt) -> bool { return (x == 0 || has1) && tile_visited(s, x ? qt1 : qt0, kt, L); };
+  auto next_union = [&](int kt) -> int {
+    for (; kt < s.nb; ++kt)
+      if (vis(0, kt) || vis(1, kt)) return kt;
+    return s.nb;
+  };
+
+  const uint32_t b_q = smem_u32(&ctl.q_full);
+  auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
+  auto b_empty = [&](int i) { return smem_u32(&ctl.empty[i]); };
+  const uint32_t b_sfull[2] = {smem_u32(&ctl.s_full[0]), smem_u32(&ctl.s_full[1])};
+  const uint32_t b_pready[2] = {smem_u32(&ctl.p_ready[0]), smem_u32(&ctl.p_ready[1])};
+  const uint32_t b_odone[2] = {smem_u32(&ctl.o_done[0]), smem_u32(&ctl.o_done[1])};
+
+  if (threadIdx.x == 0) {
+    ctl.abort_flag = 0;
+    mbar_init(b_q, 1);
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(b_full(i), 1);
+      mbar_init(b_empty(i), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(b_sfull[x], 1);
+      mbar_init(b_pready[x], 128);
+      mbar_init(b_odone[x], 1);
+    }
+    mbar_init(smem_u32(&ctl.drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl.tmem_base), 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_expect_tx(b_q, (has1 ? 2 : 1) * C::kTileBytes);
+      for (int x = 0; x < (has1 ? 2 : 1); ++x)
+        for (int c = 0; c < C::kBoxes; ++c)
+          tma_load_3d(sQ + x * C::kTileBytes + c * 16384, &tmQ, c * 64, (x ? qt1 : qt0) * 128, bh, b_q);
+      int slot = 0;
+      uint32_t ph = 0;
+      uint32_t last_par[8];
+      bool issued[8];
+      for (int i = 0; i < C::kSlots; ++i) issued[i] = false;
+      for (int kt = next_union(0); kt < s.nb; kt = next_union(kt + 1)) {
+        for (int which = 0; which < 2; ++which) {
+          if (mbar_wait(b_empty(slot), ph ^ 1, abort_flag, a.status)) {
+            mbar_expect_tx(b_full(slot), C::kTileBytes);
+            for (int c = 0; c < C::kBoxes; ++c)
+              tma_load_3d(sKV + slot * C::kTileBytes + c * 16384, which ? &tmV : &tmK, c * 64, kt * 128, bh,
+                          b_full(slot));
+            issued[slot] = true;
+            last_par[slot] = ph;
+          }
+          if (++slot == C::kSlots) {
+            slot = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (*abort_flag) {  // let copies still in flight land before the CTA exits
+        mbar_wait_drain(b_q, 0);
+        for (int i = 0; i < C::kSlots; ++i)
+          if (issued[i]) mbar_wait_drain(b_full(i), last_par[i]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool first[2] = {true, true};
+      bool any[2] = {false, false};
+      uint32_t np[2] = {0, 0};
+      int slot = 0;
+      uint32_t ph = 0;
+      auto take = [&]() -> int {  // wait for the next ring slot to be full
+        const int sl = slot;
+        mbar_wait(b_full(sl), ph, abort_flag, a.status);
+        fence_after_sync();
+        if (++slot == C::kSlots) {
+          slot = 0;
+          ph ^= 1;
+        }
+        return sl;
+      };
+      auto issue_s = [&](int x, int sk) {
+        if (*abort_flag) return;
+        const uint32_t qa = sQ + x * C::kTileBytes, ka = sKV + sk * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + C::kTmemS0 + x * 128, desc_kmajor_sw128(qa + off), desc_kmajor_sw128(ka + off), C::kIdS,
+                 kk > 0);
+        }
+        mma_commit(b_sfull[x]);
+      };
+      auto issue_pv = [&](int x, int sv) {
+        if (*abort_flag) return;
+        const uint32_t va = sKV + sv * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::kTmemO0 + x * D, tmem + C::kTmemS0 + x * 128 + kk * 8,
+                 desc_mnmajor_sw128(va + kk * 2048, 16384), C::kIdPV, (first[x] && kk == 0) ? 0u : 1u);
+        first[x] = false;
+      };
+
+      mbar_wait(b_q, 0, abort_flag, a.status);
+      fence_after_sync();
+      int kt = next_union(0);
+      if (kt < s.nb) {
+        const int sk = take();
+        for (int x = 0; x < 2; ++x)
+          if (vis(x, kt)) {
+            issue_s(x, sk);
+            any[x] = true;
+          }
+        if (!*abort_flag) mma_commit(b_empty(sk));
+        while (true) {
+          const int sv = take();
+          const int ktn = next_union(kt + 1);
+          int skn = -1;
+          for (int x = 0; x < 2; ++x) {
+            if (vis(x, kt)) {
+              mbar_wait(b_pready[x], np[x] & 1, abort_flag, a.status);
+              ++np[x];
+              fence_after_sync();
+              issue_pv(x, sv);
+            }
+            if (ktn < s.nb && vis(x, ktn)) {
+              if (skn < 0) skn = take();
+              issue_s(x, skn);
+              any[x] = true;
+            }
+          }
+          if (!*abort_flag) {
+            mma_commit(b_empty(sv));
+            if (skn >= 0) mma_commit(b_empty(skn));
+          }
+          if (ktn >= s.nb) break;
+          kt = ktn;
+        }
+      }
+      for (int x = 0; x < 2; ++x)
+        if (any[x] && !*abort_flag) mma_commit(b_odone[x]);
+      mma_commit(smem_u32(&ctl.drain));  // every MMA of this CTA has finished when this arrives
+      mbar_wait_drain(smem_u32(&ctl.drain), 0);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int x = (warp - 2) >> 2;
+    const bool active = (x == 0) || has1;
+    const int qt = x ? qt1 : qt0;
+    const int quad = warp & 3;                    // tensor-memory lane quadrant of this warp
+    const int r = quad * 32 + lane;               // row within the tile
+    const int row = qt * 128 + r;                 // row within the head
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::kTmemS0 + x * 128;
+    const uint32_t tO = tmem + lane_off + C::kTmemO0 + x * D;
+    const float sl2 = a.scale * kLog2e;
+    float m = -INFINITY, l = 0.f;
+    int cnt = 0;
+    mbar_wait(b_q, 0, abort_flag, a.status);
+    if (active) {
+      for (int kt = next_union(0); kt < s.nb; kt = next_union(kt + 1)) {
+        if (!vis(x, kt)) continue;
+        mbar_wait(b_sfull[x], cnt & 1, abort_flag, a.status);
+        fence_after_sync();
+        float sv[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tS + c * 32, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(rr[i]);
+        }
+        const int k0 = kt * 128;
+        if ((s.causal && kt == qt) || k0 + 128 > L) {
+          const int lim = min(L - k0, s.causal ? row - k0 + 1 : 128);  // keys [k0, k0+lim) are valid
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) sv[c] = -INFINITY;
+        }
+        float mx = sv[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+        const float mc = mx * sl2;
+        if (cnt == 0) {
+          m = mc;
+        } else if (__any_sync(0xffffffffu, mc > m + kRescaleLog2)) {
+          const float mn = fmaxf(m, mc);
+          const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m - mn);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tO + c * 32, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(tO + c * 32, rr);
+          }
+          l *= alpha;
+          m = mn;
+        }
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        float sum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2_approx(fmaf(sv[h * 64 + 2 * i], sl2, -mu));
+            const float p1 = ex2_approx(fmaf(sv[h * 64 + 2 * i + 1], sl2, -mu));
+            sum += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + h * 32, pk);
+        }
+        tmem_st_wait();
+        l += sum;
+        fence_before_sync();
+        mbar_arrive(b_pready[x]);
+        ++cnt;
+      }
+      // ---------------------------------------------------------------- epilogue
+      if (cnt > 0) {
+        mbar_wait(b_odone[x], 0, abort_flag, a.status);
+        fence_after_sync();
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint32_t stg = sQ + x * C::kTileBytes;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        if (cnt > 0) {
+          tmem_ld32(tO + c * 32, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
+        const uint32_t box = stg + (c >> 1) * 16384 + r * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int chunk = (c & 1) * 4 + j;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(pk[4 * j]),
+                       "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
+                       : "memory");
+        }
+      }
+      if (row < s.N) a.lse[(size_t)bh * s.N + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      fence_proxy_async_smem();
+      named_bar_sync(1 + x, 128);
+      if (warp == 2 + 4 * x && lane == 0) {
+        for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(&tmO, stg + c * 16384, c * 64, qt * 128, bh);
+        tma_store_commit();
+        tma_store_wait0();
+        if (a.tile_visits != nullptr) a.tile_visits[(size_t)bh * s.nb + qt] = cnt;
+      }
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [B*H][N][D] bf16 viewed as a 3-D tensor; 64 x 128 boxes with 128-byte swizzle. Rows past N in
+// a head read as zero and are not written.
+bool make_tmap(CUtensorMap* m, const void* ptr, int N, int D, int BH) {
+  auto enc = get_encode();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  const int BH = a.s.B * a.s.H;
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap(&tq, a.q, a.s.N, D, BH) || !make_tmap(&tk, a.k, a.s.N, D, BH) || !make_tmap(&tv, a.v, a.s.N, D, BH) ||
+      !make_tmap(&to, a.o, a.s.N, D, BH))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)((a.s.nb + 1) / 2) * BH;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, to, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace fa
+
+cudaError_t fa_launch_fwd(const FaFwdArgs& a, cudaStream_t st) {
+  return a.s.d == 64 ? fa::launch<64>(a, st) : fa::launch<128>(a, st);
+}
