@@ -21,9 +21,7 @@
 // one tile's products while the other tile's softmax runs.
 // The partial output is rescaled only when a row max grows by more than 2^8 (lazy rescaling;
 // exact, since l and O always share the same reference max).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+#include "fa_tmap.h"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -363,39 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// [B*H][N][D] bf16 viewed as a 3-D tensor; 64 x 128 boxes with 128-byte swizzle. Rows past N in
-// a head read as zero and are not written.
-bool make_tmap(CUtensorMap* m, const void* ptr, int N, int D, int BH) {
-  auto enc = get_encode();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
   using C = FwdCfg<D>;
   const int BH = a.s.B * a.s.H;
   CUtensorMap tq, tk, tv, to;
-  if (!make_tmap(&tq, a.q, a.s.N, D, BH) || !make_tmap(&tk, a.k, a.s.N, D, BH) || !make_tmap(&tv, a.v, a.s.N, D, BH) ||
-      !make_tmap(&to, a.o, a.s.N, D, BH))
+  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BH) ||
+      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BH) || !fa_make_tmap_bf16(&to, a.o, a.s.N, D, BH))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
