@@ -16,6 +16,7 @@ sample of the same workload: one head per step.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -43,6 +44,8 @@ def parse():
     p.add_argument("--impl", default="fa", choices=["fa", "reference"])
     p.add_argument("--workload", default="c4", choices=sorted(workloads.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    p.add_argument("--heads", type=int, default=None, help="override H (smaller profiling cases only)")
     return p.parse_args()
 
 
@@ -65,7 +68,7 @@ def load_peaks():
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
@@ -78,9 +81,12 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "-lms", "20"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -93,22 +99,27 @@ class ClockSampler:
         self.f.close()
         sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0, t1 = getattr(self, "t_start", 0.0), getattr(self, "t_end", float("inf"))
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if not (t0 - 0.02 <= ts <= t1 + 0.02):
+                    continue  # outside the timed region
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(names, parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+                "power_w_max": max(power) if power else None, "samples_in_timed_region": len(sm),
+                "reasons": sorted(reasons)}
 
 
 def cpu_oracle_step(inp, head):
@@ -181,8 +192,8 @@ def main():
     build.build()
     fa.lib()
 
-    inp = workloads.make_inputs(w, seed=w.seed + rank)
-    B, H, N, d = w.B, w.H, w.N, w.d
+    inp = workloads.make_inputs(w, H=args.heads, seed=w.seed + rank)
+    B, H, N, d = w.B, (w.H if args.heads is None else args.heads), w.N, w.d
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
     bm = None if inp["block_mask"] is None else inp["block_mask"].to(dev)
     sl = None if inp["seqlens_k"] is None else inp["seqlens_k"].to(dev)
@@ -217,6 +228,7 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    clocks.mark("t_start")
     start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -226,6 +238,7 @@ def main():
         ev[i][2].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
+    clocks.mark("t_end")
     clk = clocks.stop()
     barrier()
     ms = start.elapsed_time(end) / args.steps
@@ -242,40 +255,44 @@ def main():
     value = flops["total"] * world / (ms * 1e-3) / 1e12
 
     # ---- end to end through the public API with pinned host buffers
-    hq, hk, hv, hdo = (inp[n].pin_memory() for n in ("q", "k", "v", "do"))
-    ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
-    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+    def run_e2e():
+        hq, hk, hv, hdo = (inp[n].pin_memory() for n in ("q", "k", "v", "do"))
+        ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+        hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
-        hdq.copy_(dq, non_blocking=True)
-        hdk.copy_(dk, non_blocking=True)
-        hdv.copy_(dv, non_blocking=True)
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(dk, non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e2.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = s2.elapsed_time(e2) / args.steps
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = flops["total"] * world / (e2e_ms * 1e-3) / 1e12
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s2.elapsed_time(e2) / args.steps
+        if pg is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        return {"value": flops["total"] * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    e2e = None if args.no_e2e else run_e2e()
 
     peaks = load_peaks()
     # Dominant launch group: the backward call (pre + main + post in one event span).
@@ -293,8 +310,7 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "fa_bwd (pre + main + post, one event span)", "achieved": bwd_tflops,
                      "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak, "traffic": None,
                      "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)"},
-        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+        "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }

@@ -2,25 +2,32 @@
 //
 // Three launches on the caller's stream:
 //   pre   D_i = sum_k dO_ik O_ik (fp32, from the stored bf16 O) and a cleared fp32 dQ accumulator;
-//   main  one CTA per (128-key tile j, head): K_j and V_j stay in shared memory while the 128-row
-//         query tiles i that can see them stream through a TMA ring. The score tile is recomputed
-//         from Q, K and the saved log-sum-exp instead of being stored ("FlashAttention." plate,
-//         "Never write the scores"), and the softmax gradient is applied tile by tile:
+//   main  one CTA per (128-key tile j, head): K_j and V_j stay in shared memory while the query
+//         rows that can see them stream through a TMA ring, BM rows per step (BM = 64 at d = 128,
+//         128 at d = 64). The score tile is recomputed from Q, K and the saved log-sum-exp instead
+//         of being stored ("FlashAttention." plate, "Never write the scores"), and the softmax
+//         gradient is applied tile by tile:
 //           S^T = K_j Q_i^T,  dP^T = V_j dO_i^T                  (tcgen05, into tensor memory)
 //           P^T = exp(c S^T - LSE_i),  dS^T = P^T * (dP^T - D_i)  (one thread per key row)
 //           dV_j += P^T dO_i,  dK_j += dS^T Q_i                  (A operand from tensor memory)
-//           dQ_i += dS K_j                                       (fp32 atomics into the accumulator)
+//           dQ_i += dS K_j                                       (added into the fp32 accumulator)
 //         dK_j = c * acc and dV_j leave through shared memory and TMA stores.
 //   post  dQ = bf16(c * accumulator).
-// For d = 128 the dQ product is formed transposed, dQ_i^T = K_j^T dS_i^T, so the tensor-memory
-// lane is the head dimension and each warp's atomics cover 128 contiguous bytes of one dQ row.
-// For d = 64 it is formed as dS_i K_j (lane = query row), with 16-byte vector atomics.
+// d = 128: dQ_i is formed transposed, dQ_i^T = K_j^T dS_i^T (tensor-memory lane = head dimension),
+//          staged row-major in shared memory and added into the accumulator by one bulk
+//          reduce-add of the bulk-copy engine per step. Two tensor-memory buffers [S^T | dP^T]
+//          alternate between steps (dQ^T is written over its buffer's S^T once P^T is consumed),
+//          so the S^T/dP^T products of step i+2 wait only for step i's dQ^T to be read out.
+// d = 64:  dQ_i = dS_i K_j (lane = query row) in its own tensor-memory columns, added with 16-byte
+//          vector atomics.
 //
-// CTA layout (256 threads): warp 0 TMA producer, warp 1 MMA issuer and tensor-memory owner,
-// warps 4-7 the elementwise warpgroup (thread = key row of the tile; lane quadrant = warp % 4).
-// Tensor memory: d = 128: dK [0,128) dV [128,256) S^T and dQ^T [256,384) dP^T [384,512);
+// CTA layout (384 threads): warp 0 TMA producer; warp 1 MMA issuer and tensor-memory owner;
+// warps 4-7 elementwise warpgroup (thread = key row; lane quadrant = warp % 4), which also writes
+// dK; warps 8-11 dQ warpgroup (reads dQ out of tensor memory, adds it into the accumulator), which
+// also writes dV. The two warpgroups run concurrently on different steps.
+// Tensor memory: d = 128: dK [0,128) dV [128,256), buffer b: S^T/dQ^T [256+128b, +64), dP^T [+64, +128);
 //                d = 64:  dK [0,64) dV [64,128) S^T [128,256) dP^T [256,384) dQ [384,448).
-// P^T and dS^T (bf16) are written over the first 64 columns of S^T and dP^T.
+// P^T and dS^T (bf16) are written over the first BM/2 columns of S^T and dP^T.
 #include "fa_tmap.h"
 #include "sm103_ptx.cuh"
 
@@ -29,32 +36,50 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
 
 template <int D>
 struct BwdCfg {
-  static constexpr int kBoxes = D / 64;
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStages = D == 128 ? 2 : 3;
-  static constexpr int kDsBytes = 128 * 128 * 2;
-  static constexpr int kSmem = (2 + 2 * kStages) * kTileBytes + kDsBytes + 1024;
-  static constexpr uint32_t kTdK = 0, kTdV = D, kTS = 2 * D, kTdP = 2 * D + 128;
-  static constexpr uint32_t kTdQ = D == 128 ? kTS : 2 * D + 256;
-  static constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+  static constexpr int BM = D == 128 ? 64 : 128;     // query rows per step
+  static constexpr int kBufs = D == 128 ? 2 : 1;     // tensor-memory [S^T | dP^T] buffers
+  static constexpr int kBoxes = D / 64;              // 64-column boxes per row
+  static constexpr int kKVBytes = 128 * D * 2;       // K or V tile (128 rows)
+  static constexpr int kQBox = BM * 128;             // one 64-column box of a Q or dO tile
+  static constexpr int kQBytes = BM * D * 2;         // Q or dO tile (BM rows)
+  static constexpr int kStages = D == 128 ? 3 : 2;   // Q/dO ring depth
+  static constexpr int kDsBytes = 128 * BM * 2;      // dS^T tile [128 keys][BM queries], per buffer
+  static constexpr int kDqBytes = D == 128 ? BM * D * 4 : 0;  // fp32 dQ staging for the bulk add
+  static constexpr int kSmem = 2 * kKVBytes + kStages * 2 * kQBytes + kBufs * kDsBytes + kDqBytes + 1024;
+  static constexpr uint32_t kTdK = 0, kTdV = D;
+  static constexpr uint32_t kTS0 = 2 * D;            // S^T of buffer b at kTS0 + b * 2 * BM
+  static constexpr uint32_t kTdQ64 = 2 * D + 2 * BM * kBufs;  // separate dQ columns (d = 64)
+  static constexpr uint32_t kIdS = idesc_bf16(128, BM, false, false);
   static constexpr uint32_t kIdG = idesc_bf16(128, D, false, true);
-  static constexpr uint32_t kIdQ = D == 128 ? idesc_bf16(128, 128, true, true) : idesc_bf16(128, D, true, true);
+  static constexpr uint32_t kIdQ = D == 128 ? idesc_bf16(128, BM, true, true) : idesc_bf16(BM, D, true, true);
+  static_assert(kSmem <= 232448 - 1536, "shared memory budget");
 };
 
 struct BwdSmemCtl {
   uint64_t kv_full;
   uint64_t full[3];
   uint64_t empty[3];
-  uint64_t s_full, p_ready, dq_full, dq_free, done, drain;
+  uint64_t s_full[2], p_ready[2], dq_full[2], dq_free[2];
+  uint64_t done, drain;
   uint32_t tmem_base;
   int abort_flag;
-  float lse2[128];  // LSE * log2(e) of the current query tile
-  float dvec[128];  // D of the current query tile
+  float lse2[2][64];  // LSE * log2(e) per query of the step, per buffer (d = 128)
+  float dvec[2][64];  // D per query of the step, per buffer (d = 128)
 };
+
+// d = 64 uses one buffer of 128 queries: it reuses the same arrays as [1][128].
+template <int D>
+__device__ __forceinline__ float* lse_row(BwdSmemCtl& c, int buf) {
+  return D == 128 ? c.lse2[buf] : &c.lse2[0][0];
+}
+template <int D>
+__device__ __forceinline__ float* dvec_row(BwdSmemCtl& c, int buf) {
+  return D == 128 ? c.dvec[buf] : &c.dvec[0][0];
+}
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
@@ -109,13 +134,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                   const FaBwdArgs a) {
   using C = BwdCfg<D>;
+  constexpr int BM = C::BM;
+  constexpr int NB = C::kBufs;
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sK = smem_u32(smem);
-  const uint32_t sV = sK + C::kTileBytes;
-  const uint32_t sStage0 = sV + C::kTileBytes;  // stage s: Q at +2s tiles, dO at +2s+1 tiles
-  const uint32_t sDs = sK + (2 + 2 * C::kStages) * C::kTileBytes;
+  const uint32_t sV = sK + C::kKVBytes;
+  const uint32_t sStage0 = sV + C::kKVBytes;  // stage s: Q at +2s, dO at +2s+1 (kQBytes each)
+  const uint32_t sDs0 = sStage0 + C::kStages * 2 * C::kQBytes;
+  const uint32_t sDq = sDs0 + NB * C::kDsBytes;
   volatile int* abort_flag = &ctl.abort_flag;
 
   const AttnShape& s = a.s;
@@ -125,20 +153,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int b = bh / s.H;
   const int L = key_len(s, b);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nv = (s.N + BM - 1) / BM;  // BM-row query steps
 
-  auto next_q = [&](int qt) -> int {
-    for (; qt < s.nb; ++qt)
-      if (tile_visited(s, qt, kt, L)) return qt;
-    return s.nb;
+  // Query steps v (rows v*BM ..) are visited iff their 128-row tile is visited for this key tile.
+  auto next_v = [&](int v) -> int {
+    for (; v < nv; ++v)
+      if (tile_visited(s, (v * BM) / 128, kt, L)) return v;
+    return nv;
   };
-  auto sQs = [&](int st) { return sStage0 + (2 * st) * C::kTileBytes; };
-  auto sdOs = [&](int st) { return sStage0 + (2 * st + 1) * C::kTileBytes; };
+  auto sQs = [&](int st) { return sStage0 + (2 * st) * C::kQBytes; };
+  auto sdOs = [&](int st) { return sStage0 + (2 * st + 1) * C::kQBytes; };
+  auto sDs = [&](int buf) { return sDs0 + buf * C::kDsBytes; };
+  auto tS = [&](int buf) { return C::kTS0 + buf * 2 * BM; };
+  auto tdP = [&](int buf) { return C::kTS0 + buf * 2 * BM + BM; };
+  auto tdQ = [&](int buf) { return D == 128 ? tS(buf) : C::kTdQ64; };
 
   const uint32_t b_kv = smem_u32(&ctl.kv_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
   auto b_empty = [&](int i) { return smem_u32(&ctl.empty[i]); };
-  const uint32_t b_sfull = smem_u32(&ctl.s_full), b_pready = smem_u32(&ctl.p_ready);
-  const uint32_t b_dqfull = smem_u32(&ctl.dq_full), b_dqfree = smem_u32(&ctl.dq_free);
+  auto b_sfull = [&](int i) { return smem_u32(&ctl.s_full[i]); };
+  auto b_pready = [&](int i) { return smem_u32(&ctl.p_ready[i]); };
+  auto b_dqfull = [&](int i) { return smem_u32(&ctl.dq_full[i]); };
+  auto b_dqfree = [&](int i) { return smem_u32(&ctl.dq_free[i]); };
   const uint32_t b_done = smem_u32(&ctl.done), b_drain = smem_u32(&ctl.drain);
 
   if (threadIdx.x == 0) {
@@ -148,10 +184,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_full(i), 1);
       mbar_init(b_empty(i), 1);
     }
-    mbar_init(b_sfull, 1);
-    mbar_init(b_pready, 128);
-    mbar_init(b_dqfull, 1);
-    mbar_init(b_dqfree, 128);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(b_sfull(i), 1);
+      mbar_init(b_pready(i), 128);
+      mbar_init(b_dqfull(i), 1);
+      mbar_init(b_dqfree(i), 128);
+    }
     mbar_init(b_done, 1);
     mbar_init(b_drain, 1);
     fence_mbar_init();
@@ -164,41 +202,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
-  const bool any_work = next_q(0) < s.nb;
+  const bool any_work = next_v(0) < nv;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0 && any_work) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmdO);
-      mbar_expect_tx(b_kv, 2 * C::kTileBytes);
+      mbar_expect_tx(b_kv, 2 * C::kKVBytes);
       for (int c = 0; c < C::kBoxes; ++c) {
         tma_load_3d(sK + c * 16384, &tmK, c * 64, kt * 128, bh, b_kv);
         tma_load_3d(sV + c * 16384, &tmV, c * 64, kt * 128, bh, b_kv);
       }
-      int st = 0;
-      uint32_t ph = 0;
       uint32_t last_par[3];
       bool issued[3] = {false, false, false};
-      for (int qt = next_q(0); qt < s.nb; qt = next_q(qt + 1)) {
-        if (mbar_wait(b_empty(st), ph ^ 1, abort_flag, a.status)) {
-          mbar_expect_tx(b_full(st), 2 * C::kTileBytes);
+      uint32_t i = 0;
+      for (int v = next_v(0); v < nv; v = next_v(v + 1), ++i) {
+        const int st = i % C::kStages;
+        const uint32_t par = (i / C::kStages) & 1;
+        if (mbar_wait(b_empty(st), par ^ 1, abort_flag, a.status)) {
+          mbar_expect_tx(b_full(st), 2 * C::kQBytes);
           for (int c = 0; c < C::kBoxes; ++c) {
-            tma_load_3d(sQs(st) + c * 16384, &tmQ, c * 64, qt * 128, bh, b_full(st));
-            tma_load_3d(sdOs(st) + c * 16384, &tmdO, c * 64, qt * 128, bh, b_full(st));
+            tma_load_3d(sQs(st) + c * C::kQBox, &tmQ, c * 64, v * BM, bh, b_full(st));
+            tma_load_3d(sdOs(st) + c * C::kQBox, &tmdO, c * 64, v * BM, bh, b_full(st));
           }
           issued[st] = true;
-          last_par[st] = ph;
-        }
-        if (++st == C::kStages) {
-          st = 0;
-          ph ^= 1;
+          last_par[st] = par;
         }
       }
-      if (*abort_flag) {
+      if (*abort_flag) {  // let copies still in flight land before the CTA exits
         mbar_wait_drain(b_kv, 0);
-        for (int i = 0; i < C::kStages; ++i)
-          if (issued[i]) mbar_wait_drain(b_full(i), last_par[i]);
+        for (int k = 0; k < C::kStages; ++k)
+          if (issued[k]) mbar_wait_drain(b_full(k), last_par[k]);
       }
     }
   } else if (warp == 1) {
@@ -206,54 +241,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       if (any_work) {
         mbar_wait(b_kv, 0, abort_flag, a.status);
-        int st = 0;
-        uint32_t ph = 0;
-        uint32_t it = 0;
-        for (int qt = next_q(0); qt < s.nb; qt = next_q(qt + 1), ++it) {
-          mbar_wait(b_full(st), ph, abort_flag, a.status);
-          if (it > 0) mbar_wait(b_dqfree, (it - 1) & 1, abort_flag, a.status);
+        fence_after_sync();
+        // S^T and dP^T of step `it` into buffer it % NB.
+        auto issue_sdp = [&](uint32_t it) {
+          const int st = it % C::kStages, buf = it % NB;
+          mbar_wait(b_full(st), (it / C::kStages) & 1, abort_flag, a.status);
           fence_after_sync();
+          if (*abort_flag) return;
           const uint32_t q_s = sQs(st), do_s = sdOs(st);
-          if (!*abort_flag) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              mma_ss(tmem + C::kTS, desc_kmajor_sw128(sK + off), desc_kmajor_sw128(q_s + off), C::kIdS, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              mma_ss(tmem + C::kTdP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(do_s + off), C::kIdS, kk > 0);
-            }
-            mma_commit(b_sfull);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ok = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+            mma_ss(tmem + tS(buf), desc_kmajor_sw128(sK + ok), desc_kmajor_sw128(q_s + oq), C::kIdS, kk > 0);
           }
-          mbar_wait(b_pready, it & 1, abort_flag, a.status);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ok = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+            mma_ss(tmem + tdP(buf), desc_kmajor_sw128(sV + ok), desc_kmajor_sw128(do_s + oq), C::kIdS, kk > 0);
+          }
+          mma_commit(b_sfull(buf));
+        };
+        uint32_t n_issued = 0;  // steps whose S^T/dP^T have been issued
+        int ahead = next_v(0);
+        for (int k = 0; k < NB && ahead < nv; ++k, ahead = next_v(ahead + 1)) issue_sdp(n_issued++);
+        uint32_t it = 0;
+        for (int v = next_v(0); v < nv; v = next_v(v + 1), ++it) {
+          const int st = it % C::kStages, buf = it % NB;
+          const uint32_t q_s = sQs(st), do_s = sdOs(st);
+          mbar_wait(b_pready(buf), (it / NB) & 1, abort_flag, a.status);
+          if (D == 64 && it > 0) mbar_wait(b_dqfree(0), (it - 1) & 1, abort_flag, a.status);  // dQ columns read out
           fence_after_sync();
           if (!*abort_flag) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + C::kTdV, tmem + C::kTS + kk * 8, desc_mnmajor_sw128(do_s + kk * 2048, 16384), C::kIdG,
+            for (int kk = 0; kk < BM / 16; ++kk)
+              mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_mnmajor_sw128(do_s + kk * 2048, C::kQBox), C::kIdG,
                      (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + C::kTdK, tmem + C::kTdP + kk * 8, desc_mnmajor_sw128(q_s + kk * 2048, 16384), C::kIdG,
+            for (int kk = 0; kk < BM / 16; ++kk)
+              mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_mnmajor_sw128(q_s + kk * 2048, C::kQBox), C::kIdG,
                      (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               if constexpr (D == 128) {
-                mma_ss(tmem + C::kTdQ, desc_mnmajor_sw128(sK + kk * 2048, 16384),
-                       desc_mnmajor_sw128(sDs + kk * 2048, 16384), C::kIdQ, kk > 0);
+                mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sK + kk * 2048, 16384),
+                       desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384), C::kIdQ, kk > 0);
               } else {
-                mma_ss(tmem + C::kTdQ, desc_mnmajor_sw128(sDs + kk * 2048, 16384),
+                mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384),
                        desc_mnmajor_sw128(sK + kk * 2048, 16384), C::kIdQ, kk > 0);
               }
             }
-            mma_commit(b_dqfull);
+            mma_commit(b_dqfull(buf));
             mma_commit(b_empty(st));
           }
-          if (++st == C::kStages) {
-            st = 0;
-            ph ^= 1;
+          if (ahead < nv) {
+            // Buffer `buf` is reused by step it + NB: at d = 128 its S^T columns hold dQ^T of this step.
+            if (D == 128) mbar_wait(b_dqfree(buf), (it / NB) & 1, abort_flag, a.status);
+            issue_sdp(n_issued++);
+            ahead = next_v(ahead + 1);
           }
         }
         if (!*abort_flag) mma_commit(b_done);
@@ -262,150 +306,163 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_wait_drain(b_drain, 0);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------------ elementwise warpgroup
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // key row of the tile (and head-dimension lane of dQ^T)
-    const int key = kt * 128 + r;
+    const int r = quad * 32 + lane;  // tensor-memory lane: key row (and head dimension of dQ^T)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::kTS, tdP = tmem + lane_off + C::kTdP;
-    const uint32_t tdQ = tmem + lane_off + C::kTdQ;
-    const float sl2 = a.scale * kLog2e;
     const float* LSE = a.lse + (size_t)bh * s.N;
     const float* Dv = a.dvec + (size_t)bh * s.N;
     float* dQa = a.dqacc + (size_t)bh * s.N * D;
-    const bool key_ok = key < L;
+    const bool elementwise = warp < 8;
     uint32_t it = 0;
-    for (int qt = next_q(0); qt < s.nb; qt = next_q(qt + 1), ++it) {
-      const int q0 = qt * 128;
-      named_bar_sync(1, 128);  // every thread is done with the previous tile's LSE and D
-      {
-        const int q = q0 + r;
-        ctl.lse2[r] = q < s.N ? LSE[q] * kLog2e : 0.f;
-        ctl.dvec[r] = q < s.N ? Dv[q] : 0.f;
-      }
-      named_bar_sync(1, 128);
-      mbar_wait(b_sfull, it & 1, abort_flag, a.status);
-      fence_after_sync();
-      const bool need_mask = (s.causal && qt == kt) || (kt * 128 + 128 > L) || (q0 + 128 > s.N);
+    if (elementwise) {
+      // ---------------------------------------------------------------- P^T and dS^T
+      const int key = kt * 128 + r;
+      const bool key_ok = key < L;
+      const float sl2 = a.scale * kLog2e;
+      for (int v = next_v(0); v < nv; v = next_v(v + 1), ++it) {
+        const int q0 = v * BM;
+        const int buf = it % NB;
+        float* lrow = lse_row<D>(ctl, buf);
+        float* drow = dvec_row<D>(ctl, buf);
+        named_bar_sync(1, 128);  // every thread is done with this buffer's previous LSE and D
+        if (r < BM) {
+          const int q = q0 + r;
+          lrow[r] = q < s.N ? LSE[q] * kLog2e : 0.f;
+          drow[r] = q < s.N ? Dv[q] : 0.f;
+        }
+        named_bar_sync(1, 128);
+        mbar_wait(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);
+        fence_after_sync();
+        const bool need_mask = (s.causal && (q0 / 128) == kt) || (kt * 128 + 128 > L) || (q0 + BM > s.N);
+        const uint32_t ts = tmem + lane_off + tS(buf), tdp = tmem + lane_off + tdP(buf);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + c * 32, sr);
-        tmem_ld32(tdP + c * 32, dr);
-        tmem_ld_wait();
-        uint32_t pk[16], dk[16];
+        for (int c = 0; c < BM / 32; ++c) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(ts + c * 32, sr);
+          tmem_ld32(tdp + c * 32, dr);
+          tmem_ld_wait();
+          uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float pp[2], dd[2];
+          for (int t = 0; t < 32; t += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lrow + c * 32 + t);
+            const float4 d4 = *reinterpret_cast<const float4*>(drow + c * 32 + t);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pp[4], dd[4];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qq = c * 32 + t + u;
-            float p = ex2_approx(fmaf(__uint_as_float(sr[t + u]), sl2, -ctl.lse2[qq]));
-            if (need_mask) {
-              const int q = q0 + qq;
-              const bool ok = key_ok && q < s.N && !(s.causal && key > q);
-              p = ok ? p : 0.f;
+            for (int u = 0; u < 4; ++u) {
+              float p = ex2_approx(fmaf(__uint_as_float(sr[t + u]), sl2, -lv[u]));
+              if (need_mask) {
+                const int q = q0 + c * 32 + t + u;
+                p = (key_ok && q < s.N && !(s.causal && key > q)) ? p : 0.f;
+              }
+              pp[u] = p;
+              dd[u] = p * (__uint_as_float(dr[t + u]) - dv4[u]);
             }
-            pp[u] = p;
-            dd[u] = p * (__uint_as_float(dr[t + u]) - ctl.dvec[qq]);
+            pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
+            pk[(t >> 1) + 1] = pack_bf16x2(pp[2], pp[3]);
+            dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
+            dk[(t >> 1) + 1] = pack_bf16x2(dd[2], dd[3]);
           }
-          pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
-          dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
-        }
-        tmem_st16(tS + c * 16, pk);
-        tmem_st16(tdP + c * 16, dk);
-        const uint32_t box = sDs + (c >> 1) * 16384 + r * 128;
+          tmem_st16(ts + c * 16, pk);
+          tmem_st16(tdp + c * 16, dk);
+          const uint32_t box = sDs(buf) + (c >> 1) * 16384 + r * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int chunk = (c & 1) * 4 + j;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(dk[4 * j]),
-                       "r"(dk[4 * j + 1]), "r"(dk[4 * j + 2]), "r"(dk[4 * j + 3])
-                       : "memory");
+          for (int j = 0; j < 4; ++j) {
+            const int chunk = (c & 1) * 4 + j;
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(dk[4 * j]),
+                         "r"(dk[4 * j + 1]), "r"(dk[4 * j + 2]), "r"(dk[4 * j + 3])
+                         : "memory");
+          }
         }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        fence_before_sync();
+        mbar_arrive(b_pready(buf));
       }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      fence_before_sync();
-      mbar_arrive(b_pready);
-
-      mbar_wait(b_dqfull, it & 1, abort_flag, a.status);
-      fence_after_sync();
-      if constexpr (D == 128) {
-        // dQ^T: this thread holds head-dimension r of dQ for the tile's 128 queries.
+    } else {
+      // ---------------------------------------------------------------- dQ into the accumulator
+      for (int v = next_v(0); v < nv; v = next_v(v + 1), ++it) {
+        const int q0 = v * BM;
+        const int buf = it % NB;
+        mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
+        fence_after_sync();
+        const uint32_t tq = tmem + lane_off + tdQ(buf);
+        if constexpr (D == 128) {
+          // dQ^T: lane r = head dimension, columns = the step's BM queries.
+          uint32_t vals[BM];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tdQ + c * 32, v);
+          for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
           tmem_ld_wait();
+          fence_before_sync();
+          mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
+          if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
+          named_bar_sync(2, 128);
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const int q = q0 + c * 32 + t;
-            if (q < s.N) atomicAdd(dQa + (size_t)q * D + r, __uint_as_float(v[t]));
+          for (int qq = 0; qq < BM; ++qq)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
+          fence_proxy_async_smem();
+          named_bar_sync(2, 128);
+          if (threadIdx.x == 256 && !*abort_flag) {
+            const int rows = min(BM, s.N - q0);
+            bulk_reduce_add_f32(dQa + (size_t)q0 * D, sDq, (uint32_t)(rows * D * 4));
+            tma_store_commit();
           }
-        }
-      } else {
-        // dQ: this thread holds query row r of the tile.
-        const int q = q0 + r;
+        } else {
+          // dQ: lane r = query row of the step, 64 head-dimension columns.
+          uint32_t vals[D];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tdQ + c * 32, v);
+          for (int c = 0; c < D / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
           tmem_ld_wait();
+          fence_before_sync();
+          mbar_arrive(b_dqfree(0));
+          const int q = q0 + r;
           if (q < s.N) {
 #pragma unroll
-            for (int t = 0; t < 32; t += 4)
-              atomicAdd(reinterpret_cast<float4*>(dQa + (size_t)q * D + c * 32 + t),
-                        make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
-                                    __uint_as_float(v[t + 3])));
+            for (int t = 0; t < D; t += 4)
+              atomicAdd(reinterpret_cast<float4*>(dQa + (size_t)q * D + t),
+                        make_float4(__uint_as_float(vals[t]), __uint_as_float(vals[t + 1]),
+                                    __uint_as_float(vals[t + 2]), __uint_as_float(vals[t + 3])));
           }
         }
       }
-      fence_before_sync();
-      mbar_arrive(b_dqfree);
+      if (threadIdx.x == 256) tma_store_wait0();
     }
 
-    // ---------------------------------------------------------------- epilogue: dK, dV
+    // ---------------------------------------------------------------- epilogue: dK (warps 4-7), dV (8-11)
     if (it > 0) {
       mbar_wait(b_done, 0, abort_flag, a.status);
       fence_after_sync();
     }
-    const uint32_t stgK = sStage0, stgV = sStage0 + C::kTileBytes;  // stage 0 Q / dO buffers
+    const uint32_t tacc = tmem + lane_off + (elementwise ? C::kTdK : C::kTdV);
+    const float mul = elementwise ? a.scale : 1.f;
+    const uint32_t stg = sStage0 + (elementwise ? 0 : 2 * C::kQBytes);  // Q/dO stage 0 or 1 (a K-sized tile)
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t tacc = tmem + lane_off + (which ? C::kTdV : C::kTdK);
-      const float mul = which ? 1.f : a.scale;
-      const uint32_t stg = which ? stgV : stgK;
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t vv[32];
+      if (it > 0) {
+        tmem_ld32(tacc + c * 32, vv);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        if (it > 0) {
-          tmem_ld32(tacc + c * 32, v);
-          tmem_ld_wait();
-        } else {
+        for (int i = 0; i < 32; ++i) vv[i] = 0u;
+      }
+      uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        uint32_t pk[16];
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(vv[2 * i]) * mul, __uint_as_float(vv[2 * i + 1]) * mul);
+      const uint32_t box = stg + (c >> 1) * 16384 + r * 128;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-        const uint32_t box = stg + (c >> 1) * 16384 + r * 128;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int chunk = (c & 1) * 4 + j;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(pk[4 * j]),
-                       "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
-                       : "memory");
-        }
+      for (int j = 0; j < 4; ++j) {
+        const int chunk = (c & 1) * 4 + j;
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(pk[4 * j]),
+                     "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
+                     : "memory");
       }
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (warp == 4 && lane == 0) {
-      for (int c = 0; c < C::kBoxes; ++c) {
-        tma_store_3d(&tmdK, stgK + c * 16384, c * 64, kt * 128, bh);
-        tma_store_3d(&tmdV, stgV + c * 16384, c * 64, kt * 128, bh);
-      }
+    named_bar_sync(elementwise ? 1 : 2, 128);
+    if (lane == 0 && (warp == 4 || warp == 8)) {
+      for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(elementwise ? &tmdK : &tmdV, stg + c * 16384, c * 64, kt * 128, bh);
       tma_store_commit();
       tma_store_wait0();
     }
@@ -428,8 +485,8 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   const int grid_ew = sms * 8;
   const int BH = a.s.B * a.s.H;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BH) ||
-      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BH) || !fa_make_tmap_bf16(&tdo, a.dout, a.s.N, D, BH) ||
+  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH, C::BM) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BH) ||
+      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BH) || !fa_make_tmap_bf16(&tdo, a.dout, a.s.N, D, BH, C::BM) ||
       !fa_make_tmap_bf16(&tdk, a.dk, a.s.N, D, BH) || !fa_make_tmap_bf16(&tdv, a.dv, a.s.N, D, BH))
     return cudaErrorInvalidValue;
   bwd_pre_kernel<D><<<grid_ew, 256, 0, st>>>(a);

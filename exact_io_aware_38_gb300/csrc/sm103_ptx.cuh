@@ -95,6 +95,13 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Element-wise add of `bytes` contiguous fp32 from shared memory into global memory, performed by
+// the bulk-copy engine (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+               "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
