@@ -28,6 +28,8 @@
 // Tensor memory: d = 128: dK [0,128) dV [128,256), buffer b: S^T/dQ^T [256+128b, +64), dP^T [+64, +128);
 //                d = 64:  dK [0,64) dV [64,128) S^T [128,256) dP^T [256,384) dQ [384,448).
 // P^T and dS^T (bf16) are written over the first BM/2 columns of S^T and dP^T.
+#include <type_traits>
+
 #include "fa_tmap.h"
 #include "sm103_ptx.cuh"
 
@@ -59,7 +61,7 @@ struct BwdCfg {
   static_assert(kSmem <= 232448 - 1536, "shared memory budget");
 };
 
-struct BwdSmemCtl {
+struct alignas(16) BwdSmemCtl {
   uint64_t kv_full;
   uint64_t full[3];
   uint64_t empty[3];
@@ -67,8 +69,8 @@ struct BwdSmemCtl {
   uint64_t done, drain;
   uint32_t tmem_base;
   int abort_flag;
-  float lse2[2][64];  // LSE * log2(e) per query of the step, per buffer (d = 128)
-  float dvec[2][64];  // D per query of the step, per buffer (d = 128)
+  alignas(16) float lse2[2][64];  // LSE * log2(e) per query of the step, per buffer (d = 128)
+  alignas(16) float dvec[2][64];  // D per query of the step, per buffer (d = 128)
 };
 
 // d = 64 uses one buffer of 128 queries: it reuses the same arrays as [1][128].
@@ -335,45 +337,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_after_sync();
         const bool need_mask = (s.causal && (q0 / 128) == kt) || (kt * 128 + 128 > L) || (q0 + BM > s.N);
         const uint32_t ts = tmem + lane_off + tS(buf), tdp = tmem + lane_off + tdP(buf);
+        // P^T, dS^T for the step's BM queries, 32 at a time; the mask is resolved per step so the
+        // unmasked body has no branches.
+        auto step = [&](auto mask_tag) {
+          constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-        for (int c = 0; c < BM / 32; ++c) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(ts + c * 32, sr);
-          tmem_ld32(tdp + c * 32, dr);
-          tmem_ld_wait();
-          uint32_t pk[16], dk[16];
+          for (int c = 0; c < BM / 32; ++c) {
+            uint32_t sr[32], dr[32];
+            tmem_ld32(ts + c * 32, sr);
+            tmem_ld32(tdp + c * 32, dr);
+            tmem_ld_wait();
+            uint32_t pk[16], dk[16];
 #pragma unroll
-          for (int t = 0; t < 32; t += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lrow + c * 32 + t);
-            const float4 d4 = *reinterpret_cast<const float4*>(drow + c * 32 + t);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pp[4], dd[4];
+            for (int t = 0; t < 32; t += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lrow + c * 32 + t);
+              const float4 d4 = *reinterpret_cast<const float4*>(drow + c * 32 + t);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+              float pp[4], dd[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float p = ex2_approx(fmaf(__uint_as_float(sr[t + u]), sl2, -lv[u]));
-              if (need_mask) {
-                const int q = q0 + c * 32 + t + u;
-                p = (key_ok && q < s.N && !(s.causal && key > q)) ? p : 0.f;
+              for (int u = 0; u < 4; ++u) {
+                float p = ex2_approx(fmaf(__uint_as_float(sr[t + u]), sl2, -lv[u]));
+                if constexpr (MASK) {
+                  const int q = q0 + c * 32 + t + u;
+                  p = (key_ok && q < s.N && !(s.causal && key > q)) ? p : 0.f;
+                }
+                pp[u] = p;
+                dd[u] = p * (__uint_as_float(dr[t + u]) - dv4[u]);
               }
-              pp[u] = p;
-              dd[u] = p * (__uint_as_float(dr[t + u]) - dv4[u]);
+              pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
+              pk[(t >> 1) + 1] = pack_bf16x2(pp[2], pp[3]);
+              dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
+              dk[(t >> 1) + 1] = pack_bf16x2(dd[2], dd[3]);
             }
-            pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
-            pk[(t >> 1) + 1] = pack_bf16x2(pp[2], pp[3]);
-            dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
-            dk[(t >> 1) + 1] = pack_bf16x2(dd[2], dd[3]);
-          }
-          tmem_st16(ts + c * 16, pk);
-          tmem_st16(tdp + c * 16, dk);
-          const uint32_t box = sDs(buf) + (c >> 1) * 16384 + r * 128;
+            tmem_st16(ts + c * 16, pk);
+            tmem_st16(tdp + c * 16, dk);
+            const uint32_t box = sDs(buf) + (c >> 1) * 16384 + r * 128;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int chunk = (c & 1) * 4 + j;
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(dk[4 * j]),
-                         "r"(dk[4 * j + 1]), "r"(dk[4 * j + 2]), "r"(dk[4 * j + 3])
-                         : "memory");
+            for (int j = 0; j < 4; ++j) {
+              const int chunk = (c & 1) * 4 + j;
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)),
+                           "r"(dk[4 * j]), "r"(dk[4 * j + 1]), "r"(dk[4 * j + 2]), "r"(dk[4 * j + 3])
+                           : "memory");
+            }
           }
-        }
+        };
+        if (need_mask)
+          step(std::true_type{});
+        else
+          step(std::false_type{});
         tmem_st_wait();
         fence_proxy_async_smem();
         fence_before_sync();

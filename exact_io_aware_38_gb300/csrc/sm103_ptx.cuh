@@ -42,12 +42,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// Test whether the phase with the given parity has completed. If it has not, the thread is
+// suspended until it completes or kSuspendNs pass, so waiting warps leave the issue slots of
+// their SM sub-partition to the warps that compute.
+constexpr uint32_t kSuspendNs = 1000000u;  // 1 ms
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -58,15 +62,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (*abort_flag) return false;
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitNs) {
-        *abort_flag = 1;
-        report_status(status, FA_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitNs) {
+      *abort_flag = 1;
+      report_status(status, FA_ERR_DEVICE_TIMEOUT);
+      return false;
     }
   }
 }
@@ -74,9 +76,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // A wait used only while draining on the abort path: bounded, ignores the abort flag.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 0;; ++it) {
+  for (;;) {
     if (mbar_try(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer() - t0 > kWaitNs) return false;
+    if (globaltimer() - t0 > kWaitNs) return false;
   }
 }
 
