@@ -244,62 +244,77 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (any_work) {
         mbar_wait(b_kv, 0, abort_flag, a.status);
         fence_after_sync();
-        // S^T and dP^T of step `it` into buffer it % NB.
-        auto issue_sdp = [&](uint32_t it) {
-          const int st = it % C::kStages, buf = it % NB;
-          mbar_wait(b_full(st), (it / C::kStages) & 1, abort_flag, a.status);
-          fence_after_sync();
-          if (*abort_flag) return;
-          const uint32_t q_s = sQs(st), do_s = sdOs(st);
+        // The issuer serves two chains at once: S^T/dP^T of step sn (needs its Q/dO tile and, at
+        // d = 128, the dQ^T of step sn - NB read out of the same buffer) and the gradient products
+        // of step g (needs P^T/dS^T of step g). It issues whichever is ready, so neither chain's
+        // latency stalls the other.
+        int n = 0;
+        for (int v = next_v(0); v < nv; v = next_v(v + 1)) ++n;
+        int g = 0, sn = 0;
+        uint64_t t_last = globaltimer();
+        while (g < n && !*abort_flag) {
+          bool progressed = false;
+          if (sn < n && sn < g + NB) {
+            const int st = sn % C::kStages, buf = sn % NB;
+            bool ok = mbar_test(b_full(st), (sn / C::kStages) & 1);
+            if (D == 128 && sn >= NB) ok = ok && mbar_test(b_dqfree(buf), ((sn - NB) / NB) & 1);
+            if (ok) {
+              fence_after_sync();
+              const uint32_t q_s = sQs(st), do_s = sdOs(st);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ok = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
-            mma_ss(tmem + tS(buf), desc_kmajor_sw128(sK + ok), desc_kmajor_sw128(q_s + oq), C::kIdS, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ok = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
-            mma_ss(tmem + tdP(buf), desc_kmajor_sw128(sV + ok), desc_kmajor_sw128(do_s + oq), C::kIdS, kk > 0);
-          }
-          mma_commit(b_sfull(buf));
-        };
-        uint32_t n_issued = 0;  // steps whose S^T/dP^T have been issued
-        int ahead = next_v(0);
-        for (int k = 0; k < NB && ahead < nv; ++k, ahead = next_v(ahead + 1)) issue_sdp(n_issued++);
-        uint32_t it = 0;
-        for (int v = next_v(0); v < nv; v = next_v(v + 1), ++it) {
-          const int st = it % C::kStages, buf = it % NB;
-          const uint32_t q_s = sQs(st), do_s = sdOs(st);
-          mbar_wait(b_pready(buf), (it / NB) & 1, abort_flag, a.status);
-          if (D == 64 && it > 0) mbar_wait(b_dqfree(0), (it - 1) & 1, abort_flag, a.status);  // dQ columns read out
-          fence_after_sync();
-          if (!*abort_flag) {
-#pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk)
-              mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_mnmajor_sw128(do_s + kk * 2048, C::kQBox), C::kIdG,
-                     (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk)
-              mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_mnmajor_sw128(q_s + kk * 2048, C::kQBox), C::kIdG,
-                     (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              if constexpr (D == 128) {
-                mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sK + kk * 2048, 16384),
-                       desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384), C::kIdQ, kk > 0);
-              } else {
-                mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384),
-                       desc_mnmajor_sw128(sK + kk * 2048, 16384), C::kIdQ, kk > 0);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+                mma_ss(tmem + tS(buf), desc_kmajor_sw128(sK + okk), desc_kmajor_sw128(q_s + oq), C::kIdS, kk > 0);
               }
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+                mma_ss(tmem + tdP(buf), desc_kmajor_sw128(sV + okk), desc_kmajor_sw128(do_s + oq), C::kIdS, kk > 0);
+              }
+              mma_commit(b_sfull(buf));
+              ++sn;
+              progressed = true;
             }
-            mma_commit(b_dqfull(buf));
-            mma_commit(b_empty(st));
           }
-          if (ahead < nv) {
-            // Buffer `buf` is reused by step it + NB: at d = 128 its S^T columns hold dQ^T of this step.
-            if (D == 128) mbar_wait(b_dqfree(buf), (it / NB) & 1, abort_flag, a.status);
-            issue_sdp(n_issued++);
-            ahead = next_v(ahead + 1);
+          if (g < sn) {
+            const int st = g % C::kStages, buf = g % NB;
+            bool ok = mbar_test(b_pready(buf), (g / NB) & 1);
+            if (D == 64 && g > 0) ok = ok && mbar_test(b_dqfree(0), (g - 1) & 1);  // dQ columns read out
+            if (ok) {
+              fence_after_sync();
+              const uint32_t q_s = sQs(st), do_s = sdOs(st);
+#pragma unroll
+              for (int kk = 0; kk < BM / 16; ++kk)
+                mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_mnmajor_sw128(do_s + kk * 2048, C::kQBox),
+                       C::kIdG, (g > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int kk = 0; kk < BM / 16; ++kk)
+                mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_mnmajor_sw128(q_s + kk * 2048, C::kQBox),
+                       C::kIdG, (g > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                if constexpr (D == 128) {
+                  mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sK + kk * 2048, 16384),
+                         desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384), C::kIdQ, kk > 0);
+                } else {
+                  mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384),
+                         desc_mnmajor_sw128(sK + kk * 2048, 16384), C::kIdQ, kk > 0);
+                }
+              }
+              mma_commit(b_dqfull(buf));
+              mma_commit(b_empty(st));
+              ++g;
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            t_last = globaltimer();
+          } else {
+            __nanosleep(32);
+            if (globaltimer() - t_last > kWaitNs) {
+              *abort_flag = 1;
+              report_status(a.status, FA_ERR_DEVICE_TIMEOUT);
+            }
           }
         }
         if (!*abort_flag) mma_commit(b_done);
