@@ -21,6 +21,8 @@
 // one tile's products while the other tile's softmax runs.
 // The partial output is rescaled only when a row max grows by more than 2^8 (lazy rescaling;
 // exact, since l and O always share the same reference max).
+#include <type_traits>
+
 #include "fa_tmap.h"
 #include "sm103_ptx.cuh"
 
@@ -254,25 +256,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!vis(x, kt)) continue;
         mbar_wait(b_sfull[x], cnt & 1, abort_flag, a.status);
         fence_after_sync();
-        float sv[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tS + c * 32, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(rr[i]);
-        }
         const int k0 = kt * 128;
-        if ((s.causal && kt == qt) || k0 + 128 > L) {
-          const int lim = min(L - k0, s.causal ? row - k0 + 1 : 128);  // keys [k0, k0+lim) are valid
+        const bool masked = (s.causal && kt == qt) || k0 + 128 > L;
+        const int lim = min(L - k0, s.causal ? row - k0 + 1 : 128);  // keys [k0, k0 + lim) are valid
+        // Pass 1: row max of the (masked) scores, read from tensor memory 32 columns at a time.
+        auto row_max = [&](auto mask_tag) -> float {
+          constexpr bool MASK = decltype(mask_tag)::value;
+          float pm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= lim) sv[c] = -INFINITY;
-        }
-        float mx = sv[0];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tS + c * 32, rr);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+            for (int i = 0; i < 32; ++i) {
+              float v = __uint_as_float(rr[i]);
+              if constexpr (MASK) v = (c * 32 + i < lim) ? v : -INFINITY;
+              pm[i & 3] = fmaxf(pm[i & 3], v);
+            }
+          }
+          return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+        };
+        const float mx = masked ? row_max(std::true_type{}) : row_max(std::false_type{});
         const float mc = mx * sl2;
         if (cnt == 0) {
           m = mc;
@@ -292,19 +297,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mn;
         }
         const float mu = (m == -INFINITY) ? 0.f : m;
-        float sum = 0.f;
+        // Pass 2: P = exp2(c log2(e) s - m) in bf16 over the first 64 columns of S (each chunk is
+        // written only over columns already read), and the row sum of P.
+        auto exp_pass = [&](auto mask_tag) -> float {
+          constexpr bool MASK = decltype(mask_tag)::value;
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tS + c * 32, rr);
+            tmem_ld_wait();
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2_approx(fmaf(sv[h * 64 + 2 * i], sl2, -mu));
-            const float p1 = ex2_approx(fmaf(sv[h * 64 + 2 * i + 1], sl2, -mu));
-            sum += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
+            for (int i = 0; i < 16; ++i) {
+              float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), sl2, -mu));
+              float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), sl2, -mu));
+              if constexpr (MASK) {
+                p0 = (c * 32 + 2 * i < lim) ? p0 : 0.f;
+                p1 = (c * 32 + 2 * i + 1 < lim) ? p1 : 0.f;
+              }
+              ps[i & 3] += p0 + p1;
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + c * 16, pk);
           }
-          tmem_st32(tS + h * 32, pk);
-        }
+          return (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        };
+        const float sum = masked ? exp_pass(std::true_type{}) : exp_pass(std::false_type{});
         tmem_st_wait();
         l += sum;
         fence_before_sync();
