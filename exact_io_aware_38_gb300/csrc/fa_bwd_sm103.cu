@@ -49,7 +49,9 @@ struct BwdCfg {
   static constexpr int kQBox = BM * 128;             // one 64-column box of a Q or dO tile
   static constexpr int kQBytes = BM * D * 2;         // Q or dO tile (BM rows)
   static constexpr int kStages = D == 128 ? 3 : 2;   // Q/dO ring depth
-  static constexpr int kDsBytes = 128 * BM * 2;      // dS^T tile [128 keys][BM queries], per buffer
+  // dS^T tile [128 keys][BM queries] per buffer, in 128-byte-swizzled rows of 64 queries (a step
+  // of 32 queries uses the first half of each row).
+  static constexpr int kDsBytes = 128 * (BM < 64 ? 64 : BM) * 2;
   static constexpr int kDqBytes = D == 128 ? BM * D * 4 : 0;  // fp32 dQ staging for the bulk add
   static constexpr int kSmem = 2 * kKVBytes + kStages * 2 * kQBytes + kBufs * kDsBytes + kDqBytes + 1024;
   static constexpr uint32_t kTdK = 0, kTdV = D;
@@ -59,28 +61,32 @@ struct BwdCfg {
   static constexpr uint32_t kIdG = idesc_bf16(128, D, false, true);
   static constexpr uint32_t kIdQ = D == 128 ? idesc_bf16(128, BM, true, true) : idesc_bf16(BM, D, true, true);
   static_assert(kSmem <= 232448 - 1536, "shared memory budget");
+  static_assert(2 * kKVBytes <= kStages * 2 * kQBytes, "dK and dV staging reuse the Q/dO ring");
+  static_assert(kStages <= 4 && kBufs <= 4, "barrier arrays of the control block");
 };
+
+constexpr int kMaxStages = 4;
+constexpr int kMaxBufs = 4;
 
 struct alignas(16) BwdSmemCtl {
   uint64_t kv_full;
-  uint64_t full[3];
-  uint64_t empty[3];
-  uint64_t s_full[2], p_ready[2], dq_full[2], dq_free[2];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t s_full[kMaxBufs], p_ready[kMaxBufs], dq_full[kMaxBufs], dq_free[kMaxBufs];
   uint64_t done, drain;
   uint32_t tmem_base;
   int abort_flag;
-  alignas(16) float lse2[2][64];  // LSE * log2(e) per query of the step, per buffer (d = 128)
-  alignas(16) float dvec[2][64];  // D per query of the step, per buffer (d = 128)
+  alignas(16) float lse2[128];  // LSE * log2(e) per query of the step: [buffer][BM]
+  alignas(16) float dvec[128];  // D per query of the step: [buffer][BM]
 };
 
-// d = 64 uses one buffer of 128 queries: it reuses the same arrays as [1][128].
 template <int D>
 __device__ __forceinline__ float* lse_row(BwdSmemCtl& c, int buf) {
-  return D == 128 ? c.lse2[buf] : &c.lse2[0][0];
+  return c.lse2 + buf * BwdCfg<D>::BM;
 }
 template <int D>
 __device__ __forceinline__ float* dvec_row(BwdSmemCtl& c, int buf) {
-  return D == 128 ? c.dvec[buf] : &c.dvec[0][0];
+  return c.dvec + buf * BwdCfg<D>::BM;
 }
 
 template <int D>
@@ -216,8 +222,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sK + c * 16384, &tmK, c * 64, kt * 128, bh, b_kv);
         tma_load_3d(sV + c * 16384, &tmV, c * 64, kt * 128, bh, b_kv);
       }
-      uint32_t last_par[3];
-      bool issued[3] = {false, false, false};
+      uint32_t last_par[kMaxStages];
+      bool issued[kMaxStages] = {};
       uint32_t i = 0;
       for (int v = next_v(0); v < nv; v = next_v(v + 1), ++i) {
         const int st = i % C::kStages;
@@ -336,6 +342,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int key = kt * 128 + r;
       const bool key_ok = key < L;
       const float sl2 = a.scale * kLog2e;
+      // LSE and D of a step are loaded one step ahead, so their latency overlaps the previous step.
+      auto fetch = [&](int v, float& lv, float& dv) {
+        const int q = v * BM + r;
+        const bool ok = v < nv && r < BM && q < s.N;
+        lv = ok ? LSE[q] * kLog2e : 0.f;
+        dv = ok ? Dv[q] : 0.f;
+      };
+      float next_l, next_d;
+      fetch(next_v(0), next_l, next_d);
       for (int v = next_v(0); v < nv; v = next_v(v + 1), ++it) {
         const int q0 = v * BM;
         const int buf = it % NB;
@@ -343,11 +358,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float* drow = dvec_row<D>(ctl, buf);
         named_bar_sync(1, 128);  // every thread is done with this buffer's previous LSE and D
         if (r < BM) {
-          const int q = q0 + r;
-          lrow[r] = q < s.N ? LSE[q] * kLog2e : 0.f;
-          drow[r] = q < s.N ? Dv[q] : 0.f;
+          lrow[r] = next_l;
+          drow[r] = next_d;
         }
         named_bar_sync(1, 128);
+        fetch(next_v(v + 1), next_l, next_d);
         mbar_wait(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);
         fence_after_sync();
         const bool need_mask = (s.causal && (q0 / 128) == kt) || (kt * 128 + 128 > L) || (q0 + BM > s.N);
@@ -461,7 +476,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     const uint32_t tacc = tmem + lane_off + (elementwise ? C::kTdK : C::kTdV);
     const float mul = elementwise ? a.scale : 1.f;
-    const uint32_t stg = sStage0 + (elementwise ? 0 : 2 * C::kQBytes);  // Q/dO stage 0 or 1 (a K-sized tile)
+    const uint32_t stg = sStage0 + (elementwise ? 0 : C::kKVBytes);  // the (idle) Q/dO ring holds dK, dV
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t vv[32];
