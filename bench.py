@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import datetime
+import hashlib
 import json
 import os
 import statistics
@@ -120,6 +121,31 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None, "samples_in_timed_region": len(sm),
                 "reasons": sorted(reasons)}
+
+
+def kernel_traffic(name, workload_name, heads_override):
+    """DRAM bytes per launch of `name` from the committed ncu record, or None when the record is
+    for another workload or the kernel source has changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))[name]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    except (OSError, KeyError, ValueError):
+        return None
+    if heads_override is not None or not rec["workload"].startswith(workload_name + ":"):
+        return None
+    if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_prefix"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+def max_over_ranks(value, pg, device):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if pg is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
 
 
 def cpu_oracle_step(inp, head):
@@ -244,10 +270,7 @@ def main():
     ms = start.elapsed_time(end) / args.steps
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, pg, dev)
     assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
 
     flops = rl.attention_flops(B, H, N, d, causal=w.causal,
@@ -285,10 +308,7 @@ def main():
         e2.record(stream)
         torch.cuda.synchronize()
         e2e_ms = s2.elapsed_time(e2) / args.steps
-        if pg is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, pg, dev)
         return {"value": flops["total"] * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
@@ -307,8 +327,10 @@ def main():
                    "parallelism": f"replicas x{world}", "l2": "inputs 4 x 64 MiB > 129 MB L2; no flush"},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops},
-        "roofline": {"bound": "tensor", "kernel": "fa_bwd (pre + main + post, one event span)", "achieved": bwd_tflops,
-                     "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak, "traffic": None,
+        "roofline": {"bound": "tensor", "kernel": "bwd_tc_kernel (timed as the fa_bwd span: pre + main + post)",
+                     "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak,
+                     "traffic": kernel_traffic(f"bwd_tc_kernel<{d}>", w.name, args.heads),
+                     "traffic_unit": "DRAM bytes per launch (ncu, profiles/traffic.json)",
                      "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)"},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
