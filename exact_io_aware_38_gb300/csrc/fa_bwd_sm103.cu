@@ -258,7 +258,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int v = next_v(0); v < nv; v = next_v(v + 1)) ++n;
         int g = 0, sn = 0;
         uint64_t t_last = globaltimer();
-        while (g < n && !*abort_flag) {
+        // The abort flag is read only when nothing was issuable (a shared-memory load right
+        // behind tcgen05 MMAs waits for them to be dispatched).
+        while (g < n) {
           bool progressed = false;
           if (sn < n && sn < g + NB) {
             const int st = sn % C::kStages, buf = sn % NB;
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (progressed) {
             t_last = globaltimer();
           } else {
+            if (*abort_flag) break;
             __nanosleep(32);
             if (globaltimer() - t_last > kWaitNs) {
               *abort_flag = 1;

@@ -174,8 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return sl;
       };
+      // No abort-flag reads on the issue path (see mbar_wait): after an abort the remaining MMAs
+      // run on stale data and complete normally.
       auto issue_s = [&](int x, int sk) {
-        if (*abort_flag) return;
         const uint32_t qa = sQ + x * C::kTileBytes, ka = sKV + sk * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -186,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(b_sfull[x]);
       };
       auto issue_pv = [&](int x, int sv) {
-        if (*abort_flag) return;
         const uint32_t va = sKV + sv * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(x, sk);
             any[x] = true;
           }
-        if (!*abort_flag) mma_commit(b_empty(sk));
+        mma_commit(b_empty(sk));
         while (true) {
           const int sv = take();
           const int ktn = next_union(kt + 1);
@@ -223,16 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               any[x] = true;
             }
           }
-          if (!*abort_flag) {
-            mma_commit(b_empty(sv));
-            if (skn >= 0) mma_commit(b_empty(skn));
-          }
+          mma_commit(b_empty(sv));
+          if (skn >= 0) mma_commit(b_empty(skn));
           if (ktn >= s.nb) break;
           kt = ktn;
         }
       }
       for (int x = 0; x < 2; ++x)
-        if (any[x] && !*abort_flag) mma_commit(b_odone[x]);
+        if (any[x]) mma_commit(b_odone[x]);
       mma_commit(smem_u32(&ctl.drain));  // every MMA of this CTA has finished when this arrives
       mbar_wait_drain(smem_u32(&ctl.drain), 0);
     }

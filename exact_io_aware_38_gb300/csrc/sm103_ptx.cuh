@@ -68,14 +68,15 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Returns false (and records the error)
-// on timeout, or at once if the CTA has already aborted.
+// on timeout, or once the CTA has aborted. The abort flag is read only after a failed test: a
+// shared-memory load issued right behind tcgen05 MMAs waits for them to be dispatched, so the
+// fast path touches nothing but the barrier.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  if (*abort_flag) return false;
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-    if (mbar_try(bar, parity)) return true;
     if (*abort_flag) return false;
+    if (mbar_try(bar, parity)) return true;
     if (globaltimer() - t0 > kWaitNs) {
       *abort_flag = 1;
       report_status(status, FA_ERR_DEVICE_TIMEOUT);
