@@ -21,7 +21,8 @@
 // d = 64:  dQ_i = dS_i K_j (lane = query row) in its own tensor-memory columns, added with 16-byte
 //          vector atomics.
 //
-// CTA layout (384 threads): warp 0 TMA producer; warp 1 MMA issuer and tensor-memory owner;
+// CTA layout (384 threads): warp 0 TMA producer; warp 1 S^T/dP^T MMA issuer and tensor-memory owner;
+// warp 2 gradient MMA issuer;
 // warps 4-7 elementwise warpgroup (thread = key row; lane quadrant = warp % 4), which also writes
 // dK; warps 8-11 dQ warpgroup (reads dQ out of tensor memory, adds it into the accumulator), which
 // also writes dV. The two warpgroups run concurrently on different steps.
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_dqfree(i), 128);
     }
     mbar_init(b_done, 1);
-    mbar_init(b_drain, 1);
+    mbar_init(b_drain, 2);  // one commit per MMA issuer
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -244,89 +245,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (issued[k]) mbar_wait_drain(b_full(k), last_par[k]);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Two issuing threads, one per dependency chain: a thread issuing tcgen05 MMAs blocks while
+    // the tensor core's queue is full, so one issuer could not react to the other chain.
+    //   warp 1: S^T/dP^T of step sn into buffer sn % NB, once its Q/dO tile has landed and (d = 128)
+    //           the buffer's dQ^T of step sn - NB has been read out (that read-out follows the
+    //           completion of all of step sn - NB's gradient MMAs, including dV's read of P^T);
+    //   warp 2: dV, dK and dQ of step g, once P^T/dS^T of step g are in place (which follows the
+    //           completion of step g's S^T/dP^T).
     if (lane == 0) {
       if (any_work) {
         mbar_wait(b_kv, 0, abort_flag, a.status);
-        fence_after_sync();
-        // The issuer serves two chains at once: S^T/dP^T of step sn (needs its Q/dO tile and, at
-        // d = 128, the dQ^T of step sn - NB read out of the same buffer) and the gradient products
-        // of step g (needs P^T/dS^T of step g). It issues whichever is ready, so neither chain's
-        // latency stalls the other.
         int n = 0;
         for (int v = next_v(0); v < nv; v = next_v(v + 1)) ++n;
-        int g = 0, sn = 0;
-        uint64_t t_last = globaltimer();
-        // The abort flag is read only when nothing was issuable (a shared-memory load right
-        // behind tcgen05 MMAs waits for them to be dispatched).
-        while (g < n) {
-          bool progressed = false;
-          if (sn < n && sn < g + NB) {
+        if (warp == 1) {
+          for (int sn = 0; sn < n; ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
-            bool ok = mbar_test(b_full(st), (sn / C::kStages) & 1);
-            if (D == 128 && sn >= NB) ok = ok && mbar_test(b_dqfree(buf), ((sn - NB) / NB) & 1);
-            if (ok) {
+            mbar_wait(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
+            if (sn >= NB) {
+              mbar_wait(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
-              const uint32_t q_s = sQs(st), do_s = sdOs(st);
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
-                mma_ss(tmem + tS(buf), desc_kmajor_sw128(sK + okk), desc_kmajor_sw128(q_s + oq), C::kIdS, kk > 0);
-              }
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
-                mma_ss(tmem + tdP(buf), desc_kmajor_sw128(sV + okk), desc_kmajor_sw128(do_s + oq), C::kIdS, kk > 0);
-              }
-              mma_commit(b_sfull(buf));
-              ++sn;
-              progressed = true;
             }
+            const uint32_t q_s = sQs(st), do_s = sdOs(st);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+              mma_ss(tmem + tS(buf), desc_kmajor_sw128(sK + okk), desc_kmajor_sw128(q_s + oq), C::kIdS, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+              mma_ss(tmem + tdP(buf), desc_kmajor_sw128(sV + okk), desc_kmajor_sw128(do_s + oq), C::kIdS, kk > 0);
+            }
+            mma_commit(b_sfull(buf));
           }
-          if (g < sn) {
+        } else {
+          for (int g = 0; g < n; ++g) {
             const int st = g % C::kStages, buf = g % NB;
-            bool ok = mbar_test(b_pready(buf), (g / NB) & 1);
-            if (D == 64 && g > 0) ok = ok && mbar_test(b_dqfree(0), (g - 1) & 1);  // dQ columns read out
-            if (ok) {
-              fence_after_sync();
-              const uint32_t q_s = sQs(st), do_s = sdOs(st);
+            mbar_wait(b_pready(buf), (g / NB) & 1, abort_flag, a.status);
+            if (D == 64 && g > 0) mbar_wait(b_dqfree(0), (g - 1) & 1, abort_flag, a.status);  // dQ columns read out
+            fence_after_sync();
+            const uint32_t q_s = sQs(st), do_s = sdOs(st);
 #pragma unroll
-              for (int kk = 0; kk < BM / 16; ++kk)
-                mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_mnmajor_sw128(do_s + kk * 2048, C::kQBox),
-                       C::kIdG, (g > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BM / 16; ++kk)
+              mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_mnmajor_sw128(do_s + kk * 2048, C::kQBox), C::kIdG,
+                     (g > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-              for (int kk = 0; kk < BM / 16; ++kk)
-                mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_mnmajor_sw128(q_s + kk * 2048, C::kQBox),
-                       C::kIdG, (g > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BM / 16; ++kk)
+              mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_mnmajor_sw128(q_s + kk * 2048, C::kQBox), C::kIdG,
+                     (g > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                if constexpr (D == 128) {
-                  mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sK + kk * 2048, 16384),
-                         desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384), C::kIdQ, kk > 0);
-                } else {
-                  mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384),
-                         desc_mnmajor_sw128(sK + kk * 2048, 16384), C::kIdQ, kk > 0);
-                }
+            for (int kk = 0; kk < 8; ++kk) {
+              if constexpr (D == 128) {
+                mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sK + kk * 2048, 16384),
+                       desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384), C::kIdQ, kk > 0);
+              } else {
+                mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384),
+                       desc_mnmajor_sw128(sK + kk * 2048, 16384), C::kIdQ, kk > 0);
               }
-              mma_commit(b_dqfull(buf));
-              mma_commit(b_empty(st));
-              ++g;
-              progressed = true;
             }
+            mma_commit(b_dqfull(buf));
+            mma_commit(b_empty(st));
           }
-          if (progressed) {
-            t_last = globaltimer();
-          } else {
-            if (*abort_flag) break;
-            __nanosleep(32);
-            if (globaltimer() - t_last > kWaitNs) {
-              *abort_flag = 1;
-              report_status(a.status, FA_ERR_DEVICE_TIMEOUT);
-            }
-          }
+          mma_commit(b_done);  // the last gradient MMAs complete after every S^T/dP^T
         }
-        if (!*abort_flag) mma_commit(b_done);
       }
       mma_commit(b_drain);
       mbar_wait_drain(b_drain, 0);
