@@ -299,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // written only over columns already read), and the row sum of P.
         auto exp_pass = [&](auto mask_tag) -> float {
           constexpr bool MASK = decltype(mask_tag)::value;
-          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+          const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-mu, -mu);
+          float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t rr[32];
@@ -308,18 +309,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), sl2, -mu));
-              float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), sl2, -mu));
+              const float2 x = fma2(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sc2, nm2);
+              float p0 = ex2_approx(x.x);
+              float p1 = ex2_approx(x.y);
               if constexpr (MASK) {
                 p0 = (c * 32 + 2 * i < lim) ? p0 : 0.f;
                 p1 = (c * 32 + 2 * i + 1 < lim) ? p1 : 0.f;
               }
-              ps[i & 3] += p0 + p1;
+              ps[i & 1] = add2(ps[i & 1], make_float2(p0, p1));
               pk[i] = pack_bf16x2(p0, p1);
             }
             tmem_st16(tS + c * 16, pk);
           }
-          return (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          return (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
         };
         const float sum = masked ? exp_pass(std::true_type{}) : exp_pass(std::false_type{});
         tmem_st_wait();
