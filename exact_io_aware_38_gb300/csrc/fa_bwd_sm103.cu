@@ -368,22 +368,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int t = 0; t < 32; t += 4) {
               const float4 l4 = *reinterpret_cast<const float4*>(lrow + c * 32 + t);
               const float4 d4 = *reinterpret_cast<const float4*>(drow + c * 32 + t);
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-              float pp[4], dd[4];
+              const float2 sc2 = make_float2(sl2, sl2);
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                float p = ex2_approx(fmaf(__uint_as_float(sr[t + u]), sl2, -lv[u]));
+              for (int u = 0; u < 4; u += 2) {
+                const float2 lv = u == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
+                const float2 dv2 = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+                const float2 x = fma2(make_float2(__uint_as_float(sr[t + u]), __uint_as_float(sr[t + u + 1])), sc2, lv);
+                float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                 if constexpr (MASK) {
                   const int q = q0 + c * 32 + t + u;
-                  p = (key_ok && q < s.N && !(s.causal && key > q)) ? p : 0.f;
+                  p.x = (key_ok && q < s.N && !(s.causal && key > q)) ? p.x : 0.f;
+                  p.y = (key_ok && q + 1 < s.N && !(s.causal && key > q + 1)) ? p.y : 0.f;
                 }
-                pp[u] = p;
-                dd[u] = p * (__uint_as_float(dr[t + u]) - dv4[u]);
+                const float2 dd =
+                    mul2(p, sub2(make_float2(__uint_as_float(dr[t + u]), __uint_as_float(dr[t + u + 1])), dv2));
+                pk[(t + u) >> 1] = pack_bf16x2(p.x, p.y);
+                dk[(t + u) >> 1] = pack_bf16x2(dd.x, dd.y);
               }
-              pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
-              pk[(t >> 1) + 1] = pack_bf16x2(pp[2], pp[3]);
-              dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
-              dk[(t >> 1) + 1] = pack_bf16x2(dd[2], dd[3]);
             }
             tmem_st16(ts + c * 16, pk);
             tmem_st16(tdp + c * 16, dk);
