@@ -267,10 +267,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tS + c * 32, rr);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              float v = __uint_as_float(rr[i]);
-              if constexpr (MASK) v = (c * 32 + i < lim) ? v : -INFINITY;
-              pm[i & 3] = fmaxf(pm[i & 3], v);
+            for (int i = 0; i < 32; i += 2) {
+              float v0 = __uint_as_float(rr[i]), v1 = __uint_as_float(rr[i + 1]);
+              if constexpr (MASK) {
+                v0 = (c * 32 + i < lim) ? v0 : -INFINITY;
+                v1 = (c * 32 + i + 1 < lim) ? v1 : -INFINITY;
+              }
+              pm[(i >> 1) & 3] = fmax3(pm[(i >> 1) & 3], v0, v1);
             }
           }
           return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
