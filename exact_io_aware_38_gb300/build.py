@@ -81,6 +81,28 @@ def build(extra=(), verbose=False, force=False) -> str:
     return LIB
 
 
+TEST_WITHHOLD_LIB = os.path.join(OUT_DIR, "libfa_withhold_kv.so")
+
+
+def build_withhold_kv_test_lib() -> str:
+    """Test-only variant whose forward producer never loads K/V and whose waits give up after
+    50 ms: used to check that a wait that runs out returns FA_ERR_DEVICE_TIMEOUT cleanly."""
+    os.makedirs(OUT_DIR, exist_ok=True)
+    cc = nvcc()
+    extra = ["-DFA_TEST_WITHHOLD_KV"]
+    objs = []
+    for src in _sources():
+        obj = os.path.join(OUT_DIR, "withhold_" + os.path.basename(src)[:-3] + ".o")
+        r = subprocess.run([cc] + _flags(extra) + ["-c", src, "-o", obj], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        objs.append(obj)
+    r = subprocess.run([cc] + ARCH + ["-shared", "-o", TEST_WITHHOLD_LIB] + objs, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return TEST_WITHHOLD_LIB
+
+
 if __name__ == "__main__":
     extra = ["-DFA_DEBUG_BOUNDS"] if "--debug-bounds" in sys.argv else []
     print(build(extra, verbose="-v" in sys.argv, force=True))

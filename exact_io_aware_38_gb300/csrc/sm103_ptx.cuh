@@ -21,7 +21,11 @@ namespace tc {
 // Every wait is bounded: after kWaitNs without progress the waiter records FA_ERR_DEVICE_TIMEOUT,
 // raises the CTA's abort flag, and every later wait of the CTA returns immediately. The kernels
 // keep one control flow for all threads either way, so no named barrier is left short of arrivals.
+#ifdef FA_TEST_WITHHOLD_KV
+constexpr uint64_t kWaitNs = 50000000ull;    // 50 ms in the timeout-path test build
+#else
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+#endif
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
