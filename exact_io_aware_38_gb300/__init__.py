@@ -5,8 +5,8 @@ library's CUDA kernels. PyTorch provides device memory and the current stream. T
 fallback: if the library is missing, every call raises.
 
 Raw C-ABI names (same signatures as ``include/fa.h``, pointers as ints):
-    fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_status_string, fa_bwd_noalloc
-Tensor helpers:
+    fa_fwd, fa_bwd, fa_fwd_gqa, fa_bwd_gqa, fa_bwd_workspace_bytes, fa_status_string, fa_bwd_noalloc
+Tensor helpers (grouped-query attention when k, v have fewer heads than q):
     fwd(q, k, v, ...) -> (o, lse);  bwd(q, k, v, o, lse, do, ...) -> (dq, dk, dv)
 """
 
@@ -29,6 +29,9 @@ _SIGS = {
     "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P,
                     ctypes.c_size_t, _P, _P]),
+    "fa_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P]),
+    "fa_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P,
+                        ctypes.c_size_t, _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P]),
 }
@@ -80,6 +83,18 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, se
                             workspace, workspace_bytes, dev_status, stream))
 
 
+def fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, causal, block_mask, seqlens_k, scale, tile_visits, dev_status,
+               stream) -> int:
+    return int(lib().fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, causal, block_mask, seqlens_k, scale, tile_visits,
+                                dev_status, stream))
+
+
+def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k, scale, workspace,
+               workspace_bytes, dev_status, stream) -> int:
+    return int(lib().fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k,
+                                scale, workspace, workspace_bytes, dev_status, stream))
+
+
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, seqlens_k, scale, dev_status,
                    stream) -> int:
     """fa_bwd without a workspace: for callers that cannot allocate device memory (see fa.h)."""
@@ -103,6 +118,16 @@ def _check_qkv(*ts):
         raise ValueError("expected [B, H, N, d]")
 
 
+def _check_kv(q, k, v):
+    """k, v: [B, Hkv, N, d] with Hkv dividing q's head count H; returns Hkv."""
+    _check_qkv(k, v)
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if (k.shape[0], k.shape[2], k.shape[3]) != (B, N, d) or H % Hkv != 0:
+        raise ValueError("k, v must be [B, Hkv, N, d] with Hkv dividing the query head count")
+    return Hkv
+
+
 def _masks(block_mask, seqlens_k, N, B, dev):
     nb = (N + 127) // 128
     if block_mask is not None:
@@ -123,16 +148,19 @@ def _stream(stream):
 
 def fwd(q, k, v, *, causal=False, block_mask=None, seqlens_k=None, scale=None, out=None, lse=None,
         tile_visits=None, status=None, stream=None):
-    """O, LSE = attention(q, k, v) on the current CUDA stream. Outputs are allocated unless given."""
-    _check_qkv(q, k, v)
+    """O, LSE = attention(q, k, v) on the current CUDA stream. Outputs are allocated unless given.
+    k and v may have fewer heads than q (grouped-query attention, fa_fwd_gqa)."""
+    _check_qkv(q)
+    Hkv = _check_kv(q, k, v)
     B, H, N, d = q.shape
     _masks(block_mask, seqlens_k, N, B, q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     _check_qkv(q, o)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, int(causal),
-                _ptr(block_mask), _ptr(seqlens_k), scale, _ptr(tile_visits), _ptr(status), _stream(stream))
+    rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, N, d,
+                    int(causal), _ptr(block_mask), _ptr(seqlens_k), scale, _ptr(tile_visits), _ptr(status),
+                    _stream(stream))
     if rc != 0:
         raise FaError(rc)
     return o, lse
@@ -140,20 +168,25 @@ def fwd(q, k, v, *, causal=False, block_mask=None, seqlens_k=None, scale=None, o
 
 def bwd(q, k, v, o, lse, do, *, causal=False, block_mask=None, seqlens_k=None, scale=None, dq=None, dk=None, dv=None,
         workspace=None, status=None, stream=None):
-    """dQ, dK, dV of attention on the current CUDA stream (outputs/workspace allocated unless given)."""
-    _check_qkv(q, k, v, o, do)
+    """dQ, dK, dV of attention on the current CUDA stream (outputs/workspace allocated unless given).
+    k and v may have fewer heads than q (grouped-query attention, fa_bwd_gqa); dk, dv are shaped like k."""
+    _check_qkv(q, o, do)
+    Hkv = _check_kv(q, k, v)
     B, H, N, d = q.shape
     _masks(block_mask, seqlens_k, N, B, q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    _check_qkv(q, dq)
+    _check_qkv(k, dk, dv)
     nbytes = fa_bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
-                dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(causal), _ptr(block_mask), _ptr(seqlens_k), scale,
-                workspace.data_ptr(), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    rc = fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, d, int(causal), _ptr(block_mask),
+                    _ptr(seqlens_k), scale, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                    _ptr(status), _stream(stream))
     if rc != 0:
         raise FaError(rc)
     return dq, dk, dv

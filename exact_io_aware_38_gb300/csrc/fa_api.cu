@@ -21,10 +21,14 @@ int check_shape(int B, int H, int N, int d, int causal, float scale) {
   return FA_OK;
 }
 
-fa::AttnShape make_shape(int B, int H, int N, int d, int causal, const uint8_t* bm, const int32_t* sl) {
+// K/V heads: each must serve the same number of query heads.
+inline bool check_kv_heads(int H, int Hkv) { return Hkv >= 1 && Hkv <= H && H % Hkv == 0; }
+
+fa::AttnShape make_shape(int B, int H, int Hkv, int N, int d, int causal, const uint8_t* bm, const int32_t* sl) {
   fa::AttnShape s;
   s.B = B;
   s.H = H;
+  s.Hkv = Hkv;
   s.N = N;
   s.d = d;
   s.nb = (N + fa::kTile - 1) / fa::kTile;
@@ -52,12 +56,13 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
-           const uint8_t* block_mask, const int32_t* seqlens_k, float scale, int32_t* tile_visits, int* dev_status,
-           void* stream) {
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+               int causal, const uint8_t* block_mask, const int32_t* seqlens_k, float scale, int32_t* tile_visits,
+               int* dev_status, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   const int rc = check_shape(B, H, N, d, causal, scale);
   if (rc != FA_OK) return rc;
+  if (!check_kv_heads(H, Hkv)) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       !aligned(seqlens_k, 4) || !aligned(tile_visits, 4) || !aligned(dev_status, 4))
     return FA_ERR_MISALIGNED;
@@ -67,12 +72,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.v = v;
   a.o = o;
   a.lse = lse;
-  a.s = make_shape(B, H, N, d, causal, block_mask, seqlens_k);
+  a.s = make_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
   a.scale = scale;
   a.tile_visits = tile_visits;
   a.status = dev_status;
   const cudaError_t e = fa_launch_fwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
+           const uint8_t* block_mask, const int32_t* seqlens_k, float scale, int32_t* tile_visits, int* dev_status,
+           void* stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, block_mask, seqlens_k, scale, tile_visits, dev_status,
+                    stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -81,13 +93,14 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   return round_up(rows * sizeof(float)) + round_up(rows * d * sizeof(float));
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
-           void* dk, void* dv, int B, int H, int N, int d, int causal, const uint8_t* block_mask,
-           const int32_t* seqlens_k, float scale, void* workspace, size_t workspace_bytes, int* dev_status,
-           void* stream) {
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+               void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal,
+               const uint8_t* block_mask, const int32_t* seqlens_k, float scale, void* workspace,
+               size_t workspace_bytes, int* dev_status, void* stream) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
   const int rc = check_shape(B, H, N, d, causal, scale);
   if (rc != FA_OK) return rc;
+  if (!check_kv_heads(H, Hkv)) return FA_ERR_INVALID_ARG;
   const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
   if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
@@ -107,11 +120,19 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.dv = dv;
   a.dvec = static_cast<float*>(workspace);
   a.dqacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * sizeof(float)));
-  a.s = make_shape(B, H, N, d, causal, block_mask, seqlens_k);
+  a.s = make_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
   a.scale = scale;
   a.status = dev_status;
   const cudaError_t e = fa_launch_bwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, int B, int H, int N, int d, int causal, const uint8_t* block_mask,
+           const int32_t* seqlens_k, float scale, void* workspace, size_t workspace_bytes, int* dev_status,
+           void* stream) {
+  return fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, N, d, causal, block_mask, seqlens_k, scale, workspace,
+                    workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -156,19 +156,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = &ctl.abort_flag;
 
   const AttnShape& s = a.s;
-  const int BH = s.B * s.H;
-  const int kt = blockIdx.x / BH;  // key tile: small kt (most causal work) first
-  const int bh = blockIdx.x % BH;
-  const int b = bh / s.H;
+  const int BHkv = s.B * s.Hkv;
+  const int kt = blockIdx.x / BHkv;  // key tile: small kt (most causal work) first
+  const int bkv = blockIdx.x % BHkv;  // K/V head (b, hk) whose dK, dV this CTA owns
+  const int b = bkv / s.Hkv;
+  const int G = s.H / s.Hkv;                       // query heads sharing this K/V head
+  const int bh0 = b * s.H + (bkv % s.Hkv) * G;     // the group's first query head
   const int L = key_len(s, b);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nv = (s.N + BM - 1) / BM;  // BM-row query steps
 
   // Query steps v (rows v*BM ..) are visited iff their 128-row tile is visited for this key tile.
+  // The pattern is the same for every query head of the group; a step is a (group head gi, v)
+  // pair, heads outer, so dK and dV sum over the group in tensor memory.
   auto next_v = [&](int v) -> int {
     for (; v < nv; ++v)
       if (tile_visited(s, (v * BM) / 128, kt, L)) return v;
     return nv;
+  };
+  auto advance = [&](int& gi, int& v) {
+    v = next_v(v + 1);
+    if (v >= nv) {
+      ++gi;
+      v = next_v(0);
+    }
   };
   auto sQs = [&](int st) { return sStage0 + (2 * st) * C::kQBytes; };
   auto sdOs = [&](int st) { return sStage0 + (2 * st + 1) * C::kQBytes; };
@@ -220,20 +231,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tmdO);
       mbar_expect_tx(b_kv, 2 * C::kKVBytes);
       for (int c = 0; c < C::kBoxes; ++c) {
-        tma_load_3d(sK + c * 16384, &tmK, c * 64, kt * 128, bh, b_kv);
-        tma_load_3d(sV + c * 16384, &tmV, c * 64, kt * 128, bh, b_kv);
+        tma_load_3d(sK + c * 16384, &tmK, c * 64, kt * 128, bkv, b_kv);
+        tma_load_3d(sV + c * 16384, &tmV, c * 64, kt * 128, bkv, b_kv);
       }
       uint32_t last_par[kMaxStages];
       bool issued[kMaxStages] = {};
       uint32_t i = 0;
-      for (int v = next_v(0); v < nv; v = next_v(v + 1), ++i) {
+      for (int gi = 0, v = next_v(0); gi < G && v < nv; advance(gi, v), ++i) {
         const int st = i % C::kStages;
         const uint32_t par = (i / C::kStages) & 1;
         if (mbar_wait(b_empty(st), par ^ 1, abort_flag, a.status)) {
           mbar_expect_tx(b_full(st), 2 * C::kQBytes);
           for (int c = 0; c < C::kBoxes; ++c) {
-            tma_load_3d(sQs(st) + c * C::kQBox, &tmQ, c * 64, v * BM, bh, b_full(st));
-            tma_load_3d(sdOs(st) + c * C::kQBox, &tmdO, c * 64, v * BM, bh, b_full(st));
+            tma_load_3d(sQs(st) + c * C::kQBox, &tmQ, c * 64, v * BM, bh0 + gi, b_full(st));
+            tma_load_3d(sdOs(st) + c * C::kQBox, &tmdO, c * 64, v * BM, bh0 + gi, b_full(st));
           }
           issued[st] = true;
           last_par[st] = par;
@@ -259,6 +270,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_wait(b_kv, 0, abort_flag, a.status);
         int n = 0;
         for (int v = next_v(0); v < nv; v = next_v(v + 1)) ++n;
+        n *= G;
         if (warp == 1) {
           for (int sn = 0; sn < n; ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
@@ -318,9 +330,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // tensor-memory lane: key row (and head dimension of dQ^T)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const float* LSE = a.lse + (size_t)bh * s.N;
-    const float* Dv = a.dvec + (size_t)bh * s.N;
-    float* dQa = a.dqacc + (size_t)bh * s.N * D;
     const bool elementwise = warp < 8;
     uint32_t it = 0;
     if (elementwise) {
@@ -329,15 +338,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool key_ok = key < L;
       const float sl2 = a.scale * kLog2e;
       // LSE and D of a step are loaded one step ahead, so their latency overlaps the previous step.
-      auto fetch = [&](int v, float& lv, float& dv) {
+      auto fetch = [&](int gi, int v, float& lv, float& dv) {
         const int q = v * BM + r;
-        const bool ok = v < nv && r < BM && q < s.N;
-        lv = ok ? LSE[q] * kLog2e : 0.f;
-        dv = ok ? Dv[q] : 0.f;
+        const bool ok = gi < G && v < nv && r < BM && q < s.N;
+        const size_t row = (size_t)(bh0 + gi) * s.N + q;
+        lv = ok ? a.lse[row] * kLog2e : 0.f;
+        dv = ok ? a.dvec[row] : 0.f;
       };
       float next_l, next_d;
-      fetch(next_v(0), next_l, next_d);
-      for (int v = next_v(0); v < nv; v = next_v(v + 1), ++it) {
+      fetch(0, next_v(0), next_l, next_d);
+      for (int gi = 0, v = next_v(0); gi < G && v < nv; ++it) {
         const int q0 = v * BM;
         const int buf = it % NB;
         float* lrow = lse_row<D>(ctl, buf);
@@ -348,7 +358,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           drow[r] = next_d;
         }
         named_bar_sync(1, 128);
-        fetch(next_v(v + 1), next_l, next_d);
+        int gn = gi, vn = v;
+        advance(gn, vn);
+        fetch(gn, vn, next_l, next_d);
         mbar_wait(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);
         fence_after_sync();
         const bool need_mask = (s.causal && (q0 / 128) == kt) || (kt * 128 + 128 > L) || (q0 + BM > s.N);
@@ -406,12 +418,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_proxy_async_smem();
         fence_before_sync();
         mbar_arrive(b_pready(buf));
+        gi = gn;
+        v = vn;
       }
     } else {
       // ---------------------------------------------------------------- dQ into the accumulator
-      for (int v = next_v(0); v < nv; v = next_v(v + 1), ++it) {
+      for (int gi = 0, v = next_v(0); gi < G && v < nv; advance(gi, v), ++it) {
         const int q0 = v * BM;
         const int buf = it % NB;
+        float* dQa = a.dqacc + (size_t)(bh0 + gi) * s.N * D;
         mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
         fence_after_sync();
         const uint32_t tq = tmem + lane_off + tdQ(buf);
@@ -490,7 +505,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fence_proxy_async_smem();
     named_bar_sync(elementwise ? 1 : 2, 128);
     if (lane == 0 && (warp == 4 || warp == 8)) {
-      for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(elementwise ? &tmdK : &tmdV, stg + c * 16384, c * 64, kt * 128, bh);
+      for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(elementwise ? &tmdK : &tmdV, stg + c * 16384, c * 64, kt * 128, bkv);
       tma_store_commit();
       tma_store_wait0();
     }
@@ -511,18 +526,18 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid_ew = sms * 8;
-  const int BH = a.s.B * a.s.H;
+  const int BH = a.s.B * a.s.H, BHkv = a.s.B * a.s.Hkv;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH, C::BM) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BH) ||
-      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BH) || !fa_make_tmap_bf16(&tdo, a.dout, a.s.N, D, BH, C::BM) ||
-      !fa_make_tmap_bf16(&tdk, a.dk, a.s.N, D, BH) || !fa_make_tmap_bf16(&tdv, a.dv, a.s.N, D, BH))
+  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH, C::BM) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BHkv) ||
+      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BHkv) || !fa_make_tmap_bf16(&tdo, a.dout, a.s.N, D, BH, C::BM) ||
+      !fa_make_tmap_bf16(&tdk, a.dk, a.s.N, D, BHkv) || !fa_make_tmap_bf16(&tdv, a.dv, a.s.N, D, BHkv))
     return cudaErrorInvalidValue;
   bwd_pre_kernel<D><<<grid_ew, 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)a.s.nb * BH;
+  const long long grid = (long long)a.s.nb * BHkv;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   bwd_tc_kernel<D><<<(unsigned)grid, kBwdThreads, C::kSmem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
   e = cudaGetLastError();

@@ -18,6 +18,7 @@ constexpr int kTile = 128;  // mask granularity and tile size (query rows x keys
 
 struct AttnShape {
   int B, H, N, d;
+  int Hkv;     // K/V heads; query head h reads K/V head h / (H / Hkv) (grouped-query attention)
   int nb;      // ceil(N / 128)
   int causal;  // 0/1
   const uint8_t* block_mask;  // [nb * nb] or null

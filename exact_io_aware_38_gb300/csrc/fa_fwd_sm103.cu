@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = blockIdx.x % BH;
   const int pair = s.causal ? (npairs - 1 - pidx) : pidx;  // longest causal work first
   const int b = bh / s.H;
+  const int bkv = b * s.Hkv + (bh % s.H) / (s.H / s.Hkv);  // K/V head of this query head
   const int L = key_len(s, b);
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
   const bool has1 = qt1 < s.nb;
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
             mbar_expect_tx(b_full(slot), C::kTileBytes);
             for (int c = 0; c < C::kBoxes; ++c)
-              tma_load_3d(sKV + slot * C::kTileBytes + c * 16384, which ? &tmV : &tmK, c * 64, kt * 128, bh,
+              tma_load_3d(sKV + slot * C::kTileBytes + c * 16384, which ? &tmV : &tmK, c * 64, kt * 128, bkv,
                           b_full(slot));
             issued[slot] = true;
             last_par[slot] = ph;
@@ -392,10 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const int BH = a.s.B * a.s.H;
+  const int BH = a.s.B * a.s.H, BHkv = a.s.B * a.s.Hkv;
   CUtensorMap tq, tk, tv, to;
-  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BH) ||
-      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BH) || !fa_make_tmap_bf16(&to, a.o, a.s.N, D, BH))
+  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BHkv) ||
+      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BHkv) || !fa_make_tmap_bf16(&to, a.o, a.s.N, D, BH))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;

@@ -18,6 +18,8 @@ Workloads (shapes from the five benchmark configurations; seeds 1000 + index):
   c5  B1 H16 N16384 d64   128x128 block mask: band {(I, I), (I, I-1)} plus every other block
                           kept independently with probability 0.08 (u < 0.08, u uniform, drawn
                           over the whole grid in row-major order)
+Grouped-query variant (K and V drawn with Hkv heads, [B, Hkv, N, d]; seed 1006):
+  c4g B1 H32 Hkv8 N8192 d128 causal   (c4's shape with four query heads per K/V head)
 """
 
 from __future__ import annotations
@@ -43,7 +45,12 @@ class Workload:
     backward: bool = True
     qk_std: float = 1.0
     seed: int = 1000
+    Hkv: int | None = None  # K/V heads (grouped-query attention); None = H
     note: str = field(default="", compare=False)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.Hkv is None else self.Hkv
 
     @property
     def scale(self) -> float:
@@ -60,6 +67,8 @@ WORKLOADS = {
     "c3": Workload("c3", 8, 12, 1024, 64, causal=True, qk_std=3.0, seed=1003, note="GPT-2 shape, causal, Q/K std 3"),
     "c4": Workload("c4", 1, 32, 8192, 128, causal=True, seed=1004, note="long-context causal (headline)"),
     "c5": Workload("c5", 1, 16, 16384, 64, block_sparse=True, seed=1005, note="block-sparse, band + 8% random"),
+    "c4g": Workload("c4g", 1, 32, 8192, 128, causal=True, seed=1006, Hkv=8,
+                    note="long-context causal, grouped-query (8 K/V heads)"),
 }
 
 
@@ -78,22 +87,24 @@ def make_inputs(w: Workload, *, B: int | None = None, H: int | None = None, N: i
                 seed: int | None = None) -> dict:
     """Host (CPU) tensors for workload ``w``; B, H, N and seed may be overridden (smaller tests).
 
-    Returns dict with q, k, v, do (bf16 [B,H,N,d]), seqlens_k (int32 [B] or None),
-    block_mask (uint8 [nb, nb] or None), causal, scale.
+    Returns dict with q, do (bf16 [B,H,N,d]), k, v (bf16 [B,Hkv,N,d]), seqlens_k (int32 [B] or
+    None), block_mask (uint8 [nb, nb] or None), causal, scale. An H override keeps H / Hkv.
     """
+    G = w.H // w.kv_heads
     B = w.B if B is None else B
     H = w.H if H is None else H
     N = w.N if N is None else N
+    if H % G:
+        raise ValueError(f"H={H} is not a multiple of the workload's group size {G}")
     g = torch.Generator("cpu").manual_seed(w.seed if seed is None else seed)
-    shape = (B, H, N, w.d)
 
-    def draw(std):
-        return (torch.randn(shape, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+    def draw(std, heads):
+        return (torch.randn((B, heads, N, w.d), generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
 
-    q = draw(w.qk_std)
-    k = draw(w.qk_std)
-    v = draw(1.0)
-    do = draw(1.0)
+    q = draw(w.qk_std, H)
+    k = draw(w.qk_std, H // G)
+    v = draw(1.0, H // G)
+    do = draw(1.0, H)
     seqlens = None
     mask = None
     if w.key_padding:

@@ -102,6 +102,31 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
 /*
+ * Grouped-query attention (multi-query when Hkv = 1): "Flash Attention: IO-Aware Attention
+ * Computation", paragraph 16 (K/V heads shared by groups of query heads, to shrink the K/V cache).
+ * The page names the variant only; the reading adopted: H query heads and Hkv K/V heads with
+ * H % Hkv == 0 and G = H / Hkv; query head h (of sequence b) attends with K/V head h / G, i.e.
+ * exactly fa_fwd on K and V with each K/V head repeated G times along the head axis. The backward
+ * gradients dK, dV of a K/V head are the sums over its G query heads of what fa_bwd would give for
+ * the repeated tensors.
+ *   q, o, dout, dq  bf16 [B, H, N, d];  k, v, dk, dv  bf16 [B, Hkv, N, d];  lse fp32 [B, H, N]
+ *   tile_visits     [B * H * nb] (per query head); workspace as fa_bwd_workspace_bytes(B, H, N, d)
+ * Every other argument, the launches and the errors are as for fa_fwd / fa_bwd; Hkv outside
+ * [1, H] or not dividing H returns FA_ERR_INVALID_ARG. fa_fwd and fa_bwd are the Hkv = H case.
+ * The backward main pass runs one CTA per (key tile, K/V head); it loops over the group's query
+ * heads, so dK and dV stay exact sums in fp32 and are run-to-run identical.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int Hkv, int N, int d, int causal,
+               const uint8_t* block_mask, const int32_t* seqlens_k, float scale,
+               int32_t* tile_visits, int* dev_status, void* stream);
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+               const float* lse, void* dq, void* dk, void* dv,
+               int B, int H, int Hkv, int N, int d, int causal,
+               const uint8_t* block_mask, const int32_t* seqlens_k, float scale,
+               void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
+/*
  * Backward pass that allocates nothing, for callers that cannot allocate device memory (a plugin
  * or custom operator inside another framework receives only its input and output buffers; the
  * host framework owns the memory pool, and a cudaMalloc of its own would bypass that pool's

@@ -7,6 +7,7 @@ from .attention import (  # noqa: F401
     head_dq,
     head_forward,
     head_row_stats,
+    kv_head,
     tile_grid,
     valid_matrix,
 )

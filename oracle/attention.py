@@ -34,6 +34,12 @@ Readings where the pages are silent (all are the plainest reading):
     Block-sparse attention is exact for the masked problem (the abstract calls it approximate only
     relative to dense attention; the essay "Flash Attention: IO-Aware Attention Computation",
     paragraph 5, describes it as skipping zero or irrelevant blocks).
+  * grouped-query attention (the essay, paragraph 16, names multi-query and grouped-query
+    attention, K/V heads shared across query heads, and fixes nothing more): K and V may have
+    Hkv heads with Hkv dividing H; consecutive groups of G = H / Hkv query heads share one K/V
+    head (query head h reads K/V head h // G, see ``kv_head``). The forward pass is the definition
+    above with each K/V head repeated G times; dK and dV of a K/V head are, by the chain rule, the
+    sums of the per-query-head dK and dV over its group.
 
 Memory
 ------
@@ -228,37 +234,59 @@ def _map_heads(fn, B, H, workers):
         return list(ex.map(fn, heads))
 
 
+def kv_head(h, H, Hkv):
+    """K/V head that query head h reads when H query heads share Hkv K/V heads: consecutive groups
+    of G = H / Hkv query heads share one (grouped-query attention; Hkv = H is ordinary multi-head
+    attention, Hkv = 1 multi-query attention)."""
+    if Hkv < 1 or H % Hkv != 0:
+        raise ValueError(f"{Hkv} K/V heads cannot be shared evenly by {H} query heads")
+    return h // (H // Hkv)
+
+
 def attention_forward(q, k, v, scale, causal=False, block_mask=None, seqlens_k=None, workers=None):
-    """O [B,H,N,d] and LSE [B,H,N] in float64 for inputs laid out [B, H, N, d]."""
+    """O [B,H,N,d] and LSE [B,H,N] in float64; q is [B, H, N, d], k and v [B, Hkv, N, d]
+    (Hkv dividing H; Hkv = H for ordinary multi-head attention)."""
     q, k, v = _as64(q), _as64(k), _as64(v)
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     o = np.empty((B, H, N, v.shape[3]))
     lse = np.empty((B, H, N))
 
     def one(bh):
         b, h = bh
-        o[b, h], lse[b, h] = head_forward(q[b, h], k[b, h], v[b, h], scale, causal, block_mask, _key_len(seqlens_k, b))
+        hk = kv_head(h, H, Hkv)
+        o[b, h], lse[b, h] = head_forward(q[b, h], k[b, hk], v[b, hk], scale, causal, block_mask,
+                                          _key_len(seqlens_k, b))
 
     _map_heads(one, B, H, workers)
     return o, lse
 
 
 def attention_backward(q, k, v, do, scale, causal=False, block_mask=None, seqlens_k=None, workers=None):
-    """dQ, dK, dV [B,H,N,d] in float64 (the full gradient; N x N fp64 per head in memory)."""
+    """dQ [B,H,N,d] and dK, dV [B,Hkv,N,d] in float64 (the full gradient; N x N fp64 per head in
+    memory). With Hkv < H, dK and dV of a K/V head sum the contributions of its query heads."""
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     dq = np.empty_like(q)
-    dk = np.empty_like(k)
-    dv = np.empty_like(v)
+    dk_h = np.empty((B, H, N, k.shape[3]))  # per query head, summed over each group below
+    dv_h = np.empty((B, H, N, v.shape[3]))
 
     def one(bh):
         b, h = bh
         L = _key_len(seqlens_k, b)
-        args = (q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, block_mask, L)
+        hk = kv_head(h, H, Hkv)
+        args = (q[b, h], k[b, hk], v[b, hk], do[b, h], scale, causal, block_mask, L)
         dq[b, h] = head_dq(*args)
-        dk[b, h], dv[b, h] = head_dkdv(*args)
+        dk_h[b, h], dv_h[b, h] = head_dkdv(*args)
 
     _map_heads(one, B, H, workers)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            dk[b, kv_head(h, H, Hkv)] += dk_h[b, h]
+            dv[b, kv_head(h, H, Hkv)] += dv_h[b, h]
     return dq, dk, dv
 
 

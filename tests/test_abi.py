@@ -88,6 +88,30 @@ def test_bwd_validation(L, kw, rc):
     assert bwd_rc(**kw) == rc
 
 
+def gqa_fwd_rc(**kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=4, Hkv=2, N=128, d=64, causal=0, block_mask=None, seqlens_k=None,
+                scale=0.125, tile_visits=None, dev_status=None, stream=None)
+    args.update(kw)
+    return fa.fa_fwd_gqa(**args)
+
+
+def gqa_bwd_rc(**kw):
+    args = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, B=1, H=4, Hkv=2, N=128, d=64, causal=0,
+                block_mask=None, seqlens_k=None, scale=0.125, workspace=A, workspace_bytes=1 << 30, dev_status=None,
+                stream=None)
+    args.update(kw)
+    return fa.fa_bwd_gqa(**args)
+
+
+@pytest.mark.parametrize("kw,rc", [
+    (dict(Hkv=0), -1), (dict(Hkv=-2), -1), (dict(Hkv=3), -1), (dict(Hkv=8), -1), (dict(H=6, Hkv=4), -1),
+    (dict(k=None), -1), (dict(d=96), -2), (dict(v=A + 8), -3),
+])
+def test_gqa_validation(L, kw, rc):
+    assert gqa_fwd_rc(**kw) == rc
+    assert gqa_bwd_rc(**kw) == rc
+
+
 def test_binding_refuses_cpu_tensors(L):
     import torch
 

@@ -157,6 +157,29 @@ def test_repeatable():
     assert (a["dq"].float() - b["dq"].float()).abs().max() <= 1e-2
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (8, 1), (6, 3), (4, 4)])
+@pytest.mark.parametrize("N,kind", [(129, "dense"), (300, "causal"), (384, "causal+pad+block")])
+def test_gqa_parity(H, Hkv, N, kind, d):
+    """Grouped-query attention: K/V heads shared by H / Hkv query heads; dK, dV summed per group."""
+    inp = small_inputs(2, H, N, d, kind, seed=N * 7 + H * 3 + Hkv + d)
+    inp["k"] = inp["k"][:, :Hkv].contiguous()
+    inp["v"] = inp["v"][:, :Hkv].contiguous()
+    got = full_check(inp)
+    assert got["dk"].shape == inp["k"].shape and got["dv"].shape == inp["v"].shape
+
+
+def test_gqa_repeatable():
+    """dK and dV of shared heads are summed in one CTA's tensor memory: identical bits per run."""
+    inp = small_inputs(1, 8, 640, 128, "causal", 11)
+    inp["k"] = inp["k"][:, :2].contiguous()
+    inp["v"] = inp["v"][:, :2].contiguous()
+    a = run_gpu(inp)
+    b = run_gpu(inp)
+    for n in ("o", "lse", "dk", "dv"):
+        assert torch.equal(a[n], b[n]), n
+
+
 @pytest.mark.parametrize("name", ["c1", "c2", "c3"])
 def test_config_full(name):
     w = workloads.WORKLOADS[name]
@@ -164,24 +187,33 @@ def test_config_full(name):
 
 
 def sampled_check(inp, heads, n_rows, n_cols, seed):
-    """Full-size launch; the oracle evaluates sampled heads, rows and key columns one by one."""
+    """Full-size launch; the oracle evaluates sampled K/V heads (b, hk), and for each the query
+    heads that share it, on sampled rows and key columns one by one."""
     got = run_gpu(inp, backward=True, visits=True)
     B, H, N, d = inp["q"].shape
+    Hkv = inp["k"].shape[1]
     a = oracle_args(inp)
+    c = inp["scale"]
     rng = np.random.default_rng(seed)
-    for (b, h) in heads:
-        q, k, v, do = (f64(inp[n][b, h]) for n in ("q", "k", "v", "do"))
+    for (b, hk) in heads:
+        k, v = (f64(inp[n][b, hk]) for n in ("k", "v"))
         L = None if a["seqlens_k"] is None else int(a["seqlens_k"][b])
-        rows = np.sort(rng.choice(N, n_rows, replace=False))
         cols = np.sort(rng.choice(N, n_cols, replace=False))
-        om, lm = oracle.head_forward(q, k, v, inp["scale"], a["causal"], a["block_mask"], L, rows=rows)
-        check_o_lse(got["o"][b, h][rows], got["lse"][b, h][rows], om, lm)
-        stats = oracle.head_row_stats(q, k, v, do, inp["scale"], a["causal"], a["block_mask"], L)
-        dq = oracle.head_dq(q, k, v, do, inp["scale"], a["causal"], a["block_mask"], L, rows=rows)
-        dk, dv = oracle.head_dkdv(q, k, v, do, inp["scale"], a["causal"], a["block_mask"], L, cols=cols, stats=stats)
-        rel_fro(got["dq"][b, h][rows], dq)
-        rel_fro(got["dk"][b, h][cols], dk)
-        rel_fro(got["dv"][b, h][cols], dv)
+        dk = np.zeros((n_cols, d))
+        dv = np.zeros((n_cols, d))
+        for h in [h for h in range(H) if oracle.kv_head(h, H, Hkv) == hk]:
+            q, do = (f64(inp[n][b, h]) for n in ("q", "do"))
+            rows = np.sort(rng.choice(N, n_rows, replace=False))
+            om, lm = oracle.head_forward(q, k, v, c, a["causal"], a["block_mask"], L, rows=rows)
+            check_o_lse(got["o"][b, h][rows], got["lse"][b, h][rows], om, lm)
+            stats = oracle.head_row_stats(q, k, v, do, c, a["causal"], a["block_mask"], L)
+            dq = oracle.head_dq(q, k, v, do, c, a["causal"], a["block_mask"], L, rows=rows)
+            rel_fro(got["dq"][b, h][rows], dq)
+            dkh, dvh = oracle.head_dkdv(q, k, v, do, c, a["causal"], a["block_mask"], L, cols=cols, stats=stats)
+            dk += dkh
+            dv += dvh
+        rel_fro(got["dk"][b, hk][cols], dk)
+        rel_fro(got["dv"][b, hk][cols], dv)
     # Properties at full size, every head: finite outputs; sum_j dK_j = 0 (rows of dS sum to 0).
     for n in ("o", "dq", "dk", "dv"):
         assert torch.isfinite(got[n].float()).all(), n
@@ -194,6 +226,12 @@ def sampled_check(inp, heads, n_rows, n_cols, seed):
 def test_config_c4_sampled():
     inp = workloads.make_inputs(workloads.WORKLOADS["c4"])
     sampled_check(inp, heads=[(0, 0), (0, 31)], n_rows=384, n_cols=384, seed=4)
+
+
+def test_config_c4g_sampled():
+    """The long-context causal shape with 8 K/V heads, each shared by 4 query heads."""
+    inp = workloads.make_inputs(workloads.WORKLOADS["c4g"])
+    sampled_check(inp, heads=[(0, 0), (0, 7)], n_rows=256, n_cols=384, seed=6)
 
 
 def test_config_c5_sampled():

@@ -223,8 +223,75 @@ def pin_library_crosscheck():
             assert np.abs(a - b.grad.numpy()[0, 0]).max() <= 1e-11
 
 
+def pin_gqa_head_mapping():
+    """Grouped-query attention: with V of K/V head hk equal to the constant 10 b + hk, every valid
+    row of O of query head h equals 10 b + h // G (rows of P sum to 1), for G = H / Hkv."""
+    B, H, N, d = 2, 6, 9, 4
+    for Hkv in (1, 2, 3, 6):
+        q = RNG.standard_normal((B, H, N, d))
+        k = RNG.standard_normal((B, Hkv, N, d))
+        v = np.empty((B, Hkv, N, d))
+        for b in range(B):
+            for hk in range(Hkv):
+                v[b, hk] = 10 * b + hk
+        o, _ = oracle.attention_forward(q, k, v, 0.5, causal=True, workers=1)
+        G = H // Hkv
+        for b in range(B):
+            for h in range(H):
+                assert np.abs(o[b, h] - (10 * b + h // G)).max() <= 1e-12, (Hkv, b, h)
+
+
+def pin_gqa_finite_differences():
+    """Central differences of L = sum(dO * O) with K/V heads shared by two or four query heads:
+    each entry of a shared K or V moves the outputs of every query head of its group."""
+    B, H, N, d = 1, 4, 7, 3
+    h_step = 1e-6
+    for Hkv, causal, L in ((2, True, None), (1, False, 5)):
+        q, do = RNG.standard_normal((B, H, N, d)), RNG.standard_normal((B, H, N, d))
+        k, v = RNG.standard_normal((B, Hkv, N, d)), RNG.standard_normal((B, Hkv, N, d))
+        sl = None if L is None else np.array([L], dtype=np.int32)
+        kw = dict(causal=causal, seqlens_k=sl, workers=1)
+
+        def loss():
+            return float((oracle.attention_forward(q, k, v, 0.7, **kw)[0] * do).sum())
+
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.7, **kw)
+        assert dk.shape == k.shape and dv.shape == v.shape
+        for x, g in ((q, dq), (k, dk), (v, dv)):
+            flat = list(np.ndindex(x.shape))
+            for idx in [flat[t] for t in RNG.choice(len(flat), 16, replace=False)]:
+                x0 = x[idx]
+                x[idx] = x0 + h_step
+                lp = loss()
+                x[idx] = x0 - h_step
+                lm = loss()
+                x[idx] = x0
+                num = (lp - lm) / (2 * h_step)
+                assert abs(num - g[idx]) <= 1e-6 * max(1.0, abs(num)), (idx, num, g[idx])
+
+
+def pin_gqa_library_crosscheck():
+    """torch SDPA in float64 with its own grouped-query option (K/V heads expanded by
+    repeat_interleave), and autograd, against the oracle for G = 4."""
+    B, H, Hkv, N, d = 1, 8, 2, 140, 16
+    q, do = RNG.standard_normal((B, H, N, d)), RNG.standard_normal((B, H, N, d))
+    k, v = RNG.standard_normal((B, Hkv, N, d)), RNG.standard_normal((B, Hkv, N, d))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    G = H // Hkv
+    # torch's own expansion of shared K/V heads (the enable_gqa option applies the same rule)
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk.repeat_interleave(G, dim=1),
+                                                          tv.repeat_interleave(G, dim=1), is_causal=True, scale=0.25)
+    to.backward(torch.tensor(do))
+    o, _ = oracle.attention_forward(q, k, v, 0.25, causal=True, workers=1)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.25, causal=True, workers=1)
+    assert np.abs(o - to.detach().numpy()).max() <= 1e-12
+    for a, b in ((dq, tq), (dk, tk), (dv, tv)):
+        assert np.abs(a - b.grad.numpy()).max() <= 1e-11
+
+
 PINS = [pin_row_sums, pin_q_zero, pin_one_hot, pin_mask_equivalence, pin_n1, pin_finite_differences,
-        pin_grad_identities, pin_library_crosscheck]
+        pin_grad_identities, pin_library_crosscheck, pin_gqa_head_mapping, pin_gqa_finite_differences,
+        pin_gqa_library_crosscheck]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -304,7 +371,12 @@ def _mut_row_stats_no_D(q, k, v, do, scale, causal=False, block_mask=None, key_l
     return m_all, l_all, np.zeros(n)
 
 
+def _mut_kv_head_interleaved(h, H, Hkv):
+    return h % Hkv
+
+
 MUTANTS = [
+    ("kv_head", _mut_kv_head_interleaved),
     ("scores", _mut_scores_no_scale),
     ("valid_matrix", _mut_valid_reversed_causal),
     ("valid_matrix", _mut_valid_transposed_blocks),
