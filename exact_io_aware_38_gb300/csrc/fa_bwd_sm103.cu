@@ -169,8 +169,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // Query steps v (rows v*BM ..) are visited iff their 128-row tile is visited for this key tile.
   // The pattern is the same for every query head of the group; a step is a (group head gi, v)
   // pair, heads outer, so dK and dV sum over the group in tensor memory.
+  // No step is visited when the key tile lies past the key length; with the causal mask the first
+  // candidate is the key tile's own diagonal step. Scans start there.
+  const int v_lo = kt * 128 >= L ? nv : (s.causal ? (kt * 128) / BM : 0);
   auto next_v = [&](int v) -> int {
-    for (; v < nv; ++v)
+    for (v = v < v_lo ? v_lo : v; v < nv; ++v)
       if (tile_visited(s, (v * BM) / 128, kt, L)) return v;
     return nv;
   };
@@ -265,12 +268,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //           completion of all of step sn - NB's gradient MMAs, including dV's read of P^T);
     //   warp 2: dV, dK and dQ of step g, once P^T/dS^T of step g are in place (which follows the
     //           completion of step g's S^T/dP^T).
+    int n = 0;  // visited steps, counted by the whole warp
+    for (int v0 = v_lo; v0 < nv; v0 += 32) {
+      const int v = v0 + lane;
+      n += __popc(__ballot_sync(0xffffffffu, v < nv && tile_visited(s, (v * BM) / 128, kt, L)));
+    }
+    n *= G;
     if (lane == 0) {
       if (any_work) {
         mbar_wait(b_kv, 0, abort_flag, a.status);
-        int n = 0;
-        for (int v = next_v(0); v < nv; v = next_v(v + 1)) ++n;
-        n *= G;
         if (warp == 1) {
           for (int sn = 0; sn < n; ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
@@ -468,7 +474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
-      if (threadIdx.x == 256) tma_store_wait0();
+      if (threadIdx.x == 256) tma_store_wait_read0();  // the staging is read before the CTA exits
     }
 
     // ---------------------------------------------------------------- epilogue: dK (warps 4-7), dV (8-11)
@@ -507,7 +513,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && (warp == 4 || warp == 8)) {
       for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(elementwise ? &tmdK : &tmdV, stg + c * 16384, c * 64, kt * 128, bkv);
       tma_store_commit();
-      tma_store_wait0();
+      tma_store_wait_read0();
     }
   }
 

@@ -83,8 +83,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   auto vis = [&](int x, int kt) -> bool { return (x == 0 || has1) && tile_visited(s, x ? qt1 : qt0, kt, L); };
+  // Key tiles past the key length, or (causal) past the later query tile's diagonal, are never
+  // visited; scans stop there.
+  int kt_end = (L + 127) / 128;
+  if (s.causal) kt_end = min(kt_end, (has1 ? qt1 : qt0) + 1);
   auto next_union = [&](int kt) -> int {
-    for (; kt < s.nb; ++kt)
+    for (; kt < kt_end; ++kt)
       if (vis(0, kt) || vis(1, kt)) return kt;
     return s.nb;
   };
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 2 + 4 * x && lane == 0) {
         for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(&tmO, stg + c * 16384, c * 64, qt * 128, bh);
         tma_store_commit();
-        tma_store_wait0();
+        tma_store_wait_read0();  // the staging is read; the writes land before the grid completes
         if (a.tile_visits != nullptr) a.tile_visits[(size_t)bh * s.nb + qt] = cnt;
       }
     }
