@@ -9,7 +9,8 @@
 // the end. Scores never leave the chip. Tiles with no valid (query, key) pair are skipped whole.
 //
 // CTA layout (320 threads, one CTA per SM): two 128-row query tiles Q0, Q1 share every K/V tile.
-//   warp 0      TMA producer: Q0, Q1 once, then K_j, V_j through an NS-slot ring of 128-key tiles.
+//   warp 0      TMA producer: Q0, Q1 once, the first K tile alone, then one ring stage per visited
+//               key tile j: V_j and K_j+1 in one buffer (kStages buffers).
 //   warp 1      MMA issuer (one thread) and tensor-memory owner: S_x = Q_x K_j^T (both operands
 //               K-major in smem) and O_x += P_x V_j (P_x from tensor memory, V_j MN-major in smem).
 //   warps 2-5   softmax for Q0; warps 6-9 softmax for Q1. Thread t of a warpgroup owns one query
@@ -19,6 +20,11 @@
 // P_x is written as bf16 over the first 64 columns of S_x.
 // MMA issue order per key tile j: PV0(j), S0(j+1), PV1(j), S1(j+1), so the tensor core computes
 // one tile's products while the other tile's softmax runs.
+// The tensor core's instruction queue is shallow: the issuing thread runs nearly in step with the
+// pipe, and every barrier wait or commit it executes between MMA groups is time the pipe idles.
+// So the issuer waits twice per key tile: once on the stage barrier, which completes when the
+// stage's copies have landed AND tile 0's softmax has written P0 (the producer stands in with
+// 128 arrivals when tile 0 skips the key tile), and once on P1. It polls without suspending.
 // The partial output is rescaled only when a row max grows by more than 2^8 (lazy rescaling;
 // exact, since l and O always share the same reference max).
 #include <type_traits>
@@ -38,8 +44,8 @@ template <int D>
 struct FwdCfg {
   static constexpr int kBoxes = D / 64;                 // 64-column (128-byte) TMA boxes per row
   static constexpr int kTileBytes = 128 * D * 2;        // one 128-row bf16 tile
-  static constexpr int kSlots = D == 128 ? 4 : 8;       // K/V ring depth
-  static constexpr int kSmem = (2 + kSlots) * kTileBytes + 1024;
+  static constexpr int kStages = D == 128 ? 2 : 4;      // K/V ring: stage t holds V_t and K_t+1
+  static constexpr int kSmem = (2 + 2 * kStages) * kTileBytes + 1024;
   static constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
   static constexpr uint32_t kTmemS0 = 0, kTmemO0 = 256;
@@ -47,8 +53,9 @@ struct FwdCfg {
 
 struct FwdSmemCtl {
   uint64_t q_full;
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t k0_full;   // the first key tile (loaded alone, before any stage)
+  uint64_t full[4];   // stage landed and P of query tile 0 written (or stood in for)
+  uint64_t empty[4];
   uint64_t s_full[2];
   uint64_t p_ready[2];
   uint64_t o_done[2];
@@ -66,7 +73,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ FwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);                       // Q0, Q1 (later O staging)
-  const uint32_t sKV = sQ + 2 * C::kTileBytes;              // ring slots
+  const uint32_t sKV = sQ + 2 * C::kTileBytes;              // ring: stage buffer b = V then K
   volatile int* abort_flag = &ctl.abort_flag;
 
   const AttnShape& s = a.s;
@@ -93,8 +100,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return s.nb;
   };
 
-  const uint32_t b_q = smem_u32(&ctl.q_full);
+  const uint32_t b_q = smem_u32(&ctl.q_full), b_k0 = smem_u32(&ctl.k0_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
+  auto sV = [&](int b) { return sKV + (2 * b) * C::kTileBytes; };
+  auto sK = [&](int b) { return sKV + (2 * b + 1) * C::kTileBytes; };
   auto b_empty = [&](int i) { return smem_u32(&ctl.empty[i]); };
   const uint32_t b_sfull[2] = {smem_u32(&ctl.s_full[0]), smem_u32(&ctl.s_full[1])};
   const uint32_t b_pready[2] = {smem_u32(&ctl.p_ready[0]), smem_u32(&ctl.p_ready[1])};
@@ -103,8 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
     mbar_init(b_q, 1);
-    for (int i = 0; i < C::kSlots; ++i) {
-      mbar_init(b_full(i), 1);
+    mbar_init(b_k0, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(b_full(i), 1 + 128);  // the producer's arrival with the byte count, tile 0's softmax
       mbar_init(b_empty(i), 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -134,37 +144,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int x = 0; x < (has1 ? 2 : 1); ++x)
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_3d(sQ + x * C::kTileBytes + c * 16384, &tmQ, c * 64, (x ? qt1 : qt0) * 128, bh, b_q);
-      int slot = 0;
-      uint32_t ph = 0;
-      uint32_t last_par[8];
-      bool issued[8];
-      for (int i = 0; i < C::kSlots; ++i) issued[i] = false;
-      for (int kt = next_union(0); kt < s.nb; kt = next_union(kt + 1)) {
-        for (int which = 0; which < 2; ++which) {
-          // FA_TEST_WITHHOLD_KV (a test-only build) never loads K/V, so every consumer's bounded
-          // wait must run out and the kernel must return FA_ERR_DEVICE_TIMEOUT cleanly.
+      // Stage t (the t-th key tile u_t the pair visits) lands V_{u_t} and K_{u_t+1} in buffer
+      // t % kStages; the first key tile comes alone, into the K half of the last buffer. A buffer
+      // is reloaded once the MMAs of its previous stage have completed.
+      uint32_t last_par[4];
+      bool issued[4] = {false, false, false, false};
+      bool k0_issued = false;
+      int kt = next_union(0);
 #ifndef FA_TEST_WITHHOLD_KV
-          if (mbar_wait(b_empty(slot), ph ^ 1, abort_flag, a.status)) {
-#else
-          if (false) {
-#endif
-            mbar_expect_tx(b_full(slot), C::kTileBytes);
-            for (int c = 0; c < C::kBoxes; ++c)
-              tma_load_3d(sKV + slot * C::kTileBytes + c * 16384, which ? &tmV : &tmK, c * 64, kt * 128, bkv,
-                          b_full(slot));
-            issued[slot] = true;
-            last_par[slot] = ph;
-          }
-          if (++slot == C::kSlots) {
-            slot = 0;
-            ph ^= 1;
-          }
-        }
+      if (kt < s.nb) {
+        mbar_expect_tx(b_k0, C::kTileBytes);
+        for (int c = 0; c < C::kBoxes; ++c)
+          tma_load_3d(sK(C::kStages - 1) + c * 16384, &tmK, c * 64, kt * 128, bkv, b_k0);
+        k0_issued = true;
       }
-      if (*abort_flag) {  // let copies still in flight land before the CTA exits
+#endif
+      for (int t = 0; kt < s.nb; ++t) {
+        const int b = t % C::kStages;
+        const int ktn = next_union(kt + 1);
+        const int uses = t / C::kStages + (b == C::kStages - 1 ? 1 : 0);  // earlier users of buffer b
+        // FA_TEST_WITHHOLD_KV (a test-only build) never loads K/V, so every consumer's bounded
+        // wait must run out and the kernel must return FA_ERR_DEVICE_TIMEOUT cleanly.
+#ifndef FA_TEST_WITHHOLD_KV
+        if (uses == 0 || mbar_wait(b_empty(b), (uses - 1) & 1, abort_flag, a.status)) {
+#else
+        if (false) {
+#endif
+          mbar_expect_tx(b_full(b), (ktn < s.nb ? 2 : 1) * C::kTileBytes);
+          for (int c = 0; c < C::kBoxes; ++c)
+            tma_load_3d(sV(b) + c * 16384, &tmV, c * 64, kt * 128, bkv, b_full(b));
+          if (ktn < s.nb)
+            for (int c = 0; c < C::kBoxes; ++c)
+              tma_load_3d(sK(b) + c * 16384, &tmK, c * 64, ktn * 128, bkv, b_full(b));
+          if (!vis(0, kt)) mbar_arrive_cnt(b_full(b), 128);  // tile 0 has no P for this key tile
+          issued[b] = true;
+          last_par[b] = (t / C::kStages) & 1;
+        }
+        kt = ktn;
+      }
+      if (*abort_flag) {  // let copies still in flight land before the CTA exits (bounded)
         mbar_wait_drain(b_q, 0);
-        for (int i = 0; i < C::kSlots; ++i)
-          if (issued[i]) mbar_wait_drain(b_full(i), last_par[i]);
+        if (k0_issued) mbar_wait_drain(b_k0, 0);
+        // A stage barrier also counts tile 0's softmax arrivals, which an aborted CTA may never
+        // make; a copy lands within microseconds, so a short bound suffices.
+        for (int i = 0; i < C::kStages; ++i)
+          if (issued[i]) mbar_wait_drain(b_full(i), last_par[i], kDrainShortNs);
       }
     }
   } else if (warp == 1) {
@@ -173,22 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool first[2] = {true, true};
       bool any[2] = {false, false};
       uint32_t np[2] = {0, 0};
-      int slot = 0;
-      uint32_t ph = 0;
-      auto take = [&]() -> int {  // wait for the next ring slot to be full
-        const int sl = slot;
-        mbar_wait(b_full(sl), ph, abort_flag, a.status);
-        fence_after_sync();
-        if (++slot == C::kSlots) {
-          slot = 0;
-          ph ^= 1;
-        }
-        return sl;
-      };
       // No abort-flag reads on the issue path (see mbar_wait): after an abort the remaining MMAs
       // run on stale data and complete normally.
-      auto issue_s = [&](int x, int sk) {
-        const uint32_t qa = sQ + x * C::kTileBytes, ka = sKV + sk * C::kTileBytes;
+      auto issue_s = [&](int x, uint32_t ka) {
+        const uint32_t qa = sQ + x * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -197,8 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(b_sfull[x]);
       };
-      auto issue_pv = [&](int x, int sv) {
-        const uint32_t va = sKV + sv * C::kTileBytes;
+      auto issue_pv = [&](int x, uint32_t va) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + C::kTmemO0 + x * D, tmem + C::kTmemS0 + x * 128 + kk * 8,
@@ -206,36 +217,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         first[x] = false;
       };
 
-      mbar_wait(b_q, 0, abort_flag, a.status);
-      fence_after_sync();
+      // Per key tile two waits: the stage barrier (V_t and K_t+1 landed, P0 written) and P1.
+      mbar_wait_spin(b_q, 0, abort_flag, a.status);
       int kt = next_union(0);
       if (kt < s.nb) {
-        const int sk = take();
+        mbar_wait_spin(b_k0, 0, abort_flag, a.status);
+        fence_after_sync();
         for (int x = 0; x < 2; ++x)
           if (vis(x, kt)) {
-            issue_s(x, sk);
+            issue_s(x, sK(C::kStages - 1));
             any[x] = true;
           }
-        mma_commit(b_empty(sk));
-        while (true) {
-          const int sv = take();
+        mma_commit(b_empty(C::kStages - 1));
+        for (int t = 0;; ++t) {
+          const int b = t % C::kStages;
           const int ktn = next_union(kt + 1);
-          int skn = -1;
-          for (int x = 0; x < 2; ++x) {
-            if (vis(x, kt)) {
-              mbar_wait(b_pready[x], np[x] & 1, abort_flag, a.status);
-              ++np[x];
-              fence_after_sync();
-              issue_pv(x, sv);
-            }
-            if (ktn < s.nb && vis(x, ktn)) {
-              if (skn < 0) skn = take();
-              issue_s(x, skn);
-              any[x] = true;
-            }
+          mbar_wait_spin(b_full(b), (t / C::kStages) & 1, abort_flag, a.status);
+          fence_after_sync();
+          if (vis(0, kt)) issue_pv(0, sV(b));
+          if (ktn < s.nb && vis(0, ktn)) {
+            issue_s(0, sK(b));
+            any[0] = true;
           }
-          mma_commit(b_empty(sv));
-          if (skn >= 0) mma_commit(b_empty(skn));
+          if (vis(1, kt)) {
+            mbar_wait_spin(b_pready[1], np[1] & 1, abort_flag, a.status);
+            ++np[1];
+            fence_after_sync();
+            issue_pv(1, sV(b));
+          }
+          if (ktn < s.nb && vis(1, ktn)) {
+            issue_s(1, sK(b));
+            any[1] = true;
+          }
+          mma_commit(b_empty(b));
           if (ktn >= s.nb) break;
           kt = ktn;
         }
@@ -261,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cnt = 0;
     mbar_wait(b_q, 0, abort_flag, a.status);
     if (active) {
+      int t = -1;  // union index of the key tile (tile 0 reports P on stage t's barrier)
       for (int kt = next_union(0); kt < s.nb; kt = next_union(kt + 1)) {
+        ++t;
         if (!vis(x, kt)) continue;
         mbar_wait(b_sfull[x], cnt & 1, abort_flag, a.status);
         fence_after_sync();
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         l += sum;
         fence_before_sync();
-        mbar_arrive(b_pready[x]);
+        mbar_arrive(x == 0 ? b_full(t % C::kStages) : b_pready[1]);
         ++cnt;
       }
       // ---------------------------------------------------------------- epilogue

@@ -42,6 +42,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.p
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar) : "memory");
 }
+// count arrivals at once (one thread standing in for several).
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0], %1; }" ::"r"(bar), "r"(count) : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar), "r"(bytes)
                : "memory");
@@ -89,12 +93,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same bounded wait, polling without suspending: for the threads that issue tensor-core
+// work, where the wake-up latency of a suspended wait would leave the pipe idle. The abort flag
+// and the clock are read only every 256 polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int* status) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitNs) {
+        *abort_flag = 1;
+        report_status(status, FA_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // A wait used only while draining on the abort path: bounded, ignores the abort flag.
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+constexpr uint64_t kDrainShortNs = 1000000ull;  // 1 ms: ample for copies already in flight
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
   const uint64_t t0 = globaltimer();
   for (;;) {
     if (mbar_try(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 
