@@ -276,13 +276,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     n *= G;
     if (lane == 0) {
       if (any_work) {
-        mbar_wait(b_kv, 0, abort_flag, a.status);
+        mbar_wait_spin(b_kv, 0, abort_flag, a.status);
         if (warp == 1) {
           for (int sn = 0; sn < n; ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
-            mbar_wait(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
+            mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
             if (sn >= NB) {
-              mbar_wait(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+              mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
             }
             const uint32_t q_s = sQs(st), do_s = sdOs(st);
@@ -301,8 +301,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         } else {
           for (int g = 0; g < n; ++g) {
             const int st = g % C::kStages, buf = g % NB;
-            mbar_wait(b_pready(buf), (g / NB) & 1, abort_flag, a.status);
-            if (D == 64 && g > 0) mbar_wait(b_dqfree(0), (g - 1) & 1, abort_flag, a.status);  // dQ columns read out
+            mbar_wait_spin(b_pready(buf), (g / NB) & 1, abort_flag, a.status);
+            if (D == 64 && g > 0) mbar_wait_spin(b_dqfree(0), (g - 1) & 1, abort_flag, a.status);  // dQ columns read out
             fence_after_sync();
             const uint32_t q_s = sQs(st), do_s = sdOs(st);
 #pragma unroll
@@ -343,12 +343,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int key = kt * 128 + r;
       const bool key_ok = key < L;
       const float sl2 = a.scale * kLog2e;
-      // LSE and D of a step are loaded one step ahead, so their latency overlaps the previous step.
+      // LSE and D of a step are loaded one step ahead and consumed only when they are stored for
+      // the next step, so the load latency overlaps a whole step.
       auto fetch = [&](int gi, int v, float& lv, float& dv) {
         const int q = v * BM + r;
         const bool ok = gi < G && v < nv && r < BM && q < s.N;
         const size_t row = (size_t)(bh0 + gi) * s.N + q;
-        lv = ok ? a.lse[row] * kLog2e : 0.f;
+        lv = ok ? a.lse[row] : 0.f;
         dv = ok ? a.dvec[row] : 0.f;
       };
       float next_l, next_d;
@@ -358,16 +359,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int buf = it % NB;
         float* lrow = lse_row<D>(ctl, buf);
         float* drow = dvec_row<D>(ctl, buf);
-        named_bar_sync(1, 128);  // every thread is done with this buffer's previous LSE and D
+        // With two row buffers, every thread finished reading this one (step it - 2) before the
+        // barrier of step it - 1; with one, a barrier must separate the last reads from the writes.
+        if (NB == 1) named_bar_sync(1, 128);
         if (r < BM) {
-          lrow[r] = next_l;
+          lrow[r] = next_l * kLog2e;
           drow[r] = next_d;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 128);  // the rows are written before anyone reads them
         int gn = gi, vn = v;
         advance(gn, vn);
         fetch(gn, vn, next_l, next_d);
-        mbar_wait(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);
+        mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // on the critical path
         fence_after_sync();
         const bool need_mask = (s.causal && (q0 / 128) == kt) || (kt * 128 + 128 > L) || (q0 + BM > s.N);
         const uint32_t ts = tmem + lane_off + tS(buf), tdp = tmem + lane_off + tdP(buf);
