@@ -123,18 +123,28 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def sources_sha256(paths):
+    """sha256 prefix over the named source files (relative to the repo root), in order."""
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(p.encode())
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(name, workload_name, heads_override):
     """DRAM bytes per launch of `name` from the committed ncu record, or None when the record is
-    for another workload or the kernel source has changed since the counters were taken."""
+    for another workload or any source the kernel is built from has changed since the counters
+    were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path))[name]
-        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
-    except (OSError, KeyError, ValueError):
+        digest = sources_sha256(rec["sources"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
     if heads_override is not None or not rec["workload"].startswith(workload_name + ":"):
         return None
-    if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_prefix"]:
+    if digest != rec["sources_sha256_prefix"]:
         return None
     return rec["dram_bytes_per_launch"]
 

@@ -73,7 +73,7 @@ struct alignas(16) BwdSmemCtl {
   uint64_t kv_full;
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t s_full[kMaxBufs], p_ready[kMaxBufs], dq_full[kMaxBufs], dq_free[kMaxBufs];
+  uint64_t s_full[kMaxBufs], p_ready[kMaxBufs], dq_full[kMaxBufs], dq_free[kMaxBufs], s_free[kMaxBufs];
   uint64_t done, drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -189,7 +189,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto sDs = [&](int buf) { return sDs0 + buf * C::kDsBytes; };
   auto tS = [&](int buf) { return C::kTS0 + buf * 2 * BM; };
   auto tdP = [&](int buf) { return C::kTS0 + buf * 2 * BM + BM; };
-  auto tdQ = [&](int buf) { return D == 128 ? tS(buf) : C::kTdQ64; };
+  // d = 128: dQ^T of a step accumulates over its buffer's dP^T columns (free once dK has read
+  // dS^T there), so the next S^T into the buffer waits only for dV's read of P^T.
+  auto tdQ = [&](int buf) { return D == 128 ? tdP(buf) : C::kTdQ64; };
 
   const uint32_t b_kv = smem_u32(&ctl.kv_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto b_pready = [&](int i) { return smem_u32(&ctl.p_ready[i]); };
   auto b_dqfull = [&](int i) { return smem_u32(&ctl.dq_full[i]); };
   auto b_dqfree = [&](int i) { return smem_u32(&ctl.dq_free[i]); };
+  auto b_sfree = [&](int i) { return smem_u32(&ctl.s_free[i]); };
   const uint32_t b_done = smem_u32(&ctl.done), b_drain = smem_u32(&ctl.drain);
 
   if (threadIdx.x == 0) {
@@ -212,6 +215,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_pready(i), 128);
       mbar_init(b_dqfull(i), 1);
       mbar_init(b_dqfree(i), 128);
+      mbar_init(b_sfree(i), 1);
     }
     mbar_init(b_done, 1);
     mbar_init(b_drain, 2);  // one commit per MMA issuer
@@ -263,9 +267,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------------ MMA issuers
     // Two issuing threads, one per dependency chain: a thread issuing tcgen05 MMAs blocks while
     // the tensor core's queue is full, so one issuer could not react to the other chain.
-    //   warp 1: S^T/dP^T of step sn into buffer sn % NB, once its Q/dO tile has landed and (d = 128)
-    //           the buffer's dQ^T of step sn - NB has been read out (that read-out follows the
-    //           completion of all of step sn - NB's gradient MMAs, including dV's read of P^T);
+    //   warp 1: S^T/dP^T of step sn into buffer sn % NB, once its Q/dO tile has landed. d = 128:
+    //           S^T once dV of step sn - NB has read P^T (the s_free commit), dP^T once that
+    //           step's dQ^T, accumulated over the dP^T columns after dK read dS^T there, has been
+    //           read out. d = 64 (one buffer, dQ in its own columns): both once every MMA of step
+    //           sn - 1 has completed and dQ is read out;
     //   warp 2: dV, dK and dQ of step g, once P^T/dS^T of step g are in place (which follows the
     //           completion of step g's S^T/dP^T).
     int n = 0;  // visited steps, counted by the whole warp
@@ -282,7 +288,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int st = sn % C::kStages, buf = sn % NB;
             mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
             if (sn >= NB) {
-              mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+              if constexpr (D == 128)  // dV of step sn - NB has read P^T from these columns
+                mbar_wait_spin(b_sfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+              else  // (one buffer) every MMA of step sn - 1 has completed and dQ is read out
+                mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
             }
             const uint32_t q_s = sQs(st), do_s = sdOs(st);
@@ -290,6 +299,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
               mma_ss(tmem + tS(buf), desc_kmajor_sw128(sK + okk), desc_kmajor_sw128(q_s + oq), C::kIdS, kk > 0);
+            }
+            if (D == 128 && sn >= NB) {  // dQ^T of step sn - NB has been read out of these columns
+              mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+              fence_after_sync();
             }
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -309,6 +322,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int kk = 0; kk < BM / 16; ++kk)
               mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_mnmajor_sw128(do_s + kk * 2048, C::kQBox), C::kIdG,
                      (g > 0 || kk > 0) ? 1u : 0u);
+            if (D == 128) mma_commit(b_sfree(buf));  // P^T read: the S^T columns are free
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
               mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_mnmajor_sw128(q_s + kk * 2048, C::kQBox), C::kIdG,
