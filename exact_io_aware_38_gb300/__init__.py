@@ -5,9 +5,12 @@ library's CUDA kernels. PyTorch provides device memory and the current stream. T
 fallback: if the library is missing, every call raises.
 
 Raw C-ABI names (same signatures as ``include/fa.h``, pointers as ints):
-    fa_fwd, fa_bwd, fa_fwd_gqa, fa_bwd_gqa, fa_bwd_workspace_bytes, fa_status_string, fa_bwd_noalloc
+    fa_fwd, fa_bwd, fa_fwd_gqa, fa_bwd_gqa, fa_bwd_workspace_bytes, fa_status_string, fa_bwd_noalloc,
+    fa_fwd_varlen, fa_bwd_varlen, fa_bwd_varlen_workspace_bytes (with the Strides / VarlenProblem structs)
 Tensor helpers (grouped-query attention when k, v have fewer heads than q):
     fwd(q, k, v, ...) -> (o, lse);  bwd(q, k, v, o, lse, do, ...) -> (dq, dk, dv)
+    fwd_varlen(q, k, v, ...), bwd_varlen(...): [B, N, H, d] views with any strides, or packed
+    [rows, H, d] sequences located by cu_seqlens; query and key lengths may differ.
 """
 
 from __future__ import annotations
@@ -24,6 +27,23 @@ _lib = None
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
+
+
+class Strides(ctypes.Structure):
+    """fa_strides: element strides of a [batch][row][head][d] view."""
+    _fields_ = [("row", ctypes.c_int64), ("head", ctypes.c_int64), ("batch", ctypes.c_int64)]
+
+
+class VarlenProblem(ctypes.Structure):
+    """fa_varlen_problem (include/fa.h)."""
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("Hkv", ctypes.c_int), ("d", ctypes.c_int),
+                ("seqlen_q", ctypes.c_int), ("seqlen_k", ctypes.c_int),
+                ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+                ("rows_q", ctypes.c_int), ("rows_k", ctypes.c_int), ("causal", ctypes.c_int),
+                ("scale", ctypes.c_float)]
+
+
+_VP = ctypes.POINTER(VarlenProblem)
 _SIGS = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
@@ -32,6 +52,10 @@ _SIGS = {
     "fa_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "fa_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P,
                         ctypes.c_size_t, _P, _P]),
+    "fa_fwd_varlen": (_I, [_VP, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, _P]),
+    "fa_bwd_varlen_workspace_bytes": (ctypes.c_size_t, [_VP]),
+    "fa_bwd_varlen": (_I, [_VP, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, Strides,
+                           _P, Strides, _P, Strides, _P, ctypes.c_size_t, _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P]),
 }
@@ -93,6 +117,20 @@ def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block
                workspace_bytes, dev_status, stream) -> int:
     return int(lib().fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k,
                                 scale, workspace, workspace_bytes, dev_status, stream))
+
+
+def fa_fwd_varlen(p, q, sq, k, sk, v, sv, o, so, lse, dev_status, stream) -> int:
+    return int(lib().fa_fwd_varlen(ctypes.byref(p), q, sq, k, sk, v, sv, o, so, lse, dev_status, stream))
+
+
+def fa_bwd_varlen_workspace_bytes(p) -> int:
+    return int(lib().fa_bwd_varlen_workspace_bytes(ctypes.byref(p)))
+
+
+def fa_bwd_varlen(p, q, sq, k, sk, v, sv, o, so, dout, sdo, lse, dq, sdq, dk, sdk, dv, sdv, workspace,
+                  workspace_bytes, dev_status, stream) -> int:
+    return int(lib().fa_bwd_varlen(ctypes.byref(p), q, sq, k, sk, v, sv, o, so, dout, sdo, lse, dq, sdq, dk, sdk, dv,
+                                   sdv, workspace, workspace_bytes, dev_status, stream))
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, seqlens_k, scale, dev_status,
@@ -187,6 +225,86 @@ def bwd(q, k, v, o, lse, do, *, causal=False, block_mask=None, seqlens_k=None, s
                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, d, int(causal), _ptr(block_mask),
                     _ptr(seqlens_k), scale, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                     _ptr(status), _stream(stream))
+    if rc != 0:
+        raise FaError(rc)
+    return dq, dk, dv
+
+
+# ----------------------------------------------------------------------------- varlen / strided
+
+
+def _view(t, packed):
+    """Strides of a [B, N, H, d] view (or a packed [rows, H, d] tensor) as fa_strides."""
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.stride(-1) == 1):
+        raise ValueError("tensors must be bf16 CUDA tensors with a contiguous last (head) dimension")
+    if packed:
+        if t.dim() != 3:
+            raise ValueError("packed tensors are [rows, heads, d]")
+        return Strides(t.stride(0), t.stride(1), 0)
+    if t.dim() != 4:
+        raise ValueError("fixed-length tensors are [B, N, H, d] views")
+    return Strides(t.stride(1), t.stride(2), t.stride(0))
+
+
+def _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale):
+    packed = cu_seqlens_q is not None
+    if packed != (cu_seqlens_k is not None):
+        raise ValueError("give both cu_seqlens_q and cu_seqlens_k, or neither")
+    d = q.shape[-1]
+    H, Hkv = q.shape[-2], k.shape[-2]
+    if packed:
+        for cu in (cu_seqlens_q, cu_seqlens_k):
+            if not (cu.dtype == torch.int32 and cu.is_contiguous() and cu.device == q.device and cu.dim() == 1):
+                raise ValueError("cu_seqlens must be contiguous int32 [B + 1] tensors on the tensors' device")
+        if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 >= 2 entries")
+        if max_seqlen_q is None or max_seqlen_k is None:
+            raise ValueError("packed batches need max_seqlen_q and max_seqlen_k")
+        B, Nq, Nk = cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k)
+        rows_q, rows_k = q.shape[0], k.shape[0]
+    else:
+        B, Nq, Nk = q.shape[0], q.shape[1], k.shape[1]
+        rows_q = rows_k = 0
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    p = VarlenProblem(B, H, Hkv, d, Nq, Nk, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), rows_q, rows_k, int(causal),
+                      scale)
+    return p, packed
+
+
+def _lse_shape(q, p, packed):
+    return (p.H, q.shape[0]) if packed else (p.B, p.H, p.seqlen_q)
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, *,
+               causal=False, scale=None, out=None, lse=None, status=None, stream=None):
+    """O, LSE for a fixed-length batch of [B, N, H, d] views (any strides; N_q may differ from
+    N_k) or a packed batch ([rows, H, d] tensors with cu_seqlens). Causal is aligned to the
+    bottom-right corner. LSE is [B, H, N_q] (fixed) or [H, rows_q] (packed)."""
+    p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty(_lse_shape(q, p, packed), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = fa_fwd_varlen(p, q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed), v.data_ptr(),
+                       _view(v, packed), o.data_ptr(), _view(o, packed), lse.data_ptr(), _ptr(status), _stream(stream))
+    if rc != 0:
+        raise FaError(rc)
+    return o, lse
+
+
+def bwd_varlen(q, k, v, o, lse, do, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, *,
+               causal=False, scale=None, dq=None, dk=None, dv=None, workspace=None, status=None, stream=None):
+    """dQ, dK, dV for the batch layouts of fwd_varlen (outputs shaped like q, k, v)."""
+    p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = fa_bwd_varlen_workspace_bytes(p)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    rc = fa_bwd_varlen(p, q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed), v.data_ptr(),
+                       _view(v, packed), o.data_ptr(), _view(o, packed), do.data_ptr(), _view(do, packed),
+                       lse.data_ptr(), dq.data_ptr(), _view(dq, packed), dk.data_ptr(), _view(dk, packed),
+                       dv.data_ptr(), _view(dv, packed), workspace.data_ptr(),
+                       workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
     if rc != 0:
         raise FaError(rc)
     return dq, dk, dv

@@ -11,31 +11,171 @@ inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int check_shape(int B, int H, int N, int d, int causal, float scale) {
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+// Tensors are limited to 2^31 elements (int element offsets inside the kernels' tile math).
+constexpr double kMaxElems = 2147483648.0;
+
+int check_common(int B, int H, int Hkv, int d, int causal, float scale) {
+  if (B < 1 || H < 1) return FA_ERR_INVALID_ARG;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  const double elems = (double)B * H * N * d;
-  if (elems >= 2147483648.0) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
-// K/V heads: each must serve the same number of query heads.
-inline bool check_kv_heads(int H, int Hkv) { return Hkv >= 1 && Hkv <= H && H % Hkv == 0; }
+int check_shape(int B, int H, int N, int d, int causal, float scale) {
+  if (N < 1) return FA_ERR_INVALID_ARG;
+  const int rc = check_common(B, H, H, d, causal, scale);
+  if (rc != FA_OK) return rc;
+  if ((double)B * H * N * d >= kMaxElems) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
 
-fa::AttnShape make_shape(int B, int H, int Hkv, int N, int d, int causal, const uint8_t* bm, const int32_t* sl) {
-  fa::AttnShape s;
+FaStrides contiguous(int heads, int N, int d) {
+  FaStrides t;
+  t.row = d;
+  t.head = (long long)N * d;
+  t.batch = (long long)heads * N * d;
+  return t;
+}
+
+fa::AttnShape fixed_shape(int B, int H, int Hkv, int N, int d, int causal, const uint8_t* bm, const int32_t* sl) {
+  fa::AttnShape s{};
   s.B = B;
   s.H = H;
   s.Hkv = Hkv;
-  s.N = N;
   s.d = d;
-  s.nb = (N + fa::kTile - 1) / fa::kTile;
+  s.Nq = s.Nk = N;
+  s.nbq = s.nbk = (N + fa::kTile - 1) / fa::kTile;
   s.causal = causal;
   s.block_mask = bm;
   s.seqlens_k = sl;
   return s;
+}
+
+// Varlen problem -> shape; FA_OK or an error code.
+int varlen_shape(const fa_varlen_problem* p, fa::AttnShape* out) {
+  if (p == nullptr) return FA_ERR_INVALID_ARG;
+  const int rc = check_common(p->B, p->H, p->Hkv, p->d, p->causal, p->scale);
+  if (rc != FA_OK) return rc;
+  if (p->seqlen_q < 1 || p->seqlen_k < 1) return FA_ERR_INVALID_ARG;
+  const bool packed = p->cu_seqlens_q != nullptr;
+  if (packed != (p->cu_seqlens_k != nullptr)) return FA_ERR_INVALID_ARG;
+  if (packed && (p->rows_q < 1 || p->rows_k < 1)) return FA_ERR_INVALID_ARG;
+  if (!aligned(p->cu_seqlens_q, 4) || !aligned(p->cu_seqlens_k, 4)) return FA_ERR_MISALIGNED;
+  fa::AttnShape s{};
+  s.B = p->B;
+  s.H = p->H;
+  s.Hkv = p->Hkv;
+  s.d = p->d;
+  s.Nq = p->seqlen_q;
+  s.Nk = p->seqlen_k;
+  s.nbq = (s.Nq + fa::kTile - 1) / fa::kTile;
+  s.nbk = (s.Nk + fa::kTile - 1) / fa::kTile;
+  s.causal = p->causal;
+  s.cu_q = p->cu_seqlens_q;
+  s.cu_k = p->cu_seqlens_k;
+  s.rows_q = packed ? p->rows_q : 0;
+  s.rows_k = packed ? p->rows_k : 0;
+  const double rq = packed ? (double)p->rows_q : (double)p->B * p->seqlen_q;
+  const double rk = packed ? (double)p->rows_k : (double)p->B * p->seqlen_k;
+  if (rq * p->H * p->d >= kMaxElems || rk * p->Hkv * p->d >= kMaxElems) return FA_ERR_UNSUPPORTED;
+  *out = s;
+  return FA_OK;
+}
+
+// Strides of a caller tensor: positive multiples of 8 elements (16 bytes, the TMA rule); the
+// batch stride is unused (and replaced by a valid one) for packed batches and single sequences.
+int take_strides(const fa_strides& in, bool packed, int B, int rows, int heads, FaStrides* out) {
+  if (in.row <= 0 || in.head <= 0 || in.row % 8 || in.head % 8) return FA_ERR_INVALID_ARG;
+  FaStrides t;
+  t.row = in.row;
+  t.head = in.head;
+  t.batch = in.batch;
+  if (packed || B == 1) {
+    const long long span = (long long)in.row * rows + (long long)in.head * heads;
+    t.batch = (span + 7) / 8 * 8;
+  } else if (in.batch <= 0 || in.batch % 8) {
+    return FA_ERR_INVALID_ARG;
+  }
+  *out = t;
+  return FA_OK;
+}
+
+size_t per_row(const fa::AttnShape& s) { return s.cu_q != nullptr ? (size_t)s.H * s.rows_q : (size_t)s.B * s.H * s.Nq; }
+
+size_t workspace_for(const fa::AttnShape& s) {
+  const size_t rows = per_row(s);
+  return round_up(rows * sizeof(float)) + round_up(rows * s.d * sizeof(float));
+}
+
+int launch_fwd(const fa::AttnShape& s, const void* q, FaStrides sq, const void* k, FaStrides sk, const void* v,
+               FaStrides sv, void* o, FaStrides so, float* lse, float scale, int32_t* tile_visits, int* dev_status,
+               void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(tile_visits, 4) || !aligned(dev_status, 4))
+    return FA_ERR_MISALIGNED;
+  FaFwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  a.so = so;
+  a.s = s;
+  a.scale = scale;
+  a.tile_visits = tile_visits;
+  a.status = dev_status;
+  const cudaError_t e = fa_launch_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+struct BwdTensors {
+  const void *q, *k, *v, *o, *dout;
+  const float* lse;
+  void *dq, *dk, *dv;
+  FaStrides sq, sk, sv, so, sdo, sdq, sdk, sdv;
+};
+
+int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* workspace, size_t workspace_bytes,
+               int* dev_status, void* stream) {
+  if (!t.q || !t.k || !t.v || !t.o || !t.dout || !t.lse || !t.dq || !t.dk || !t.dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < workspace_for(s)) return FA_ERR_INVALID_ARG;
+  if (!aligned(t.q, 16) || !aligned(t.k, 16) || !aligned(t.v, 16) || !aligned(t.o, 16) || !aligned(t.dout, 16) ||
+      !aligned(t.dq, 16) || !aligned(t.dk, 16) || !aligned(t.dv, 16) || !aligned(t.lse, 4) ||
+      !aligned(workspace, kAlign) || !aligned(dev_status, 4))
+    return FA_ERR_MISALIGNED;
+  FaBwdArgs a;
+  a.q = t.q;
+  a.k = t.k;
+  a.v = t.v;
+  a.o = t.o;
+  a.dout = t.dout;
+  a.lse = t.lse;
+  a.dq = t.dq;
+  a.dk = t.dk;
+  a.dv = t.dv;
+  a.sq = t.sq;
+  a.sk = t.sk;
+  a.sv = t.sv;
+  a.so = t.so;
+  a.sdo = t.sdo;
+  a.sdq = t.sdq;
+  a.sdk = t.sdk;
+  a.sdv = t.sdv;
+  const size_t rows = per_row(s);
+  a.dvec = static_cast<float*>(workspace);
+  a.dqacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * sizeof(float)));
+  a.s = s;
+  a.scale = scale;
+  a.status = dev_status;
+  const cudaError_t e = fa_launch_bwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
@@ -45,7 +185,7 @@ extern "C" {
 const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
-    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument (null pointer, size, flag or scale)";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument (null pointer, size, flag, stride or scale)";
     case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dimension or tensor size";
     case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: tensor pointer not 16-byte aligned";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call or kernel launch failed";
@@ -62,22 +202,11 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   const int rc = check_shape(B, H, N, d, causal, scale);
   if (rc != FA_OK) return rc;
-  if (!check_kv_heads(H, Hkv)) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
-      !aligned(seqlens_k, 4) || !aligned(tile_visits, 4) || !aligned(dev_status, 4))
-    return FA_ERR_MISALIGNED;
-  FaFwdArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.o = o;
-  a.lse = lse;
-  a.s = make_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
-  a.scale = scale;
-  a.tile_visits = tile_visits;
-  a.status = dev_status;
-  const cudaError_t e = fa_launch_fwd(a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!aligned(seqlens_k, 4)) return FA_ERR_MISALIGNED;
+  const fa::AttnShape s = fixed_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
+  return launch_fwd(s, q, contiguous(H, N, d), k, contiguous(Hkv, N, d), v, contiguous(Hkv, N, d), o,
+                    contiguous(H, N, d), lse, scale, tile_visits, dev_status, stream);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
@@ -89,8 +218,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d, 0, 1.f) != FA_OK) return 0;
-  const size_t rows = (size_t)B * H * N;
-  return round_up(rows * sizeof(float)) + round_up(rows * d * sizeof(float));
+  return workspace_for(fixed_shape(B, H, H, N, d, 0, nullptr, nullptr));
 }
 
 int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -100,31 +228,22 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
   const int rc = check_shape(B, H, N, d, causal, scale);
   if (rc != FA_OK) return rc;
-  if (!check_kv_heads(H, Hkv)) return FA_ERR_INVALID_ARG;
-  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
-  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
-      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, kAlign) ||
-      !aligned(seqlens_k, 4) || !aligned(dev_status, 4))
-    return FA_ERR_MISALIGNED;
-  const size_t rows = (size_t)B * H * N;
-  FaBwdArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.o = o;
-  a.dout = dout;
-  a.lse = lse;
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
-  a.dvec = static_cast<float*>(workspace);
-  a.dqacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * sizeof(float)));
-  a.s = make_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
-  a.scale = scale;
-  a.status = dev_status;
-  const cudaError_t e = fa_launch_bwd(a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!aligned(seqlens_k, 4)) return FA_ERR_MISALIGNED;
+  const fa::AttnShape s = fixed_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
+  BwdTensors t;
+  t.q = q;
+  t.k = k;
+  t.v = v;
+  t.o = o;
+  t.dout = dout;
+  t.lse = lse;
+  t.dq = dq;
+  t.dk = dk;
+  t.dv = dv;
+  t.sq = t.so = t.sdo = t.sdq = contiguous(H, N, d);
+  t.sk = t.sv = t.sdk = t.sdv = contiguous(Hkv, N, d);
+  return launch_bwd(s, t, scale, workspace, workspace_bytes, dev_status, stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
@@ -133,6 +252,59 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* stream) {
   return fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, N, d, causal, block_mask, seqlens_k, scale, workspace,
                     workspace_bytes, dev_status, stream);
+}
+
+int fa_fwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                  const void* v, fa_strides sv, void* o, fa_strides so, float* lse, int* dev_status, void* stream) {
+  fa::AttnShape s;
+  int rc = varlen_shape(p, &s);
+  if (rc != FA_OK) return rc;
+  const bool packed = s.cu_q != nullptr;
+  const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk;
+  FaStrides tq, tk, tv, to;
+  if ((rc = take_strides(sq, packed, s.B, rq, s.H, &tq)) != FA_OK ||
+      (rc = take_strides(sk, packed, s.B, rk, s.Hkv, &tk)) != FA_OK ||
+      (rc = take_strides(sv, packed, s.B, rk, s.Hkv, &tv)) != FA_OK ||
+      (rc = take_strides(so, packed, s.B, rq, s.H, &to)) != FA_OK)
+    return rc;
+  return launch_fwd(s, q, tq, k, tk, v, tv, o, to, lse, p->scale, nullptr, dev_status, stream);
+}
+
+size_t fa_bwd_varlen_workspace_bytes(const fa_varlen_problem* p) {
+  fa::AttnShape s;
+  if (varlen_shape(p, &s) != FA_OK) return 0;
+  return workspace_for(s);
+}
+
+int fa_bwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                  const void* v, fa_strides sv, const void* o, fa_strides so, const void* dout, fa_strides sdo,
+                  const float* lse, void* dq, fa_strides sdq, void* dk, fa_strides sdk, void* dv, fa_strides sdv,
+                  void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+  fa::AttnShape s;
+  int rc = varlen_shape(p, &s);
+  if (rc != FA_OK) return rc;
+  const bool packed = s.cu_q != nullptr;
+  const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk;
+  BwdTensors t;
+  t.q = q;
+  t.k = k;
+  t.v = v;
+  t.o = o;
+  t.dout = dout;
+  t.lse = lse;
+  t.dq = dq;
+  t.dk = dk;
+  t.dv = dv;
+  if ((rc = take_strides(sq, packed, s.B, rq, s.H, &t.sq)) != FA_OK ||
+      (rc = take_strides(sk, packed, s.B, rk, s.Hkv, &t.sk)) != FA_OK ||
+      (rc = take_strides(sv, packed, s.B, rk, s.Hkv, &t.sv)) != FA_OK ||
+      (rc = take_strides(so, packed, s.B, rq, s.H, &t.so)) != FA_OK ||
+      (rc = take_strides(sdo, packed, s.B, rq, s.H, &t.sdo)) != FA_OK ||
+      (rc = take_strides(sdq, packed, s.B, rq, s.H, &t.sdq)) != FA_OK ||
+      (rc = take_strides(sdk, packed, s.B, rk, s.Hkv, &t.sdk)) != FA_OK ||
+      (rc = take_strides(sdv, packed, s.B, rk, s.Hkv, &t.sdv)) != FA_OK)
+    return rc;
+  return launch_bwd(s, t, p->scale, workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -90,32 +90,57 @@ __device__ __forceinline__ float* dvec_row(BwdSmemCtl& c, int buf) {
   return c.dvec + buf * BwdCfg<D>::BM;
 }
 
+// Per-row arrays (D, the fp32 dQ accumulator) use the LSE's row order: fixed length
+// [B][H][Nq], packed [H][rows_q]. Row R of that order sits at these coordinates of the
+// [batch][row][head][d] tensors.
+__device__ __forceinline__ void row_coords(const AttnShape& s, size_t R, int& b, int& row, int& h) {
+  if (s.cu_q != nullptr) {
+    b = 0;
+    h = (int)(R / s.rows_q);
+    row = (int)(R % s.rows_q);
+  } else {
+    b = (int)(R / ((size_t)s.H * s.Nq));
+    const size_t rem = R % ((size_t)s.H * s.Nq);
+    h = (int)(rem / s.Nq);
+    row = (int)(rem % s.Nq);
+  }
+}
+
+__host__ __device__ inline size_t per_row_count(const AttnShape& s) {
+  return s.cu_q != nullptr ? (size_t)s.H * s.rows_q : (size_t)s.B * s.H * s.Nq;
+}
+
+// D = rowsum(dO * O) per query row (one warp per row) and a cleared dQ accumulator.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
   constexpr int PER = D / 32;
-  const size_t rows = (size_t)a.s.B * a.s.H * a.s.N;
+  const size_t rows = per_row_count(a.s);
   const int lane = threadIdx.x & 31;
   const size_t warp0 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
   const __nv_bfloat16* O = reinterpret_cast<const __nv_bfloat16*>(a.o);
   const __nv_bfloat16* dO = reinterpret_cast<const __nv_bfloat16*>(a.dout);
   for (size_t r = warp0; r < rows; r += nwarps) {
-    const size_t base = r * D + lane * PER;
+    int b, row, h;
+    row_coords(a.s, r, b, row, h);
+    const __nv_bfloat16* op = O + elem_offset(a.so, b, row, h) + lane * PER;
+    const __nv_bfloat16* gp = dO + elem_offset(a.sdo, b, row, h) + lane * PER;
+    float* acc_row = a.dqacc + r * D + lane * PER;
     float acc = 0.f;
     if constexpr (PER == 2) {
-      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(O + base);
-      const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
+      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(op);
+      const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(gp);
       acc = __bfloat162float(x.x) * __bfloat162float(y.x) + __bfloat162float(x.y) * __bfloat162float(y.y);
-      *reinterpret_cast<float2*>(a.dqacc + base) = make_float2(0.f, 0.f);
+      *reinterpret_cast<float2*>(acc_row) = make_float2(0.f, 0.f);
     } else {
-      const uint2 xs = *reinterpret_cast<const uint2*>(O + base);
-      const uint2 ys = *reinterpret_cast<const uint2*>(dO + base);
+      const uint2 xs = *reinterpret_cast<const uint2*>(op);
+      const uint2 ys = *reinterpret_cast<const uint2*>(gp);
       const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&xs);
       const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&ys);
 #pragma unroll
       for (int i = 0; i < 2; ++i)
         acc += __bfloat162float(x[i].x) * __bfloat162float(y[i].x) + __bfloat162float(x[i].y) * __bfloat162float(y[i].y);
-      *reinterpret_cast<float4*>(a.dqacc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(acc_row) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -123,16 +148,21 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
   }
 }
 
+// dQ = scale * accumulator, in bf16, four elements per thread and iteration.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const FaBwdArgs a) {
-  const size_t n4 = (size_t)a.s.B * a.s.H * a.s.N * D / 4;
+  const size_t n4 = per_row_count(a.s) * D / 4;
   __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t R = i / (D / 4);
+    const int col = (int)(i % (D / 4)) * 4;
+    int b, row, h;
+    row_coords(a.s, R, b, row, h);
     const float4 x = reinterpret_cast<const float4*>(a.dqacc)[i];
     uint2 out;
     out.x = pack_bf16x2(x.x * a.scale, x.y * a.scale);
     out.y = pack_bf16x2(x.z * a.scale, x.w * a.scale);
-    reinterpret_cast<uint2*>(dq)[i] = out;
+    *reinterpret_cast<uint2*>(dq + elem_offset(a.sdq, b, row, h) + col) = out;
   }
 }
 
@@ -159,22 +189,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int BHkv = s.B * s.Hkv;
   const int kt = blockIdx.x / BHkv;  // key tile: small kt (most causal work) first
   const int bkv = blockIdx.x % BHkv;  // K/V head (b, hk) whose dK, dV this CTA owns
-  const int b = bkv / s.Hkv;
-  const int G = s.H / s.Hkv;                       // query heads sharing this K/V head
-  const int bh0 = b * s.H + (bkv % s.Hkv) * G;     // the group's first query head
-  const int L = key_len(s, b);
+  const int b = bkv / s.Hkv, hk = bkv % s.Hkv;
+  const int G = s.H / s.Hkv;  // query heads sharing this K/V head
+  const int h0 = hk * G;      // the group's first query head
+  const SeqInfo seq = seq_info(s, b);
+  if (kt * 128 >= seq.krows) return;  // no such key rows in this (packed) sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nv = (s.N + BM - 1) / BM;  // BM-row query steps
+  const int nv = (seq.Lq + BM - 1) / BM;  // BM-row query steps
 
   // Query steps v (rows v*BM ..) are visited iff their 128-row tile is visited for this key tile.
   // The pattern is the same for every query head of the group; a step is a (group head gi, v)
   // pair, heads outer, so dK and dV sum over the group in tensor memory.
   // No step is visited when the key tile lies past the key length; with the causal mask the first
   // candidate is the key tile's own diagonal step. Scans start there.
-  const int v_lo = kt * 128 >= L ? nv : (s.causal ? (kt * 128) / BM : 0);
+  const int v_lo = kt * 128 >= seq.Lk ? nv : (s.causal ? max(kt * 128 - seq.off, 0) / BM : 0);
   auto next_v = [&](int v) -> int {
     for (v = v < v_lo ? v_lo : v; v < nv; ++v)
-      if (tile_visited(s, (v * BM) / 128, kt, L)) return v;
+      if (tile_visited(s, seq, (v * BM) / 128, kt)) return v;
     return nv;
   };
   auto advance = [&](int& gi, int& v) {
@@ -238,8 +269,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tmdO);
       mbar_expect_tx(b_kv, 2 * C::kKVBytes);
       for (int c = 0; c < C::kBoxes; ++c) {
-        tma_load_3d(sK + c * 16384, &tmK, c * 64, kt * 128, bkv, b_kv);
-        tma_load_3d(sV + c * 16384, &tmV, c * 64, kt * 128, bkv, b_kv);
+        tma_load_4d(sK + c * 16384, &tmK, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_kv);
+        tma_load_4d(sV + c * 16384, &tmV, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_kv);
       }
       uint32_t last_par[kMaxStages];
       bool issued[kMaxStages] = {};
@@ -250,8 +281,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (mbar_wait(b_empty(st), par ^ 1, abort_flag, a.status)) {
           mbar_expect_tx(b_full(st), 2 * C::kQBytes);
           for (int c = 0; c < C::kBoxes; ++c) {
-            tma_load_3d(sQs(st) + c * C::kQBox, &tmQ, c * 64, v * BM, bh0 + gi, b_full(st));
-            tma_load_3d(sdOs(st) + c * C::kQBox, &tmdO, c * 64, v * BM, bh0 + gi, b_full(st));
+            tma_load_4d(sQs(st) + c * C::kQBox, &tmQ, c * 64, seq.q0 + v * BM, h0 + gi, seq.bb, b_full(st));
+            tma_load_4d(sdOs(st) + c * C::kQBox, &tmdO, c * 64, seq.q0 + v * BM, h0 + gi, seq.bb, b_full(st));
           }
           issued[st] = true;
           last_par[st] = par;
@@ -277,7 +308,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int n = 0;  // visited steps, counted by the whole warp
     for (int v0 = v_lo; v0 < nv; v0 += 32) {
       const int v = v0 + lane;
-      n += __popc(__ballot_sync(0xffffffffu, v < nv && tile_visited(s, (v * BM) / 128, kt, L)));
+      n += __popc(__ballot_sync(0xffffffffu, v < nv && tile_visited(s, seq, (v * BM) / 128, kt)));
     }
     n *= G;
     if (lane == 0) {
@@ -355,14 +386,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (elementwise) {
       // ---------------------------------------------------------------- P^T and dS^T
       const int key = kt * 128 + r;
-      const bool key_ok = key < L;
+      const bool key_ok = key < seq.Lk;
       const float sl2 = a.scale * kLog2e;
       // LSE and D of a step are loaded one step ahead and consumed only when they are stored for
       // the next step, so the load latency overlaps a whole step.
       auto fetch = [&](int gi, int v, float& lv, float& dv) {
         const int q = v * BM + r;
-        const bool ok = gi < G && v < nv && r < BM && q < s.N;
-        const size_t row = (size_t)(bh0 + gi) * s.N + q;
+        const bool ok = gi < G && v < nv && r < BM && q < seq.Lq;
+        const size_t row = row_base(s, seq, b, h0 + gi) + q;
         lv = ok ? a.lse[row] : 0.f;
         dv = ok ? a.dvec[row] : 0.f;
       };
@@ -386,7 +417,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fetch(gn, vn, next_l, next_d);
         mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // on the critical path
         fence_after_sync();
-        const bool need_mask = (s.causal && (q0 / 128) == kt) || (kt * 128 + 128 > L) || (q0 + BM > s.N);
+        const bool need_mask =
+            (s.causal && kt * 128 + 127 > q0 + seq.off) || (kt * 128 + 128 > seq.Lk) || (q0 + BM > seq.Lq);
         const uint32_t ts = tmem + lane_off + tS(buf), tdp = tmem + lane_off + tdP(buf);
         // P^T, dS^T for the step's BM queries, 32 at a time; the mask is resolved per step so the
         // unmasked body has no branches.
@@ -412,8 +444,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                 if constexpr (MASK) {
                   const int q = q0 + c * 32 + t + u;
-                  p.x = (key_ok && q < s.N && !(s.causal && key > q)) ? p.x : 0.f;
-                  p.y = (key_ok && q + 1 < s.N && !(s.causal && key > q + 1)) ? p.y : 0.f;
+                  p.x = (key_ok && q < seq.Lq && !(s.causal && key > q + seq.off)) ? p.x : 0.f;
+                  p.y = (key_ok && q + 1 < seq.Lq && !(s.causal && key > q + 1 + seq.off)) ? p.y : 0.f;
                 }
                 const float2 dd =
                     mul2(p, sub2(make_float2(__uint_as_float(dr[t + u]), __uint_as_float(dr[t + u + 1])), dv2));
@@ -449,7 +481,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int gi = 0, v = next_v(0); gi < G && v < nv; advance(gi, v), ++it) {
         const int q0 = v * BM;
         const int buf = it % NB;
-        float* dQa = a.dqacc + (size_t)(bh0 + gi) * s.N * D;
+        float* dQa = a.dqacc + row_base(s, seq, b, h0 + gi) * D;
         mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
         fence_after_sync();
         const uint32_t tq = tmem + lane_off + tdQ(buf);
@@ -469,7 +501,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fence_proxy_async_smem();
           named_bar_sync(2, 128);
           if (threadIdx.x == 256 && !*abort_flag) {
-            const int rows = min(BM, s.N - q0);
+            const int rows = min(BM, seq.Lq - q0);
             bulk_reduce_add_f32(dQa + (size_t)q0 * D, sDq, (uint32_t)(rows * D * 4));
             tma_store_commit();
           }
@@ -482,7 +514,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fence_before_sync();
           mbar_arrive(b_dqfree(0));
           const int q = q0 + r;
-          if (q < s.N) {
+          if (q < seq.Lq) {
 #pragma unroll
             for (int t = 0; t < D; t += 4)
               atomicAdd(reinterpret_cast<float4*>(dQa + (size_t)q * D + t),
@@ -502,6 +534,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tacc = tmem + lane_off + (elementwise ? C::kTdK : C::kTdV);
     const float mul = elementwise ? a.scale : 1.f;
     const uint32_t stg = sStage0 + (elementwise ? 0 : C::kKVBytes);  // the (idle) Q/dO ring holds dK, dV
+    // A packed sequence's last key tile is stored row by row: a tile-wide copy would write the
+    // next sequence's rows.
+    const bool direct = s.cu_q != nullptr && kt * 128 + 128 > seq.krows;
+    const int key = kt * 128 + r;
+    __nv_bfloat16* grow = reinterpret_cast<__nv_bfloat16*>(elementwise ? a.dk : a.dv) +
+                          elem_offset(elementwise ? a.sdk : a.sdv, seq.bb, seq.k0 + key, hk);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t vv[32];
@@ -516,6 +554,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         pk[i] = pack_bf16x2(__uint_as_float(vv[2 * i]) * mul, __uint_as_float(vv[2 * i + 1]) * mul);
+      if (direct) {
+        if (key < seq.krows) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(grow + c * 32 + j * 8) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+        continue;
+      }
       const uint32_t box = stg + (c >> 1) * 16384 + r * 128;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -527,8 +573,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     fence_proxy_async_smem();
     named_bar_sync(elementwise ? 1 : 2, 128);
-    if (lane == 0 && (warp == 4 || warp == 8)) {
-      for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(elementwise ? &tmdK : &tmdV, stg + c * 16384, c * 64, kt * 128, bkv);
+    if (lane == 0 && (warp == 4 || warp == 8) && !direct) {
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_store_4d(elementwise ? &tmdK : &tmdV, stg + c * 16384, c * 64, seq.k0 + kt * 128, hk, seq.bb);
       tma_store_commit();
       tma_store_wait_read0();
     }
@@ -549,18 +596,24 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid_ew = sms * 8;
-  const int BH = a.s.B * a.s.H, BHkv = a.s.B * a.s.Hkv;
+  const AttnShape& s = a.s;
+  const bool packed = s.cu_q != nullptr;
+  const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk, nbatch = packed ? 1 : s.B;
+  const int BHkv = s.B * s.Hkv;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH, C::BM) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BHkv) ||
-      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BHkv) || !fa_make_tmap_bf16(&tdo, a.dout, a.s.N, D, BH, C::BM) ||
-      !fa_make_tmap_bf16(&tdk, a.dk, a.s.N, D, BHkv) || !fa_make_tmap_bf16(&tdv, a.dv, a.s.N, D, BHkv))
+  if (!fa_make_tmap_bf16(&tq, a.q, D, rq, s.H, nbatch, a.sq.row, a.sq.head, a.sq.batch, C::BM) ||
+      !fa_make_tmap_bf16(&tk, a.k, D, rk, s.Hkv, nbatch, a.sk.row, a.sk.head, a.sk.batch) ||
+      !fa_make_tmap_bf16(&tv, a.v, D, rk, s.Hkv, nbatch, a.sv.row, a.sv.head, a.sv.batch) ||
+      !fa_make_tmap_bf16(&tdo, a.dout, D, rq, s.H, nbatch, a.sdo.row, a.sdo.head, a.sdo.batch, C::BM) ||
+      !fa_make_tmap_bf16(&tdk, a.dk, D, rk, s.Hkv, nbatch, a.sdk.row, a.sdk.head, a.sdk.batch) ||
+      !fa_make_tmap_bf16(&tdv, a.dv, D, rk, s.Hkv, nbatch, a.sdv.row, a.sdv.head, a.sdv.batch))
     return cudaErrorInvalidValue;
   bwd_pre_kernel<D><<<grid_ew, 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)a.s.nb * BHkv;
+  const long long grid = (long long)s.nbk * BHkv;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   bwd_tc_kernel<D><<<(unsigned)grid, kBwdThreads, C::kSmem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
   e = cudaGetLastError();

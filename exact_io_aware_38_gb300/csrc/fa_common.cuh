@@ -1,9 +1,12 @@
 // Shared device/host definitions of the attention kernels (sm_103a).
 //
 // The mask predicate here is the one every kernel applies; it follows the readings stated in
-// include/fa.h: key j is valid for query i iff (!causal || j <= i) && j < L_b && the 128 x 128
-// block (i/128, j/128) is kept by the block mask. Whole 128 x 128 tiles with no valid pair are
-// skipped; only diagonal and tail tiles apply the element predicate.
+// include/fa.h. Sequence b has L_q query rows and L_k keys (fixed-length batches: L_q = N_q and
+// L_k = N_k, or the key length of seqlens_k; packed batches: from cu_seqlens). Key j is valid for
+// query i iff j < L_k, (!causal || j <= i + L_k - L_q) (causal aligned to the bottom-right corner;
+// the square case is j <= i) and the 128 x 128 block (i/128, j/128) is kept by the block mask.
+// Whole 128 x 128 tiles with no valid pair are skipped; only tiles that straddle the diagonal or
+// the key end apply the element predicate.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -17,30 +20,65 @@ namespace fa {
 constexpr int kTile = 128;  // mask granularity and tile size (query rows x keys)
 
 struct AttnShape {
-  int B, H, N, d;
+  int B, H, d;
   int Hkv;     // K/V heads; query head h reads K/V head h / (H / Hkv) (grouped-query attention)
-  int nb;      // ceil(N / 128)
-  int causal;  // 0/1
-  const uint8_t* block_mask;  // [nb * nb] or null
-  const int32_t* seqlens_k;   // [B] or null
+  int Nq, Nk;  // fixed length: the lengths; packed: the maximum lengths (the grid covers these)
+  int nbq, nbk;  // ceil(Nq / 128), ceil(Nk / 128)
+  int causal;    // 0/1, bottom-right aligned
+  const uint8_t* block_mask;  // [nbq * nbk] or null (fixed length only)
+  const int32_t* seqlens_k;   // [B] or null (fixed length only)
+  const int32_t* cu_q;        // [B + 1] or null: packed query rows of sequence b are cu_q[b] .. cu_q[b+1]
+  const int32_t* cu_k;        // [B + 1], set exactly when cu_q is
+  int rows_q, rows_k;         // packed: rows of the packed Q/O/dO/dQ and K/V/dK/dV tensors
 };
 
-// Effective key length of sequence b: min(max(L_b, 0), N).
-__device__ __forceinline__ int key_len(const AttnShape& s, int b) {
-  int L = s.N;
-  if (s.seqlens_k != nullptr) {
-    L = __ldg(s.seqlens_k + b);
-    L = L < 0 ? 0 : (L > s.N ? s.N : L);
+// One sequence of the batch, resolved once per CTA.
+struct SeqInfo {
+  int Lq, Lk;  // query rows and valid keys
+  int q0, k0;  // first row of the sequence in the tensor's row dimension (packed), else 0
+  int bb;      // batch coordinate of the tensor maps (fixed length), else 0
+  int off;     // causal offset (keys - queries of the sequence): key j visible to query i iff j <= i + off
+  int krows;   // key rows that exist in the tensor for this sequence (dK/dV rows to write)
+};
+
+__device__ __forceinline__ int clampi(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+__device__ __forceinline__ SeqInfo seq_info(const AttnShape& s, int b) {
+  SeqInfo r;
+  if (s.cu_q != nullptr) {
+    // Lengths are clamped to the maxima the grid covers and rows to the tensors' extents, so a
+    // malformed cu_seqlens can never index outside the buffers.
+    r.q0 = clampi(__ldg(s.cu_q + b), 0, s.rows_q);
+    r.k0 = clampi(__ldg(s.cu_k + b), 0, s.rows_k);
+    r.Lq = clampi(__ldg(s.cu_q + b + 1) - r.q0, 0, min(s.Nq, s.rows_q - r.q0));
+    r.Lk = clampi(__ldg(s.cu_k + b + 1) - r.k0, 0, min(s.Nk, s.rows_k - r.k0));
+    r.bb = 0;
+    r.krows = r.Lk;
+  } else {
+    r.q0 = r.k0 = 0;
+    r.Lq = s.Nq;
+    r.Lk = s.Nk;
+    if (s.seqlens_k != nullptr) r.Lk = clampi(__ldg(s.seqlens_k + b), 0, s.Nk);
+    r.bb = b;
+    r.krows = s.Nk;
   }
-  return L;
+  // Causal alignment uses the sequence's key count; key padding (seqlens_k) is a separate mask.
+  r.off = (s.cu_q != nullptr ? r.Lk : s.Nk) - r.Lq;
+  return r;
 }
 
 // Is the (query tile qt, key tile kt) block visited? True iff it holds at least one valid pair.
-__device__ __forceinline__ bool tile_visited(const AttnShape& s, int qt, int kt, int L) {
-  if (s.causal && kt > qt) return false;
-  if (kt * kTile >= L) return false;
-  if (s.block_mask != nullptr && __ldg(s.block_mask + (size_t)qt * s.nb + kt) == 0) return false;
+__device__ __forceinline__ bool tile_visited(const AttnShape& s, const SeqInfo& q, int qt, int kt) {
+  if (qt * kTile >= q.Lq || kt * kTile >= q.Lk) return false;
+  if (s.causal && kt * kTile > qt * kTile + (kTile - 1) + q.off) return false;
+  if (s.block_mask != nullptr && __ldg(s.block_mask + (size_t)qt * s.nbk + kt) == 0) return false;
   return true;
+}
+
+// First index of (b, h)'s rows in the per-row arrays (LSE, and the backward's D and fp32 dQ
+// accumulator): fixed length [B][H][Nq]; packed [H][rows_q] (a sequence's rows are contiguous).
+__device__ __forceinline__ size_t row_base(const AttnShape& s, const SeqInfo& q, int b, int h) {
+  return s.cu_q != nullptr ? (size_t)h * s.rows_q + q.q0 : ((size_t)b * s.H + h) * s.Nq;
 }
 
 // Record an in-kernel error (first writer wins); never traps.
@@ -68,11 +106,21 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 }  // namespace fa
 
+// Element strides of a bf16 tensor addressed as [batch][row][head][d] (d contiguous).
+struct FaStrides {
+  long long row, head, batch;
+};
+
+__device__ __forceinline__ size_t elem_offset(const FaStrides& t, int b, int row, int h) {
+  return (size_t)b * t.batch + (size_t)row * t.row + (size_t)h * t.head;
+}
+
 // Host-side launch entry points of the kernel translation units (called by fa_api.cu).
 struct FaFwdArgs {
   const void *q, *k, *v;
   void* o;
   float* lse;
+  FaStrides sq, sk, sv, so;
   fa::AttnShape s;
   float scale;
   int32_t* tile_visits;
@@ -83,8 +131,9 @@ struct FaBwdArgs {
   const void *q, *k, *v, *o, *dout;
   const float* lse;
   void *dq, *dk, *dv;
-  float* dvec;   // D, fp32 [B,H,N]
-  float* dqacc;  // fp32 [B,H,N,d]
+  FaStrides sq, sk, sv, so, sdo, sdq, sdk, sdv;
+  float* dvec;   // D, fp32, one per query row (laid out like the LSE)
+  float* dqacc;  // fp32 dQ accumulator, d per query row (laid out like the LSE)
   fa::AttnShape s;
   float scale;
   int* status;

@@ -78,26 +78,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const AttnShape& s = a.s;
   const int BH = s.B * s.H;
-  const int npairs = (s.nb + 1) >> 1;
+  const int npairs = (s.nbq + 1) >> 1;
   const int pidx = blockIdx.x / BH;
   const int bh = blockIdx.x % BH;
   const int pair = s.causal ? (npairs - 1 - pidx) : pidx;  // longest causal work first
-  const int b = bh / s.H;
-  const int bkv = b * s.Hkv + (bh % s.H) / (s.H / s.Hkv);  // K/V head of this query head
-  const int L = key_len(s, b);
+  const int b = bh / s.H, h = bh % s.H;
+  const int hk = h / (s.H / s.Hkv);  // K/V head of this query head
+  const SeqInfo seq = seq_info(s, b);
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
-  const bool has1 = qt1 < s.nb;
+  if (qt0 * 128 >= seq.Lq) return;  // a packed sequence shorter than the grid's maximum
+  const bool has1 = qt1 * 128 < seq.Lq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  auto vis = [&](int x, int kt) -> bool { return (x == 0 || has1) && tile_visited(s, x ? qt1 : qt0, kt, L); };
-  // Key tiles past the key length, or (causal) past the later query tile's diagonal, are never
+  auto vis = [&](int x, int kt) -> bool { return (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt); };
+  // Key tiles past the key length, or (causal) past the last row's visible keys, are never
   // visited; scans stop there.
-  int kt_end = (L + 127) / 128;
-  if (s.causal) kt_end = min(kt_end, (has1 ? qt1 : qt0) + 1);
+  int kt_end = (seq.Lk + 127) / 128;
+  if (s.causal) {
+    const int last_key = min((has1 ? qt1 : qt0) * 128 + 127, seq.Lq - 1) + seq.off;
+    kt_end = last_key < 0 ? 0 : min(kt_end, last_key / 128 + 1);
+  }
   auto next_union = [&](int kt) -> int {
     for (; kt < kt_end; ++kt)
       if (vis(0, kt) || vis(1, kt)) return kt;
-    return s.nb;
+    return s.nbk;
   };
 
   const uint32_t b_q = smem_u32(&ctl.q_full), b_k0 = smem_u32(&ctl.k0_full);
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(b_q, (has1 ? 2 : 1) * C::kTileBytes);
       for (int x = 0; x < (has1 ? 2 : 1); ++x)
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_3d(sQ + x * C::kTileBytes + c * 16384, &tmQ, c * 64, (x ? qt1 : qt0) * 128, bh, b_q);
+          tma_load_4d(sQ + x * C::kTileBytes + c * 16384, &tmQ, c * 64, seq.q0 + (x ? qt1 : qt0) * 128, h, seq.bb, b_q);
       // Stage t (the t-th key tile u_t the pair visits) lands V_{u_t} and K_{u_t+1} in buffer
       // t % kStages; the first key tile comes alone, into the K half of the last buffer. A buffer
       // is reloaded once the MMAs of its previous stage have completed.
@@ -152,14 +156,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool k0_issued = false;
       int kt = next_union(0);
 #ifndef FA_TEST_WITHHOLD_KV
-      if (kt < s.nb) {
+      if (kt < s.nbk) {
         mbar_expect_tx(b_k0, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_3d(sK(C::kStages - 1) + c * 16384, &tmK, c * 64, kt * 128, bkv, b_k0);
+          tma_load_4d(sK(C::kStages - 1) + c * 16384, &tmK, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_k0);
         k0_issued = true;
       }
 #endif
-      for (int t = 0; kt < s.nb; ++t) {
+      for (int t = 0; kt < s.nbk; ++t) {
         const int b = t % C::kStages;
         const int ktn = next_union(kt + 1);
         const int uses = t / C::kStages + (b == C::kStages - 1 ? 1 : 0);  // earlier users of buffer b
@@ -170,12 +174,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #else
         if (false) {
 #endif
-          mbar_expect_tx(b_full(b), (ktn < s.nb ? 2 : 1) * C::kTileBytes);
+          mbar_expect_tx(b_full(b), (ktn < s.nbk ? 2 : 1) * C::kTileBytes);
           for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_3d(sV(b) + c * 16384, &tmV, c * 64, kt * 128, bkv, b_full(b));
-          if (ktn < s.nb)
+            tma_load_4d(sV(b) + c * 16384, &tmV, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_full(b));
+          if (ktn < s.nbk)
             for (int c = 0; c < C::kBoxes; ++c)
-              tma_load_3d(sK(b) + c * 16384, &tmK, c * 64, ktn * 128, bkv, b_full(b));
+              tma_load_4d(sK(b) + c * 16384, &tmK, c * 64, seq.k0 + ktn * 128, hk, seq.bb, b_full(b));
           if (!vis(0, kt)) mbar_arrive_cnt(b_full(b), 128);  // tile 0 has no P for this key tile
           issued[b] = true;
           last_par[b] = (t / C::kStages) & 1;
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Per key tile two waits: the stage barrier (V_t and K_t+1 landed, P0 written) and P1.
       mbar_wait_spin(b_q, 0, abort_flag, a.status);
       int kt = next_union(0);
-      if (kt < s.nb) {
+      if (kt < s.nbk) {
         mbar_wait_spin(b_k0, 0, abort_flag, a.status);
         fence_after_sync();
         for (int x = 0; x < 2; ++x)
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_spin(b_full(b), (t / C::kStages) & 1, abort_flag, a.status);
           fence_after_sync();
           if (vis(0, kt)) issue_pv(0, sV(b));
-          if (ktn < s.nb && vis(0, ktn)) {
+          if (ktn < s.nbk && vis(0, ktn)) {
             issue_s(0, sK(b));
             any[0] = true;
           }
@@ -245,12 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_after_sync();
             issue_pv(1, sV(b));
           }
-          if (ktn < s.nb && vis(1, ktn)) {
+          if (ktn < s.nbk && vis(1, ktn)) {
             issue_s(1, sK(b));
             any[1] = true;
           }
           mma_commit(b_empty(b));
-          if (ktn >= s.nb) break;
+          if (ktn >= s.nbk) break;
           kt = ktn;
         }
       }
@@ -276,14 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(b_q, 0, abort_flag, a.status);
     if (active) {
       int t = -1;  // union index of the key tile (tile 0 reports P on stage t's barrier)
-      for (int kt = next_union(0); kt < s.nb; kt = next_union(kt + 1)) {
+      for (int kt = next_union(0); kt < s.nbk; kt = next_union(kt + 1)) {
         ++t;
         if (!vis(x, kt)) continue;
         mbar_wait(b_sfull[x], cnt & 1, abort_flag, a.status);
         fence_after_sync();
         const int k0 = kt * 128;
-        const bool masked = (s.causal && kt == qt) || k0 + 128 > L;
-        const int lim = min(L - k0, s.causal ? row - k0 + 1 : 128);  // keys [k0, k0 + lim) are valid
+        const bool masked = (s.causal && k0 + 127 > qt * 128 + seq.off) || k0 + 128 > seq.Lk;
+        const int lim = min(seq.Lk - k0, s.causal ? row + seq.off - k0 + 1 : 128);  // keys [k0, k0 + lim) valid
         // Pass 1: row max of the (masked) scores, read from tensor memory 32 columns at a time.
         auto row_max = [&](auto mask_tag) -> float {
           constexpr bool MASK = decltype(mask_tag)::value;
@@ -367,6 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const uint32_t stg = sQ + x * C::kTileBytes;
+      // A packed sequence's last tile is stored row by row: a tile-wide copy would write the next
+      // sequence's rows.
+      const bool direct = s.cu_q != nullptr && qt * 128 + 128 > seq.Lq;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + elem_offset(a.so, seq.bb, seq.q0 + row, h);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
@@ -381,6 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
+        if (direct) {
+          if (row < seq.Lq) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+          continue;
+        }
         const uint32_t box = stg + (c >> 1) * 16384 + r * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -390,14 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : "memory");
         }
       }
-      if (row < s.N) a.lse[(size_t)bh * s.N + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (row < seq.Lq) a.lse[row_base(s, seq, b, h) + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       fence_proxy_async_smem();
       named_bar_sync(1 + x, 128);
       if (warp == 2 + 4 * x && lane == 0) {
-        for (int c = 0; c < C::kBoxes; ++c) tma_store_3d(&tmO, stg + c * 16384, c * 64, qt * 128, bh);
+        if (!direct)
+          for (int c = 0; c < C::kBoxes; ++c) tma_store_4d(&tmO, stg + c * 16384, c * 64, seq.q0 + qt * 128, h, seq.bb);
         tma_store_commit();
         tma_store_wait_read0();  // the staging is read; the writes land before the grid completes
-        if (a.tile_visits != nullptr) a.tile_visits[(size_t)bh * s.nb + qt] = cnt;
+        if (a.tile_visits != nullptr) a.tile_visits[(size_t)bh * s.nbq + qt] = cnt;
       }
     }
   }
@@ -413,14 +430,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const int BH = a.s.B * a.s.H, BHkv = a.s.B * a.s.Hkv;
+  const AttnShape& s = a.s;
+  const bool packed = s.cu_q != nullptr;
+  const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk, nbatch = packed ? 1 : s.B;
   CUtensorMap tq, tk, tv, to;
-  if (!fa_make_tmap_bf16(&tq, a.q, a.s.N, D, BH) || !fa_make_tmap_bf16(&tk, a.k, a.s.N, D, BHkv) ||
-      !fa_make_tmap_bf16(&tv, a.v, a.s.N, D, BHkv) || !fa_make_tmap_bf16(&to, a.o, a.s.N, D, BH))
+  if (!fa_make_tmap_bf16(&tq, a.q, D, rq, s.H, nbatch, a.sq.row, a.sq.head, a.sq.batch) ||
+      !fa_make_tmap_bf16(&tk, a.k, D, rk, s.Hkv, nbatch, a.sk.row, a.sk.head, a.sk.batch) ||
+      !fa_make_tmap_bf16(&tv, a.v, D, rk, s.Hkv, nbatch, a.sv.row, a.sv.head, a.sv.batch) ||
+      !fa_make_tmap_bf16(&to, a.o, D, rq, s.H, nbatch, a.so.row, a.so.head, a.so.batch))
     return cudaErrorInvalidValue;
+  const int BH = s.B * s.H;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)((a.s.nb + 1) / 2) * BH;
+  const long long grid = (long long)((s.nbq + 1) / 2) * BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, to, a);
   return cudaGetLastError();

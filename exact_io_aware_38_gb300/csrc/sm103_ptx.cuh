@@ -138,6 +138,20 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// 4-D tiled copies: coordinates (column, row, head, batch) of the [batch][row][head][d] view.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int x, int y, int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
 // Element-wise add of `bytes` contiguous fp32 from shared memory into global memory, performed by
 // the bulk-copy engine (both addresses 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {

@@ -127,6 +127,52 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
 /*
+ * Variable-length and strided batches.
+ * The pages fix no tensor layout; frameworks hand attention either padded [B, N, H, d] / [B, H, N, d]
+ * tensors or packed sequences (the rows of all sequences concatenated, located by cumulative
+ * lengths), often with different query and key lengths (a prompt attending a longer cache). The
+ * readings adopted:
+ *   layout     every bf16 tensor is addressed as [batch][row][head][d] with d contiguous and the
+ *              element strides of fa_strides (row, head, batch: multiples of 8 elements, > 0);
+ *              e.g. [B, H, N, d] has (d, N*d, H*N*d), [B, N, H, d] has (H*d, d, N*H*d).
+ *   packed     cu_seqlens_q/_k (device int32 [B + 1], nondecreasing from 0): sequence b owns rows
+ *              cu[b] .. cu[b+1] of the row dimension (batch strides are then ignored); rows_q and
+ *              rows_k are the row extents of the tensors (>= cu[B]); seqlen_q/_k bound the lengths
+ *              (longer sequences are truncated to the bound, rows past rows_q/_k are never read
+ *              or written). Fixed length: cu_seqlens NULL, every sequence has seqlen_q query rows
+ *              and seqlen_k keys.
+ *   causal     aligned to the bottom-right corner: with L_q queries and L_k keys, key j is visible
+ *              to query i iff j <= i + L_k - L_q (the square case is j <= i). Rows with no visible
+ *              key get O = 0 and LSE = -inf.
+ *   LSE        fp32, fixed length [B, H, seqlen_q]; packed [H, rows_q] (row r of head h at h * rows_q + r).
+ *   workspace  fa_bwd_varlen_workspace_bytes: D and the fp32 dQ accumulator, one row per LSE entry.
+ * No block mask, key-padding vector or tile counts here (use fa_fwd / fa_bwd for those). K/V may
+ * have Hkv heads as in fa_fwd_gqa. Errors, ownership and launches are as for fa_fwd / fa_bwd; a
+ * packed batch's last tile is stored row by row so no write crosses into the next sequence.
+ */
+typedef struct {
+  int64_t row, head, batch;
+} fa_strides;
+
+typedef struct {
+  int B, H, Hkv, d;
+  int seqlen_q, seqlen_k;
+  const int32_t* cu_seqlens_q; /* NULL (fixed length) or device int32 [B + 1] */
+  const int32_t* cu_seqlens_k; /* NULL exactly when cu_seqlens_q is */
+  int rows_q, rows_k;          /* packed only: row extents of the query-side / key-side tensors */
+  int causal;
+  float scale;
+} fa_varlen_problem;
+
+int fa_fwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                  const void* v, fa_strides sv, void* o, fa_strides so, float* lse, int* dev_status, void* stream);
+size_t fa_bwd_varlen_workspace_bytes(const fa_varlen_problem* p);
+int fa_bwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                  const void* v, fa_strides sv, const void* o, fa_strides so, const void* dout, fa_strides sdo,
+                  const float* lse, void* dq, fa_strides sdq, void* dk, fa_strides sdk, void* dv, fa_strides sdv,
+                  void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
+/*
  * Backward pass that allocates nothing, for callers that cannot allocate device memory (a plugin
  * or custom operator inside another framework receives only its input and output buffers; the
  * host framework owns the memory pool, and a cudaMalloc of its own would bypass that pool's

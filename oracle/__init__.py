@@ -2,7 +2,9 @@
 
 from .attention import (  # noqa: F401
     attention_backward,
+    attention_backward_varlen,
     attention_forward,
+    attention_forward_varlen,
     head_dkdv,
     head_dq,
     head_forward,

@@ -66,17 +66,19 @@ TILE = 128  # granularity of the block mask (128 x 128 blocks)
 # ----------------------------------------------------------------------------- masks
 
 
-def valid_matrix(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=TILE):
+def valid_matrix(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=TILE, offset=0):
     """Boolean validity of (query row, key) pairs for one (b, h).
 
     rows: 1-D int array of query indices; returns bool [len(rows), n_keys].
-    valid(i, j) = [not causal or j <= i] and [j < key_len] and [block_mask[i // tile, j // tile] != 0]
+    valid(i, j) = [not causal or j <= i + offset] and [j < key_len] and [block_mask[i // tile, j // tile] != 0]
+    offset = (number of keys) - (number of queries): 0 for the square case; a query block shorter
+    than its keys is aligned to the bottom-right corner (its last query sees every key).
     """
     i = np.asarray(rows, dtype=np.int64)[:, None]
     j = np.arange(n_keys, dtype=np.int64)[None, :]
     ok = np.ones((i.shape[0], n_keys), dtype=bool)
     if causal:
-        ok &= j <= i
+        ok &= j <= i + offset
     if key_len is not None:
         ok &= j < int(key_len)
     if block_mask is not None:
@@ -85,13 +87,13 @@ def valid_matrix(rows, n_keys, causal=False, block_mask=None, key_len=None, tile
     return ok
 
 
-def valid_cols(cols, n_rows, causal=False, block_mask=None, key_len=None, tile=TILE):
+def valid_cols(cols, n_rows, causal=False, block_mask=None, key_len=None, tile=TILE, offset=0):
     """Validity for all query rows against a set of key columns: bool [n_rows, len(cols)]."""
     i = np.arange(n_rows, dtype=np.int64)[:, None]
     j = np.asarray(cols, dtype=np.int64)[None, :]
     ok = np.ones((n_rows, j.shape[1]), dtype=bool)
     if causal:
-        ok &= j <= i
+        ok &= j <= i + offset
     if key_len is not None:
         ok &= j < int(key_len)
     if block_mask is not None:
@@ -152,7 +154,7 @@ def head_forward(q, k, v, scale, causal=False, block_mask=None, key_len=None, ro
     lse = np.empty(rows.shape[0])
     at = 0
     for r in _row_chunks(rows, chunk):
-        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len)
+        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len, offset=k.shape[0] - n)
         p, m, l = row_softmax(scores(q[r], k, scale), valid)
         o[at : at + r.shape[0]] = p @ v
         lse[at : at + r.shape[0]] = lse_from_stats(m, l)
@@ -167,7 +169,7 @@ def head_row_stats(q, k, v, do, scale, causal=False, block_mask=None, key_len=No
     l_all = np.empty(n)
     d_all = np.empty(n)
     for r in _row_chunks(np.arange(n), chunk):
-        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len)
+        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len, offset=k.shape[0] - n)
         p, m, l = row_softmax(scores(q[r], k, scale), valid)
         dp = do[r] @ v.T
         m_all[r] = m
@@ -183,7 +185,7 @@ def head_dq(q, k, v, do, scale, causal=False, block_mask=None, key_len=None, row
     dq = np.empty((rows.shape[0], q.shape[1]))
     at = 0
     for r in _row_chunks(rows, chunk):
-        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len)
+        valid = valid_matrix(r, k.shape[0], causal, block_mask, key_len, offset=k.shape[0] - n)
         p, _, _ = row_softmax(scores(q[r], k, scale), valid)
         dp = do[r] @ v.T
         dd = (p * dp).sum(axis=1)
@@ -204,7 +206,7 @@ def head_dkdv(q, k, v, do, scale, causal=False, block_mask=None, key_len=None, c
     if stats is None:
         stats = head_row_stats(q, k, v, do, scale, causal, block_mask, key_len)
     m, l, dd = stats
-    valid = valid_cols(cols, n, causal, block_mask, key_len)
+    valid = valid_cols(cols, n, causal, block_mask, key_len, offset=k.shape[0] - n)
     p = probs_from_stats(scores(q, k[cols], scale), valid, m, l)  # [n, |cols|]
     dp = do @ v[cols].T
     ds = p * (dp - dd[:, None])
@@ -269,8 +271,8 @@ def attention_backward(q, k, v, do, scale, causal=False, block_mask=None, seqlen
     B, H, N, d = q.shape
     Hkv = k.shape[1]
     dq = np.empty_like(q)
-    dk_h = np.empty((B, H, N, k.shape[3]))  # per query head, summed over each group below
-    dv_h = np.empty((B, H, N, v.shape[3]))
+    dk_h = np.empty((B, H, k.shape[2], k.shape[3]))  # per query head, summed over each group below
+    dv_h = np.empty((B, H, v.shape[2], v.shape[3]))
 
     def one(bh):
         b, h = bh
@@ -305,3 +307,50 @@ def tile_grid(N, causal=False, block_mask=None, key_len=None, tile=TILE):
         for jt in range(nb):
             grid[it, jt] = cols_any[jt * tile : (jt + 1) * tile].any()
     return grid
+
+
+# ----------------------------------------------------------------------------- packed sequences
+
+
+def attention_forward_varlen(q, k, v, cu_q, cu_k, scale, causal=False):
+    """Packed batch: q [rows_q, H, d], k and v [rows_k, Hkv, d]; sequence b owns query rows
+    cu_q[b]..cu_q[b+1] and keys cu_k[b]..cu_k[b+1]. Each (sequence, head) is the definition above
+    on its own rows (causal aligned to the bottom-right corner). Returns O [rows_q, H, d] and LSE
+    [H, rows_q] in float64; rows outside every sequence are left 0 and -inf."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    cu_q, cu_k = np.asarray(cu_q, dtype=np.int64), np.asarray(cu_k, dtype=np.int64)
+    H, Hkv = q.shape[1], k.shape[1]
+    o = np.zeros((q.shape[0], H, v.shape[2]))
+    lse = np.full((H, q.shape[0]), -np.inf)
+    for b in range(cu_q.shape[0] - 1):
+        qa, qe, ka, ke = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if qe <= qa:
+            continue
+        for h in range(H):
+            hk = kv_head(h, H, Hkv)
+            o[qa:qe, h], lse[h, qa:qe] = head_forward(q[qa:qe, h], k[ka:ke, hk], v[ka:ke, hk], scale, causal)
+    return o, lse
+
+
+def attention_backward_varlen(q, k, v, do, cu_q, cu_k, scale, causal=False):
+    """Gradients of L = sum(dO * O) for a packed batch (layout as attention_forward_varlen):
+    dQ [rows_q, H, d], dK and dV [rows_k, Hkv, d] (summed over each K/V head's query heads);
+    rows outside every sequence are 0."""
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    cu_q, cu_k = np.asarray(cu_q, dtype=np.int64), np.asarray(cu_k, dtype=np.int64)
+    H, Hkv = q.shape[1], k.shape[1]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(cu_q.shape[0] - 1):
+        qa, qe, ka, ke = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if qe <= qa or ke <= ka:
+            continue
+        for h in range(H):
+            hk = kv_head(h, H, Hkv)
+            args = (q[qa:qe, h], k[ka:ke, hk], v[ka:ke, hk], do[qa:qe, h], scale, causal)
+            dq[qa:qe, h] = head_dq(*args)
+            dkh, dvh = head_dkdv(*args)
+            dk[ka:ke, hk] += dkh
+            dv[ka:ke, hk] += dvh
+    return dq, dk, dv

@@ -118,3 +118,47 @@ def test_binding_refuses_cpu_tensors(L):
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fwd(q, q, q)
+
+
+def varlen_rc(bwd=False, problem=None, **kw):
+    p = fa.VarlenProblem(2, 4, 2, 64, 100, 120, None, None, 0, 0, 1, 0.125) if problem is None else problem
+    for name, val in kw.items():
+        setattr(p, name, val)
+    st = fa.Strides(4 * 64, 64, 100 * 4 * 64)
+    sk = fa.Strides(2 * 64, 64, 120 * 2 * 64)
+    if not bwd:
+        return fa.fa_fwd_varlen(p, A, st, A, sk, A, sk, A, st, A, None, None)
+    return fa.fa_bwd_varlen(p, A, st, A, sk, A, sk, A, st, A, st, A, A, st, A, sk, A, sk, A, 1 << 30, None, None)
+
+
+@pytest.mark.parametrize("kw,rc", [
+    (dict(Hkv=3), -1), (dict(B=0), -1), (dict(seqlen_q=0), -1), (dict(causal=5), -1), (dict(scale=0.0), -1),
+    (dict(d=32), -2), (dict(cu_seqlens_q=A), -1), (dict(cu_seqlens_k=A), -1),
+    (dict(cu_seqlens_q=A, cu_seqlens_k=A, rows_q=0, rows_k=10), -1),
+    (dict(cu_seqlens_q=A + 2, cu_seqlens_k=A, rows_q=10, rows_k=10), -3),
+])
+def test_varlen_validation(L, kw, rc):
+    assert varlen_rc(False, **kw) == rc
+    assert varlen_rc(True, **kw) == rc
+
+
+def test_varlen_bad_strides(L):
+    p = fa.VarlenProblem(2, 4, 4, 64, 100, 100, None, None, 0, 0, 0, 0.125)
+    good = fa.Strides(4 * 64, 64, 100 * 4 * 64)
+    for bad in (fa.Strides(0, 64, 25600), fa.Strides(4 * 64, 60, 25600), fa.Strides(4 * 64, 64, 0),
+                fa.Strides(-256, 64, 25600)):
+        assert fa.fa_fwd_varlen(p, A, bad, A, good, A, good, A, good, A, None, None) == -1
+        assert fa.fa_fwd_varlen(p, A, good, A, good, A, good, A, bad, A, None, None) == -1
+    assert fa.fa_fwd_varlen(p, A + 16, good, A, good, A, good, A, good, A + 2, None, None) == -3
+
+
+def test_varlen_workspace_bytes(L):
+    r256 = lambda x: (x + 255) // 256 * 256
+    p = fa.VarlenProblem(3, 4, 2, 128, 100, 70, None, None, 0, 0, 1, 0.1)
+    rows = 3 * 4 * 100
+    assert fa.fa_bwd_varlen_workspace_bytes(p) == r256(rows * 4) + r256(rows * 128 * 4)
+    p = fa.VarlenProblem(3, 4, 2, 64, 100, 70, A, A, 257, 180, 1, 0.1)
+    rows = 4 * 257
+    assert fa.fa_bwd_varlen_workspace_bytes(p) == r256(rows * 4) + r256(rows * 64 * 4)
+    p.Hkv = 3
+    assert fa.fa_bwd_varlen_workspace_bytes(p) == 0

@@ -1,0 +1,170 @@
+"""GPU parity for strided, unequal-length and packed batches (fa_fwd_varlen / fa_bwd_varlen)
+against the fp64 oracle, with the tolerances of test_gpu_parity.py. Causal attention is aligned to
+the bottom-right corner (key j visible to query i iff j <= i + L_k - L_q)."""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_38_gb300 as fa
+import oracle
+from exact_io_aware_38_gb300 import build, workloads
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX, REL_FRO = 2e-2, 2e-3, 1e-3, 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    fa.lib()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+
+
+def f64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def bf16(shape, g, std=1.0):
+    return (torch.randn(shape, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def check_o_lse(o, lse, o_ref, lse_ref):
+    err = np.abs(o - o_ref)
+    assert err.max() <= O_MAX and err.mean() <= O_MEAN, (err.max(), err.mean())
+    empty = np.isneginf(lse_ref)
+    assert (np.isneginf(lse) == empty).all()
+    if (~empty).any():
+        assert np.abs(lse[~empty] - lse_ref[~empty]).max() <= LSE_MAX
+
+
+def rel_fro(x, ref):
+    nr = np.linalg.norm(ref)
+    if nr == 0:
+        assert np.abs(x).max() <= 1e-3
+        return
+    r = np.linalg.norm(x - ref) / nr
+    assert r <= REL_FRO, r
+
+
+def run_status(fn):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = fn(status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bshd_views_match_contiguous_path(causal, d):
+    """The same problem through fa_fwd/fa_bwd ([B, H, N, d]) and through the strided entry on a
+    [B, N, H, d] copy: identical O, LSE, dK, dV bits (same tiles, same order); dQ to rounding."""
+    g = torch.Generator().manual_seed(31 + d)
+    B, H, N = 2, 4, 300
+    q, k, v, do = (bf16((B, H, N, d), g).cuda() for _ in range(4))
+    o1, l1 = fa.fwd(q, k, v, causal=causal)
+    dq1, dk1, dv1 = fa.bwd(q, k, v, o1, l1, do, causal=causal)
+    qs, ks, vs, dos = (t.transpose(1, 2).contiguous() for t in (q, k, v, do))  # [B, N, H, d]
+    o2, l2 = run_status(lambda st: fa.fwd_varlen(qs, ks, vs, causal=causal, status=st))
+    dq2, dk2, dv2 = run_status(lambda st: fa.bwd_varlen(qs, ks, vs, o2, l2, dos, causal=causal, status=st))
+    assert torch.equal(o1, o2.transpose(1, 2)) and torch.equal(l1, l2)
+    assert torch.equal(dk1, dk2.transpose(1, 2)) and torch.equal(dv1, dv2.transpose(1, 2))
+    assert (dq1.float() - dq2.transpose(1, 2).float()).abs().max() <= 1e-2
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(100, 300), (300, 100), (1, 257), (257, 1), (129, 129), (64, 640)])
+def test_unequal_lengths(Nq, Nk, d, causal):
+    g = torch.Generator().manual_seed(Nq * 7 + Nk + d)
+    B, H, Hkv = 2, 4, 2
+    q, do = bf16((B, Nq, H, d), g), bf16((B, Nq, H, d), g)
+    k, v = bf16((B, Nk, Hkv, d), g), bf16((B, Nk, Hkv, d), g)
+    scale = 1.0 / np.sqrt(d)
+    qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
+    o, lse = run_status(lambda st: fa.fwd_varlen(qc, kc, vc, causal=causal, scale=scale, status=st))
+    dq, dk, dv = run_status(lambda st: fa.bwd_varlen(qc, kc, vc, o, lse, doc, causal=causal, scale=scale, status=st))
+    t4 = lambda x: f64(x).transpose(0, 2, 1, 3)  # [B, N, H, d] -> [B, H, N, d]
+    ro, rl = oracle.attention_forward(t4(q), t4(k), t4(v), scale, causal=causal)
+    check_o_lse(t4(o), f64(lse), ro, rl)
+    rdq, rdk, rdv = oracle.attention_backward(t4(q), t4(k), t4(v), t4(do), scale, causal=causal)
+    rel_fro(t4(dq), rdq)
+    rel_fro(t4(dk), rdk)
+    rel_fro(t4(dv), rdv)
+
+
+PACKED = [
+    ([5, 0, 131, 300, 1], [9, 4, 131, 257, 128]),
+    ([128, 256, 77], [128, 256, 77]),
+    ([640], [1000]),
+    ([3, 200, 129, 1, 0, 64], [300, 2, 129, 1, 5, 70]),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("case", range(len(PACKED)))
+def test_packed_sequences(case, d, causal):
+    lq, lk = PACKED[case]
+    g = torch.Generator().manual_seed(100 + case * 3 + d)
+    H, Hkv = 4, 2
+    cu_q = np.cumsum([0] + lq).astype(np.int32)
+    cu_k = np.cumsum([0] + lk).astype(np.int32)
+    rows_q, rows_k = int(cu_q[-1]) + 5, int(cu_k[-1]) + 3  # spare rows outside every sequence
+    q, do = bf16((rows_q, H, d), g), bf16((rows_q, H, d), g)
+    k, v = bf16((rows_k, Hkv, d), g), bf16((rows_k, Hkv, d), g)
+    scale = 1.0 / np.sqrt(d)
+    cq, ck = torch.tensor(cu_q, device="cuda"), torch.tensor(cu_k, device="cuda")
+    mq, mk = max(max(lq), 1) + 37, max(max(lk), 1)  # the bound may exceed every length
+    qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
+    sentinel = torch.full_like(qc, float("nan"))
+    lse0 = torch.full((H, rows_q), 7.0, device="cuda")
+    dk0, dv0 = torch.full_like(kc, 3.0), torch.full_like(vc, 3.0)
+    o, lse = run_status(lambda st: fa.fwd_varlen(qc, kc, vc, cq, ck, mq, mk, causal=causal, scale=scale,
+                                                 out=sentinel, lse=lse0, status=st))
+    dq, dk, dv = run_status(lambda st: fa.bwd_varlen(qc, kc, vc, o, lse, doc, cq, ck, mq, mk, causal=causal,
+                                                     scale=scale, dk=dk0, dv=dv0, status=st))
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    # rows outside every sequence are never written (dQ's are set to zero)
+    assert torch.isnan(o[tq:].float()).all() and (lse[:, tq:] == 7.0).all()
+    assert (dk[tk:].float() == 3.0).all() and (dv[tk:].float() == 3.0).all()
+    assert (dq[tq:].float() == 0).all()
+    ro, rl = oracle.attention_forward_varlen(f64(q), f64(k), f64(v), cu_q, cu_k, scale, causal=causal)
+    check_o_lse(f64(o)[:tq], f64(lse)[:, :tq], ro[:tq], rl[:, :tq])
+    rdq, rdk, rdv = oracle.attention_backward_varlen(f64(q), f64(k), f64(v), f64(do), cu_q, cu_k, scale,
+                                                     causal=causal)
+    rel_fro(f64(dq)[:tq], rdq[:tq])
+    rel_fro(f64(dk)[:tk], rdk[:tk])
+    rel_fro(f64(dv)[:tk], rdv[:tk])
+
+
+def test_packed_long_causal_sampled():
+    """A packed batch at length 8192 (the long-context shape, 4 heads, two sequences of unequal
+    query/key lengths), checked on sampled rows and key columns per sequence."""
+    g = torch.Generator().manual_seed(9)
+    H, d = 4, 128
+    lq, lk = [8192, 3000], [8192, 5000]
+    cu_q, cu_k = np.cumsum([0] + lq).astype(np.int32), np.cumsum([0] + lk).astype(np.int32)
+    q, do = bf16((cu_q[-1], H, d), g), bf16((cu_q[-1], H, d), g)
+    k, v = bf16((cu_k[-1], H, d), g), bf16((cu_k[-1], H, d), g)
+    scale = 1.0 / np.sqrt(d)
+    cq, ck = torch.tensor(cu_q, device="cuda"), torch.tensor(cu_k, device="cuda")
+    qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
+    o, lse = run_status(lambda st: fa.fwd_varlen(qc, kc, vc, cq, ck, 8192, 8192, causal=True, scale=scale, status=st))
+    dq, dk, dv = run_status(lambda st: fa.bwd_varlen(qc, kc, vc, o, lse, doc, cq, ck, 8192, 8192, causal=True,
+                                                     scale=scale, status=st))
+    rng = np.random.default_rng(3)
+    for b in range(2):
+        sq, sk = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        h = b * 3
+        qh, kh, vh, doh = f64(q[sq, h]), f64(k[sk, h]), f64(v[sk, h]), f64(do[sq, h])
+        rows = np.sort(rng.choice(lq[b], 200, replace=False))
+        cols = np.sort(rng.choice(lk[b], 200, replace=False))
+        om, lm = oracle.head_forward(qh, kh, vh, scale, True, rows=rows)
+        check_o_lse(f64(o[sq, h])[rows], f64(lse[h, sq])[rows], om, lm)
+        rel_fro(f64(dq[sq, h])[rows], oracle.head_dq(qh, kh, vh, doh, scale, True, rows=rows))
+        rdk, rdv = oracle.head_dkdv(qh, kh, vh, doh, scale, True, cols=cols)
+        rel_fro(f64(dk[sk, h])[cols], rdk)
+        rel_fro(f64(dv[sk, h])[cols], rdv)

@@ -289,9 +289,78 @@ def pin_gqa_library_crosscheck():
         assert np.abs(a - b.grad.numpy()).max() <= 1e-11
 
 
+def pin_causal_decode_row():
+    """Bottom-right causal with one query: the query is the last position, so it sees every key
+    and the result equals unmasked attention of that row (and its gradients too)."""
+    for Lk, d in ((1, 4), (9, 3), (130, 8)):
+        q, do = RNG.standard_normal((1, d)), RNG.standard_normal((1, d))
+        k, v = RNG.standard_normal((Lk, d)), RNG.standard_normal((Lk, d))
+        oc, lc = OA.head_forward(q, k, v, 0.4, causal=True)
+        on, ln = OA.head_forward(q, k, v, 0.4, causal=False)
+        assert np.abs(oc - on).max() <= 1e-13 and np.abs(lc - ln).max() <= 1e-13
+        gc = OA.head_dkdv(q, k, v, do, 0.4, causal=True)
+        gn = OA.head_dkdv(q, k, v, do, 0.4, causal=False)
+        for x, y in zip(gc, gn):
+            assert np.abs(x - y).max() <= 1e-13
+
+
+def pin_causal_front_padding():
+    """Bottom-right alignment as an identity: with L_q < L_k, causal attention of the L_q queries
+    equals the last L_q rows of the square causal problem whose first L_k - L_q queries are
+    arbitrary; with L_q > L_k the first L_q - L_k rows see no key (O = 0, LSE = -inf) and the rest
+    equal the square problem on the last L_k queries."""
+    d = 5
+    for Lq, Lk in ((3, 11), (40, 170), (11, 3), (170, 40)):
+        q, k, v = RNG.standard_normal((Lq, d)), RNG.standard_normal((Lk, d)), RNG.standard_normal((Lk, d))
+        o, lse = OA.head_forward(q, k, v, 0.7, causal=True)
+        if Lq <= Lk:
+            qpad = np.vstack([RNG.standard_normal((Lk - Lq, d)), q])
+            os_, ls_ = OA.head_forward(qpad, k, v, 0.7, causal=True)
+            assert np.abs(o - os_[Lk - Lq:]).max() <= 1e-13 and np.abs(lse - ls_[Lk - Lq:]).max() <= 1e-13
+        else:
+            assert (o[: Lq - Lk] == 0).all() and np.isneginf(lse[: Lq - Lk]).all()
+            os_, ls_ = OA.head_forward(q[Lq - Lk:], k, v, 0.7, causal=True)
+            assert np.abs(o[Lq - Lk:] - os_).max() <= 1e-13 and np.abs(lse[Lq - Lk:] - ls_).max() <= 1e-13
+
+
+def pin_varlen_library_crosscheck():
+    """Packed batch (ragged lengths, an empty sequence, L_q != L_k, K/V heads shared by two query
+    heads) against torch SDPA in float64, one sequence at a time, with the causal mask built by
+    torch's own tril at diagonal L_k - L_q; forward and autograd gradients."""
+    H, Hkv, d = 4, 2, 6
+    lq, lk = [5, 0, 131, 17, 1], [9, 4, 131, 3, 7]
+    cu_q, cu_k = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    for causal in (False, True):
+        q, do = RNG.standard_normal((cu_q[-1] + 2, H, d)), RNG.standard_normal((cu_q[-1] + 2, H, d))
+        k, v = RNG.standard_normal((cu_k[-1], Hkv, d)), RNG.standard_normal((cu_k[-1], Hkv, d))
+        o, lse = oracle.attention_forward_varlen(q, k, v, cu_q, cu_k, 0.3, causal=causal)
+        dq, dk, dv = oracle.attention_backward_varlen(q, k, v, do, cu_q, cu_k, 0.3, causal=causal)
+        assert (o[cu_q[-1]:] == 0).all() and np.isneginf(lse[:, cu_q[-1]:]).all()
+        ref_dk, ref_dv = np.zeros_like(k), np.zeros_like(v)
+        for b in range(len(lq)):
+            if lq[b] == 0:
+                continue
+            sl_q, sl_k = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+            tq = torch.tensor(q[sl_q].transpose(1, 0, 2)[None], requires_grad=True)
+            tk = torch.tensor(k[sl_k].transpose(1, 0, 2)[None], requires_grad=True)
+            tv = torch.tensor(v[sl_k].transpose(1, 0, 2)[None], requires_grad=True)
+            mask = None
+            if causal:
+                mask = torch.ones(lq[b], lk[b], dtype=torch.bool).tril(diagonal=lk[b] - lq[b])
+            kk, vv = tk.repeat_interleave(H // Hkv, dim=1), tv.repeat_interleave(H // Hkv, dim=1)
+            to = torch.nn.functional.scaled_dot_product_attention(tq, kk, vv, attn_mask=mask, scale=0.3)
+            to = torch.nan_to_num(to)  # rows with no visible key: SDPA gives NaN, the reading is 0
+            to.backward(torch.tensor(do[sl_q].transpose(1, 0, 2)[None]))
+            assert np.abs(o[sl_q] - to.detach().numpy()[0].transpose(1, 0, 2)).max() <= 1e-12
+            assert np.abs(dq[sl_q] - torch.nan_to_num(tq.grad).numpy()[0].transpose(1, 0, 2)).max() <= 1e-11
+            ref_dk[sl_k] += torch.nan_to_num(tk.grad).numpy()[0].transpose(1, 0, 2)
+            ref_dv[sl_k] += torch.nan_to_num(tv.grad).numpy()[0].transpose(1, 0, 2)
+        assert np.abs(dk - ref_dk).max() <= 1e-11 and np.abs(dv - ref_dv).max() <= 1e-11
+
+
 PINS = [pin_row_sums, pin_q_zero, pin_one_hot, pin_mask_equivalence, pin_n1, pin_finite_differences,
         pin_grad_identities, pin_library_crosscheck, pin_gqa_head_mapping, pin_gqa_finite_differences,
-        pin_gqa_library_crosscheck]
+        pin_gqa_library_crosscheck, pin_causal_decode_row, pin_causal_front_padding, pin_varlen_library_crosscheck]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -321,12 +390,12 @@ def _mut_scores_no_scale(q_rows, k_cols, scale):
     return q_rows @ k_cols.T
 
 
-def _mut_valid_reversed_causal(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=128):
+def _mut_valid_reversed_causal(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=128, offset=0):
     i = np.asarray(rows)[:, None]
     j = np.arange(n_keys)[None, :]
     ok = np.ones((i.shape[0], n_keys), dtype=bool)
     if causal:
-        ok &= j >= i
+        ok &= j >= i + offset
     if key_len is not None:
         ok &= j < key_len
     if block_mask is not None:
@@ -334,12 +403,12 @@ def _mut_valid_reversed_causal(rows, n_keys, causal=False, block_mask=None, key_
     return ok
 
 
-def _mut_valid_transposed_blocks(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=128):
+def _mut_valid_transposed_blocks(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=128, offset=0):
     i = np.asarray(rows)[:, None]
     j = np.arange(n_keys)[None, :]
     ok = np.ones((i.shape[0], n_keys), dtype=bool)
     if causal:
-        ok &= j <= i
+        ok &= j <= i + offset
     if key_len is not None:
         ok &= j < key_len
     if block_mask is not None:
@@ -375,8 +444,16 @@ def _mut_kv_head_interleaved(h, H, Hkv):
     return h % Hkv
 
 
+def _mut_valid_top_left(rows, n_keys, causal=False, block_mask=None, key_len=None, tile=128, offset=0):
+    return _real_valid(rows, n_keys, causal, block_mask, key_len, tile, 0)
+
+
+_real_valid = OA.valid_matrix
+
+
 MUTANTS = [
     ("kv_head", _mut_kv_head_interleaved),
+    ("valid_matrix", _mut_valid_top_left),
     ("scores", _mut_scores_no_scale),
     ("valid_matrix", _mut_valid_reversed_causal),
     ("valid_matrix", _mut_valid_transposed_blocks),
@@ -398,3 +475,22 @@ def test_planted_mistake_is_caught(monkeypatch, attr, mutant):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"no pin caught the planted mistake in {attr}"
+
+
+def test_fixed_and_packed_entries_agree_for_unequal_lengths():
+    """The [B, H, N, d] entry with N_q != N_k and the packed entry (equal-length sequences) must
+    give the same numbers: both reduce to the per-head functions with the bottom-right offset."""
+    B, H, Hkv, Nq, Nk, d = 2, 4, 2, 7, 19, 3
+    q, do = RNG.standard_normal((B, H, Nq, d)), RNG.standard_normal((B, H, Nq, d))
+    k, v = RNG.standard_normal((B, Hkv, Nk, d)), RNG.standard_normal((B, Hkv, Nk, d))
+    cu_q, cu_k = np.arange(B + 1) * Nq, np.arange(B + 1) * Nk
+    pk = lambda x: x.transpose(0, 2, 1, 3).reshape(-1, x.shape[1], d)  # [B, H, N, d] -> [B*N, H, d]
+    for causal in (False, True):
+        o, lse = oracle.attention_forward(q, k, v, 0.5, causal=causal, workers=1)
+        o2, lse2 = oracle.attention_forward_varlen(pk(q), pk(k), pk(v), cu_q, cu_k, 0.5, causal=causal)
+        assert np.abs(pk(o) - o2).max() <= 1e-14
+        assert np.array_equal(lse.transpose(1, 0, 2).reshape(H, -1), lse2)
+        g1 = oracle.attention_backward(q, k, v, do, 0.5, causal=causal, workers=1)
+        g2 = oracle.attention_backward_varlen(pk(q), pk(k), pk(v), pk(do), cu_q, cu_k, 0.5, causal=causal)
+        for a, b in zip(g1, g2):
+            assert np.abs(pk(a) - b).max() <= 1e-13
