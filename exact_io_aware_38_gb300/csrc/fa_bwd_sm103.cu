@@ -148,21 +148,28 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
   }
 }
 
-// dQ = scale * accumulator, in bf16, four elements per thread and iteration.
+// dQ = scale * accumulator in bf16, one warp per query row (one coordinate lookup per row).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const FaBwdArgs a) {
-  const size_t n4 = per_row_count(a.s) * D / 4;
+  constexpr int PER = D / 32;
+  const size_t rows = per_row_count(a.s);
+  const int lane = threadIdx.x & 31;
+  const size_t warp0 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
   __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t R = i / (D / 4);
-    const int col = (int)(i % (D / 4)) * 4;
+  for (size_t r = warp0; r < rows; r += nwarps) {
     int b, row, h;
-    row_coords(a.s, R, b, row, h);
-    const float4 x = reinterpret_cast<const float4*>(a.dqacc)[i];
-    uint2 out;
-    out.x = pack_bf16x2(x.x * a.scale, x.y * a.scale);
-    out.y = pack_bf16x2(x.z * a.scale, x.w * a.scale);
-    *reinterpret_cast<uint2*>(dq + elem_offset(a.sdq, b, row, h) + col) = out;
+    row_coords(a.s, r, b, row, h);
+    __nv_bfloat16* out = dq + elem_offset(a.sdq, b, row, h) + lane * PER;
+    const float* acc = a.dqacc + r * D + lane * PER;
+    if constexpr (PER == 2) {
+      const float2 x = *reinterpret_cast<const float2*>(acc);
+      *reinterpret_cast<uint32_t*>(out) = pack_bf16x2(x.x * a.scale, x.y * a.scale);
+    } else {
+      const float4 x = *reinterpret_cast<const float4*>(acc);
+      *reinterpret_cast<uint2*>(out) =
+          make_uint2(pack_bf16x2(x.x * a.scale, x.y * a.scale), pack_bf16x2(x.z * a.scale, x.w * a.scale));
+    }
   }
 }
 
@@ -203,8 +210,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // No step is visited when the key tile lies past the key length; with the causal mask the first
   // candidate is the key tile's own diagonal step. Scans start there.
   const int v_lo = kt * 128 >= seq.Lk ? nv : (s.causal ? max(kt * 128 - seq.off, 0) / BM : 0);
+  // Without a block mask every step from v_lo on is visited (tile_visited in closed form).
   auto next_v = [&](int v) -> int {
-    for (v = v < v_lo ? v_lo : v; v < nv; ++v)
+    v = v < v_lo ? v_lo : v;
+    if (s.block_mask == nullptr) return v < nv ? v : nv;
+    for (; v < nv; ++v)
       if (tile_visited(s, seq, (v * BM) / 128, kt)) return v;
     return nv;
   };

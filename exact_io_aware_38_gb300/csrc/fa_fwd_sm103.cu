@@ -90,17 +90,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool has1 = qt1 * 128 < seq.Lq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  auto vis = [&](int x, int kt) -> bool { return (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt); };
-  // Key tiles past the key length, or (causal) past the last row's visible keys, are never
-  // visited; scans stop there.
-  int kt_end = (seq.Lk + 127) / 128;
-  if (s.causal) {
-    const int last_key = min((has1 ? qt1 : qt0) * 128 + 127, seq.Lq - 1) + seq.off;
-    kt_end = last_key < 0 ? 0 : min(kt_end, last_key / 128 + 1);
-  }
+  // Without a block mask a query tile sees exactly the key tiles 0 .. last_kt (the predicate of
+  // tile_visited in closed form); with one, each tile is looked up.
+  auto last_kt = [&](int qt) -> int {
+    if (qt * 128 >= seq.Lq || seq.Lk <= 0) return -1;
+    int l = (seq.Lk - 1) / 128;
+    if (s.causal) {
+      const int key = qt * 128 + 127 + seq.off;
+      l = key < 0 ? -1 : min(l, key / 128);
+    }
+    return l;
+  };
+  const int lim0 = last_kt(qt0), lim1 = has1 ? last_kt(qt1) : -1;
+  auto vis = [&](int x, int kt) -> bool {
+    if (s.block_mask == nullptr) return kt <= (x ? lim1 : lim0);
+    return (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt);
+  };
+  // Key tiles past both query tiles' last visible key tile are never visited; scans stop there.
+  const int kt_end = max(lim0, lim1) + 1;
   auto next_union = [&](int kt) -> int {
     for (; kt < kt_end; ++kt)
       if (vis(0, kt) || vis(1, kt)) return kt;
+    return s.nbk;
+  };
+  // The same scan, also reporting which query tiles see the key tile found (for the issuer, whose
+  // every instruction between MMA groups is time the tensor pipe idles).
+  auto next_union_vis = [&](int kt, bool& v0, bool& v1) -> int {
+    for (; kt < kt_end; ++kt) {
+      v0 = vis(0, kt);
+      v1 = vis(1, kt);
+      if (v0 || v1) return kt;
+    }
+    v0 = v1 = false;
     return s.nbk;
   };
 
@@ -223,39 +244,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Per key tile two waits: the stage barrier (V_t and K_t+1 landed, P0 written) and P1.
       mbar_wait_spin(b_q, 0, abort_flag, a.status);
-      int kt = next_union(0);
+      bool v0, v1;  // which query tiles see key tile kt
+      int kt = next_union_vis(0, v0, v1);
       if (kt < s.nbk) {
         mbar_wait_spin(b_k0, 0, abort_flag, a.status);
         fence_after_sync();
-        for (int x = 0; x < 2; ++x)
-          if (vis(x, kt)) {
-            issue_s(x, sK(C::kStages - 1));
-            any[x] = true;
-          }
+        if (v0) issue_s(0, sK(C::kStages - 1));
+        if (v1) issue_s(1, sK(C::kStages - 1));
+        any[0] = v0;
+        any[1] = v1;
         mma_commit(b_empty(C::kStages - 1));
         for (int t = 0;; ++t) {
           const int b = t % C::kStages;
-          const int ktn = next_union(kt + 1);
+          bool n0, n1;
+          const int ktn = next_union_vis(kt + 1, n0, n1);  // n0 = n1 = false past the last tile
           mbar_wait_spin(b_full(b), (t / C::kStages) & 1, abort_flag, a.status);
           fence_after_sync();
-          if (vis(0, kt)) issue_pv(0, sV(b));
-          if (ktn < s.nbk && vis(0, ktn)) {
+          if (v0) issue_pv(0, sV(b));
+          if (n0) {
             issue_s(0, sK(b));
             any[0] = true;
           }
-          if (vis(1, kt)) {
+          if (v1) {
             mbar_wait_spin(b_pready[1], np[1] & 1, abort_flag, a.status);
             ++np[1];
             fence_after_sync();
             issue_pv(1, sV(b));
           }
-          if (ktn < s.nbk && vis(1, ktn)) {
+          if (n1) {
             issue_s(1, sK(b));
             any[1] = true;
           }
           mma_commit(b_empty(b));
           if (ktn >= s.nbk) break;
           kt = ktn;
+          v0 = n0;
+          v1 = n1;
         }
       }
       for (int x = 0; x < 2; ++x)
