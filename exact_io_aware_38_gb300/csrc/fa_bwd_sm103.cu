@@ -315,6 +315,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //           sn - 1 has completed and dQ is read out;
     //   warp 2: dV, dK and dQ of step g, once P^T/dS^T of step g are in place (which follows the
     //           completion of step g's S^T/dP^T).
+    // Descriptors of the resident K and V tiles, advanced by constant byte offsets per k-step.
+    const uint64_t dK0 = desc_kmajor_sw128(sK), dV0 = desc_kmajor_sw128(sV), mK0 = desc_mnmajor_sw128(sK, 16384);
     int n = 0;  // visited steps, counted by the whole warp
     for (int v0 = v_lo; v0 < nv; v0 += 32) {
       const int v = v0 + lane;
@@ -335,11 +337,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
             }
-            const uint32_t q_s = sQs(st), do_s = sdOs(st);
+            const uint64_t dq = desc_kmajor_sw128(sQs(st)), ddo = desc_kmajor_sw128(sdOs(st));
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
-              mma_ss(tmem + tS(buf), desc_kmajor_sw128(sK + okk), desc_kmajor_sw128(q_s + oq), C::kIdS, kk > 0);
+              mma_ss(tmem + tS(buf), desc_add(dK0, okk), desc_add(dq, oq), C::kIdS, kk > 0);
             }
             if (D == 128 && sn >= NB) {  // dQ^T of step sn - NB has been read out of these columns
               mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
-              mma_ss(tmem + tdP(buf), desc_kmajor_sw128(sV + okk), desc_kmajor_sw128(do_s + oq), C::kIdS, kk > 0);
+              mma_ss(tmem + tdP(buf), desc_add(dV0, okk), desc_add(ddo, oq), C::kIdS, kk > 0);
             }
             mma_commit(b_sfull(buf));
           }
@@ -358,24 +360,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_wait_spin(b_pready(buf), (g / NB) & 1, abort_flag, a.status);
             if (D == 64 && g > 0) mbar_wait_spin(b_dqfree(0), (g - 1) & 1, abort_flag, a.status);  // dQ columns read out
             fence_after_sync();
-            const uint32_t q_s = sQs(st), do_s = sdOs(st);
+            const uint64_t mq = desc_mnmajor_sw128(sQs(st), C::kQBox), mdo = desc_mnmajor_sw128(sdOs(st), C::kQBox);
+            const uint64_t mds = desc_mnmajor_sw128(sDs(buf), 16384);
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
-              mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_mnmajor_sw128(do_s + kk * 2048, C::kQBox), C::kIdG,
+              mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_add(mdo, kk * 2048), C::kIdG,
                      (g > 0 || kk > 0) ? 1u : 0u);
             if (D == 128) mma_commit(b_sfree(buf));  // P^T read: the S^T columns are free
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
-              mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_mnmajor_sw128(q_s + kk * 2048, C::kQBox), C::kIdG,
+              mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_add(mq, kk * 2048), C::kIdG,
                      (g > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               if constexpr (D == 128) {
-                mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sK + kk * 2048, 16384),
-                       desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384), C::kIdQ, kk > 0);
+                mma_ss(tmem + tdQ(buf), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
               } else {
-                mma_ss(tmem + tdQ(buf), desc_mnmajor_sw128(sDs(buf) + kk * 2048, 16384),
-                       desc_mnmajor_sw128(sK + kk * 2048, 16384), C::kIdQ, kk > 0);
+                mma_ss(tmem + tdQ(buf), desc_add(mds, kk * 2048), desc_add(mK0, kk * 2048), C::kIdQ, kk > 0);
               }
             }
             mma_commit(b_dqfull(buf));

@@ -224,21 +224,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t np[2] = {0, 0};
       // No abort-flag reads on the issue path (see mbar_wait): after an abort the remaining MMAs
       // run on stale data and complete normally.
+      // Descriptors are built once per operand tile and advanced by constant byte offsets per k-step.
+      const uint64_t dQ[2] = {desc_kmajor_sw128(sQ), desc_kmajor_sw128(sQ + C::kTileBytes)};
       auto issue_s = [&](int x, uint32_t ka) {
-        const uint32_t qa = sQ + x * C::kTileBytes;
+        const uint64_t dq = dQ[x], dk = desc_kmajor_sw128(ka);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kTmemS0 + x * 128, desc_kmajor_sw128(qa + off), desc_kmajor_sw128(ka + off), C::kIdS,
-                 kk > 0);
+          mma_ss(tmem + C::kTmemS0 + x * 128, desc_add(dq, off), desc_add(dk, off), C::kIdS, kk > 0);
         }
         mma_commit(b_sfull[x]);
       };
       auto issue_pv = [&](int x, uint32_t va) {
+        const uint64_t dv = desc_mnmajor_sw128(va, 16384);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kTmemO0 + x * D, tmem + C::kTmemS0 + x * 128 + kk * 8,
-                 desc_mnmajor_sw128(va + kk * 2048, 16384), C::kIdPV, (first[x] && kk == 0) ? 0u : 1u);
+          mma_ts(tmem + C::kTmemO0 + x * D, tmem + C::kTmemS0 + x * 128 + kk * 8, desc_add(dv, kk * 2048), C::kIdPV,
+                 (first[x] && kk == 0) ? 0u : 1u);
         first[x] = false;
       };
 

@@ -192,6 +192,11 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t 
   return d;
 }
 
+// The descriptor of (base + byte_off), given the descriptor of base: the start-address field holds
+// address >> 4 in 14 bits and shared-memory addresses stay below 2^18, so adding byte_off >> 4
+// never carries out of the field. Saves the issuing thread rebuilding descriptors per MMA.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) { return d + (byte_off >> 4); }
+
 // kind::f16 instruction descriptor: bf16 A and B, fp32 D, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
