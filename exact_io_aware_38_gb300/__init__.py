@@ -11,6 +11,7 @@ Tensor helpers (grouped-query attention when k, v have fewer heads than q):
     fwd(q, k, v, ...) -> (o, lse);  bwd(q, k, v, o, lse, do, ...) -> (dq, dk, dv)
     fwd_varlen(q, k, v, ...), bwd_varlen(...): [B, N, H, d] views with any strides, or packed
     [rows, H, d] sequences located by cu_seqlens; query and key lengths may differ.
+    fwd_splitkv(q, k, v, ..., num_splits=None): the forward split over keys (decode shapes).
 """
 
 from __future__ import annotations
@@ -56,6 +57,10 @@ _SIGS = {
     "fa_bwd_varlen_workspace_bytes": (ctypes.c_size_t, [_VP]),
     "fa_bwd_varlen": (_I, [_VP, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, Strides,
                            _P, Strides, _P, Strides, _P, ctypes.c_size_t, _P, _P]),
+    "fa_fwd_splitkv_splits": (_I, [_VP, _I]),
+    "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_VP, _I]),
+    "fa_fwd_splitkv": (_I, [_VP, _I, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, ctypes.c_size_t, _P,
+                            _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P]),
 }
@@ -131,6 +136,20 @@ def fa_bwd_varlen(p, q, sq, k, sk, v, sv, o, so, dout, sdo, lse, dq, sdq, dk, sd
                   workspace_bytes, dev_status, stream) -> int:
     return int(lib().fa_bwd_varlen(ctypes.byref(p), q, sq, k, sk, v, sv, o, so, dout, sdo, lse, dq, sdq, dk, sdk, dv,
                                    sdv, workspace, workspace_bytes, dev_status, stream))
+
+
+def fa_fwd_splitkv_splits(p, num_sms) -> int:
+    return int(lib().fa_fwd_splitkv_splits(ctypes.byref(p), num_sms))
+
+
+def fa_fwd_splitkv_workspace_bytes(p, num_splits) -> int:
+    return int(lib().fa_fwd_splitkv_workspace_bytes(ctypes.byref(p), num_splits))
+
+
+def fa_fwd_splitkv(p, num_splits, q, sq, k, sk, v, sv, o, so, lse, workspace, workspace_bytes, dev_status,
+                   stream) -> int:
+    return int(lib().fa_fwd_splitkv(ctypes.byref(p), num_splits, q, sq, k, sk, v, sv, o, so, lse, workspace,
+                                    workspace_bytes, dev_status, stream))
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, block_mask, seqlens_k, scale, dev_status,
@@ -308,3 +327,24 @@ def bwd_varlen(q, k, v, o, lse, do, cu_seqlens_q=None, cu_seqlens_k=None, max_se
     if rc != 0:
         raise FaError(rc)
     return dq, dk, dv
+
+
+def fwd_splitkv(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, *,
+                num_splits=None, causal=False, scale=None, out=None, lse=None, workspace=None, status=None,
+                stream=None):
+    """fwd_varlen with the key tiles split into num_splits ranges whose partial results are merged
+    by their log-sum-exp (for decode shapes); num_splits=None picks about one wave of CTAs."""
+    p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale)
+    if num_splits is None:
+        num_splits = fa_fwd_splitkv_splits(p, torch.cuda.get_device_properties(q.device).multi_processor_count)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty(_lse_shape(q, p, packed), dtype=torch.float32, device=q.device) if lse is None else lse
+    nbytes = fa_fwd_splitkv_workspace_bytes(p, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    rc = fa_fwd_splitkv(p, num_splits, q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed), v.data_ptr(),
+                        _view(v, packed), o.data_ptr(), _view(o, packed), lse.data_ptr(), workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    if rc != 0:
+        raise FaError(rc)
+    return o, lse

@@ -13,6 +13,7 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 // Tensors are limited to 2^31 elements (int element offsets inside the kernels' tile math).
 constexpr double kMaxElems = 2147483648.0;
+constexpr int kMaxSplits = 256;  // splits over keys in fa_fwd_splitkv
 
 int check_common(int B, int H, int Hkv, int d, int causal, float scale) {
   if (B < 1 || H < 1) return FA_ERR_INVALID_ARG;
@@ -130,8 +131,18 @@ int launch_fwd(const fa::AttnShape& s, const void* q, FaStrides sq, const void* 
   a.scale = scale;
   a.tile_visits = tile_visits;
   a.status = dev_status;
+  a.splits = 1;
+  a.kt_chunk = s.nbk;
+  a.part_o = a.part_lse = nullptr;
+  a.part_rows = 0;
   const cudaError_t e = fa_launch_fwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Split over keys: partial launches then the merge; workspace = partial LSE, then partial O.
+size_t splitkv_bytes(const fa::AttnShape& s, int splits) {
+  const size_t rows = per_row(s) * (size_t)splits;
+  return round_up(rows * sizeof(float)) + round_up(rows * s.d * sizeof(float));
 }
 
 struct BwdTensors {
@@ -252,6 +263,68 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* stream) {
   return fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, N, d, causal, block_mask, seqlens_k, scale, workspace,
                     workspace_bytes, dev_status, stream);
+}
+
+int fa_fwd_splitkv_splits(const fa_varlen_problem* p, int num_sms) {
+  fa::AttnShape s;
+  if (varlen_shape(p, &s) != FA_OK || num_sms < 1) return 1;
+  const long long units = (long long)s.B * s.H * ((s.nbq + 1) / 2);  // CTAs without a split
+  if (units >= num_sms) return 1;
+  long long n = (num_sms + units - 1) / units;  // about one wave of CTAs
+  if (n > s.nbk) n = s.nbk;                     // at least one key tile per split
+  if (n > kMaxSplits) n = kMaxSplits;
+  return n < 1 ? 1 : (int)n;
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(const fa_varlen_problem* p, int num_splits) {
+  fa::AttnShape s;
+  if (varlen_shape(p, &s) != FA_OK || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return splitkv_bytes(s, num_splits);
+}
+
+int fa_fwd_splitkv(const fa_varlen_problem* p, int num_splits, const void* q, fa_strides sq, const void* k,
+                   fa_strides sk, const void* v, fa_strides sv, void* o, fa_strides so, float* lse, void* workspace,
+                   size_t workspace_bytes, int* dev_status, void* stream) {
+  fa::AttnShape s;
+  int rc = varlen_shape(p, &s);
+  if (rc != FA_OK) return rc;
+  if (num_splits < 1 || num_splits > kMaxSplits || !workspace) return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < splitkv_bytes(s, num_splits)) return FA_ERR_INVALID_ARG;
+  const bool packed = s.cu_q != nullptr;
+  const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk;
+  FaStrides tq, tk, tv, to;
+  if ((rc = take_strides(sq, packed, s.B, rq, s.H, &tq)) != FA_OK ||
+      (rc = take_strides(sk, packed, s.B, rk, s.Hkv, &tk)) != FA_OK ||
+      (rc = take_strides(sv, packed, s.B, rk, s.Hkv, &tv)) != FA_OK ||
+      (rc = take_strides(so, packed, s.B, rq, s.H, &to)) != FA_OK)
+    return rc;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(workspace, kAlign) || !aligned(dev_status, 4))
+    return FA_ERR_MISALIGNED;
+  FaFwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.sq = tq;
+  a.sk = tk;
+  a.sv = tv;
+  a.so = to;
+  a.s = s;
+  a.scale = p->scale;
+  a.tile_visits = nullptr;
+  a.status = dev_status;
+  a.splits = num_splits;
+  a.kt_chunk = (s.nbk + num_splits - 1) / num_splits;
+  a.part_rows = per_row(s);
+  a.part_lse = static_cast<float*>(workspace);
+  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(a.part_rows * num_splits * sizeof(float)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa_launch_fwd(a, st);
+  if (e == cudaSuccess) e = fa_launch_splitkv_merge(a, st);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_fwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,

@@ -90,26 +90,6 @@ __device__ __forceinline__ float* dvec_row(BwdSmemCtl& c, int buf) {
   return c.dvec + buf * BwdCfg<D>::BM;
 }
 
-// Per-row arrays (D, the fp32 dQ accumulator) use the LSE's row order: fixed length
-// [B][H][Nq], packed [H][rows_q]. Row R of that order sits at these coordinates of the
-// [batch][row][head][d] tensors.
-__device__ __forceinline__ void row_coords(const AttnShape& s, size_t R, int& b, int& row, int& h) {
-  if (s.cu_q != nullptr) {
-    b = 0;
-    h = (int)(R / s.rows_q);
-    row = (int)(R % s.rows_q);
-  } else {
-    b = (int)(R / ((size_t)s.H * s.Nq));
-    const size_t rem = R % ((size_t)s.H * s.Nq);
-    h = (int)(rem / s.Nq);
-    row = (int)(rem % s.Nq);
-  }
-}
-
-__host__ __device__ inline size_t per_row_count(const AttnShape& s) {
-  return s.cu_q != nullptr ? (size_t)s.H * s.rows_q : (size_t)s.B * s.H * s.Nq;
-}
-
 // D = rowsum(dO * O) per query row (one warp per row) and a cleared dQ accumulator.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {

@@ -81,6 +81,26 @@ __device__ __forceinline__ size_t row_base(const AttnShape& s, const SeqInfo& q,
   return s.cu_q != nullptr ? (size_t)h * s.rows_q + q.q0 : ((size_t)b * s.H + h) * s.Nq;
 }
 
+// Per-row arrays (D, the fp32 dQ accumulator, split partials) use the LSE's row order: fixed length
+// [B][H][Nq], packed [H][rows_q]. Row R of that order sits at these coordinates of the
+// [batch][row][head][d] tensors.
+__device__ __forceinline__ void row_coords(const AttnShape& s, size_t R, int& b, int& row, int& h) {
+  if (s.cu_q != nullptr) {
+    b = 0;
+    h = (int)(R / s.rows_q);
+    row = (int)(R % s.rows_q);
+  } else {
+    b = (int)(R / ((size_t)s.H * s.Nq));
+    const size_t rem = R % ((size_t)s.H * s.Nq);
+    h = (int)(rem / s.Nq);
+    row = (int)(rem % s.Nq);
+  }
+}
+
+__host__ __device__ inline size_t per_row_count(const AttnShape& s) {
+  return s.cu_q != nullptr ? (size_t)s.H * s.rows_q : (size_t)s.B * s.H * s.Nq;
+}
+
 // Record an in-kernel error (first writer wins); never traps.
 __device__ __forceinline__ void report_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
@@ -125,6 +145,12 @@ struct FaFwdArgs {
   float scale;
   int32_t* tile_visits;
   int* status;
+  // Split over keys: CTA split s covers key tiles [s * kt_chunk, (s + 1) * kt_chunk) and, when
+  // part_o is set, writes its normalised fp32 partial O [split][row][d] and LSE [split][row]
+  // (rows in the LSE order, part_rows per split) for the merge pass instead of O and LSE.
+  int splits, kt_chunk;
+  float *part_o, *part_lse;
+  size_t part_rows;
 };
 
 struct FaBwdArgs {
@@ -140,4 +166,5 @@ struct FaBwdArgs {
 };
 
 cudaError_t fa_launch_fwd(const FaFwdArgs& a, cudaStream_t st);
+cudaError_t fa_launch_splitkv_merge(const FaFwdArgs& a, cudaStream_t st);
 cudaError_t fa_launch_bwd(const FaBwdArgs& a, cudaStream_t st);

@@ -64,7 +64,8 @@ struct FwdSmemCtl {
   int abort_flag;
 };
 
-template <int D>
+// SPLIT: the CTA covers one split of the key tiles and writes fp32 partials (see FaFwdArgs).
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FaFwdArgs a) {
@@ -79,8 +80,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const AttnShape& s = a.s;
   const int BH = s.B * s.H;
   const int npairs = (s.nbq + 1) >> 1;
-  const int pidx = blockIdx.x / BH;
+  const int split = SPLIT ? (int)(blockIdx.x / (npairs * BH)) : 0;  // key range [kt_lo, kt_hi) of this CTA
+  const int pidx = (blockIdx.x % (npairs * BH)) / BH;
   const int bh = blockIdx.x % BH;
+  const int kt_lo = SPLIT ? split * a.kt_chunk : 0, kt_hi = SPLIT ? kt_lo + a.kt_chunk : s.nbk;
   const int pair = s.causal ? (npairs - 1 - pidx) : pidx;  // longest causal work first
   const int b = bh / s.H, h = bh % s.H;
   const int hk = h / (s.H / s.Hkv);  // K/V head of this query head
@@ -101,12 +104,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return l;
   };
-  const int lim0 = last_kt(qt0), lim1 = has1 ? last_kt(qt1) : -1;
+  const int lim0 = min(last_kt(qt0), kt_hi - 1), lim1 = has1 ? min(last_kt(qt1), kt_hi - 1) : -1;
   auto vis = [&](int x, int kt) -> bool {
     if (s.block_mask == nullptr) return kt <= (x ? lim1 : lim0);
     return (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt);
   };
-  // Key tiles past both query tiles' last visible key tile are never visited; scans stop there.
+  // Key tiles past both query tiles' last visible key tile (or past the split's range) are never
+  // visited; scans stop there, and start at the split's first key tile.
   const int kt_end = max(lim0, lim1) + 1;
   auto next_union = [&](int kt) -> int {
     for (; kt < kt_end; ++kt)
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t last_par[4];
       bool issued[4] = {false, false, false, false};
       bool k0_issued = false;
-      int kt = next_union(0);
+      int kt = next_union(kt_lo);
 #ifndef FA_TEST_WITHHOLD_KV
       if (kt < s.nbk) {
         mbar_expect_tx(b_k0, C::kTileBytes);
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Per key tile two waits: the stage barrier (V_t and K_t+1 landed, P0 written) and P1.
       mbar_wait_spin(b_q, 0, abort_flag, a.status);
       bool v0, v1;  // which query tiles see key tile kt
-      int kt = next_union_vis(0, v0, v1);
+      int kt = next_union_vis(kt_lo, v0, v1);
       if (kt < s.nbk) {
         mbar_wait_spin(b_k0, 0, abort_flag, a.status);
         fence_after_sync();
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(b_q, 0, abort_flag, a.status);
     if (active) {
       int t = -1;  // union index of the key tile (tile 0 reports P on stage t's barrier)
-      for (int kt = next_union(0); kt < s.nbk; kt = next_union(kt + 1)) {
+      for (int kt = next_union(kt_lo); kt < s.nbk; kt = next_union(kt + 1)) {
         ++t;
         if (!vis(x, kt)) continue;
         mbar_wait(b_sfull[x], cnt & 1, abort_flag, a.status);
@@ -396,52 +400,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after_sync();
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const uint32_t stg = sQ + x * C::kTileBytes;
-      // A packed sequence's last tile is stored row by row: a tile-wide copy would write the next
-      // sequence's rows.
-      const bool direct = s.cu_q != nullptr && qt * 128 + 128 > seq.Lq;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + elem_offset(a.so, seq.bb, seq.q0 + row, h);
+      if constexpr (SPLIT) {  // split over keys: normalised fp32 partials for the merge pass
+        // The tensor-memory loads are warp-collective: every lane loads, only valid rows store.
+        const bool live = row < seq.Lq;
+        const size_t R = (size_t)split * a.part_rows + row_base(s, seq, b, h) + row;
+        float* po = a.part_o + R * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        if (cnt > 0) {
-          tmem_ld32(tO + c * 32, rr);
-          tmem_ld_wait();
-        } else {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          if (cnt > 0) {
+            tmem_ld32(tO + c * 32, rr);
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
-        if (direct) {
-          if (row < seq.Lq) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int i = 0; i < 32; ++i) rr[i] = 0u;
           }
-          continue;
-        }
-        const uint32_t box = stg + (c >> 1) * 16384 + r * 128;
+          if (live) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int chunk = (c & 1) * 4 + j;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(pk[4 * j]),
-                       "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
-                       : "memory");
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(po + c * 32 + i) =
+                  make_float4(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv,
+                              __uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
+          }
         }
-      }
-      if (row < seq.Lq) a.lse[row_base(s, seq, b, h) + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      fence_proxy_async_smem();
-      named_bar_sync(1 + x, 128);
-      if (warp == 2 + 4 * x && lane == 0) {
-        if (!direct)
-          for (int c = 0; c < C::kBoxes; ++c) tma_store_4d(&tmO, stg + c * 16384, c * 64, seq.q0 + qt * 128, h, seq.bb);
-        tma_store_commit();
-        tma_store_wait_read0();  // the staging is read; the writes land before the grid completes
-        if (a.tile_visits != nullptr) a.tile_visits[(size_t)bh * s.nbq + qt] = cnt;
-      }
+        if (live) a.part_lse[R] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      } else {
+        const uint32_t stg = sQ + x * C::kTileBytes;
+        // A packed sequence's last tile is stored row by row: a tile-wide copy would write the next
+        // sequence's rows.
+        const bool direct = s.cu_q != nullptr && qt * 128 + 128 > seq.Lq;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + elem_offset(a.so, seq.bb, seq.q0 + row, h);
+  #pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          if (cnt > 0) {
+            tmem_ld32(tO + c * 32, rr);
+            tmem_ld_wait();
+          } else {
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = 0u;
+          }
+          uint32_t pk[16];
+  #pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
+          if (direct) {
+            if (row < seq.Lq) {
+  #pragma unroll
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+            continue;
+          }
+          const uint32_t box = stg + (c >> 1) * 16384 + r * 128;
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int chunk = (c & 1) * 4 + j;
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(pk[4 * j]),
+                         "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
+                         : "memory");
+          }
+        }
+        if (row < seq.Lq) a.lse[row_base(s, seq, b, h) + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        fence_proxy_async_smem();
+        named_bar_sync(1 + x, 128);
+        if (warp == 2 + 4 * x && lane == 0) {
+          if (!direct)
+            for (int c = 0; c < C::kBoxes; ++c) tma_store_4d(&tmO, stg + c * 16384, c * 64, seq.q0 + qt * 128, h, seq.bb);
+          tma_store_commit();
+          tma_store_wait_read0();  // the staging is read; the writes land before the grid completes
+          if (a.tile_visits != nullptr) a.tile_visits[(size_t)bh * s.nbq + qt] = cnt;
+        }
+      }  // normal epilogue
     }
   }
 
@@ -466,11 +496,13 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
       !fa_make_tmap_bf16(&to, a.o, D, rq, s.H, nbatch, a.so.row, a.so.head, a.so.batch))
     return cudaErrorInvalidValue;
   const int BH = s.B * s.H;
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  const bool split = a.part_o != nullptr;
+  auto kern = split ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)((s.nbq + 1) / 2) * BH;
+  const long long grid = (long long)((s.nbq + 1) / 2) * BH * (split ? a.splits : 1);
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, to, a);
+  kern<<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
@@ -479,4 +511,64 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
 
 cudaError_t fa_launch_fwd(const FaFwdArgs& a, cudaStream_t st) {
   return a.s.d == 64 ? fa::launch<64>(a, st) : fa::launch<128>(a, st);
+}
+
+namespace fa {
+namespace {
+
+// Merge of the split partials (one warp per query row): with M = max_s LSE_s and
+// w_s = exp(LSE_s - M), O = sum_s w_s O_s / sum_s w_s and LSE = M + ln sum_s w_s; a row with no
+// visible key in any split gets O = 0 and LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(256) splitkv_merge_kernel(const FaFwdArgs a) {
+  constexpr int PER = D / 32;
+  const AttnShape& s = a.s;
+  const size_t rows = (size_t)s.B * s.H * s.Nq;  // (b, h, i) with i below the longest length
+  const int lane = threadIdx.x & 31;
+  const size_t warp0 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
+  for (size_t w = warp0; w < rows; w += nwarps) {
+    const int i = (int)(w % s.Nq);
+    const int h = (int)((w / s.Nq) % s.H);
+    const int b = (int)(w / ((size_t)s.Nq * s.H));
+    const SeqInfo seq = seq_info(s, b);
+    if (i >= seq.Lq) continue;
+    const size_t R = row_base(s, seq, b, h) + i;
+    float M = -INFINITY;
+    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, a.part_lse[(size_t)sp * a.part_rows + R]);
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float W = 0.f;
+    if (M != -INFINITY) {
+      for (int sp = 0; sp < a.splits; ++sp) {
+        const size_t P = (size_t)sp * a.part_rows + R;
+        const float wt = expf(a.part_lse[P] - M);
+        W += wt;
+        const float* po = a.part_o + P * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] += wt * po[e];
+      }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o) + elem_offset(a.so, seq.bb, seq.q0 + i, h) + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+      *reinterpret_cast<uint32_t*>(out + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    if (lane == 0) a.lse[R] = W > 0.f ? M + logf(W) : -INFINITY;
+  }
+}
+
+}  // namespace
+}  // namespace fa
+
+cudaError_t fa_launch_splitkv_merge(const FaFwdArgs& a, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (a.s.d == 64)
+    fa::splitkv_merge_kernel<64><<<sms * 4, 256, 0, st>>>(a);
+  else
+    fa::splitkv_merge_kernel<128><<<sms * 4, 256, 0, st>>>(a);
+  return cudaGetLastError();
 }

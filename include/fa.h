@@ -173,6 +173,26 @@ int fa_bwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, cons
                   void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
 /*
+ * Forward split over keys, for decode-shaped problems (few query rows, long keys), where one CTA
+ * per pair of 128-row query tiles would leave most SMs idle. The pages name no decode path; the
+ * method is the same online softmax, with the key tiles of each query tile split into
+ * num_splits contiguous ranges: every range yields a partial O_s (normalised) and LSE_s over its
+ * keys, and a merge pass computes M = max_s LSE_s, w_s = exp(LSE_s - M),
+ * O = sum_s w_s O_s / sum_s w_s and LSE = M + ln sum_s w_s (exact up to rounding: the log-sum-exp
+ * over a union of key sets). Arguments, layouts and results as for fa_fwd_varlen, plus:
+ *   num_splits  1 .. 256 (a split with no visible key contributes w_s = 0);
+ *               fa_fwd_splitkv_splits(p, number of SMs) gives a count that fills about one wave
+ *   workspace   device, >= fa_fwd_splitkv_workspace_bytes(p, num_splits) bytes, 256-byte aligned:
+ *               fp32 partial LSE and O, num_splits per LSE row
+ * Launches the forward kernel (split mode) and the merge kernel on `stream`.
+ */
+int fa_fwd_splitkv_splits(const fa_varlen_problem* p, int num_sms);
+size_t fa_fwd_splitkv_workspace_bytes(const fa_varlen_problem* p, int num_splits);
+int fa_fwd_splitkv(const fa_varlen_problem* p, int num_splits, const void* q, fa_strides sq, const void* k,
+                   fa_strides sk, const void* v, fa_strides sv, void* o, fa_strides so, float* lse,
+                   void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
+/*
  * Backward pass that allocates nothing, for callers that cannot allocate device memory (a plugin
  * or custom operator inside another framework receives only its input and output buffers; the
  * host framework owns the memory pool, and a cudaMalloc of its own would bypass that pool's

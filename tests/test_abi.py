@@ -162,3 +162,21 @@ def test_varlen_workspace_bytes(L):
     assert fa.fa_bwd_varlen_workspace_bytes(p) == r256(rows * 4) + r256(rows * 64 * 4)
     p.Hkv = 3
     assert fa.fa_bwd_varlen_workspace_bytes(p) == 0
+
+
+def test_splitkv_host_rules(L):
+    r256 = lambda x: (x + 255) // 256 * 256
+    p = fa.VarlenProblem(1, 8, 2, 128, 1, 8192, None, None, 0, 0, 1, 0.1)
+    assert fa.fa_fwd_splitkv_splits(p, 152) == 19        # 8 CTAs without a split -> about one wave
+    p2 = fa.VarlenProblem(4, 32, 32, 128, 4096, 4096, None, None, 0, 0, 1, 0.1)
+    assert fa.fa_fwd_splitkv_splits(p2, 152) == 1        # enough CTAs already
+    p3 = fa.VarlenProblem(1, 1, 1, 64, 1, 300, None, None, 0, 0, 0, 0.1)
+    assert fa.fa_fwd_splitkv_splits(p3, 152) == 3        # at most one split per key tile
+    rows = 8 * 1
+    assert fa.fa_fwd_splitkv_workspace_bytes(p, 5) == r256(5 * rows * 4) + r256(5 * rows * 128 * 4)
+    assert fa.fa_fwd_splitkv_workspace_bytes(p, 0) == 0 and fa.fa_fwd_splitkv_workspace_bytes(p, 257) == 0
+    st = fa.Strides(8 * 128, 128, 8 * 128)
+    sk = fa.Strides(2 * 128, 128, 8192 * 2 * 128)
+    for ns, ws, nbytes, rc in ((0, A, 1 << 30, -1), (257, A, 1 << 30, -1), (4, None, 1 << 30, -1), (4, A, 16, -1),
+                               (4, A + 16, 1 << 30, -3)):
+        assert fa.fa_fwd_splitkv(p, ns, A, st, A, sk, A, sk, A, st, A, ws, nbytes, None, None) == rc

@@ -168,3 +168,51 @@ def test_packed_long_causal_sampled():
         rdk, rdv = oracle.head_dkdv(qh, kh, vh, doh, scale, True, cols=cols)
         rel_fro(f64(dk[sk, h])[cols], rdk)
         rel_fro(f64(dv[sk, h])[cols], rdv)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_splitkv_one_split_equals_unsplit(d):
+    """One split runs the partial pass and the merge; its O and LSE equal the plain forward bits."""
+    g = torch.Generator().manual_seed(50 + d)
+    q, k, v = bf16((2, 130, 4, d), g).cuda(), bf16((2, 700, 2, d), g).cuda(), bf16((2, 700, 2, d), g).cuda()
+    o1, l1 = fa.fwd_varlen(q, k, v, causal=True)
+    o2, l2 = run_status(lambda st: fa.fwd_splitkv(q, k, v, num_splits=1, causal=True, status=st))
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq,Nk,splits", [(1, 2049, 5), (7, 300, 2), (1, 1, 3), (128, 1000, 64), (200, 8192, 16),
+                                          (1, 8192, None)])
+def test_splitkv_decode_shapes(Nq, Nk, splits, d, causal):
+    g = torch.Generator().manual_seed(Nq + Nk + d)
+    B, H, Hkv = 2, 8, 2
+    q = bf16((B, Nq, H, d), g)
+    k, v = bf16((B, Nk, Hkv, d), g), bf16((B, Nk, Hkv, d), g)
+    scale = 1.0 / np.sqrt(d)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o, lse = run_status(lambda st: fa.fwd_splitkv(qc, kc, vc, num_splits=splits, causal=causal, scale=scale,
+                                                  status=st))
+    t4 = lambda x: f64(x).transpose(0, 2, 1, 3)
+    ro, rl = oracle.attention_forward(t4(q), t4(k), t4(v), scale, causal=causal)
+    check_o_lse(t4(o), f64(lse), ro, rl)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_splitkv_packed(causal):
+    lq, lk = [1, 4, 0, 1, 130], [5000, 900, 7, 1, 2000]
+    g = torch.Generator().manual_seed(77)
+    H, Hkv, d = 8, 4, 128
+    cu_q, cu_k = np.cumsum([0] + lq).astype(np.int32), np.cumsum([0] + lk).astype(np.int32)
+    q = bf16((cu_q[-1] + 2, H, d), g)
+    k, v = bf16((cu_k[-1], Hkv, d), g), bf16((cu_k[-1], Hkv, d), g)
+    cq, ck = torch.tensor(cu_q, device="cuda"), torch.tensor(cu_k, device="cuda")
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    scale = 1.0 / np.sqrt(d)
+    out = torch.full_like(qc, float("nan"))
+    o, lse = run_status(lambda st: fa.fwd_splitkv(qc, kc, vc, cq, ck, max(lq), max(lk), num_splits=9, causal=causal,
+                                                  scale=scale, out=out, status=st))
+    tq = int(cu_q[-1])
+    assert torch.isnan(o[tq:].float()).all()
+    ro, rl = oracle.attention_forward_varlen(f64(q), f64(k), f64(v), cu_q, cu_k, scale, causal=causal)
+    check_o_lse(f64(o)[:tq], f64(lse)[:, :tq], ro[:tq], rl[:, :tq])
