@@ -43,7 +43,8 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="fa", choices=["fa", "reference"])
-    p.add_argument("--workload", default="c4", choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--workload", default="c4", choices=sorted(workloads.WORKLOADS) + ["dec"],
+                   help="dec: decode-shaped forward (informational; its own metric, HBM GB/s)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     p.add_argument("--heads", type=int, default=None, help="override H (smaller profiling cases only)")
@@ -214,8 +215,91 @@ def run_reference(args, w):
     }), flush=True)
 
 
+# Decode shape: one new query row per sequence against an 8192-key cache, 8 K/V heads shared by 32
+# query heads (the long-context shape of the benchmark, generating one token per sequence).
+DEC = dict(B=8, H=32, Hkv=8, Nq=1, Nk=8192, d=128)
+
+
+def run_decode(args):
+    """Forward split over keys on the decode shape, timed with CUDA events on the launching
+    stream; the metric is K/V bytes read per second (the path is HBM-bound: 256 MiB of cache per
+    step, 4 KiB of queries). The unsplit forward is timed beside it."""
+    import exact_io_aware_38_gb300 as fa
+    from exact_io_aware_38_gb300 import build
+
+    build.build()
+    fa.lib()
+    dev = torch.device("cuda", 0)
+    c = DEC
+    g = torch.Generator("cpu").manual_seed(2024)
+    draw = lambda *shape: torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
+    q = draw(c["B"], c["Nq"], c["H"], c["d"])
+    k = draw(c["B"], c["Nk"], c["Hkv"], c["d"])
+    v = draw(c["B"], c["Nk"], c["Hkv"], c["d"])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((c["B"], c["H"], c["Nq"]), dtype=torch.float32, device=dev)
+    p, _ = fa._problem(q, k, None, None, None, None, True, None)
+    splits = fa.fa_fwd_splitkv_splits(p, torch.cuda.get_device_properties(dev).multi_processor_count)
+    ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(p, splits), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    ms = timed(lambda: fa.fwd_splitkv(q, k, v, num_splits=splits, causal=True, out=o, lse=lse, workspace=ws,
+                                      status=status))
+    ms_unsplit = timed(lambda: fa.fwd_varlen(q, k, v, causal=True, out=o, lse=lse, status=status))
+    sweep = {}
+    for n in (1, 2, 4, 8, 16):
+        wsn = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(p, n), dtype=torch.uint8, device=dev)
+        sweep[n] = timed(lambda: fa.fwd_splitkv(q, k, v, num_splits=n, causal=True, out=o, lse=lse, workspace=wsn,
+                                                status=status))
+    # Batch 1 (32 CTAs without a split, fewer than the SMs): where splitting over keys pays.
+    q1, k1, v1, o1 = q[:1].contiguous(), k[:1].contiguous(), v[:1].contiguous(), o[:1].contiguous()
+    lse1 = lse[:1].contiguous()
+    p1, _ = fa._problem(q1, k1, None, None, None, None, True, None)
+    s1 = fa.fa_fwd_splitkv_splits(p1, torch.cuda.get_device_properties(dev).multi_processor_count)
+    ws1 = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(p1, s1), dtype=torch.uint8, device=dev)
+    ms_b1 = timed(lambda: fa.fwd_splitkv(q1, k1, v1, num_splits=s1, causal=True, out=o1, lse=lse1, workspace=ws1,
+                                         status=status))
+    ms_b1_unsplit = timed(lambda: fa.fwd_varlen(q1, k1, v1, causal=True, out=o1, lse=lse1, status=status))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+    kv_bytes = 2 * c["B"] * c["Nk"] * c["Hkv"] * c["d"] * 2
+    kv1 = kv_bytes // c["B"]
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    print(json.dumps({
+        "metric": "decode attention forward, K/V bytes read per second (B8 H32 Hkv8 N_q1 N_k8192 d128)",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": "dec: " + " ".join(f"{k_}{v_}" for k_, v_ in c.items()), "num_splits": splits,
+                   "l2": "K/V 256 MiB > 129 MB L2; no flush"},
+        "unsplit": {"ms_per_step": ms_unsplit, "value": kv_bytes / (ms_unsplit * 1e-3) / 1e9},
+        "splits_sweep_gbs": {str(n_): kv_bytes / (t * 1e-3) / 1e9 for n_, t in sweep.items()},
+        "batch1": {"num_splits": s1, "split_gbs": kv1 / (ms_b1 * 1e-3) / 1e9,
+                   "unsplit_gbs": kv1 / (ms_b1_unsplit * 1e-3) / 1e9},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peaks['source']} HBM copy bandwidth"},
+        "gpu_launches": 2 * args.steps,  # split pass + merge per step
+    }), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload == "dec":
+        return run_decode(args)
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -268,12 +268,24 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 int fa_fwd_splitkv_splits(const fa_varlen_problem* p, int num_sms) {
   fa::AttnShape s;
   if (varlen_shape(p, &s) != FA_OK || num_sms < 1) return 1;
+  // No split once the CTAs without one cover the SMs (measured: the merge then costs more than
+  // the balance gains). Otherwise the count, with at least four key tiles per split, whose CTAs
+  // fill their waves best (the fraction of SM slots used; ties to fewer splits).
   const long long units = (long long)s.B * s.H * ((s.nbq + 1) / 2);  // CTAs without a split
   if (units >= num_sms) return 1;
-  long long n = (num_sms + units - 1) / units;  // about one wave of CTAs
-  if (n > s.nbk) n = s.nbk;                     // at least one key tile per split
-  if (n > kMaxSplits) n = kMaxSplits;
-  return n < 1 ? 1 : (int)n;
+  long long cap = s.nbk / 4;
+  if (cap > kMaxSplits) cap = kMaxSplits;
+  int best = 1;
+  double best_eff = 0.0;
+  for (long long n = 1; n <= cap; ++n) {
+    const long long ctas = n * units;
+    const double eff = (double)ctas / ((double)((ctas + num_sms - 1) / num_sms) * num_sms);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = (int)n;
+    }
+  }
+  return best;
 }
 
 size_t fa_fwd_splitkv_workspace_bytes(const fa_varlen_problem* p, int num_splits) {

@@ -72,7 +72,6 @@ constexpr int kMaxBufs = 4;
 struct alignas(16) BwdSmemCtl {
   uint64_t kv_full;
   uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
   uint64_t s_full[kMaxBufs], p_ready[kMaxBufs], dq_full[kMaxBufs], dq_free[kMaxBufs], s_free[kMaxBufs];
   uint64_t done, drain;
   uint32_t tmem_base;
@@ -216,7 +215,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const uint32_t b_kv = smem_u32(&ctl.kv_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
-  auto b_empty = [&](int i) { return smem_u32(&ctl.empty[i]); };
   auto b_sfull = [&](int i) { return smem_u32(&ctl.s_full[i]); };
   auto b_pready = [&](int i) { return smem_u32(&ctl.p_ready[i]); };
   auto b_dqfull = [&](int i) { return smem_u32(&ctl.dq_full[i]); };
@@ -229,7 +227,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(b_kv, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(b_full(i), 1);
-      mbar_init(b_empty(i), 1);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(b_sfull(i), 1);
@@ -268,7 +265,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int gi = 0, v = next_v(0); gi < G && v < nv; advance(gi, v), ++i) {
         const int st = i % C::kStages;
         const uint32_t par = (i / C::kStages) & 1;
-        if (mbar_wait(b_empty(st), par ^ 1, abort_flag, a.status)) {
+        // The stage is free once step j = i - kStages has finished its gradient MMAs (dq_full of j;
+        // its S^T/dP^T finished before them). That barrier cannot run two phases ahead of this
+        // wait: its next-but-one phase belongs to step j + 2 NB >= i, which needs a stage not
+        // loaded yet, so the parity test is unambiguous.
+        const int j = (int)i - C::kStages;
+        if (j < 0 || mbar_wait(b_dqfull(j % NB), (j / NB) & 1, abort_flag, a.status)) {
           mbar_expect_tx(b_full(st), 2 * C::kQBytes);
           for (int c = 0; c < C::kBoxes; ++c) {
             tma_load_4d(sQs(st) + c * C::kQBox, &tmQ, c * 64, seq.q0 + v * BM, h0 + gi, seq.bb, b_full(st));
@@ -359,8 +361,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_ss(tmem + tdQ(buf), desc_add(mds, kk * 2048), desc_add(mK0, kk * 2048), C::kIdQ, kk > 0);
               }
             }
-            mma_commit(b_dqfull(buf));
-            mma_commit(b_empty(st));
+            mma_commit(b_dqfull(buf));  // also frees the step's Q/dO stage for the producer
           }
           mma_commit(b_done);  // the last gradient MMAs complete after every S^T/dP^T
         }

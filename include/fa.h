@@ -181,7 +181,9 @@ int fa_bwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, cons
  * O = sum_s w_s O_s / sum_s w_s and LSE = M + ln sum_s w_s (exact up to rounding: the log-sum-exp
  * over a union of key sets). Arguments, layouts and results as for fa_fwd_varlen, plus:
  *   num_splits  1 .. 256 (a split with no visible key contributes w_s = 0);
- *               fa_fwd_splitkv_splits(p, number of SMs) gives a count that fills about one wave
+ *               fa_fwd_splitkv_splits(p, number of SMs) gives 1 when the CTAs without a split
+ *               already cover the SMs, else the count (at most one per four key tiles) whose CTAs
+ *               fill their waves best
  *   workspace   device, >= fa_fwd_splitkv_workspace_bytes(p, num_splits) bytes, 256-byte aligned:
  *               fp32 partial LSE and O, num_splits per LSE row
  * Launches the forward kernel (split mode) and the merge kernel on `stream`.
