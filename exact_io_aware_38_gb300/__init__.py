@@ -12,6 +12,8 @@ Tensor helpers (grouped-query attention when k, v have fewer heads than q):
     fwd_varlen(q, k, v, ...), bwd_varlen(...): [B, N, H, d] views with any strides, or packed
     [rows, H, d] sequences located by cu_seqlens; query and key lengths may differ.
     fwd_splitkv(q, k, v, ..., num_splits=None): the forward split over keys (decode shapes).
+    fwd_partial / merge_partials / finalize_partials: per-key-block partials and their
+    log-sum-exp merge (ring.py builds sequence-sharded ring attention on them).
 """
 
 from __future__ import annotations
@@ -61,6 +63,10 @@ _SIGS = {
     "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_VP, _I]),
     "fa_fwd_splitkv": (_I, [_VP, _I, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, ctypes.c_size_t, _P,
                             _P]),
+    "fa_partial_rows": (ctypes.c_size_t, [_VP]),
+    "fa_fwd_partial": (_I, [_VP, _P, Strides, _P, Strides, _P, Strides, _P, _P, _P, _P]),
+    "fa_merge_partials": (_I, [_VP, _P, _P, _P, _P, _P]),
+    "fa_finalize_partials": (_I, [_VP, _P, _P, _P, Strides, _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P]),
 }
@@ -337,6 +343,9 @@ def fwd_splitkv(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None
     p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale)
     if num_splits is None:
         num_splits = fa_fwd_splitkv_splits(p, torch.cuda.get_device_properties(q.device).multi_processor_count)
+        if num_splits == 1:  # no split pays: the plain forward skips the partials and the merge
+            return fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=causal,
+                              scale=scale, out=out, lse=lse, status=status, stream=stream)
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty(_lse_shape(q, p, packed), dtype=torch.float32, device=q.device) if lse is None else lse
     nbytes = fa_fwd_splitkv_workspace_bytes(p, num_splits)
@@ -345,6 +354,48 @@ def fwd_splitkv(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None
     rc = fa_fwd_splitkv(p, num_splits, q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed), v.data_ptr(),
                         _view(v, packed), o.data_ptr(), _view(o, packed), lse.data_ptr(), workspace.data_ptr(),
                         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    if rc != 0:
+        raise FaError(rc)
+    return o, lse
+
+
+# ----------------------------------------------------------------------------- partials
+
+
+def fwd_partial(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, *,
+                causal=False, scale=None, status=None, stream=None):
+    """Partial of one key block: (O fp32 [rows, d], LSE fp32 [rows]) in the LSE's row order."""
+    p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale)
+    rows = int(lib().fa_partial_rows(ctypes.byref(p)))
+    po = torch.empty((rows, p.d), dtype=torch.float32, device=q.device)
+    pl = torch.full((rows,), float("-inf"), dtype=torch.float32, device=q.device)
+    rc = int(lib().fa_fwd_partial(ctypes.byref(p), q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed),
+                                  v.data_ptr(), _view(v, packed), po.data_ptr(), pl.data_ptr(), _ptr(status),
+                                  _stream(stream)))
+    if rc != 0:
+        raise FaError(rc)
+    return po, pl
+
+
+def merge_partials(q, k, acc, part, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
+                   *, stream=None):
+    """acc <- merge(acc, part) in place (both from fwd_partial for the same query rows)."""
+    p, _ = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, False, None)
+    rc = int(lib().fa_merge_partials(ctypes.byref(p), acc[0].data_ptr(), acc[1].data_ptr(), part[0].data_ptr(),
+                                     part[1].data_ptr(), _stream(stream)))
+    if rc != 0:
+        raise FaError(rc)
+    return acc
+
+
+def finalize_partials(q, k, acc, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, *,
+                      out=None, lse=None, stream=None):
+    """bf16 O (shaped like q) and fp32 LSE (as fwd_varlen) from a merged accumulator."""
+    p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, False, None)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty(_lse_shape(q, p, packed), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = int(lib().fa_finalize_partials(ctypes.byref(p), acc[0].data_ptr(), acc[1].data_ptr(), o.data_ptr(),
+                                        _view(o, packed), lse.data_ptr(), _stream(stream)))
     if rc != 0:
         raise FaError(rc)
     return o, lse

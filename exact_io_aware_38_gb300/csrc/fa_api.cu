@@ -189,6 +189,48 @@ int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* w
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Shared by fa_fwd_splitkv and fa_fwd_partial: the split-mode forward into partial buffers, then
+// (merge) the pass that combines them into O and LSE.
+int launch_partial(const fa::AttnShape& s, const fa_varlen_problem* p, int splits, const void* q, fa_strides sq,
+                   const void* k, fa_strides sk, const void* v, fa_strides sv, void* o, fa_strides so, float* lse,
+                   float* part_o, float* part_lse, int* dev_status, cudaStream_t st, bool merge) {
+  int rc;
+  const bool packed = s.cu_q != nullptr;
+  const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk;
+  FaStrides tq, tk, tv, to{};
+  if ((rc = take_strides(sq, packed, s.B, rq, s.H, &tq)) != FA_OK ||
+      (rc = take_strides(sk, packed, s.B, rk, s.Hkv, &tk)) != FA_OK ||
+      (rc = take_strides(sv, packed, s.B, rk, s.Hkv, &tv)) != FA_OK)
+    return rc;
+  if (merge && (rc = take_strides(so, packed, s.B, rq, s.H, &to)) != FA_OK) return rc;
+  if (!q || !k || !v || !part_o || !part_lse || (merge && (!o || !lse))) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(part_o, 16) || !aligned(part_lse, 4) || !aligned(dev_status, 4))
+    return FA_ERR_MISALIGNED;
+  FaFwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = merge ? o : nullptr;
+  a.lse = merge ? lse : nullptr;
+  a.sq = tq;
+  a.sk = tk;
+  a.sv = tv;
+  a.so = to;
+  a.s = s;
+  a.scale = p->scale;
+  a.tile_visits = nullptr;
+  a.status = dev_status;
+  a.splits = splits;
+  a.kt_chunk = (s.nbk + splits - 1) / splits;
+  a.part_rows = per_row(s);
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  cudaError_t e = fa_launch_fwd(a, st);
+  if (e == cudaSuccess && merge) e = fa_launch_splitkv_merge(a, st);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -302,40 +344,63 @@ int fa_fwd_splitkv(const fa_varlen_problem* p, int num_splits, const void* q, fa
   if (rc != FA_OK) return rc;
   if (num_splits < 1 || num_splits > kMaxSplits || !workspace) return FA_ERR_INVALID_ARG;
   if (workspace_bytes < splitkv_bytes(s, num_splits)) return FA_ERR_INVALID_ARG;
-  const bool packed = s.cu_q != nullptr;
-  const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk;
-  FaStrides tq, tk, tv, to;
-  if ((rc = take_strides(sq, packed, s.B, rq, s.H, &tq)) != FA_OK ||
-      (rc = take_strides(sk, packed, s.B, rk, s.Hkv, &tk)) != FA_OK ||
-      (rc = take_strides(sv, packed, s.B, rk, s.Hkv, &tv)) != FA_OK ||
-      (rc = take_strides(so, packed, s.B, rq, s.H, &to)) != FA_OK)
-    return rc;
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
-      !aligned(workspace, kAlign) || !aligned(dev_status, 4))
+  if (!aligned(workspace, kAlign)) return FA_ERR_MISALIGNED;
+  float* part_lse = static_cast<float*>(workspace);
+  float* part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           round_up(per_row(s) * num_splits * sizeof(float)));
+  return launch_partial(s, p, num_splits, q, sq, k, sk, v, sv, o, so, lse, part_o, part_lse, dev_status,
+                        static_cast<cudaStream_t>(stream), true);
+}
+
+size_t fa_partial_rows(const fa_varlen_problem* p) {
+  fa::AttnShape s;
+  if (varlen_shape(p, &s) != FA_OK) return 0;
+  return per_row(s);
+}
+
+int fa_fwd_partial(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                   const void* v, fa_strides sv, float* part_o, float* part_lse, int* dev_status, void* stream) {
+  fa::AttnShape s;
+  const int rc = varlen_shape(p, &s);
+  if (rc != FA_OK) return rc;
+  fa_strides none{8, 8, 8};
+  return launch_partial(s, p, 1, q, sq, k, sk, v, sv, nullptr, none, nullptr, part_o, part_lse, dev_status,
+                        static_cast<cudaStream_t>(stream), false);
+}
+
+int fa_merge_partials(const fa_varlen_problem* p, float* acc_o, float* acc_lse, const float* part_o,
+                      const float* part_lse, void* stream) {
+  fa::AttnShape s;
+  const int rc = varlen_shape(p, &s);
+  if (rc != FA_OK) return rc;
+  if (!acc_o || !acc_lse || !part_o || !part_lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(acc_o, 16) || !aligned(part_o, 16) || !aligned(acc_lse, 4) || !aligned(part_lse, 4))
     return FA_ERR_MISALIGNED;
-  FaFwdArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
+  const cudaError_t e = fa_launch_merge_two(acc_o, acc_lse, part_o, part_lse, per_row(s), s.d,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_finalize_partials(const fa_varlen_problem* p, const float* acc_o, const float* acc_lse, void* o, fa_strides so,
+                         float* lse, void* stream) {
+  fa::AttnShape s;
+  int rc = varlen_shape(p, &s);
+  if (rc != FA_OK) return rc;
+  const bool packed = s.cu_q != nullptr;
+  FaStrides to;
+  if ((rc = take_strides(so, packed, s.B, packed ? s.rows_q : s.Nq, s.H, &to)) != FA_OK) return rc;
+  if (!acc_o || !acc_lse || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(acc_o, 16) || !aligned(o, 16) || !aligned(acc_lse, 4) || !aligned(lse, 4)) return FA_ERR_MISALIGNED;
+  FaFwdArgs a{};
   a.o = o;
   a.lse = lse;
-  a.sq = tq;
-  a.sk = tk;
-  a.sv = tv;
   a.so = to;
   a.s = s;
-  a.scale = p->scale;
-  a.tile_visits = nullptr;
-  a.status = dev_status;
-  a.splits = num_splits;
-  a.kt_chunk = (s.nbk + num_splits - 1) / num_splits;
+  a.splits = 1;
   a.part_rows = per_row(s);
-  a.part_lse = static_cast<float*>(workspace);
-  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(a.part_rows * num_splits * sizeof(float)));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = fa_launch_fwd(a, st);
-  if (e == cudaSuccess) e = fa_launch_splitkv_merge(a, st);
+  a.part_o = const_cast<float*>(acc_o);
+  a.part_lse = const_cast<float*>(acc_lse);
+  const cudaError_t e = fa_launch_splitkv_merge(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -167,4 +167,6 @@ struct FaBwdArgs {
 
 cudaError_t fa_launch_fwd(const FaFwdArgs& a, cudaStream_t st);
 cudaError_t fa_launch_splitkv_merge(const FaFwdArgs& a, cudaStream_t st);
+cudaError_t fa_launch_merge_two(float* acc_o, float* acc_lse, const float* part_o, const float* part_lse, size_t rows,
+                                int d, cudaStream_t st);
 cudaError_t fa_launch_bwd(const FaBwdArgs& a, cudaStream_t st);

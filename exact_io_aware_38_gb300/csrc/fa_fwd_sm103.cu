@@ -493,7 +493,9 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
   if (!fa_make_tmap_bf16(&tq, a.q, D, rq, s.H, nbatch, a.sq.row, a.sq.head, a.sq.batch) ||
       !fa_make_tmap_bf16(&tk, a.k, D, rk, s.Hkv, nbatch, a.sk.row, a.sk.head, a.sk.batch) ||
       !fa_make_tmap_bf16(&tv, a.v, D, rk, s.Hkv, nbatch, a.sv.row, a.sv.head, a.sv.batch) ||
-      !fa_make_tmap_bf16(&to, a.o, D, rq, s.H, nbatch, a.so.row, a.so.head, a.so.batch))
+      // (the partial pass writes no O; its map is then built over Q and never used)
+      !fa_make_tmap_bf16(&to, a.o ? a.o : a.q, D, rq, s.H, nbatch, a.o ? a.so.row : a.sq.row,
+                         a.o ? a.so.head : a.sq.head, a.o ? a.so.batch : a.sq.batch))
     return cudaErrorInvalidValue;
   const int BH = s.B * s.H;
   const bool split = a.part_o != nullptr;
@@ -561,6 +563,47 @@ __global__ void __launch_bounds__(256) splitkv_merge_kernel(const FaFwdArgs a) {
 
 }  // namespace
 }  // namespace fa
+
+namespace fa {
+namespace {
+
+// acc <- merge(acc, part) for every row of the partial layout (one warp per row):
+// M = max(L_a, L_p), w = exp(L - M), O = (w_a O_a + w_p O_p) / (w_a + w_p), L = M + ln(w_a + w_p).
+template <int D>
+__global__ void __launch_bounds__(256) merge_two_kernel(float* acc_o, float* acc_lse, const float* part_o,
+                                                        const float* part_lse, size_t rows) {
+  constexpr int PER = D / 32;
+  const int lane = threadIdx.x & 31;
+  const size_t warp0 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
+  for (size_t r = warp0; r < rows; r += nwarps) {
+    const float la = acc_lse[r], lp = part_lse[r];
+    const float M = fmaxf(la, lp);
+    if (M == -INFINITY) continue;  // neither saw a key: stays O = 0, LSE = -inf
+    const float wa = la == -INFINITY ? 0.f : expf(la - M), wp = lp == -INFINITY ? 0.f : expf(lp - M);
+    const float inv = 1.f / (wa + wp);
+    float* oa = acc_o + r * D + lane * PER;
+    const float* op = part_o + r * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) oa[e] = (wa * oa[e] + wp * op[e]) * inv;
+    if (lane == 0) acc_lse[r] = M + logf(wa + wp);
+  }
+}
+
+}  // namespace
+}  // namespace fa
+
+cudaError_t fa_launch_merge_two(float* acc_o, float* acc_lse, const float* part_o, const float* part_lse, size_t rows,
+                                int d, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (d == 64)
+    fa::merge_two_kernel<64><<<sms * 4, 256, 0, st>>>(acc_o, acc_lse, part_o, part_lse, rows);
+  else
+    fa::merge_two_kernel<128><<<sms * 4, 256, 0, st>>>(acc_o, acc_lse, part_o, part_lse, rows);
+  return cudaGetLastError();
+}
 
 cudaError_t fa_launch_splitkv_merge(const FaFwdArgs& a, cudaStream_t st) {
   int dev = 0, sms = 148;

@@ -195,6 +195,30 @@ int fa_fwd_splitkv(const fa_varlen_problem* p, int num_splits, const void* q, fa
                    void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
 /*
+ * Partial results and their merge, the pieces of sequence-sharded (ring) attention: the essay and
+ * the commentary describe the online softmax as associative over pieces of the key space, so
+ * attention over a union of key blocks is the log-sum-exp merge of the attentions over each
+ * block. A partial is the normalised fp32 O_b and the LSE_b of one key block, stored in the LSE's
+ * row order with d contiguous: fa_partial_rows(p) rows (B*H*seqlen_q fixed, H*rows_q packed),
+ * part_o [rows][d], part_lse [rows].
+ *   fa_fwd_partial       the forward of p (any layout and causal reading of fa_fwd_varlen) into a
+ *                        partial: no O or LSE is written; rows of no sequence are not written
+ *   fa_merge_partials    acc <- merge(acc, part) in place: M = max(L_a, L_p), w = exp(L - M),
+ *                        O = (w_a O_a + w_p O_p) / (w_a + w_p), L = M + ln(w_a + w_p); a row with
+ *                        L = -inf on both sides is left as is
+ *   fa_finalize_partials acc -> bf16 O (strides so) and fp32 LSE (layout of fa_fwd_varlen)
+ * All pointers are device pointers (16-byte aligned, LSE arrays 4-byte); work is asynchronous on
+ * `stream`. Initialise an accumulator with the first block's fa_fwd_partial.
+ */
+size_t fa_partial_rows(const fa_varlen_problem* p);
+int fa_fwd_partial(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                   const void* v, fa_strides sv, float* part_o, float* part_lse, int* dev_status, void* stream);
+int fa_merge_partials(const fa_varlen_problem* p, float* acc_o, float* acc_lse, const float* part_o,
+                      const float* part_lse, void* stream);
+int fa_finalize_partials(const fa_varlen_problem* p, const float* acc_o, const float* acc_lse, void* o,
+                         fa_strides so, float* lse, void* stream);
+
+/*
  * Backward pass that allocates nothing, for callers that cannot allocate device memory (a plugin
  * or custom operator inside another framework receives only its input and output buffers; the
  * host framework owns the memory pool, and a cudaMalloc of its own would bypass that pool's

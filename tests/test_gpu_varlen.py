@@ -216,3 +216,33 @@ def test_splitkv_packed(causal):
     assert torch.isnan(o[tq:].float()).all()
     ro, rl = oracle.attention_forward_varlen(f64(q), f64(k), f64(v), cu_q, cu_k, scale, causal=causal)
     check_o_lse(f64(o)[:tq], f64(lse)[:, :tq], ro[:tq], rl[:, :tq])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_ring_attention_simulated_on_one_gpu(causal, d):
+    """The ring's per-rank schedule run on one GPU with the library's partial, merge and finalize
+    kernels (4 blocks of 300 rows, K/V heads shared by two query heads), against the oracle."""
+    from exact_io_aware_38_gb300 import ring
+
+    g = torch.Generator().manual_seed(200 + d)
+    W, blk, B, H, Hkv = 4, 300, 1, 4, 2
+    q = bf16((B, W * blk, H, d), g)
+    k, v = bf16((B, W * blk, Hkv, d), g), bf16((B, W * blk, Hkv, d), g)
+    scale = 1.0 / np.sqrt(d)
+    t4 = lambda x: f64(x).transpose(0, 2, 1, 3)
+    ro, rl = oracle.attention_forward(t4(q), t4(k), t4(v), scale, causal=causal)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    block = lambda t, i: t[:, i * blk:(i + 1) * blk].contiguous()
+    for rank in range(W):
+        qb = block(qc, rank)
+        acc = None
+        for _, src, c in ring.ring_schedule(rank, W, causal):
+            if c is None:
+                continue
+            part = fa.fwd_partial(qb, block(kc, src), block(vc, src), causal=c, scale=scale)
+            acc = part if acc is None else fa.merge_partials(qb, block(kc, src), acc, part)
+        o, lse = fa.finalize_partials(qb, block(kc, rank), acc)
+        torch.cuda.synchronize()
+        sl = slice(rank * blk, (rank + 1) * blk)
+        check_o_lse(t4(o), f64(lse), ro[:, :, sl], rl[:, :, sl])

@@ -62,3 +62,76 @@ def test_single_process_max_is_identity():
     import bench
 
     assert bench.max_over_ranks(3.25, None, torch.device("cpu")) == 3.25
+
+
+def _ring_worker(rank, world, port, causal, q):
+    """Ring attention over 2 ranks with the oracle standing in for the kernels (fp64, CPU): checks
+    the ring's schedule, rotation and merge against whole-sequence attention."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import numpy as np
+
+        import oracle
+        from exact_io_aware_38_gb300 import ring
+
+        g = torch.Generator().manual_seed(5)
+        B, N, H, d = 1, 2 * 48, 2, 8
+        full = [torch.randn((B, N, H, d), generator=g, dtype=torch.float64) for _ in range(3)]
+        blk = N // world
+        qb, kb, vb = (t[:, rank * blk:(rank + 1) * blk].contiguous() for t in full)
+        t4 = lambda x: x.numpy().transpose(0, 2, 1, 3)
+
+        def partial(q_, k_, v_, c_):
+            o, lse = oracle.attention_forward(t4(q_), t4(k_), t4(v_), 0.35, causal=c_)
+            return torch.from_numpy(o), torch.from_numpy(lse)
+
+        def merge(acc, part):
+            (oa, la), (op, lp) = acc, part
+            m = torch.maximum(la, lp)
+            wa = torch.where(torch.isinf(la), torch.zeros_like(la), torch.exp(la - m))
+            wp = torch.where(torch.isinf(lp), torch.zeros_like(lp), torch.exp(lp - m))
+            o = (wa[..., None] * oa + wp[..., None] * op) / (wa + wp)[..., None]
+            return o, m + torch.log(wa + wp)
+
+        o, lse = ring.ring_forward(qb, kb, vb, causal=causal, partial=partial, merge=merge, finalize=lambda a: a)
+        ref_o, ref_l = oracle.attention_forward(t4(full[0]), t4(full[1]), t4(full[2]), 0.35, causal=causal)
+        err_o = float(np.abs(o.numpy() - ref_o[:, :, rank * blk:(rank + 1) * blk]).max())
+        err_l = float(np.abs(lse.numpy() - ref_l[:, :, rank * blk:(rank + 1) * blk]).max())
+        q.put((rank, err_o, err_l))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_attention_two_ranks(causal):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_ring_worker, args=(r, 2, port, causal, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, err_o, err_l in results:
+        assert err_o <= 1e-12 and err_l <= 1e-12, (rank, err_o, err_l)
+
+
+def test_ring_schedule_covers_each_block_once():
+    from exact_io_aware_38_gb300 import ring
+
+    for world in (1, 2, 3, 5):
+        for rank in range(world):
+            for causal in (False, True):
+                sched = ring.ring_schedule(rank, world, causal)
+                assert sorted(src for _, src, _ in sched) == list(range(world))
+                used = {src: c for _, src, c in sched}
+                assert used[rank] is causal  # own block: causal (square) or whole
+                for src, c in used.items():
+                    if src < rank:
+                        assert c is False
+                    elif src > rank:
+                        assert c is (None if causal else False)
