@@ -256,8 +256,8 @@ def run_decode(args):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / args.steps
 
-    ms = timed(lambda: fa.fwd_splitkv(q, k, v, num_splits=splits, causal=True, out=o, lse=lse, workspace=ws,
-                                      status=status))
+    # the library's choice: a split count, or (count 1) the plain forward
+    ms = timed(lambda: fa.fwd_splitkv(q, k, v, causal=True, out=o, lse=lse, workspace=ws, status=status))
     ms_unsplit = timed(lambda: fa.fwd_varlen(q, k, v, causal=True, out=o, lse=lse, status=status))
     sweep = {}
     for n in (1, 2, 4, 8, 16):
