@@ -43,24 +43,29 @@ constexpr int kBwdThreads = 384;
 
 template <int D>
 struct BwdCfg {
-  static constexpr int BM = D == 128 ? 64 : 128;     // query rows per step
-  static constexpr int kBufs = D == 128 ? 2 : 1;     // tensor-memory [S^T | dP^T] buffers
+  // dQ^T = K^T dS^T (lanes = head dimension) accumulated over a buffer's dP^T columns, two
+  // [S^T | dP^T] buffers of 64-query steps. At d = 64 the product keeps M = 128: its upper 64 rows
+  // read the next shared-memory tile and are never read out (half of one small product wasted for
+  // the known 128-lane layout and double buffering).
+  static constexpr bool kDqT = true;
+  static constexpr int BM = kDqT ? 64 : 128;         // query rows per step
+  static constexpr int kBufs = kDqT ? 2 : 1;         // tensor-memory [S^T | dP^T] buffers
   static constexpr int kBoxes = D / 64;              // 64-column boxes per row
   static constexpr int kKVBytes = 128 * D * 2;       // K or V tile (128 rows)
   static constexpr int kQBox = BM * 128;             // one 64-column box of a Q or dO tile
   static constexpr int kQBytes = BM * D * 2;         // Q or dO tile (BM rows)
-  static constexpr int kStages = D == 128 ? 3 : 2;   // Q/dO ring depth
+  static constexpr int kStages = kDqT ? 3 : 2;       // Q/dO ring depth
   // dS^T tile [128 keys][BM queries] per buffer, in 128-byte-swizzled rows of 64 queries (a step
   // of 32 queries uses the first half of each row).
   static constexpr int kDsBytes = 128 * (BM < 64 ? 64 : BM) * 2;
-  static constexpr int kDqBytes = D == 128 ? BM * D * 4 : 0;  // fp32 dQ staging for the bulk add
+  static constexpr int kDqBytes = kDqT ? BM * D * 4 : 0;  // fp32 dQ staging for the bulk add
   static constexpr int kSmem = 2 * kKVBytes + kStages * 2 * kQBytes + kBufs * kDsBytes + kDqBytes + 1024;
   static constexpr uint32_t kTdK = 0, kTdV = D;
   static constexpr uint32_t kTS0 = 2 * D;            // S^T of buffer b at kTS0 + b * 2 * BM
   static constexpr uint32_t kTdQ64 = 2 * D + 2 * BM * kBufs;  // separate dQ columns (d = 64)
   static constexpr uint32_t kIdS = idesc_bf16(128, BM, false, false);
   static constexpr uint32_t kIdG = idesc_bf16(128, D, false, true);
-  static constexpr uint32_t kIdQ = D == 128 ? idesc_bf16(128, BM, true, true) : idesc_bf16(BM, D, true, true);
+  static constexpr uint32_t kIdQ = kDqT ? idesc_bf16(128, BM, true, true) : idesc_bf16(BM, D, true, true);
   static_assert(kSmem <= 232448 - 1536, "shared memory budget");
   static_assert(2 * kKVBytes <= kStages * 2 * kQBytes, "dK and dV staging reuse the Q/dO ring");
   static_assert(kStages <= 4 && kBufs <= 4, "barrier arrays of the control block");
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto tdP = [&](int buf) { return C::kTS0 + buf * 2 * BM + BM; };
   // d = 128: dQ^T of a step accumulates over its buffer's dP^T columns (free once dK has read
   // dS^T there), so the next S^T into the buffer waits only for dV's read of P^T.
-  auto tdQ = [&](int buf) { return D == 128 ? tdP(buf) : C::kTdQ64; };
+  auto tdQ = [&](int buf) { return C::kDqT ? tdP(buf) : C::kTdQ64; };
 
   const uint32_t b_kv = smem_u32(&ctl.kv_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int st = sn % C::kStages, buf = sn % NB;
             mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
             if (sn >= NB) {
-              if constexpr (D == 128)  // dV of step sn - NB has read P^T from these columns
+              if constexpr (C::kDqT)  // dV of step sn - NB has read P^T from these columns
                 mbar_wait_spin(b_sfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               else  // (one buffer) every MMA of step sn - 1 has completed and dQ is read out
                 mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
               mma_ss(tmem + tS(buf), desc_add(dK0, okk), desc_add(dq, oq), C::kIdS, kk > 0);
             }
-            if (D == 128 && sn >= NB) {  // dQ^T of step sn - NB has been read out of these columns
+            if (C::kDqT && sn >= NB) {  // dQ^T of step sn - NB has been read out of these columns
               mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
             }
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int g = 0; g < n; ++g) {
             const int st = g % C::kStages, buf = g % NB;
             mbar_wait_spin(b_pready(buf), (g / NB) & 1, abort_flag, a.status);
-            if (D == 64 && g > 0) mbar_wait_spin(b_dqfree(0), (g - 1) & 1, abort_flag, a.status);  // dQ columns read out
+            if (!C::kDqT && g > 0) mbar_wait_spin(b_dqfree(0), (g - 1) & 1, abort_flag, a.status);  // dQ read out
             fence_after_sync();
             const uint64_t mq = desc_mnmajor_sw128(sQs(st), C::kQBox), mdo = desc_mnmajor_sw128(sdOs(st), C::kQBox);
             const uint64_t mds = desc_mnmajor_sw128(sDs(buf), 16384);
@@ -348,14 +353,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int kk = 0; kk < BM / 16; ++kk)
               mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_add(mdo, kk * 2048), C::kIdG,
                      (g > 0 || kk > 0) ? 1u : 0u);
-            if (D == 128) mma_commit(b_sfree(buf));  // P^T read: the S^T columns are free
+            if (C::kDqT) mma_commit(b_sfree(buf));  // P^T read: the S^T columns are free
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
               mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_add(mq, kk * 2048), C::kIdG,
                      (g > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              if constexpr (D == 128) {
+              if constexpr (C::kDqT) {
                 mma_ss(tmem + tdQ(buf), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
               } else {
                 mma_ss(tmem + tdQ(buf), desc_add(mds, kk * 2048), desc_add(mK0, kk * 2048), C::kIdQ, kk > 0);
@@ -477,8 +482,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
         fence_after_sync();
         const uint32_t tq = tmem + lane_off + tdQ(buf);
-        if constexpr (D == 128) {
-          // dQ^T: lane r = head dimension, columns = the step's BM queries.
+        if constexpr (C::kDqT) {
+          // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
+          // unused rows of the d = 64 product).
           uint32_t vals[BM];
 #pragma unroll
           for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
@@ -487,9 +493,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
           if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
           named_bar_sync(2, 128);
+          if (r < D) {
 #pragma unroll
-          for (int qq = 0; qq < BM; ++qq)
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
+            for (int qq = 0; qq < BM; ++qq)
+              asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
+          }
           fence_proxy_async_smem();
           named_bar_sync(2, 128);
           if (threadIdx.x == 256 && !*abort_flag) {
