@@ -2,33 +2,31 @@
 //
 // Three launches on the caller's stream:
 //   pre   D_i = sum_k dO_ik O_ik (fp32, from the stored bf16 O) and a cleared fp32 dQ accumulator;
-//   main  one CTA per (128-key tile j, head): K_j and V_j stay in shared memory while the query
-//         rows that can see them stream through a TMA ring, BM rows per step (BM = 64 at d = 128,
-//         128 at d = 64). The score tile is recomputed from Q, K and the saved log-sum-exp instead
-//         of being stored ("FlashAttention." plate, "Never write the scores"), and the softmax
-//         gradient is applied tile by tile:
+//   main  one CTA per (128-key tile j, K/V head): K_j and V_j stay in shared memory while the
+//         query rows that can see them stream through a TMA ring, 64 rows per step. The score tile
+//         is recomputed from Q, K and the saved log-sum-exp instead of being stored
+//         ("FlashAttention." plate, "Never write the scores"), and the softmax gradient is applied
+//         tile by tile:
 //           S^T = K_j Q_i^T,  dP^T = V_j dO_i^T                  (tcgen05, into tensor memory)
 //           P^T = exp(c S^T - LSE_i),  dS^T = P^T * (dP^T - D_i)  (one thread per key row)
 //           dV_j += P^T dO_i,  dK_j += dS^T Q_i                  (A operand from tensor memory)
-//           dQ_i += dS K_j                                       (added into the fp32 accumulator)
+//           dQ_i^T = K_j^T dS_i^T                                (added into the fp32 accumulator)
 //         dK_j = c * acc and dV_j leave through shared memory and TMA stores.
 //   post  dQ = bf16(c * accumulator).
-// d = 128: dQ_i is formed transposed, dQ_i^T = K_j^T dS_i^T (tensor-memory lane = head dimension),
-//          staged row-major in shared memory and added into the accumulator by one bulk
-//          reduce-add of the bulk-copy engine per step. Two tensor-memory buffers [S^T | dP^T]
-//          alternate between steps (dQ^T is written over its buffer's S^T once P^T is consumed),
-//          so the S^T/dP^T products of step i+2 wait only for step i's dQ^T to be read out.
-// d = 64:  dQ_i = dS_i K_j (lane = query row) in its own tensor-memory columns, added with 16-byte
-//          vector atomics.
+// dQ_i is formed transposed (tensor-memory lane = head dimension; at d = 64 the product keeps
+// M = 128 and its upper rows are unused), staged row-major in shared memory and added into the
+// accumulator by one bulk reduce-add of the bulk-copy engine per step. Two tensor-memory buffers
+// [S^T | dP^T] alternate between steps; dQ^T accumulates over its buffer's dP^T columns once dK
+// has read dS^T there, so S^T of step i+2 waits only for dV of step i and dP^T for the read-out
+// of step i's dQ^T.
 //
 // CTA layout (384 threads): warp 0 TMA producer; warp 1 S^T/dP^T MMA issuer and tensor-memory owner;
 // warp 2 gradient MMA issuer;
 // warps 4-7 elementwise warpgroup (thread = key row; lane quadrant = warp % 4), which also writes
 // dK; warps 8-11 dQ warpgroup (reads dQ out of tensor memory, adds it into the accumulator), which
 // also writes dV. The two warpgroups run concurrently on different steps.
-// Tensor memory: d = 128: dK [0,128) dV [128,256), buffer b: S^T/dQ^T [256+128b, +64), dP^T [+64, +128);
-//                d = 64:  dK [0,64) dV [64,128) S^T [128,256) dP^T [256,384) dQ [384,448).
-// P^T and dS^T (bf16) are written over the first BM/2 columns of S^T and dP^T.
+// Tensor memory: dK [0,d) dV [d,2d), buffer b: S^T [2d+128b, +64), dP^T / dQ^T [+64, +128).
+// P^T and dS^T (bf16) are written over the first 32 columns of S^T and dP^T.
 #include <type_traits>
 
 #include "fa_tmap.h"
@@ -43,29 +41,27 @@ constexpr int kBwdThreads = 384;
 
 template <int D>
 struct BwdCfg {
-  // dQ^T = K^T dS^T (lanes = head dimension) accumulated over a buffer's dP^T columns, two
-  // [S^T | dP^T] buffers of 64-query steps. At d = 64 the product keeps M = 128: its upper 64 rows
-  // read the next shared-memory tile and are never read out (half of one small product wasted for
-  // the known 128-lane layout and double buffering).
-  static constexpr bool kDqT = true;
-  static constexpr int BM = kDqT ? 64 : 128;         // query rows per step
-  static constexpr int kBufs = kDqT ? 2 : 1;         // tensor-memory [S^T | dP^T] buffers
+  // Steps of 64 queries through two [S^T | dP^T] tensor-memory buffers; dQ^T = K^T dS^T (lanes =
+  // head dimension) accumulates over its buffer's dP^T columns. At d = 64 that product keeps
+  // M = 128: its upper 64 rows read the next shared-memory tile and are never read out (half of
+  // one small product wasted for the known 128-lane layout and the double buffering).
+  static constexpr int BM = 64;                      // query rows per step
+  static constexpr int kBufs = 2;                    // tensor-memory [S^T | dP^T] buffers
   static constexpr int kBoxes = D / 64;              // 64-column boxes per row
   static constexpr int kKVBytes = 128 * D * 2;       // K or V tile (128 rows)
   static constexpr int kQBox = BM * 128;             // one 64-column box of a Q or dO tile
   static constexpr int kQBytes = BM * D * 2;         // Q or dO tile (BM rows)
-  static constexpr int kStages = kDqT ? 3 : 2;       // Q/dO ring depth
+  static constexpr int kStages = 3;                  // Q/dO ring depth
   // dS^T tile [128 keys][BM queries] per buffer, in 128-byte-swizzled rows of 64 queries (a step
   // of 32 queries uses the first half of each row).
-  static constexpr int kDsBytes = 128 * (BM < 64 ? 64 : BM) * 2;
-  static constexpr int kDqBytes = kDqT ? BM * D * 4 : 0;  // fp32 dQ staging for the bulk add
+  static constexpr int kDsBytes = 128 * BM * 2;
+  static constexpr int kDqBytes = BM * D * 4;        // fp32 dQ staging for the bulk add
   static constexpr int kSmem = 2 * kKVBytes + kStages * 2 * kQBytes + kBufs * kDsBytes + kDqBytes + 1024;
   static constexpr uint32_t kTdK = 0, kTdV = D;
   static constexpr uint32_t kTS0 = 2 * D;            // S^T of buffer b at kTS0 + b * 2 * BM
-  static constexpr uint32_t kTdQ64 = 2 * D + 2 * BM * kBufs;  // separate dQ columns (d = 64)
   static constexpr uint32_t kIdS = idesc_bf16(128, BM, false, false);
   static constexpr uint32_t kIdG = idesc_bf16(128, D, false, true);
-  static constexpr uint32_t kIdQ = kDqT ? idesc_bf16(128, BM, true, true) : idesc_bf16(BM, D, true, true);
+  static constexpr uint32_t kIdQ = idesc_bf16(128, BM, true, true);
   static_assert(kSmem <= 232448 - 1536, "shared memory budget");
   static_assert(2 * kKVBytes <= kStages * 2 * kQBytes, "dK and dV staging reuse the Q/dO ring");
   static_assert(kStages <= 4 && kBufs <= 4, "barrier arrays of the control block");
@@ -76,7 +72,7 @@ constexpr int kMaxBufs = 4;
 
 struct alignas(16) BwdSmemCtl {
   uint64_t kv_full;
-  uint64_t full[kMaxStages];
+  uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t s_full[kMaxBufs], p_ready[kMaxBufs], dq_full[kMaxBufs], dq_free[kMaxBufs], s_free[kMaxBufs];
   uint64_t done, drain;
   uint32_t tmem_base;
@@ -209,6 +205,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       v = next_v(0);
     }
   };
+  // The same scan for a whole warp with the same v (the elementwise and dQ warps, where it sits on
+  // the per-step critical path): 32 candidates per block-mask probe.
+  auto next_v_warp = [&](int v) -> int {
+    v = v < v_lo ? v_lo : v;
+    if (s.block_mask == nullptr) return v < nv ? v : nv;
+    const int lane_id = threadIdx.x & 31;
+    for (; v < nv; v += 32) {
+      const int c = v + lane_id;
+      const unsigned hit = __ballot_sync(0xffffffffu, c < nv && tile_visited(s, seq, (c * BM) / 128, kt));
+      if (hit) return v + __ffs(hit) - 1;
+    }
+    return nv;
+  };
+  auto advance_warp = [&](int& gi, int& v) {
+    v = next_v_warp(v + 1);
+    if (v >= nv) {
+      ++gi;
+      v = next_v_warp(0);
+    }
+  };
   auto sQs = [&](int st) { return sStage0 + (2 * st) * C::kQBytes; };
   auto sdOs = [&](int st) { return sStage0 + (2 * st + 1) * C::kQBytes; };
   auto sDs = [&](int buf) { return sDs0 + buf * C::kDsBytes; };
@@ -216,12 +232,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto tdP = [&](int buf) { return C::kTS0 + buf * 2 * BM + BM; };
   // d = 128: dQ^T of a step accumulates over its buffer's dP^T columns (free once dK has read
   // dS^T there), so the next S^T into the buffer waits only for dV's read of P^T.
-  auto tdQ = [&](int buf) { return C::kDqT ? tdP(buf) : C::kTdQ64; };
+  auto tdQ = [&](int buf) { return tdP(buf); };
 
   const uint32_t b_kv = smem_u32(&ctl.kv_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
   auto b_sfull = [&](int i) { return smem_u32(&ctl.s_full[i]); };
   auto b_pready = [&](int i) { return smem_u32(&ctl.p_ready[i]); };
+  auto b_empty = [&](int i) { return smem_u32(&ctl.empty[i]); };
   auto b_dqfull = [&](int i) { return smem_u32(&ctl.dq_full[i]); };
   auto b_dqfree = [&](int i) { return smem_u32(&ctl.dq_free[i]); };
   auto b_sfree = [&](int i) { return smem_u32(&ctl.s_free[i]); };
@@ -232,6 +249,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(b_kv, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(b_full(i), 1);
+      mbar_init(b_empty(i), 1);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(b_sfull(i), 1);
@@ -270,12 +288,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int gi = 0, v = next_v(0); gi < G && v < nv; advance(gi, v), ++i) {
         const int st = i % C::kStages;
         const uint32_t par = (i / C::kStages) & 1;
-        // The stage is free once step j = i - kStages has finished its gradient MMAs (dq_full of j;
-        // its S^T/dP^T finished before them). That barrier cannot run two phases ahead of this
-        // wait: its next-but-one phase belongs to step j + 2 NB >= i, which needs a stage not
-        // loaded yet, so the parity test is unambiguous.
+        // The stage is free once dV and dK of step j = i - kStages have read it (its S^T/dP^T
+        // finished before them), which the gradient issuer commits to the stage's own barrier. One
+        // barrier per stage keeps the parity test unambiguous: its next phase belongs to step i, not
+        // loaded yet. (The NB-deep dq_full barriers would not: their next phase after j is step
+        // j + NB < i, which can complete before this wait is polled.)
         const int j = (int)i - C::kStages;
-        if (j < 0 || mbar_wait(b_dqfull(j % NB), (j / NB) & 1, abort_flag, a.status)) {
+        if (j < 0 || mbar_wait(b_empty(j % C::kStages), (j / C::kStages) & 1, abort_flag, a.status)) {
           mbar_expect_tx(b_full(st), 2 * C::kQBytes);
           for (int c = 0; c < C::kBoxes; ++c) {
             tma_load_4d(sQs(st) + c * C::kQBox, &tmQ, c * 64, seq.q0 + v * BM, h0 + gi, seq.bb, b_full(st));
@@ -295,11 +314,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------------ MMA issuers
     // Two issuing threads, one per dependency chain: a thread issuing tcgen05 MMAs blocks while
     // the tensor core's queue is full, so one issuer could not react to the other chain.
-    //   warp 1: S^T/dP^T of step sn into buffer sn % NB, once its Q/dO tile has landed. d = 128:
-    //           S^T once dV of step sn - NB has read P^T (the s_free commit), dP^T once that
-    //           step's dQ^T, accumulated over the dP^T columns after dK read dS^T there, has been
-    //           read out. d = 64 (one buffer, dQ in its own columns): both once every MMA of step
-    //           sn - 1 has completed and dQ is read out;
+    //   warp 1: S^T/dP^T of step sn into buffer sn % NB, once its Q/dO tile has landed: S^T once
+    //           dV of step sn - NB has read P^T (the s_free commit), dP^T once that step's dQ^T,
+    //           accumulated over the dP^T columns after dK read dS^T there, has been read out;
     //   warp 2: dV, dK and dQ of step g, once P^T/dS^T of step g are in place (which follows the
     //           completion of step g's S^T/dP^T).
     // Descriptors of the resident K and V tiles, advanced by constant byte offsets per k-step.
@@ -317,11 +334,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int sn = 0; sn < n; ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
             mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
-            if (sn >= NB) {
-              if constexpr (C::kDqT)  // dV of step sn - NB has read P^T from these columns
-                mbar_wait_spin(b_sfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
-              else  // (one buffer) every MMA of step sn - 1 has completed and dQ is read out
-                mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+            if (sn >= NB) {  // dV of step sn - NB has read P^T from these columns
+              mbar_wait_spin(b_sfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
             }
             const uint64_t dq = desc_kmajor_sw128(sQs(st)), ddo = desc_kmajor_sw128(sdOs(st));
@@ -330,7 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
               mma_ss(tmem + tS(buf), desc_add(dK0, okk), desc_add(dq, oq), C::kIdS, kk > 0);
             }
-            if (C::kDqT && sn >= NB) {  // dQ^T of step sn - NB has been read out of these columns
+            if (sn >= NB) {  // dQ^T of step sn - NB has been read out of these columns
               mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
             }
@@ -345,7 +359,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int g = 0; g < n; ++g) {
             const int st = g % C::kStages, buf = g % NB;
             mbar_wait_spin(b_pready(buf), (g / NB) & 1, abort_flag, a.status);
-            if (!C::kDqT && g > 0) mbar_wait_spin(b_dqfree(0), (g - 1) & 1, abort_flag, a.status);  // dQ read out
             fence_after_sync();
             const uint64_t mq = desc_mnmajor_sw128(sQs(st), C::kQBox), mdo = desc_mnmajor_sw128(sdOs(st), C::kQBox);
             const uint64_t mds = desc_mnmajor_sw128(sDs(buf), 16384);
@@ -353,20 +366,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int kk = 0; kk < BM / 16; ++kk)
               mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_add(mdo, kk * 2048), C::kIdG,
                      (g > 0 || kk > 0) ? 1u : 0u);
-            if (C::kDqT) mma_commit(b_sfree(buf));  // P^T read: the S^T columns are free
+            mma_commit(b_sfree(buf));  // P^T read: the S^T columns are free
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
               mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_add(mq, kk * 2048), C::kIdG,
                      (g > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(b_empty(st));  // dV and dK have read the step's Q/dO stage
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              if constexpr (C::kDqT) {
-                mma_ss(tmem + tdQ(buf), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
-              } else {
-                mma_ss(tmem + tdQ(buf), desc_add(mds, kk * 2048), desc_add(mK0, kk * 2048), C::kIdQ, kk > 0);
-              }
-            }
-            mma_commit(b_dqfull(buf));  // also frees the step's Q/dO stage for the producer
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + tdQ(buf), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
+            mma_commit(b_dqfull(buf));
           }
           mma_commit(b_done);  // the last gradient MMAs complete after every S^T/dP^T
         }
@@ -395,22 +404,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         dv = ok ? a.dvec[row] : 0.f;
       };
       float next_l, next_d;
-      fetch(0, next_v(0), next_l, next_d);
-      for (int gi = 0, v = next_v(0); gi < G && v < nv; ++it) {
+      fetch(0, next_v_warp(0), next_l, next_d);
+      for (int gi = 0, v = next_v_warp(0); gi < G && v < nv; ++it) {
         const int q0 = v * BM;
         const int buf = it % NB;
         float* lrow = lse_row<D>(ctl, buf);
         float* drow = dvec_row<D>(ctl, buf);
         // With two row buffers, every thread finished reading this one (step it - 2) before the
-        // barrier of step it - 1; with one, a barrier must separate the last reads from the writes.
-        if (NB == 1) named_bar_sync(1, 128);
+        // barrier of step it - 1, so only one barrier per step is needed.
+        static_assert(NB == 2, "row buffers");
         if (r < BM) {
           lrow[r] = next_l * kLog2e;
           drow[r] = next_d;
         }
         named_bar_sync(1, 128);  // the rows are written before anyone reads them
         int gn = gi, vn = v;
-        advance(gn, vn);
+        advance_warp(gn, vn);
         fetch(gn, vn, next_l, next_d);
         mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // on the critical path
         fence_after_sync();
@@ -475,52 +484,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     } else {
       // ---------------------------------------------------------------- dQ into the accumulator
-      for (int gi = 0, v = next_v(0); gi < G && v < nv; advance(gi, v), ++it) {
+      for (int gi = 0, v = next_v_warp(0); gi < G && v < nv; advance_warp(gi, v), ++it) {
         const int q0 = v * BM;
         const int buf = it % NB;
         float* dQa = a.dqacc + row_base(s, seq, b, h0 + gi) * D;
         mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
         fence_after_sync();
         const uint32_t tq = tmem + lane_off + tdQ(buf);
-        if constexpr (C::kDqT) {
-          // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
-          // unused rows of the d = 64 product).
-          uint32_t vals[BM];
+        // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
+        // unused rows of the d = 64 product).
+        uint32_t vals[BM];
 #pragma unroll
-          for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
-          tmem_ld_wait();
-          fence_before_sync();
-          mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
-          if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
-          named_bar_sync(2, 128);
-          if (r < D) {
+        for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
+        tmem_ld_wait();
+        fence_before_sync();
+        mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
+        if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
+        named_bar_sync(2, 128);
+        if (r < D) {
 #pragma unroll
-            for (int qq = 0; qq < BM; ++qq)
-              asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(2, 128);
-          if (threadIdx.x == 256 && !*abort_flag) {
-            const int rows = min(BM, seq.Lq - q0);
-            bulk_reduce_add_f32(dQa + (size_t)q0 * D, sDq, (uint32_t)(rows * D * 4));
-            tma_store_commit();
-          }
-        } else {
-          // dQ: lane r = query row of the step, 64 head-dimension columns.
-          uint32_t vals[D];
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
-          tmem_ld_wait();
-          fence_before_sync();
-          mbar_arrive(b_dqfree(0));
-          const int q = q0 + r;
-          if (q < seq.Lq) {
-#pragma unroll
-            for (int t = 0; t < D; t += 4)
-              atomicAdd(reinterpret_cast<float4*>(dQa + (size_t)q * D + t),
-                        make_float4(__uint_as_float(vals[t]), __uint_as_float(vals[t + 1]),
-                                    __uint_as_float(vals[t + 2]), __uint_as_float(vals[t + 3])));
-          }
+          for (int qq = 0; qq < BM; ++qq)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (threadIdx.x == 256 && !*abort_flag) {
+          const int rows = min(BM, seq.Lq - q0);
+          bulk_reduce_add_f32(dQa + (size_t)q0 * D, sDq, (uint32_t)(rows * D * 4));
+          tma_store_commit();
         }
       }
       if (threadIdx.x == 256) tma_store_wait_read0();  // the staging is read before the CTA exits

@@ -92,7 +92,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   dev_status, stream: as for fa_fwd
  * Launches, in order on `stream`: a pre-pass (D = rowsum(dO * O), dQ accumulator cleared), the main
  * pass (one CTA per key tile, looping over the query tiles it is visible to) and a post-pass
- * (dQ fp32 -> bf16). dQ is accumulated with fp32 atomics, so its bits may differ between runs by
+ * (dQ fp32 -> bf16). dQ is accumulated with fp32 reduce-adds, so its bits may differ between runs by
  * the order of additions; dK, dV, O and LSE are run-to-run identical.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
