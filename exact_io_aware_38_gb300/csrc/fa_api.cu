@@ -105,9 +105,11 @@ int take_strides(const fa_strides& in, bool packed, int B, int rows, int heads, 
 
 size_t per_row(const fa::AttnShape& s) { return s.cu_q != nullptr ? (size_t)s.H * s.rows_q : (size_t)s.B * s.H * s.Nq; }
 
+// Backward workspace: D, the fp32 dQ accumulator, then one aligned block holding the main kernel's
+// key-tile counter.
 size_t workspace_for(const fa::AttnShape& s) {
   const size_t rows = per_row(s);
-  return round_up(rows * sizeof(float)) + round_up(rows * s.d * sizeof(float));
+  return round_up(rows * sizeof(float)) + round_up(rows * s.d * sizeof(float)) + kAlign;
 }
 
 int launch_fwd(const fa::AttnShape& s, const void* q, FaStrides sq, const void* k, FaStrides sk, const void* v,
@@ -182,6 +184,8 @@ int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* w
   const size_t rows = per_row(s);
   a.dvec = static_cast<float*>(workspace);
   a.dqacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * sizeof(float)));
+  a.tile_counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + round_up(rows * sizeof(float)) +
+                                          round_up(rows * s.d * sizeof(float)));
   a.s = s;
   a.scale = scale;
   a.status = dev_status;

@@ -1,9 +1,11 @@
 // Backward attention on the 5th-generation tensor cores (sm_103a).
 //
 // Three launches on the caller's stream:
-//   pre   D_i = sum_k dO_ik O_ik (fp32, from the stored bf16 O) and a cleared fp32 dQ accumulator;
-//   main  one CTA per (128-key tile j, K/V head): K_j and V_j stay in shared memory while the
-//         query rows that can see them stream through a TMA ring, 64 rows per step. The score tile
+//   pre   D_i = sum_k dO_ik O_ik (fp32, from the stored bf16 O), a cleared fp32 dQ accumulator and
+//         a cleared key-tile counter;
+//   main  persistent, one CTA per SM, taking (128-key tile j, K/V head) pairs from the counter,
+//         heavy tiles first: K_j and V_j stay in shared memory while the query rows that can see
+//         them stream through a TMA ring, 64 rows per step. The score tile
 //         is recomputed from Q, K and the saved log-sum-exp instead of being stored
 //         ("FlashAttention." plate, "Never write the scores"), and the softmax gradient is applied
 //         tile by tile:
@@ -11,7 +13,9 @@
 //           P^T = exp(c S^T - LSE_i),  dS^T = P^T * (dP^T - D_i)  (one thread per key row)
 //           dV_j += P^T dO_i,  dK_j += dS^T Q_i                  (A operand from tensor memory)
 //           dQ_i^T = K_j^T dS_i^T                                (added into the fp32 accumulator)
-//         dK_j = c * acc and dV_j leave through shared memory and TMA stores.
+//         dK_j = c * acc and dV_j are read out of tensor memory and stored from registers while
+//         the next tile's K, V and first Q/dO steps load; the ring and the step counters run on
+//         across tiles, so only the next tile's first gradient products wait for that read-out.
 //   post  dQ = bf16(c * accumulator).
 // dQ_i is formed transposed (tensor-memory lane = head dimension; at d = 64 the product keeps
 // M = 128 and its upper rows are unused), staged row-major in shared memory and added into the
@@ -63,7 +67,6 @@ struct BwdCfg {
   static constexpr uint32_t kIdG = idesc_bf16(128, D, false, true);
   static constexpr uint32_t kIdQ = idesc_bf16(128, BM, true, true);
   static_assert(kSmem <= 232448 - 1536, "shared memory budget");
-  static_assert(2 * kKVBytes <= kStages * 2 * kQBytes, "dK and dV staging reuse the Q/dO ring");
   static_assert(kStages <= 4 && kBufs <= 4, "barrier arrays of the control block");
 };
 
@@ -74,9 +77,12 @@ struct alignas(16) BwdSmemCtl {
   uint64_t kv_full;
   uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t s_full[kMaxBufs], p_ready[kMaxBufs], dq_full[kMaxBufs], dq_free[kMaxBufs], s_free[kMaxBufs];
-  uint64_t done, drain;
+  uint64_t done, acc_free, drain;
+  uint64_t tq_full[2], tq_empty[2];  // key-tile queue
   uint32_t tmem_base;
   int abort_flag;
+  int tile_q[2];      // key-tile queue slots
+  int tile_bc[2][2];  // the tile index shared within each warpgroup, two slots each
   alignas(16) float lse2[128];  // LSE * log2(e) per query of the step: [buffer][BM]
   alignas(16) float dvec[128];  // D per query of the step: [buffer][BM]
 };
@@ -100,6 +106,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
   const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
   const __nv_bfloat16* O = reinterpret_cast<const __nv_bfloat16*>(a.o);
   const __nv_bfloat16* dO = reinterpret_cast<const __nv_bfloat16*>(a.dout);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.tile_counter = 0;  // the main kernel's key-tile counter
   for (size_t r = warp0; r < rows; r += nwarps) {
     int b, row, h;
     row_coords(a.s, r, b, row, h);
@@ -153,11 +160,74 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const FaBwdArgs a) {
   }
 }
 
+// One key tile of the persistent backward kernel: the (key tile, K/V head) pair whose dK, dV it
+// owns and the query steps that can see it. Every role derives the same values from the tile index.
+struct BwdTile {
+  int kt, b, hk, h0;
+  SeqInfo seq;
+  int nv;    // 64-row query steps of the sequence
+  int v_lo;  // first candidate step (the key tile's diagonal step with the causal mask)
+  bool live;  // the key tile has rows in this sequence (packed sequences end early)
+};
+
+__device__ __forceinline__ BwdTile bwd_tile(const AttnShape& s, int tile, int BM) {
+  BwdTile t;
+  const int BHkv = s.B * s.Hkv;
+  t.kt = tile / BHkv;  // key tile: small kt (most causal work) first
+  const int bkv = tile % BHkv;
+  t.b = bkv / s.Hkv;
+  t.hk = bkv % s.Hkv;
+  t.h0 = t.hk * (s.H / s.Hkv);  // the group's first query head
+  t.seq = seq_info(s, t.b);
+  t.live = t.kt * 128 < t.seq.krows;
+  t.nv = (t.seq.Lq + BM - 1) / BM;
+  // No step is visited when the key tile lies past the key length; with the causal mask the first
+  // candidate is the key tile's own diagonal step. Scans start there.
+  t.v_lo = t.kt * 128 >= t.seq.Lk ? t.nv : (s.causal ? max(t.kt * 128 - t.seq.off, 0) / BM : 0);
+  return t;
+}
+
+// Query steps v (rows v*BM ..) are visited iff their 128-row tile is visited for the key tile. The
+// pattern is the same for every query head of the group; a step is a (group head gi, v) pair, heads
+// outer, so dK and dV sum over the group in tensor memory. Without a block mask every step from
+// v_lo on is visited (tile_visited in closed form). The next visited step is found by a whole warp
+// with the same v, 32 candidates per block-mask probe (a serial scan would put one dependent load
+// per skipped step on the path of the thread that waits on it).
+__device__ __forceinline__ int bwd_next_v_warp(const AttnShape& s, const BwdTile& t, int v, int BM) {
+  v = v < t.v_lo ? t.v_lo : v;
+  if (s.block_mask == nullptr) return v < t.nv ? v : t.nv;
+  const int lane_id = threadIdx.x & 31;
+  for (; v < t.nv; v += 32) {
+    const int c = v + lane_id;
+    const unsigned hit = __ballot_sync(0xffffffffu, c < t.nv && tile_visited(s, t.seq, (c * BM) / 128, t.kt));
+    if (hit) return v + __ffs(hit) - 1;
+  }
+  return t.nv;
+}
+
+// Visited steps of the tile for one query head, counted by a whole warp: every step from v_lo on
+// without a block mask; with one, eight block-mask loads per lane are in flight before the votes.
+__device__ __forceinline__ int bwd_count_steps(const AttnShape& s, const BwdTile& t, int BM) {
+  if (s.block_mask == nullptr) return t.nv > t.v_lo ? t.nv - t.v_lo : 0;
+  const int lane_id = threadIdx.x & 31;
+  int n = 0;
+  for (int v0 = t.v_lo; v0 < t.nv; v0 += 8 * 32) {
+    bool hit[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int v = v0 + u * 32 + lane_id;
+      hit[u] = v < t.nv && tile_visited(s, t.seq, (v * BM) / 128, t.kt);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) n += __popc(__ballot_sync(0xffffffffu, hit[u]));
+  }
+  return n;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                   const FaBwdArgs a) {
   using C = BwdCfg<D>;
   constexpr int BM = C::BM;
@@ -171,78 +241,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sDs0 = sStage0 + C::kStages * 2 * C::kQBytes;
   const uint32_t sDq = sDs0 + NB * C::kDsBytes;
   volatile int* abort_flag = &ctl.abort_flag;
+  volatile int* tile_q = ctl.tile_q;
 
   const AttnShape& s = a.s;
-  const int BHkv = s.B * s.Hkv;
-  const int kt = blockIdx.x / BHkv;  // key tile: small kt (most causal work) first
-  const int bkv = blockIdx.x % BHkv;  // K/V head (b, hk) whose dK, dV this CTA owns
-  const int b = bkv / s.Hkv, hk = bkv % s.Hkv;
-  const int G = s.H / s.Hkv;  // query heads sharing this K/V head
-  const int h0 = hk * G;      // the group's first query head
-  const SeqInfo seq = seq_info(s, b);
-  if (kt * 128 >= seq.krows) return;  // no such key rows in this (packed) sequence
+  const int G = s.H / s.Hkv;  // query heads sharing a K/V head
+  const int ntiles = s.nbk * s.B * s.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nv = (seq.Lq + BM - 1) / BM;  // BM-row query steps
 
-  // Query steps v (rows v*BM ..) are visited iff their 128-row tile is visited for this key tile.
-  // The pattern is the same for every query head of the group; a step is a (group head gi, v)
-  // pair, heads outer, so dK and dV sum over the group in tensor memory.
-  // No step is visited when the key tile lies past the key length; with the causal mask the first
-  // candidate is the key tile's own diagonal step. Scans start there.
-  const int v_lo = kt * 128 >= seq.Lk ? nv : (s.causal ? max(kt * 128 - seq.off, 0) / BM : 0);
-  // Without a block mask every step from v_lo on is visited (tile_visited in closed form).
-  auto next_v = [&](int v) -> int {
-    v = v < v_lo ? v_lo : v;
-    if (s.block_mask == nullptr) return v < nv ? v : nv;
-    for (; v < nv; ++v)
-      if (tile_visited(s, seq, (v * BM) / 128, kt)) return v;
-    return nv;
-  };
-  auto advance = [&](int& gi, int& v) {
-    v = next_v(v + 1);
-    if (v >= nv) {
-      ++gi;
-      v = next_v(0);
-    }
-  };
-  // The same scan for a whole warp with the same v (the elementwise and dQ warps, where it sits on
-  // the per-step critical path): 32 candidates per block-mask probe.
-  auto next_v_warp = [&](int v) -> int {
-    v = v < v_lo ? v_lo : v;
-    if (s.block_mask == nullptr) return v < nv ? v : nv;
-    const int lane_id = threadIdx.x & 31;
-    for (; v < nv; v += 32) {
-      const int c = v + lane_id;
-      const unsigned hit = __ballot_sync(0xffffffffu, c < nv && tile_visited(s, seq, (c * BM) / 128, kt));
-      if (hit) return v + __ffs(hit) - 1;
-    }
-    return nv;
-  };
-  auto advance_warp = [&](int& gi, int& v) {
-    v = next_v_warp(v + 1);
-    if (v >= nv) {
-      ++gi;
-      v = next_v_warp(0);
-    }
-  };
   auto sQs = [&](int st) { return sStage0 + (2 * st) * C::kQBytes; };
   auto sdOs = [&](int st) { return sStage0 + (2 * st + 1) * C::kQBytes; };
   auto sDs = [&](int buf) { return sDs0 + buf * C::kDsBytes; };
   auto tS = [&](int buf) { return C::kTS0 + buf * 2 * BM; };
   auto tdP = [&](int buf) { return C::kTS0 + buf * 2 * BM + BM; };
-  // d = 128: dQ^T of a step accumulates over its buffer's dP^T columns (free once dK has read
-  // dS^T there), so the next S^T into the buffer waits only for dV's read of P^T.
+  // dQ^T of a step accumulates over its buffer's dP^T columns (free once dK has read dS^T there),
+  // so the next S^T into the buffer waits only for dV's read of P^T.
   auto tdQ = [&](int buf) { return tdP(buf); };
 
   const uint32_t b_kv = smem_u32(&ctl.kv_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
+  auto b_empty = [&](int i) { return smem_u32(&ctl.empty[i]); };
   auto b_sfull = [&](int i) { return smem_u32(&ctl.s_full[i]); };
   auto b_pready = [&](int i) { return smem_u32(&ctl.p_ready[i]); };
-  auto b_empty = [&](int i) { return smem_u32(&ctl.empty[i]); };
   auto b_dqfull = [&](int i) { return smem_u32(&ctl.dq_full[i]); };
   auto b_dqfree = [&](int i) { return smem_u32(&ctl.dq_free[i]); };
   auto b_sfree = [&](int i) { return smem_u32(&ctl.s_free[i]); };
-  const uint32_t b_done = smem_u32(&ctl.done), b_drain = smem_u32(&ctl.drain);
+  auto b_tqfull = [&](int i) { return smem_u32(&ctl.tq_full[i]); };
+  auto b_tqempty = [&](int i) { return smem_u32(&ctl.tq_empty[i]); };
+  const uint32_t b_done = smem_u32(&ctl.done), b_accfree = smem_u32(&ctl.acc_free), b_drain = smem_u32(&ctl.drain);
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
@@ -258,8 +283,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_dqfree(i), 128);
       mbar_init(b_sfree(i), 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_tqfull(i), 1);
+      mbar_init(b_tqempty(i), 4);  // the two issuers and the leaders of the two warpgroups
+    }
     mbar_init(b_done, 1);
-    mbar_init(b_drain, 2);  // one commit per MMA issuer
+    mbar_init(b_accfree, 256);  // every thread of the two warpgroups, after reading dK or dV
+    mbar_init(b_drain, 2);      // one commit per MMA issuer
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -270,45 +300,98 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
-  const bool any_work = next_v(0) < nv;
+
+  // Key tiles come from a counter shared by all CTAs (the first one is the CTA's own index), in
+  // the heavy-first order of the tile index. The producer takes each one and publishes it through
+  // a two-slot queue; every other role reads the same sequence from there. Item w's phase of a
+  // slot's full barrier cannot be confused with item w + 2's: that one is published only after all
+  // four readers of item w have arrived on the slot's empty barrier.
+  auto take_tile = [&](int w) -> int {  // one reader thread per role
+    int tile = ntiles;  // an abandoned wait ends the loop
+    if (mbar_wait(b_tqfull(w & 1), (w >> 1) & 1, abort_flag, a.status)) tile = tile_q[w & 1];
+    mbar_arrive(b_tqempty(w & 1));
+    return tile;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0 && any_work) {
+    // Lane 0 takes the tiles, waits and issues the copies; with a block mask the whole warp walks
+    // the steps with it (the mask is scanned 32 candidates per load).
+    const bool walk = lane == 0 || s.block_mask != nullptr;
+    if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmdO);
-      mbar_expect_tx(b_kv, 2 * C::kKVBytes);
-      for (int c = 0; c < C::kBoxes; ++c) {
-        tma_load_4d(sK + c * 16384, &tmK, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_kv);
-        tma_load_4d(sV + c * 16384, &tmV, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_kv);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+    }
+    uint32_t last_par[kMaxStages];
+    bool issued[kMaxStages] = {};
+    bool kv_any = false;
+    uint32_t kv_par = 0;
+    uint32_t i = 0;  // Q/dO ring position, continued across key tiles
+    int wt = 0;      // key tiles with work so far
+    for (int w = 0;; ++w) {
+      int tile = ntiles;
+      if (lane == 0 && (w < 2 || mbar_wait(b_tqempty(w & 1), ((w - 2) >> 1) & 1, abort_flag, a.status))) {
+        tile = w == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.tile_counter, 1);
+        tile_q[w & 1] = tile;
+        mbar_arrive(b_tqfull(w & 1));  // release: the index is visible to every waiter of the phase
       }
-      uint32_t last_par[kMaxStages];
-      bool issued[kMaxStages] = {};
-      uint32_t i = 0;
-      for (int gi = 0, v = next_v(0); gi < G && v < nv; advance(gi, v), ++i) {
-        const int st = i % C::kStages;
-        const uint32_t par = (i / C::kStages) & 1;
-        // The stage is free once dV and dK of step j = i - kStages have read it (its S^T/dP^T
-        // finished before them), which the gradient issuer commits to the stage's own barrier. One
-        // barrier per stage keeps the parity test unambiguous: its next phase belongs to step i, not
-        // loaded yet. (The NB-deep dq_full barriers would not: their next phase after j is step
-        // j + NB < i, which can complete before this wait is polled.)
-        const int j = (int)i - C::kStages;
-        if (j < 0 || mbar_wait(b_empty(j % C::kStages), (j / C::kStages) & 1, abort_flag, a.status)) {
-          mbar_expect_tx(b_full(st), 2 * C::kQBytes);
-          for (int c = 0; c < C::kBoxes; ++c) {
-            tma_load_4d(sQs(st) + c * C::kQBox, &tmQ, c * 64, seq.q0 + v * BM, h0 + gi, seq.bb, b_full(st));
-            tma_load_4d(sdOs(st) + c * C::kQBox, &tmdO, c * 64, seq.q0 + v * BM, h0 + gi, seq.bb, b_full(st));
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (tile >= ntiles) break;
+      const BwdTile T = bwd_tile(s, tile, BM);
+      const int v_first = T.live ? bwd_next_v_warp(s, T, 0, BM) : T.nv;
+      if (v_first >= T.nv) continue;
+      // K and V of this tile overwrite the previous tile's once all its MMAs have completed (its
+      // done commit); the first two Q/dO steps are requested before that wait, since their stages
+      // are released earlier.
+      bool kv_issued = false;
+      auto issue_kv = [&]() {  // lane 0
+        kv_issued = true;
+        if (wt > 0 && !mbar_wait(b_done, (wt - 1) & 1, abort_flag, a.status)) return;
+        mbar_expect_tx(b_kv, 2 * C::kKVBytes);
+        for (int c = 0; c < C::kBoxes; ++c) {
+          tma_load_4d(sK + c * 16384, &tmK, c * 64, T.seq.k0 + T.kt * 128, T.hk, T.seq.bb, b_kv);
+          tma_load_4d(sV + c * 16384, &tmV, c * 64, T.seq.k0 + T.kt * 128, T.hk, T.seq.bb, b_kv);
+        }
+        kv_any = true;
+        kv_par = wt & 1;
+      };
+      if (lane == 0 && wt == 0) issue_kv();
+      int l = 0;
+      for (int gi = 0, v = v_first; walk && gi < G && v < T.nv; ++i, ++l) {
+        if (lane == 0) {
+          if (l == 2 && !kv_issued) issue_kv();
+          const int st = i % C::kStages;
+          const uint32_t par = (i / C::kStages) & 1;
+          // The stage is free once dV and dK of step j = i - kStages have read it (its S^T/dP^T
+          // finished before them), which the gradient issuer commits to the stage's own barrier.
+          // One barrier per stage keeps the parity test unambiguous: its next phase belongs to
+          // step i, not loaded yet.
+          const int j = (int)i - C::kStages;
+          if (j < 0 || mbar_wait(b_empty(j % C::kStages), (j / C::kStages) & 1, abort_flag, a.status)) {
+            mbar_expect_tx(b_full(st), 2 * C::kQBytes);
+            for (int c = 0; c < C::kBoxes; ++c) {
+              tma_load_4d(sQs(st) + c * C::kQBox, &tmQ, c * 64, T.seq.q0 + v * BM, T.h0 + gi, T.seq.bb, b_full(st));
+              tma_load_4d(sdOs(st) + c * C::kQBox, &tmdO, c * 64, T.seq.q0 + v * BM, T.h0 + gi, T.seq.bb, b_full(st));
+            }
+            issued[st] = true;
+            last_par[st] = par;
           }
-          issued[st] = true;
-          last_par[st] = par;
+        }
+        v = bwd_next_v_warp(s, T, v + 1, BM);
+        if (v >= T.nv) {
+          ++gi;
+          v = v_first;
         }
       }
-      if (*abort_flag) {  // let copies still in flight land before the CTA exits
-        mbar_wait_drain(b_kv, 0);
-        for (int k = 0; k < C::kStages; ++k)
-          if (issued[k]) mbar_wait_drain(b_full(k), last_par[k]);
-      }
+      if (lane == 0 && !kv_issued) issue_kv();
+      ++wt;
+    }
+    if (lane == 0 && *abort_flag) {  // let copies still in flight land before the CTA exits
+      if (kv_any) mbar_wait_drain(b_kv, kv_par);
+      for (int k = 0; k < C::kStages; ++k)
+        if (issued[k]) mbar_wait_drain(b_full(k), last_par[k]);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------------ MMA issuers
@@ -318,20 +401,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //           dV of step sn - NB has read P^T (the s_free commit), dP^T once that step's dQ^T,
     //           accumulated over the dP^T columns after dK read dS^T there, has been read out;
     //   warp 2: dV, dK and dQ of step g, once P^T/dS^T of step g are in place (which follows the
-    //           completion of step g's S^T/dP^T).
+    //           completion of step g's S^T/dP^T); a tile's first dV and dK (which overwrite the
+    //           accumulators) once the previous tile's dK and dV have been read out.
+    // Step counters run on across key tiles, so the ring and the buffers never drain between them.
     // Descriptors of the resident K and V tiles, advanced by constant byte offsets per k-step.
     const uint64_t dK0 = desc_kmajor_sw128(sK), dV0 = desc_kmajor_sw128(sV), mK0 = desc_mnmajor_sw128(sK, 16384);
-    int n = 0;  // visited steps, counted by the whole warp
-    for (int v0 = v_lo; v0 < nv; v0 += 32) {
-      const int v = v0 + lane;
-      n += __popc(__ballot_sync(0xffffffffu, v < nv && tile_visited(s, seq, (v * BM) / 128, kt)));
-    }
-    n *= G;
-    if (lane == 0) {
-      if (any_work) {
-        mbar_wait_spin(b_kv, 0, abort_flag, a.status);
+    uint32_t sn = 0;  // global step counter (lane 0)
+    int wt = 0;
+    for (int w = 0;; ++w) {
+      int tile = 0;
+      if (lane == 0) tile = take_tile(w);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (tile >= ntiles) break;
+      const BwdTile T = bwd_tile(s, tile, BM);
+      if (!T.live) continue;
+      const int n = bwd_count_steps(s, T, BM) * G;
+      if (n == 0) continue;
+      if (lane == 0) {
         if (warp == 1) {
-          for (int sn = 0; sn < n; ++sn) {
+          mbar_wait_spin(b_kv, wt & 1, abort_flag, a.status);
+          fence_after_sync();
+          for (int l = 0; l < n; ++l, ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
             mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
             if (sn >= NB) {  // dV of step sn - NB has read P^T from these columns
@@ -356,30 +446,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(b_sfull(buf));
           }
         } else {
-          for (int g = 0; g < n; ++g) {
-            const int st = g % C::kStages, buf = g % NB;
-            mbar_wait_spin(b_pready(buf), (g / NB) & 1, abort_flag, a.status);
+          if (wt > 0) {  // the previous tile's dK and dV have left tensor memory
+            mbar_wait_spin(b_accfree, (wt - 1) & 1, abort_flag, a.status);
+            fence_after_sync();
+          }
+          for (int l = 0; l < n; ++l, ++sn) {
+            const int st = sn % C::kStages, buf = sn % NB;
+            mbar_wait_spin(b_pready(buf), (sn / NB) & 1, abort_flag, a.status);
             fence_after_sync();
             const uint64_t mq = desc_mnmajor_sw128(sQs(st), C::kQBox), mdo = desc_mnmajor_sw128(sdOs(st), C::kQBox);
             const uint64_t mds = desc_mnmajor_sw128(sDs(buf), 16384);
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
               mma_ts(tmem + C::kTdV, tmem + tS(buf) + kk * 8, desc_add(mdo, kk * 2048), C::kIdG,
-                     (g > 0 || kk > 0) ? 1u : 0u);
+                     (l > 0 || kk > 0) ? 1u : 0u);
             mma_commit(b_sfree(buf));  // P^T read: the S^T columns are free
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
               mma_ts(tmem + C::kTdK, tmem + tdP(buf) + kk * 8, desc_add(mq, kk * 2048), C::kIdG,
-                     (g > 0 || kk > 0) ? 1u : 0u);
+                     (l > 0 || kk > 0) ? 1u : 0u);
             mma_commit(b_empty(st));  // dV and dK have read the step's Q/dO stage
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               mma_ss(tmem + tdQ(buf), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
             mma_commit(b_dqfull(buf));
           }
-          mma_commit(b_done);  // the last gradient MMAs complete after every S^T/dP^T
+          mma_commit(b_done);  // the tile's last MMAs complete after every S^T/dP^T of it
         }
       }
+      ++wt;
+    }
+    if (lane == 0) {
       mma_commit(b_drain);
       mbar_wait_drain(b_drain, 0);
     }
@@ -388,188 +485,200 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = quad * 32 + lane;  // tensor-memory lane: key row (and head dimension of dQ^T)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const bool elementwise = warp < 8;
-    uint32_t it = 0;
-    if (elementwise) {
-      // ---------------------------------------------------------------- P^T and dS^T
-      const int key = kt * 128 + r;
-      const bool key_ok = key < seq.Lk;
-      const float sl2 = a.scale * kLog2e;
-      // LSE and D of a step are loaded one step ahead and consumed only when they are stored for
-      // the next step, so the load latency overlaps a whole step.
-      auto fetch = [&](int gi, int v, float& lv, float& dv) {
-        const int q = v * BM + r;
-        const bool ok = gi < G && v < nv && r < BM && q < seq.Lq;
-        const size_t row = row_base(s, seq, b, h0 + gi) + q;
-        lv = ok ? a.lse[row] : 0.f;
-        dv = ok ? a.dvec[row] : 0.f;
-      };
-      float next_l, next_d;
-      fetch(0, next_v_warp(0), next_l, next_d);
-      for (int gi = 0, v = next_v_warp(0); gi < G && v < nv; ++it) {
-        const int q0 = v * BM;
-        const int buf = it % NB;
-        float* lrow = lse_row<D>(ctl, buf);
-        float* drow = dvec_row<D>(ctl, buf);
-        // With two row buffers, every thread finished reading this one (step it - 2) before the
-        // barrier of step it - 1, so only one barrier per step is needed.
-        static_assert(NB == 2, "row buffers");
-        if (r < BM) {
-          lrow[r] = next_l * kLog2e;
-          drow[r] = next_d;
-        }
-        named_bar_sync(1, 128);  // the rows are written before anyone reads them
-        int gn = gi, vn = v;
-        advance_warp(gn, vn);
-        fetch(gn, vn, next_l, next_d);
-        mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // on the critical path
-        fence_after_sync();
-        const bool need_mask =
-            (s.causal && kt * 128 + 127 > q0 + seq.off) || (kt * 128 + 128 > seq.Lk) || (q0 + BM > seq.Lq);
-        const uint32_t ts = tmem + lane_off + tS(buf), tdp = tmem + lane_off + tdP(buf);
-        // P^T, dS^T for the step's BM queries, 32 at a time; the mask is resolved per step so the
-        // unmasked body has no branches.
-        auto step = [&](auto mask_tag) {
-          constexpr bool MASK = decltype(mask_tag)::value;
+    const int grp_bar = elementwise ? 1 : 2;             // the warpgroup's named barrier
+    const int leader = elementwise ? 128 : 256;          // its reader of the tile queue
+    volatile int* tile_bc = ctl.tile_bc[elementwise ? 0 : 1];
+    const float sl2 = a.scale * kLog2e;
+    uint32_t it = 0;  // global step counter
+    int wt = 0;
+    for (int w = 0;; ++w) {
+      // The warpgroup agrees on the tile: its leader reads the queue and shares the index (two
+      // slots, so a slot is rewritten only after the next iteration's barrier).
+      if (threadIdx.x == leader) tile_bc[w & 1] = take_tile(w);
+      named_bar_sync(grp_bar, 128);
+      const int tile = tile_bc[w & 1];
+      if (tile >= ntiles) break;
+      const BwdTile T = bwd_tile(s, tile, BM);
+      if (!T.live) continue;
+      const SeqInfo& seq = T.seq;
+      const int kt = T.kt;
+      const int v_first = bwd_next_v_warp(s, T, 0, BM);
+      const bool any_work = v_first < T.nv;
+      if (elementwise) {
+        // -------------------------------------------------------------- P^T and dS^T
+        const int key = kt * 128 + r;
+        const bool key_ok = key < seq.Lk;
+        // LSE and D of a step are loaded one step ahead and consumed only when they are stored
+        // for the next step, so the load latency overlaps a whole step.
+        auto fetch = [&](int gi, int v, float& lv, float& dv) {
+          const int q = v * BM + r;
+          const bool ok = gi < G && v < T.nv && r < BM && q < seq.Lq;
+          const size_t row = row_base(s, seq, T.b, T.h0 + gi) + q;
+          lv = ok ? a.lse[row] : 0.f;
+          dv = ok ? a.dvec[row] : 0.f;
+        };
+        float next_l, next_d;
+        fetch(0, v_first, next_l, next_d);
+        for (int gi = 0, v = v_first; gi < G && v < T.nv; ++it) {
+          const int q0 = v * BM;
+          const int buf = it % NB;
+          float* lrow = lse_row<D>(ctl, buf);
+          float* drow = dvec_row<D>(ctl, buf);
+          // With two row buffers, every thread finished reading this one (step it - 2) before the
+          // barrier of step it - 1, so only one barrier per step is needed.
+          static_assert(NB == 2, "row buffers");
+          if (r < BM) {
+            lrow[r] = next_l * kLog2e;
+            drow[r] = next_d;
+          }
+          named_bar_sync(1, 128);  // the rows are written before anyone reads them
+          int gn = gi, vn = bwd_next_v_warp(s, T, v + 1, BM);
+          if (vn >= T.nv) {
+            ++gn;
+            vn = v_first;
+          }
+          fetch(gn, vn, next_l, next_d);
+          mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // on the critical path
+          fence_after_sync();
+          const bool need_mask =
+              (s.causal && kt * 128 + 127 > q0 + seq.off) || (kt * 128 + 128 > seq.Lk) || (q0 + BM > seq.Lq);
+          const uint32_t ts = tmem + lane_off + tS(buf), tdp = tmem + lane_off + tdP(buf);
+          // P^T, dS^T for the step's BM queries, 32 at a time; the mask is resolved per step so
+          // the unmasked body has no branches.
+          auto step = [&](auto mask_tag) {
+            constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-          for (int c = 0; c < BM / 32; ++c) {
-            uint32_t sr[32], dr[32];
-            tmem_ld32(ts + c * 32, sr);
-            tmem_ld32(tdp + c * 32, dr);
-            tmem_ld_wait();
-            uint32_t pk[16], dk[16];
+            for (int c = 0; c < BM / 32; ++c) {
+              uint32_t sr[32], dr[32];
+              tmem_ld32(ts + c * 32, sr);
+              tmem_ld32(tdp + c * 32, dr);
+              tmem_ld_wait();
+              uint32_t pk[16], dk[16];
 #pragma unroll
-            for (int t = 0; t < 32; t += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lrow + c * 32 + t);
-              const float4 d4 = *reinterpret_cast<const float4*>(drow + c * 32 + t);
-              const float2 sc2 = make_float2(sl2, sl2);
+              for (int t = 0; t < 32; t += 4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(lrow + c * 32 + t);
+                const float4 d4 = *reinterpret_cast<const float4*>(drow + c * 32 + t);
+                const float2 sc2 = make_float2(sl2, sl2);
 #pragma unroll
-              for (int u = 0; u < 4; u += 2) {
-                const float2 lv = u == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
-                const float2 dv2 = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
-                const float2 x = fma2(make_float2(__uint_as_float(sr[t + u]), __uint_as_float(sr[t + u + 1])), sc2, lv);
-                float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                if constexpr (MASK) {
-                  const int q = q0 + c * 32 + t + u;
-                  p.x = (key_ok && q < seq.Lq && !(s.causal && key > q + seq.off)) ? p.x : 0.f;
-                  p.y = (key_ok && q + 1 < seq.Lq && !(s.causal && key > q + 1 + seq.off)) ? p.y : 0.f;
+                for (int u = 0; u < 4; u += 2) {
+                  const float2 lv = u == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
+                  const float2 dv2 = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+                  const float2 x =
+                      fma2(make_float2(__uint_as_float(sr[t + u]), __uint_as_float(sr[t + u + 1])), sc2, lv);
+                  float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                  if constexpr (MASK) {
+                    const int q = q0 + c * 32 + t + u;
+                    p.x = (key_ok && q < seq.Lq && !(s.causal && key > q + seq.off)) ? p.x : 0.f;
+                    p.y = (key_ok && q + 1 < seq.Lq && !(s.causal && key > q + 1 + seq.off)) ? p.y : 0.f;
+                  }
+                  const float2 dd =
+                      mul2(p, sub2(make_float2(__uint_as_float(dr[t + u]), __uint_as_float(dr[t + u + 1])), dv2));
+                  pk[(t + u) >> 1] = pack_bf16x2(p.x, p.y);
+                  dk[(t + u) >> 1] = pack_bf16x2(dd.x, dd.y);
                 }
-                const float2 dd =
-                    mul2(p, sub2(make_float2(__uint_as_float(dr[t + u]), __uint_as_float(dr[t + u + 1])), dv2));
-                pk[(t + u) >> 1] = pack_bf16x2(p.x, p.y);
-                dk[(t + u) >> 1] = pack_bf16x2(dd.x, dd.y);
+              }
+              tmem_st16(ts + c * 16, pk);
+              tmem_st16(tdp + c * 16, dk);
+              const uint32_t box = sDs(buf) + (c >> 1) * 16384 + r * 128;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int chunk = (c & 1) * 4 + j;
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)),
+                             "r"(dk[4 * j]), "r"(dk[4 * j + 1]), "r"(dk[4 * j + 2]), "r"(dk[4 * j + 3])
+                             : "memory");
               }
             }
-            tmem_st16(ts + c * 16, pk);
-            tmem_st16(tdp + c * 16, dk);
-            const uint32_t box = sDs(buf) + (c >> 1) * 16384 + r * 128;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int chunk = (c & 1) * 4 + j;
-              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)),
-                           "r"(dk[4 * j]), "r"(dk[4 * j + 1]), "r"(dk[4 * j + 2]), "r"(dk[4 * j + 3])
-                           : "memory");
-            }
-          }
-        };
-        if (need_mask)
-          step(std::true_type{});
-        else
-          step(std::false_type{});
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        fence_before_sync();
-        mbar_arrive(b_pready(buf));
-        gi = gn;
-        v = vn;
-      }
-    } else {
-      // ---------------------------------------------------------------- dQ into the accumulator
-      for (int gi = 0, v = next_v_warp(0); gi < G && v < nv; advance_warp(gi, v), ++it) {
-        const int q0 = v * BM;
-        const int buf = it % NB;
-        float* dQa = a.dqacc + row_base(s, seq, b, h0 + gi) * D;
-        mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
-        fence_after_sync();
-        const uint32_t tq = tmem + lane_off + tdQ(buf);
-        // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
-        // unused rows of the d = 64 product).
-        uint32_t vals[BM];
-#pragma unroll
-        for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
-        tmem_ld_wait();
-        fence_before_sync();
-        mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
-        if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
-        named_bar_sync(2, 128);
-        if (r < D) {
-#pragma unroll
-          for (int qq = 0; qq < BM; ++qq)
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
+          };
+          if (need_mask)
+            step(std::true_type{});
+          else
+            step(std::false_type{});
+          tmem_st_wait();
+          fence_proxy_async_smem();
+          fence_before_sync();
+          mbar_arrive(b_pready(buf));
+          gi = gn;
+          v = vn;
         }
-        fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (threadIdx.x == 256 && !*abort_flag) {
-          const int rows = min(BM, seq.Lq - q0);
-          bulk_reduce_add_f32(dQa + (size_t)q0 * D, sDq, (uint32_t)(rows * D * 4));
-          tma_store_commit();
-        }
-      }
-      if (threadIdx.x == 256) tma_store_wait_read0();  // the staging is read before the CTA exits
-    }
-
-    // ---------------------------------------------------------------- epilogue: dK (warps 4-7), dV (8-11)
-    if (it > 0) {
-      mbar_wait(b_done, 0, abort_flag, a.status);
-      fence_after_sync();
-    }
-    const uint32_t tacc = tmem + lane_off + (elementwise ? C::kTdK : C::kTdV);
-    const float mul = elementwise ? a.scale : 1.f;
-    const uint32_t stg = sStage0 + (elementwise ? 0 : C::kKVBytes);  // the (idle) Q/dO ring holds dK, dV
-    // A packed sequence's last key tile is stored row by row: a tile-wide copy would write the
-    // next sequence's rows.
-    const bool direct = s.cu_q != nullptr && kt * 128 + 128 > seq.krows;
-    const int key = kt * 128 + r;
-    __nv_bfloat16* grow = reinterpret_cast<__nv_bfloat16*>(elementwise ? a.dk : a.dv) +
-                          elem_offset(elementwise ? a.sdk : a.sdv, seq.bb, seq.k0 + key, hk);
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t vv[32];
-      if (it > 0) {
-        tmem_ld32(tacc + c * 32, vv);
-        tmem_ld_wait();
       } else {
+        // -------------------------------------------------------------- dQ into the accumulator
+        for (int gi = 0, v = v_first; gi < G && v < T.nv; ++it) {
+          const int q0 = v * BM;
+          const int buf = it % NB;
+          float* dQa = a.dqacc + row_base(s, seq, T.b, T.h0 + gi) * D;
+          mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
+          fence_after_sync();
+          const uint32_t tq = tmem + lane_off + tdQ(buf);
+          // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
+          // unused rows of the d = 64 product).
+          uint32_t vals[BM];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) vv[i] = 0u;
+          for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
+          tmem_ld_wait();
+          fence_before_sync();
+          mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
+          if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
+          named_bar_sync(2, 128);
+          if (r < D) {
+#pragma unroll
+            for (int qq = 0; qq < BM; ++qq)
+              asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(2, 128);
+          if (threadIdx.x == 256 && !*abort_flag) {
+            const int rows = min(BM, seq.Lq - q0);
+            bulk_reduce_add_f32(dQa + (size_t)q0 * D, sDq, (uint32_t)(rows * D * 4));
+            tma_store_commit();
+          }
+          v = bwd_next_v_warp(s, T, v + 1, BM);
+          if (v >= T.nv) {
+            ++gi;
+            v = v_first;
+          }
+        }
       }
-      uint32_t pk[16];
+
+      // -------------------------------------------------------------- dK (warps 4-7), dV (8-11)
+      // Read out of tensor memory, released for the next tile's first products, then stored
+      // straight from registers (no shared-memory staging competes with the next tile's loads).
+      const float mul = elementwise ? a.scale : 1.f;
+      const int key = kt * 128 + r;
+      const bool store = key < seq.krows;
+      __nv_bfloat16* grow = reinterpret_cast<__nv_bfloat16*>(elementwise ? a.dk : a.dv) +
+                            elem_offset(elementwise ? a.sdk : a.sdv, seq.bb, seq.k0 + (store ? key : 0), T.hk);
+      if (any_work) {
+        mbar_wait(b_done, wt & 1, abort_flag, a.status);
+        fence_after_sync();
+      }
+      const uint32_t tacc = tmem + lane_off + (elementwise ? C::kTdK : C::kTdV);
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = pack_bf16x2(__uint_as_float(vv[2 * i]) * mul, __uint_as_float(vv[2 * i + 1]) * mul);
-      if (direct) {
-        if (key < seq.krows) {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t vv[32];
+        if (any_work) {
+          tmem_ld32(tacc + c * 32, vv);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) vv[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(vv[2 * i]) * mul, __uint_as_float(vv[2 * i + 1]) * mul);
+        if (store) {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             *reinterpret_cast<uint4*>(grow + c * 32 + j * 8) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
-        continue;
       }
-      const uint32_t box = stg + (c >> 1) * 16384 + r * 128;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int chunk = (c & 1) * 4 + j;
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(box + ((chunk ^ (r & 7)) << 4)), "r"(pk[4 * j]),
-                     "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
-                     : "memory");
+      if (any_work) {  // the accumulators may be overwritten by the next tile's first products
+        fence_before_sync();
+        mbar_arrive(b_accfree);
+        ++wt;
       }
     }
-    fence_proxy_async_smem();
-    named_bar_sync(elementwise ? 1 : 2, 128);
-    if (lane == 0 && (warp == 4 || warp == 8) && !direct) {
-      for (int c = 0; c < C::kBoxes; ++c)
-        tma_store_4d(elementwise ? &tmdK : &tmdV, stg + c * 16384, c * 64, seq.k0 + kt * 128, hk, seq.bb);
-      tma_store_commit();
-      tma_store_wait_read0();
-    }
+    if (threadIdx.x == 256) tma_store_wait_read0();  // the staging is read before the CTA exits
   }
 
   fence_before_sync();
@@ -590,25 +699,26 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   const AttnShape& s = a.s;
   const bool packed = s.cu_q != nullptr;
   const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk, nbatch = packed ? 1 : s.B;
-  const int BHkv = s.B * s.Hkv;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  CUtensorMap tq, tk, tv, tdo;
   if (!fa_make_tmap_bf16(&tq, a.q, D, rq, s.H, nbatch, a.sq.row, a.sq.head, a.sq.batch, C::BM) ||
       !fa_make_tmap_bf16(&tk, a.k, D, rk, s.Hkv, nbatch, a.sk.row, a.sk.head, a.sk.batch) ||
       !fa_make_tmap_bf16(&tv, a.v, D, rk, s.Hkv, nbatch, a.sv.row, a.sv.head, a.sv.batch) ||
-      !fa_make_tmap_bf16(&tdo, a.dout, D, rq, s.H, nbatch, a.sdo.row, a.sdo.head, a.sdo.batch, C::BM) ||
-      !fa_make_tmap_bf16(&tdk, a.dk, D, rk, s.Hkv, nbatch, a.sdk.row, a.sdk.head, a.sdk.batch) ||
-      !fa_make_tmap_bf16(&tdv, a.dv, D, rk, s.Hkv, nbatch, a.sdv.row, a.sdv.head, a.sdv.batch))
+      !fa_make_tmap_bf16(&tdo, a.dout, D, rq, s.H, nbatch, a.sdo.row, a.sdo.head, a.sdo.batch, C::BM))
     return cudaErrorInvalidValue;
   bwd_pre_kernel<D><<<grid_ew, 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)s.nbk * BHkv;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  bwd_tc_kernel<D><<<(unsigned)grid, kBwdThreads, C::kSmem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // Persistent: one CTA per SM (shared memory allows one), key tiles handed out by the counter.
+  const long long ntiles = (long long)s.nbk * s.B * s.Hkv;
+  if (ntiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (ntiles > 0) {
+    const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
+    bwd_tc_kernel<D><<<grid, kBwdThreads, C::kSmem, st>>>(tq, tk, tv, tdo, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   bwd_post_kernel<D><<<grid_ew, 256, 0, st>>>(a);
   return cudaGetLastError();
 }

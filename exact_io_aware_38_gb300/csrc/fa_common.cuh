@@ -160,6 +160,7 @@ struct FaBwdArgs {
   FaStrides sq, sk, sv, so, sdo, sdq, sdk, sdv;
   float* dvec;   // D, fp32, one per query row (laid out like the LSE)
   float* dqacc;  // fp32 dQ accumulator, d per query row (laid out like the LSE)
+  int* tile_counter;  // key tiles handed out so far by the persistent main kernel (workspace)
   fa::AttnShape s;
   float scale;
   int* status;

@@ -38,6 +38,7 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 320;
+constexpr int kVisWords = 64;  // key tiles covered by the per-CTA visibility bitmap: 2048
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
@@ -62,10 +63,12 @@ struct FwdSmemCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  uint32_t vis[2][kVisWords];  // block mask: bit kt of query tile x's word kt / 32 = tile visited
 };
 
 // SPLIT: the CTA covers one split of the key tiles and writes fp32 partials (see FaFwdArgs).
-template <int D, bool SPLIT>
+// MASKED: a block mask is given (never with SPLIT); without one, visibility is in closed form.
+template <int D, bool SPLIT, bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FaFwdArgs a) {
@@ -105,14 +108,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     return l;
   };
   const int lim0 = min(last_kt(qt0), kt_hi - 1), lim1 = has1 ? min(last_kt(qt1), kt_hi - 1) : -1;
-  auto vis = [&](int x, int kt) -> bool {
-    if (s.block_mask == nullptr) return kt <= (x ? lim1 : lim0);
-    return (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt);
-  };
   // Key tiles past both query tiles' last visible key tile (or past the split's range) are never
   // visited; scans stop there, and start at the split's first key tile.
   const int kt_end = max(lim0, lim1) + 1;
+  // With a block mask the CTA first turns its two mask rows into a bitmap in shared memory, so
+  // finding the next visited key tile is a word read and a bit scan instead of one dependent
+  // mask load per skipped tile (longer rows than the bitmap holds are looked up tile by tile).
+  const bool bitmap = MASKED && kt_end <= 32 * kVisWords;
+  auto vis = [&](int x, int kt) -> bool {
+    if constexpr (!MASKED) return kt <= (x ? lim1 : lim0);
+    if (bitmap) return (ctl.vis[x][kt >> 5] >> (kt & 31)) & 1u;
+    return (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt);
+  };
   auto next_union = [&](int kt) -> int {
+    if (MASKED && bitmap) {
+      for (; kt < kt_end; kt = (kt | 31) + 1) {
+        const uint32_t m = (ctl.vis[0][kt >> 5] | ctl.vis[1][kt >> 5]) >> (kt & 31);
+        if (m) return kt + __ffs(m) - 1;
+      }
+      return s.nbk;
+    }
     for (; kt < kt_end; ++kt)
       if (vis(0, kt) || vis(1, kt)) return kt;
     return s.nbk;
@@ -120,6 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The same scan, also reporting which query tiles see the key tile found (for the issuer, whose
   // every instruction between MMA groups is time the tensor pipe idles).
   auto next_union_vis = [&](int kt, bool& v0, bool& v1) -> int {
+    if (MASKED && bitmap) {
+      kt = next_union(kt);
+      v0 = kt < s.nbk && vis(0, kt);
+      v1 = kt < s.nbk && vis(1, kt);
+      return kt;
+    }
     for (; kt < kt_end; ++kt) {
       v0 = vis(0, kt);
       v1 = vis(1, kt);
@@ -157,6 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl.tmem_base), 512);
     tmem_relinquish();
+  }
+  if (MASKED && bitmap) {  // one vote per 32 key tiles of a query tile; only [kt_lo, kt_end) is ever read
+    const int words = (kt_end + 31) >> 5;
+    for (int idx = warp; idx < 2 * words; idx += kThreads / 32) {
+      const int x = idx & 1, wd = idx >> 1, kt = wd * 32 + lane;
+      const bool bit = kt >= kt_lo && kt < kt_end && (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt);
+      const uint32_t m = __ballot_sync(0xffffffffu, bit);
+      if (lane == 0) ctl.vis[x][wd] = m;
+    }
   }
   fence_before_sync();
   __syncthreads();
@@ -499,7 +529,9 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   const int BH = s.B * s.H;
   const bool split = a.part_o != nullptr;
-  auto kern = split ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
+  if (split && s.block_mask != nullptr) return cudaErrorInvalidValue;  // no split path takes a mask
+  auto kern = split ? fwd_tc_kernel<D, true, false>
+                    : (s.block_mask != nullptr ? fwd_tc_kernel<D, false, true> : fwd_tc_kernel<D, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)((s.nbq + 1) / 2) * BH * (split ? a.splits : 1);

@@ -77,7 +77,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int32_t* tile_visits, int* dev_status, void* stream);
 
 /* Bytes of device workspace fa_bwd needs: D (fp32 [B,H,N]) and the fp32 dQ accumulator
- * ([B,H,N,d]), each rounded up to 256 bytes. Returns 0 for invalid sizes. */
+ * ([B,H,N,d]), each rounded up to 256 bytes, then 256 bytes for the main pass's key-tile counter.
+ * Returns 0 for invalid sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
@@ -90,8 +91,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   workspace         device, >= fa_bwd_workspace_bytes(B, H, N, d) bytes, 256-byte aligned;
  *                     scratch only (its contents on entry are ignored and on exit undefined)
  *   dev_status, stream: as for fa_fwd
- * Launches, in order on `stream`: a pre-pass (D = rowsum(dO * O), dQ accumulator cleared), the main
- * pass (one CTA per key tile, looping over the query tiles it is visible to) and a post-pass
+ * Launches, in order on `stream`: a pre-pass (D = rowsum(dO * O), dQ accumulator and key-tile
+ * counter cleared), the main pass (one CTA per SM, each taking key tiles from the counter and
+ * looping over the query tiles that can see them) and a post-pass
  * (dQ fp32 -> bf16). dQ is accumulated with fp32 reduce-adds, so its bits may differ between runs by
  * the order of additions; dK, dV, O and LSE are run-to-run identical.
  */
@@ -113,8 +115,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  *   tile_visits     [B * H * nb] (per query head); workspace as fa_bwd_workspace_bytes(B, H, N, d)
  * Every other argument, the launches and the errors are as for fa_fwd / fa_bwd; Hkv outside
  * [1, H] or not dividing H returns FA_ERR_INVALID_ARG. fa_fwd and fa_bwd are the Hkv = H case.
- * The backward main pass runs one CTA per (key tile, K/V head); it loops over the group's query
- * heads, so dK and dV stay exact sums in fp32 and are run-to-run identical.
+ * The backward main pass owns each (key tile, K/V head) in one CTA; it loops over the group's
+ * query heads, so dK and dV stay exact sums in fp32 and are run-to-run identical.
  */
 int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
                int B, int H, int Hkv, int N, int d, int causal,
@@ -145,7 +147,8 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
  *              to query i iff j <= i + L_k - L_q (the square case is j <= i). Rows with no visible
  *              key get O = 0 and LSE = -inf.
  *   LSE        fp32, fixed length [B, H, seqlen_q]; packed [H, rows_q] (row r of head h at h * rows_q + r).
- *   workspace  fa_bwd_varlen_workspace_bytes: D and the fp32 dQ accumulator, one row per LSE entry.
+ *   workspace  fa_bwd_varlen_workspace_bytes: D and the fp32 dQ accumulator, one row per LSE entry,
+ *              and the key-tile counter (laid out as for fa_bwd_workspace_bytes).
  * No block mask, key-padding vector or tile counts here (use fa_fwd / fa_bwd for those). K/V may
  * have Hkv heads as in fa_fwd_gqa. Errors, ownership and launches are as for fa_fwd / fa_bwd; a
  * packed batch's last tile is stored row by row so no write crosses into the next sequence.

@@ -47,7 +47,7 @@ def test_workspace_bytes(L):
     B, H, N, d = 2, 3, 130, 64
     rows = B * H * N
     r256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == r256(rows * 4) + r256(rows * d * 4)
+    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == r256(rows * 4) + r256(rows * d * 4) + 256
     assert fa.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
     assert fa.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
 
@@ -156,10 +156,10 @@ def test_varlen_workspace_bytes(L):
     r256 = lambda x: (x + 255) // 256 * 256
     p = fa.VarlenProblem(3, 4, 2, 128, 100, 70, None, None, 0, 0, 1, 0.1)
     rows = 3 * 4 * 100
-    assert fa.fa_bwd_varlen_workspace_bytes(p) == r256(rows * 4) + r256(rows * 128 * 4)
+    assert fa.fa_bwd_varlen_workspace_bytes(p) == r256(rows * 4) + r256(rows * 128 * 4) + 256
     p = fa.VarlenProblem(3, 4, 2, 64, 100, 70, A, A, 257, 180, 1, 0.1)
     rows = 4 * 257
-    assert fa.fa_bwd_varlen_workspace_bytes(p) == r256(rows * 4) + r256(rows * 64 * 4)
+    assert fa.fa_bwd_varlen_workspace_bytes(p) == r256(rows * 4) + r256(rows * 64 * 4) + 256
     p.Hkv = 3
     assert fa.fa_bwd_varlen_workspace_bytes(p) == 0
 
