@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_kv = [&]() {  // lane 0
         kv_issued = true;
         if (wt > 0 && !mbar_wait(b_done, (wt - 1) & 1, abort_flag, a.status)) return;
+#ifndef FA_TEST_WITHHOLD_KV  // a test-only build never loads K/V: every wait on them must run out
         mbar_expect_tx(b_kv, 2 * C::kKVBytes);
         for (int c = 0; c < C::kBoxes; ++c) {
           tma_load_4d(sK + c * 16384, &tmK, c * 64, T.seq.k0 + T.kt * 128, T.hk, T.seq.bb, b_kv);
@@ -356,6 +357,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         kv_any = true;
         kv_par = wt & 1;
+#endif
       };
       if (lane == 0 && wt == 0) issue_kv();
       int l = 0;

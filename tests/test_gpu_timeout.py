@@ -1,7 +1,7 @@
 """Failure detection without a GPU fault: every wait inside the kernels is bounded. A test-only
-build of the library whose forward producer never loads K/V (the flag nothing sets) must make
-the consumers' waits run out; the kernel must record FA_ERR_DEVICE_TIMEOUT in the status word,
-release its tensor memory and return, and the GPU must stay usable for a normal call."""
+build of the library whose forward and backward producers never load K/V (the flag nothing sets)
+must make the consumers' waits run out; the kernel must record FA_ERR_DEVICE_TIMEOUT in the status
+word, release its tensor memory and return, and the GPU must stay usable for a normal call."""
 
 import ctypes
 
@@ -44,3 +44,46 @@ def test_bounded_wait_reports_timeout_and_gpu_stays_usable():
     ro, rl = oracle.attention_forward(f(inp["q"]), f(inp["k"]), f(inp["v"]), 0.088, causal=True)
     assert np.abs(f(o2.cpu()) - ro).max() <= 2e-2
     assert np.abs(lse2.cpu().double().numpy() - rl).max() <= 1e-3
+
+
+def test_backward_bounded_wait_reports_timeout_and_gpu_stays_usable():
+    """The persistent backward under the same test build: its key-tile queue, the per-tile done and
+    accumulator-release waits and the step barriers all give up, every role leaves its tile loop
+    (512 key tiles, so each CTA takes several after its abort), and the next normal call on the
+    context is correct."""
+    build.build()
+    path = build.build_withhold_kv_test_lib()
+    L = ctypes.CDLL(path)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.fa_bwd.restype = I
+    L.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, ctypes.c_float, P, ctypes.c_size_t, P, P]
+    L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B, H, N, d, scale = 1, 64, 1024, 64, 0.125
+    g = torch.Generator("cuda").manual_seed(11)
+    q, k, v, o, do = (torch.randn((B, H, N, d), generator=g, device="cuda").to(torch.bfloat16) for _ in range(5))
+    lse = torch.randn((B, H, N), generator=g, device="cuda")
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    nbytes = int(L.fa_bwd_workspace_bytes(B, H, N, d))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    rc = L.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, 1, None, None, scale, ws.data_ptr(),
+                  nbytes, status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == -5  # FA_ERR_DEVICE_TIMEOUT
+
+    # The context and the GPU are still healthy: the real library's backward matches the oracle.
+    B, H, N = 1, 2, 384
+    inp = workloads.random_inputs(B, H, N, d, seed=5)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    status.zero_()
+    o, lse = fa.fwd(q, k, v, causal=True, scale=scale, status=status)
+    dq2, dk2, dv2 = fa.bwd(q, k, v, o, lse, do, causal=True, scale=scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    f = lambda t: t.double().numpy()
+    ref = oracle.attention_backward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["do"]), scale, causal=True)
+    for got, want in zip((dq2, dk2, dv2), ref):
+        assert np.linalg.norm(f(got.cpu()) - want) <= 2e-2 * np.linalg.norm(want)
