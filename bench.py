@@ -178,6 +178,17 @@ def cpu_oracle_step(inp, head):
         oracle.head_dkdv(q, k, v, do, c, causal, bm, L, cols=np.arange(a, min(N, a + 2048)), stats=stats)
 
 
+def useful_padding(w, seqlens, H, N, d, ms, world):
+    """The secondary figure under key padding: 4 H d N sum_b L_b FLOPs per forward (x3.5 with the
+    backward) over the same step time. None without key padding, and with the causal mask, where
+    that count is not the work done."""
+    if seqlens is None or w.causal:
+        return None
+    fl = 3.5 * rl.useful_padding_flops(H, N, d, np.asarray(seqlens))
+    return {"value": fl * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "count": "4 H d N sum_b L_b per forward, x3.5 with the backward (key padding; secondary)"}
+
+
 def sample_flops(w, inp):
     f = rl.attention_flops(1, 1, w.N, w.d, causal=w.causal,
                            block_mask=None if inp["block_mask"] is None else inp["block_mask"].numpy())
@@ -441,6 +452,9 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    up = useful_padding(w, None if inp["seqlens_k"] is None else inp["seqlens_k"].numpy(), H, N, d, ms, world)
+    if up is not None:
+        result["useful_padding"] = up
     if rank == 0 and not args.no_cpu_baseline:
         t0 = time.perf_counter()
         cpu_oracle_step(inp, (0, 0))
