@@ -178,6 +178,12 @@ def cpu_oracle_step(inp, head):
         oracle.head_dkdv(q, k, v, do, c, causal, bm, L, cols=np.arange(a, min(N, a + 2048)), stats=stats)
 
 
+def percentiles(xs, qs=(10, 50, 90)):
+    """Nearest-rank percentiles of the per-step times (ms)."""
+    v = sorted(xs)
+    return [v[min(len(v) - 1, max(0, -(-q * len(v) // 100) - 1))] for q in qs]
+
+
 def useful_padding(w, seqlens, H, N, d, ms, world):
     """The secondary figure under key padding: 4 H d N sum_b L_b FLOPs per forward (x3.5 with the
     backward) over the same step time. None without key padding, and with the causal mask, where
@@ -382,6 +388,7 @@ def main():
     ms = start.elapsed_time(end) / args.steps
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    step_pct = percentiles([e[0].elapsed_time(e[2]) for e in ev])  # this rank's steps
     ms = max_over_ranks(ms, pg, dev)
     assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
 
@@ -443,6 +450,7 @@ def main():
                    "parallelism": f"replicas x{world}", "l2": l2_note},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops},
+        "step_ms_p10_p50_p90": step_pct,
         "roofline": {"bound": "tensor", "kernel": "bwd_tc_kernel (timed as the fa_bwd span: pre + main + post)",
                      "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak,
                      "traffic": kernel_traffic(f"bwd_tc_kernel<{d}>", w.name, args.heads),

@@ -17,3 +17,12 @@ def test_useful_padding_figure():
     # No key padding, or a causal mask: no secondary figure.
     assert bench.useful_padding(dense, None, 16, 512, 64, 1.0, 1) is None
     assert bench.useful_padding(SimpleNamespace(causal=True), [384], 16, 512, 64, 1.0, 1) is None
+
+
+def test_step_percentiles_nearest_rank():
+    import bench
+
+    xs = [float(i) for i in range(1, 21)]  # 20 steps, 1 .. 20 ms, shuffled order must not matter
+    assert bench.percentiles(list(reversed(xs))) == [2.0, 10.0, 18.0]
+    assert bench.percentiles([5.0]) == [5.0, 5.0, 5.0]
+    assert bench.percentiles([3.0, 1.0, 2.0], qs=(0, 100)) == [1.0, 3.0]
