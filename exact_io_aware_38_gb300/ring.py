@@ -1,4 +1,4 @@
-"""Sequence-sharded ring attention (forward) built on the library's partials.
+"""Sequence-sharded ring attention (forward and backward) built on the library's kernels.
 
 The commentary on the FlashAttention paper notes that the online softmax is associative over
 pieces of the key space, which is what lets ring attention shard a long sequence across devices:
@@ -10,8 +10,16 @@ merge of fa_merge_partials. Causal attention with equal blocks: the rank's own b
 (the rotation still passes them on). Each received block lands in a local buffer before it is
 used (point-to-point copies, no multicast).
 
-Out of scope: the backward pass, load balancing of the causal case (e.g. zig-zag block orders),
-overlap of the rotation with the compute.
+The backward pass follows the same schedule. With each query row's final O and log-sum-exp over
+all keys, one (query block, key block) pair's share of the gradients is exactly what the fused
+backward kernel computes for that pair: P = exp(c S - LSE) is the row's softmax restricted to the
+block and D = rowsum(dO * O) is the whole row's. So each step runs fa_bwd_varlen on the block it
+holds; dQ accumulates on the rank, and the fp32 dK, dV accumulators travel with their K/V block.
+After the last step a rank holds block rank + 1 and its accumulators, so one more rotation delivers
+every block's dK, dV to its owner.
+
+Out of scope: load balancing of the causal case (e.g. zig-zag block orders), overlap of the
+rotation with the compute.
 """
 
 from __future__ import annotations
@@ -68,3 +76,31 @@ def ring_forward(q, k, v, *, causal=False, scale=None, group=None, partial=None,
         if step + 1 < world:
             kv = rotate_fn(kv, group)
     return finalize(acc)
+
+
+def ring_backward(q, k, v, o, lse, do, *, causal=False, scale=None, group=None, partial_bwd=None, rotate_fn=None):
+    """dQ, dK, dV of this rank's blocks ([B, N_block, H, d] views, as for ring_forward; o and lse
+    are ring_forward's results for this rank's queries, do the gradient of o). `partial_bwd`
+    (q, k_blk, v_blk, o, lse, do, causal) -> (dq, dk, dv) shares and `rotate_fn` default to the
+    library's backward kernel and torch.distributed point-to-point copies."""
+    partial_bwd = partial_bwd or (lambda q_, k_, v_, o_, l_, do_, c_: fa.bwd_varlen(q_, k_, v_, o_, l_, do_,
+                                                                                   causal=c_, scale=scale))
+    rotate_fn = rotate_fn or rotate
+    world = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    acc = torch.float32 if q.dtype in (torch.bfloat16, torch.float16) else q.dtype  # sums of the shares
+    kv = [k, v]
+    dq = torch.zeros(q.shape, dtype=acc, device=q.device)
+    dkv = [torch.zeros(k.shape, dtype=acc, device=k.device), torch.zeros(v.shape, dtype=acc, device=v.device)]
+    for step, _src, c in ring_schedule(rank, world, causal):
+        if c is not None:
+            gq, gk, gv = partial_bwd(q, kv[0], kv[1], o, lse, do, c)
+            dq += gq.to(acc)
+            dkv[0] += gk.to(acc)
+            dkv[1] += gv.to(acc)
+        if step + 1 < world:
+            moved = rotate_fn(kv + dkv, group)  # the block and its accumulators travel together
+            kv, dkv = moved[:2], moved[2:]
+    if world > 1:
+        dkv = rotate_fn(dkv, group)  # block rank + 1's accumulators to their owner; ours arrive
+    return dq.to(q.dtype), dkv[0].to(k.dtype), dkv[1].to(v.dtype)

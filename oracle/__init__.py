@@ -2,6 +2,7 @@
 
 from .attention import (  # noqa: F401
     attention_backward,
+    attention_backward_block,
     attention_backward_varlen,
     attention_forward,
     attention_forward_varlen,

@@ -292,6 +292,40 @@ def attention_backward(q, k, v, do, scale, causal=False, block_mask=None, seqlen
     return dq, dk, dv
 
 
+def attention_backward_block(q, k, v, o, lse, do, scale, causal=False):
+    """One block of keys' share of the gradients, given each query row's final O and log-sum-exp
+    over all of its keys: the pieces that a sequence-sharded backward pass adds up.
+
+    q, o, do [B,H,Nq,d] and lse [B,H,Nq] belong to the query rows; k, v [B,Hkv,Nk,d] are one block
+    of their keys. P_ij = exp(s_ij - LSE_i) on the block's valid keys (the row's softmax over all
+    keys, restricted to the block); D_i = sum_k dO_ik O_ik (the whole row's D, from the final O);
+    dP = dO V^T and dS = P * (dP - D). By the chain rule of L = sum(dO * O), the block's dV = P^T dO
+    and dK = c dS^T Q, and its share of dQ is c dS K. Over a partition of the keys the shares of dQ
+    add up to attention_backward's dQ, and each block's dK, dV are that block's rows of it.
+    `causal` is the square (own-block) case; dK, dV of a K/V head sum its group's query heads."""
+    q, k, v, o, lse, do = (_as64(x) for x in (q, k, v, o, lse, do))
+    B, H, Nq, _ = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    valid = valid_matrix(np.arange(Nq), Nk, causal, offset=Nk - Nq)
+    for b in range(B):
+        for h in range(H):
+            hk = kv_head(h, H, Hkv)
+            lrow = lse[b, h][:, None]
+            live = valid & np.isfinite(lrow)  # a row with no valid key anywhere has no gradient
+            s = scores(q[b, h], k[b, hk], scale)
+            p = np.where(live, np.exp(np.where(live, s - np.where(np.isfinite(lrow), lrow, 0.0), 0.0)), 0.0)
+            dp = do[b, h] @ v[b, hk].T
+            D = np.sum(do[b, h] * o[b, h], axis=1, keepdims=True)
+            ds = p * (dp - D)
+            dq[b, h] = scale * (ds @ k[b, hk])
+            dk[b, hk] += scale * (ds.T @ q[b, h])
+            dv[b, hk] += p.T @ do[b, h]
+    return dq, dk, dv
+
+
 def tile_grid(N, causal=False, block_mask=None, key_len=None, tile=TILE):
     """bool [nb, nb]: (query tile I, key tile J) holds at least one valid (i, j) pair, for one head.
 

@@ -246,3 +246,44 @@ def test_ring_attention_simulated_on_one_gpu(causal, d):
         torch.cuda.synchronize()
         sl = slice(rank * blk, (rank + 1) * blk)
         check_o_lse(t4(o), f64(lse), ro[:, :, sl], rl[:, :, sl])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_ring_backward_simulated_on_one_gpu(causal, d):
+    """The ring backward's per-rank schedule on one GPU: each (query block, key block) share from
+    the library's backward with the rows' final O and LSE (from the ring forward), dQ summed per
+    query block and dK, dV per key block in fp32, against the whole-sequence oracle gradients."""
+    from exact_io_aware_38_gb300 import ring
+
+    g = torch.Generator().manual_seed(300 + d)
+    W, blk, B, H, Hkv = 3, 260, 1, 4, 2
+    q, do = bf16((B, W * blk, H, d), g), bf16((B, W * blk, H, d), g)
+    k, v = bf16((B, W * blk, Hkv, d), g), bf16((B, W * blk, Hkv, d), g)
+    scale = 1.0 / np.sqrt(d)
+    t4 = lambda x: f64(x).transpose(0, 2, 1, 3)
+    rq, rk, rv = oracle.attention_backward(t4(q), t4(k), t4(v), t4(do), scale, causal=causal)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    block = lambda t, i: t[:, i * blk:(i + 1) * blk].contiguous()
+    dq = torch.zeros((B, W * blk, H, d), dtype=torch.float32, device="cuda")
+    dk = torch.zeros((B, W * blk, Hkv, d), dtype=torch.float32, device="cuda")
+    dv = torch.zeros_like(dk)
+    for rank in range(W):
+        qb, dob = block(qc, rank), block(doc, rank)
+        acc = None
+        for _, src, c in ring.ring_schedule(rank, W, causal):
+            if c is None:
+                continue
+            part = fa.fwd_partial(qb, block(kc, src), block(vc, src), causal=c, scale=scale)
+            acc = part if acc is None else fa.merge_partials(qb, block(kc, src), acc, part)
+        ob, lb = fa.finalize_partials(qb, block(kc, rank), acc)
+        for _, src, c in ring.ring_schedule(rank, W, causal):
+            if c is None:
+                continue
+            gq, gk, gv = fa.bwd_varlen(qb, block(kc, src), block(vc, src), ob, lb, dob, causal=c, scale=scale)
+            dq[:, rank * blk:(rank + 1) * blk] += gq.float()
+            dk[:, src * blk:(src + 1) * blk] += gk.float()
+            dv[:, src * blk:(src + 1) * blk] += gv.float()
+    torch.cuda.synchronize()
+    for got, want in ((dq, rq), (dk, rk), (dv, rv)):
+        rel_fro(f64(got).transpose(0, 2, 1, 3), want)

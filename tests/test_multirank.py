@@ -120,6 +120,62 @@ def test_ring_attention_two_ranks(causal):
         assert err_o <= 1e-12 and err_l <= 1e-12, (rank, err_o, err_l)
 
 
+def _ring_bwd_worker(rank, world, port, causal, q):
+    """Ring backward over `world` ranks with the oracle's per-block share standing in for the
+    kernel (fp64, CPU): checks the rotation of the dK/dV accumulators and the final delivery
+    against whole-sequence gradients."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import numpy as np
+
+        import oracle
+        from exact_io_aware_38_gb300 import ring
+
+        g = torch.Generator().manual_seed(7)
+        B, N, H, Hkv, d, c = 1, world * 20, 4, 2, 6, 0.35
+        qf = torch.randn((B, N, H, d), generator=g, dtype=torch.float64)
+        kf, vf = (torch.randn((B, N, Hkv, d), generator=g, dtype=torch.float64) for _ in range(2))
+        dof = torch.randn((B, N, H, d), generator=g, dtype=torch.float64)
+        t4 = lambda x: np.ascontiguousarray(x.numpy().transpose(0, 2, 1, 3))
+        back = lambda a: torch.from_numpy(np.ascontiguousarray(a.transpose(0, 2, 1, 3)))
+        of, lf = oracle.attention_forward(t4(qf), t4(kf), t4(vf), c, causal=causal)
+        blk = N // world
+        sl = slice(rank * blk, (rank + 1) * blk)
+        qb, kb, vb, dob = (t[:, sl].contiguous() for t in (qf, kf, vf, dof))
+        ob, lb = back(of)[:, sl].contiguous(), torch.from_numpy(lf[:, :, sl].copy())
+
+        def partial_bwd(q_, k_, v_, o_, l_, do_, c_):
+            gq, gk, gv = oracle.attention_backward_block(t4(q_), t4(k_), t4(v_), t4(o_), l_.numpy(), t4(do_), c,
+                                                         causal=c_)
+            return back(gq), back(gk), back(gv)
+
+        dq, dk, dv = ring.ring_backward(qb, kb, vb, ob, lb, dob, causal=causal, partial_bwd=partial_bwd)
+        rq, rk, rv = (back(x)[:, sl] for x in oracle.attention_backward(t4(qf), t4(kf), t4(vf), t4(dof), c,
+                                                                         causal=causal))
+        q.put((rank, float((dq - rq).abs().max()), float((dk - rk).abs().max()), float((dv - rv).abs().max())))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_backward(causal, world):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_ring_bwd_worker, args=(r, world, port, causal, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, eq, ek, ev in results:
+        assert max(eq, ek, ev) <= 1e-12, (rank, eq, ek, ev)
+
+
 def test_ring_schedule_covers_each_block_once():
     from exact_io_aware_38_gb300 import ring
 

@@ -358,9 +358,39 @@ def pin_varlen_library_crosscheck():
         assert np.abs(dk - ref_dk).max() <= 1e-11 and np.abs(dv - ref_dv).max() <= 1e-11
 
 
+def pin_block_backward_shares():
+    """Sequence-sharded backward: with the rows' final O and LSE, the per-key-block shares of
+    attention_backward_block add up to the whole-sequence gradients (causal: own block square,
+    earlier blocks whole, later blocks absent), for query blocks against key blocks of a 3-way
+    partition, grouped K/V heads included."""
+    W, blk, H, Hkv, d, c = 3, 10, 4, 2, 5, 0.4
+    N = W * blk
+    for causal in (False, True):
+        q, do = RNG.standard_normal((1, H, N, d)), RNG.standard_normal((1, H, N, d))
+        k, v = RNG.standard_normal((1, Hkv, N, d)), RNG.standard_normal((1, Hkv, N, d))
+        o, lse = oracle.attention_forward(q, k, v, c, causal=causal)
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, c, causal=causal)
+        sq, sk, sv = np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dv)
+        for r in range(W):
+            rq = slice(r * blk, (r + 1) * blk)
+            for src in range(W):
+                if causal and src > r:
+                    continue
+                ks = slice(src * blk, (src + 1) * blk)
+                gq, gk, gv = OA.attention_backward_block(q[:, :, rq], k[:, :, ks], v[:, :, ks], o[:, :, rq],
+                                                         lse[:, :, rq], do[:, :, rq], c,
+                                                         causal=causal and src == r)
+                sq[:, :, rq] += gq
+                sk[:, :, ks] += gk
+                sv[:, :, ks] += gv
+        assert np.abs(sq - dq).max() <= 1e-12
+        assert np.abs(sk - dk).max() <= 1e-12 and np.abs(sv - dv).max() <= 1e-12
+
+
 PINS = [pin_row_sums, pin_q_zero, pin_one_hot, pin_mask_equivalence, pin_n1, pin_finite_differences,
         pin_grad_identities, pin_library_crosscheck, pin_gqa_head_mapping, pin_gqa_finite_differences,
-        pin_gqa_library_crosscheck, pin_causal_decode_row, pin_causal_front_padding, pin_varlen_library_crosscheck]
+        pin_gqa_library_crosscheck, pin_causal_decode_row, pin_causal_front_padding, pin_varlen_library_crosscheck,
+        pin_block_backward_shares]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -451,7 +481,13 @@ def _mut_valid_top_left(rows, n_keys, causal=False, block_mask=None, key_len=Non
 _real_valid = OA.valid_matrix
 
 
+def _mut_block_local_softmax(q, k, v, o, lse, do, scale, causal=False):
+    # the block's own softmax (its own LSE and D) instead of the row's over all keys
+    return oracle.attention_backward(q, k, v, do, scale, causal=causal)
+
+
 MUTANTS = [
+    ("attention_backward_block", _mut_block_local_softmax),
     ("kv_head", _mut_kv_head_interleaved),
     ("valid_matrix", _mut_valid_top_left),
     ("scores", _mut_scores_no_scale),
