@@ -1,0 +1,300 @@
+"""A model of the backward main kernel's barrier protocol, checked over random interleavings.
+
+The roles of bwd_tc_kernel (exact_io_aware_38_gb300/csrc/fa_bwd_sm103.cu) are modelled as
+generators with the kernel's waits, arrivals and commits: the TMA producer with the key-tile queue,
+the S^T/dP^T issuer, the gradient issuer, the elementwise and dQ warpgroups. Each tick resumes a
+random role whose wait would pass, completes a random TMA copy, or retires the head of either
+issuer's in-order MMA queue (a commit arrives when it reaches the head). mbarriers follow the
+hardware rule: a phase completes when its arrivals and transaction bytes are in, and
+try_wait.parity(P) passes iff the current phase's parity differs from P, so a waiter that falls
+two phases behind waits forever. Checked: no deadlock, and no writer issued while readers of the
+data it overwrites are unfinished (a Q/dO stage or K/V reloaded, TMEM columns or the dS tile
+rewritten, the dK/dV accumulators overwritten before their read-out).
+
+The same model with the earlier producer release (waiting on the two dq_full barriers for step
+i - 3) must deadlock on some interleaving: that aliasing hang is what the per-stage release fixes,
+and finding it shows the model can see that class of error.
+"""
+import random
+
+KST, NB = 3, 2
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.phase, self.tx = name, count, count, 0, 0
+
+    def arrive(self, n=1):
+        self.pending -= n
+        if self.pending < 0:
+            raise AssertionError(f"{self.name}: more arrivals than the count")
+        self._maybe()
+
+    def expect_tx(self, b):
+        self.tx += b
+        self.arrive()
+
+    def tx_done(self, b):
+        self.tx -= b
+        self._maybe()
+
+    def _maybe(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def passes(self, parity):
+        return (self.phase & 1) != parity
+
+
+def run(tiles, seed, release="stage"):
+    rnd = random.Random(seed)
+    B = {}
+
+    def bar(n, c):
+        B[n] = Bar(n, c)
+
+    bar("kv", 1)
+    for i in range(KST):
+        bar(f"full{i}", 1)
+        bar(f"empty{i}", 1)
+    for i in range(NB):
+        for n in ("sfull", "dqfull", "sfree"):
+            bar(f"{n}{i}", 1)
+        bar(f"pready{i}", 1)  # 128 elementwise threads, modelled as one arrival
+        bar(f"dqfree{i}", 1)  # 128 dQ threads
+    for i in range(2):
+        bar(f"tqfull{i}", 1)
+        bar(f"tqempty{i}", 4)
+    bar("done", 1)
+    bar("accfree", 2)  # the two warpgroups
+    bar("drain", 2)
+
+    ntiles = len(tiles)
+    tile_q = [None, None]
+    counter = [0]
+    grid = 1
+    loads = []  # pending TMA copies: (barrier, bytes, what)
+    pipe = {1: [], 2: []}
+    done = set()  # completed MMAs / copies / read-outs: ("S", step) ...
+    errors = []
+
+    def need(cond, msg):
+        if not cond:
+            errors.append(msg)
+
+    def wait(name, parity):
+        while not B[name].passes(parity):
+            yield (name, parity)
+
+    def take_tile(w):
+        yield from wait(f"tqfull{w & 1}", (w >> 1) & 1)
+        t = tile_q[w & 1]
+        B[f"tqempty{w & 1}"].arrive()
+        return t
+
+    def mma(who, label):
+        pipe[who].append(("mma", label))
+
+    def commit(who, name):
+        pipe[who].append(("commit", name))
+
+    # step -> work-tile index, filled by the producer (all roles walk the same sequence)
+    step_tile = {}
+
+    def producer():
+        i, wt, w = 0, 0, 0
+        while True:
+            if w >= 2:
+                yield from wait(f"tqempty{w & 1}", ((w - 2) >> 1) & 1)
+            t = w if w == 0 else grid + counter[0]
+            if w > 0:
+                counter[0] += 1
+            t = min(t, ntiles)
+            tile_q[w & 1] = t
+            B[f"tqfull{w & 1}"].arrive()
+            w += 1
+            yield None
+            if t >= ntiles:
+                return
+            n = tiles[t]
+            if n == 0:
+                continue
+            kv_issued = False
+
+            def issue_kv():
+                if wt > 0:
+                    yield from wait("done", (wt - 1) & 1)
+                    # every MMA of the previous work tile has completed (K and V are read by them)
+                    for s in [s for s, tt in step_tile.items() if tt == wt - 1]:
+                        for k in ("S", "dP", "dQ"):
+                            need((k, s) in done, f"K/V of work tile {wt} loaded before {k}{s} completed")
+                B["kv"].expect_tx(2)
+                loads.append(("kv", 2, ("kv", wt)))
+
+            if wt == 0:
+                yield from issue_kv()
+                kv_issued = True
+            for l in range(n):
+                if l == 2 and not kv_issued:
+                    yield from issue_kv()
+                    kv_issued = True
+                st, j = i % KST, i - KST
+                if j >= 0:
+                    if release == "stage":  # the kernel: one release barrier per stage
+                        yield from wait(f"empty{j % KST}", (j // KST) & 1)
+                    else:  # an earlier form: the NB-deep dq_full barriers of the TMEM buffers
+                        yield from wait(f"dqfull{j % NB}", (j // NB) & 1)
+                    for k in ("S", "dP", "dV", "dK"):
+                        need((k, j) in done, f"stage {st} reloaded for step {i} before {k}{j} completed")
+                step_tile[i] = wt
+                B[f"full{st}"].expect_tx(1)
+                loads.append((f"full{st}", 1, ("qdo", i)))
+                i += 1
+                yield None
+            if not kv_issued:
+                yield from issue_kv()
+            wt += 1
+
+    def issuer1():
+        sn, wt, w = 0, 0, 0
+        while True:
+            t = yield from take_tile(w)
+            w += 1
+            if t >= ntiles:
+                break
+            n = tiles[t]
+            if n == 0:
+                continue
+            yield from wait("kv", wt & 1)
+            need(("kv", wt) in done, f"S issuer saw K/V of work tile {wt} before they landed")
+            for _ in range(n):
+                st, buf = sn % KST, sn % NB
+                yield from wait(f"full{st}", (sn // KST) & 1)
+                need(("qdo", sn) in done, f"S^T{sn} issued before its Q/dO landed")
+                if sn >= NB:
+                    yield from wait(f"sfree{buf}", ((sn - NB) // NB) & 1)
+                    need(("dV", sn - NB) in done, f"S^T{sn} over P^T before dV{sn - NB} completed")
+                mma(1, ("S", sn))
+                if sn >= NB:
+                    yield from wait(f"dqfree{buf}", ((sn - NB) // NB) & 1)
+                    for k in ("dK", "dQ", "rdQ"):
+                        need((k, sn - NB) in done, f"dP^T{sn} over dS^T/dQ^T before {k}{sn - NB}")
+                mma(1, ("dP", sn))
+                commit(1, f"sfull{buf}")
+                sn += 1
+                yield None
+            wt += 1
+        commit(1, "drain")
+
+    def issuer2():
+        g, wt, w = 0, 0, 0
+        while True:
+            t = yield from take_tile(w)
+            w += 1
+            if t >= ntiles:
+                break
+            n = tiles[t]
+            if n == 0:
+                continue
+            if wt > 0:
+                yield from wait("accfree", (wt - 1) & 1)
+                need(("acc_ew", wt - 1) in done and ("acc_dq", wt - 1) in done,
+                     f"accumulators of work tile {wt - 1} overwritten before their read-out")
+            for _ in range(n):
+                st, buf = g % KST, g % NB
+                yield from wait(f"pready{buf}", (g // NB) & 1)
+                need(("P", g) in done, f"dV{g} issued before P/dS of step {g} were written")
+                mma(2, ("dV", g))
+                commit(2, f"sfree{buf}")
+                mma(2, ("dK", g))
+                commit(2, f"empty{st}")
+                mma(2, ("dQ", g))
+                commit(2, f"dqfull{buf}")
+                g += 1
+                yield None
+            commit(2, "done")
+            wt += 1
+        commit(2, "drain")
+
+    def group(kind):
+        it, wt, w = 0, 0, 0
+        while True:
+            t = yield from take_tile(w)
+            w += 1
+            if t >= ntiles:
+                break
+            n = tiles[t]
+            for _ in range(n):
+                buf = it % NB
+                if kind == "ew":
+                    yield from wait(f"sfull{buf}", (it // NB) & 1)
+                    need(("S", it) in done and ("dP", it) in done, f"P/dS of step {it} before S/dP completed")
+                    if it >= NB:  # dS^T into the shared-memory tile read by dQ of step it - NB
+                        need(("dQ", it - NB) in done, f"dS^T{it} written before dQ{it - NB} completed")
+                    done.add(("P", it))
+                    B[f"pready{buf}"].arrive()
+                else:
+                    yield from wait(f"dqfull{buf}", (it // NB) & 1)
+                    need(("dQ", it) in done, f"dQ^T{it} read before it completed")
+                    done.add(("rdQ", it))
+                    B[f"dqfree{buf}"].arrive()
+                it += 1
+                yield None
+            if n > 0:
+                yield from wait("done", wt & 1)
+                last = [s for s, tt in step_tile.items() if tt == wt]
+                for s in last:
+                    need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
+                yield None
+                done.add(("acc_" + kind, wt))
+                B["accfree"].arrive()
+                wt += 1
+
+    roles = {"prod": producer(), "i1": issuer1(), "i2": issuer2(), "ew": group("ew"), "dr": group("dq")}
+    blocked = {k: None for k in roles}
+    alive = set(roles)
+    for tick in range(400000):
+        cands = [("role", k) for k in alive if blocked[k] is None or B[blocked[k][0]].passes(blocked[k][1])]
+        if loads:
+            cands.append(("load", None))
+        cands += [("pipe", w) for w in (1, 2) if pipe[w]]
+        if not cands:
+            if alive:
+                return "deadlock", errors + [f"deadlock: {sorted((k, blocked[k]) for k in alive)}"]
+            return "ok", errors
+        c = rnd.choice(cands)
+        if c[0] == "role":
+            k = c[1]
+            try:
+                blocked[k] = next(roles[k])
+            except StopIteration:
+                alive.discard(k)
+        elif c[0] == "load":
+            name, b, what = loads.pop(rnd.randrange(len(loads)))
+            done.add(what)
+            B[name].tx_done(b)
+        else:
+            op = pipe[c[1]].pop(0)
+            if op[0] == "mma":
+                done.add(op[1])
+            else:
+                B[op[1]].arrive()
+    return "timeout", errors
+
+
+def _cases(n):
+    for seed in range(n):
+        r = random.Random(seed * 7919)
+        yield [r.choice([0, 0, 1, 1, 2, 3, 4, 5, 7]) for _ in range(r.randint(1, 10))], seed
+
+
+def test_protocol_has_no_deadlock_or_hazard():
+    for tiles, seed in _cases(3000):
+        res, errs = run(tiles, seed)
+        assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
+
+
+def test_model_finds_the_earlier_release_race():
+    hangs = [seed for tiles, seed in _cases(3000) if run(tiles, seed, release="dq_full")[0] == "deadlock"]
+    assert hangs, "the model no longer sees the aliasing deadlock of the earlier release"
