@@ -17,42 +17,14 @@ and finding it shows the model can see that class of error.
 """
 import random
 
+from mbarrier_model import Machine
+
 KST, NB = 3, 2
 
 
-class Bar:
-    def __init__(self, name, count):
-        self.name, self.count, self.pending, self.phase, self.tx = name, count, count, 0, 0
-
-    def arrive(self, n=1):
-        self.pending -= n
-        if self.pending < 0:
-            raise AssertionError(f"{self.name}: more arrivals than the count")
-        self._maybe()
-
-    def expect_tx(self, b):
-        self.tx += b
-        self.arrive()
-
-    def tx_done(self, b):
-        self.tx -= b
-        self._maybe()
-
-    def _maybe(self):
-        if self.pending == 0 and self.tx == 0:
-            self.phase += 1
-            self.pending = self.count
-
-    def passes(self, parity):
-        return (self.phase & 1) != parity
-
-
 def run(tiles, seed, release="stage"):
-    rnd = random.Random(seed)
-    B = {}
-
-    def bar(n, c):
-        B[n] = Bar(n, c)
+    M = Machine(seed)
+    B, bar, wait, need, done, mma, commit = M.B, M.bar, M.wait, M.need, M.done, M.mma, M.commit
 
     bar("kv", 1)
     for i in range(KST):
@@ -74,30 +46,11 @@ def run(tiles, seed, release="stage"):
     tile_q = [None, None]
     counter = [0]
     grid = 1
-    loads = []  # pending TMA copies: (barrier, bytes, what)
-    pipe = {1: [], 2: []}
-    done = set()  # completed MMAs / copies / read-outs: ("S", step) ...
-    errors = []
-
-    def need(cond, msg):
-        if not cond:
-            errors.append(msg)
-
-    def wait(name, parity):
-        while not B[name].passes(parity):
-            yield (name, parity)
-
     def take_tile(w):
         yield from wait(f"tqfull{w & 1}", (w >> 1) & 1)
         t = tile_q[w & 1]
         B[f"tqempty{w & 1}"].arrive()
         return t
-
-    def mma(who, label):
-        pipe[who].append(("mma", label))
-
-    def commit(who, name):
-        pipe[who].append(("commit", name))
 
     # step -> work-tile index, filled by the producer (all roles walk the same sequence)
     step_tile = {}
@@ -129,8 +82,7 @@ def run(tiles, seed, release="stage"):
                     for s in [s for s, tt in step_tile.items() if tt == wt - 1]:
                         for k in ("S", "dP", "dQ"):
                             need((k, s) in done, f"K/V of work tile {wt} loaded before {k}{s} completed")
-                B["kv"].expect_tx(2)
-                loads.append(("kv", 2, ("kv", wt)))
+                M.load("kv", 2, ("kv", wt))
 
             if wt == 0:
                 yield from issue_kv()
@@ -148,8 +100,7 @@ def run(tiles, seed, release="stage"):
                     for k in ("S", "dP", "dV", "dK"):
                         need((k, j) in done, f"stage {st} reloaded for step {i} before {k}{j} completed")
                 step_tile[i] = wt
-                B[f"full{st}"].expect_tx(1)
-                loads.append((f"full{st}", 1, ("qdo", i)))
+                M.load(f"full{st}", 1, ("qdo", i))
                 i += 1
                 yield None
             if not kv_issued:
@@ -252,35 +203,7 @@ def run(tiles, seed, release="stage"):
                 wt += 1
 
     roles = {"prod": producer(), "i1": issuer1(), "i2": issuer2(), "ew": group("ew"), "dr": group("dq")}
-    blocked = {k: None for k in roles}
-    alive = set(roles)
-    for tick in range(400000):
-        cands = [("role", k) for k in alive if blocked[k] is None or B[blocked[k][0]].passes(blocked[k][1])]
-        if loads:
-            cands.append(("load", None))
-        cands += [("pipe", w) for w in (1, 2) if pipe[w]]
-        if not cands:
-            if alive:
-                return "deadlock", errors + [f"deadlock: {sorted((k, blocked[k]) for k in alive)}"]
-            return "ok", errors
-        c = rnd.choice(cands)
-        if c[0] == "role":
-            k = c[1]
-            try:
-                blocked[k] = next(roles[k])
-            except StopIteration:
-                alive.discard(k)
-        elif c[0] == "load":
-            name, b, what = loads.pop(rnd.randrange(len(loads)))
-            done.add(what)
-            B[name].tx_done(b)
-        else:
-            op = pipe[c[1]].pop(0)
-            if op[0] == "mma":
-                done.add(op[1])
-            else:
-                B[op[1]].arrive()
-    return "timeout", errors
+    return M.run(roles), M.errors
 
 
 def _cases(n):

@@ -1,0 +1,161 @@
+"""A model of the forward kernel's barrier protocol, checked over random interleavings.
+
+The roles of fwd_tc_kernel (exact_io_aware_38_gb300/csrc/fa_fwd_sm103.cu) for one CTA (two query
+tiles against the union of the key tiles they see) are modelled with the kernel's waits, arrivals
+and commits (tests/mbarrier_model.py gives the machine and the mbarrier rule):
+  producer   Q once; the first key tile's K alone into the K half of the last ring buffer; then
+             stage t in buffer t % stages: V of union tile t and K of tile t + 1 under one
+             arrive.expect_tx, after the buffer's previous use has been released (empty); when
+             query tile 0 skips tile t it also arrives for tile 0's softmax (the stand-in);
+  issuer     S_x(0); then per tile: wait stage t (its copies and tile 0's P_0(t)), PV_0(t),
+             S_0(t+1), wait P_1(t), PV_1(t), S_1(t+1), release the buffer; O done at the end;
+  softmax x  per visible tile: wait S_x, write P_x over S_x (reading O_x for the rescale), arrive
+             on stage t's barrier (x = 0) or on p_ready (x = 1); at the end wait for O.
+Checked: no deadlock, and no hazard: a buffer reloaded before the MMAs that read its V and K
+completed; an MMA issued before its operands landed or its P was written; S_x overwritten before
+its P_x was written; O_x rescaled while an earlier PV_x is unfinished; O read before all PV_x.
+A planted mistake (the buffer's release committed before its last reader is issued) must be found.
+"""
+import random
+
+from mbarrier_model import Machine
+
+
+def run(union, has1, stages, seed, early_release=False):
+    """union: [(v0, v1)] per union key tile (at least one of the two set)."""
+    M = Machine(seed)
+    B, bar, wait, need, done = M.B, M.bar, M.wait, M.need, M.done
+    bar("q", 1)
+    bar("k0", 1)
+    for i in range(stages):
+        bar(f"full{i}", 2)  # the producer's arrive.expect_tx + tile 0's softmax (or the stand-in)
+        bar(f"empty{i}", 1)
+    for x in (0, 1):
+        bar(f"sfull{x}", 1)
+        bar(f"odone{x}", 1)
+    bar("pready1", 1)  # 128 softmax threads of tile 1, modelled as one arrival
+    U = len(union)
+    vis = lambda x, t: t < U and bool(union[t][x])
+
+    def producer():
+        M.load("q", 1, ("Q",))
+        if U == 0:
+            return
+        M.load("k0", 1, ("K", 0))
+        for t in range(U):
+            b = t % stages
+            uses = t // stages + (1 if b == stages - 1 else 0)
+            if uses > 0:
+                yield from wait(f"empty{b}", (uses - 1) & 1)
+                tv, tk = t - stages, t - stages + 1  # previous V and K of this buffer
+                for x in (0, 1):
+                    if tv >= 0 and vis(x, tv):
+                        need((f"PV{x}", tv) in done, f"buffer {b} reloaded before PV{x}({tv}) completed")
+                    if vis(x, tk):
+                        need((f"S{x}", tk) in done, f"buffer {b} reloaded before S{x}({tk}) completed")
+            M.expect(f"full{b}", 2 if t + 1 < U else 1)
+            M.copy(f"full{b}", 1, ("V", t))
+            if t + 1 < U:
+                M.copy(f"full{b}", 1, ("K", t + 1))
+            if not vis(0, t):
+                B[f"full{b}"].arrive()  # stands in for tile 0's softmax
+            yield None
+
+    def issuer():
+        last_p = {0: None, 1: None}  # the latest tile whose P_x the issuer has consumed
+
+        def issue_s(x, t):
+            need(("K", t) in done, f"S{x}({t}) issued before K({t}) landed")
+            if last_p[x] is not None:
+                need((f"P{x}", last_p[x]) in done, f"S{x}({t}) over S{x} before P{x}({last_p[x]}) was written")
+            M.mma("i", (f"S{x}", t))
+            M.commit("i", f"sfull{x}")
+
+        def issue_pv(x, t):
+            need(("V", t) in done, f"PV{x}({t}) issued before V({t}) landed")
+            need((f"P{x}", t) in done, f"PV{x}({t}) issued before P{x}({t}) was written")
+            M.mma("i", (f"PV{x}", t))
+            last_p[x] = t
+
+        yield from wait("q", 0)
+        if U == 0:
+            return
+        yield from wait("k0", 0)
+        for x in (0, 1):
+            if vis(x, 0):
+                issue_s(x, 0)
+        M.commit("i", f"empty{stages - 1}")
+        np1 = 0
+        for t in range(U):
+            b = t % stages
+            yield from wait(f"full{b}", (t // stages) & 1)
+            if early_release:
+                M.commit("i", f"empty{b}")
+            if vis(0, t):
+                issue_pv(0, t)
+            if vis(0, t + 1):
+                issue_s(0, t + 1)
+            if vis(1, t):
+                yield from wait("pready1", np1 & 1)
+                np1 += 1
+                issue_pv(1, t)
+            if vis(1, t + 1):
+                issue_s(1, t + 1)
+            if not early_release:
+                M.commit("i", f"empty{b}")
+            yield None
+        for x in (0, 1):
+            if any(vis(x, t) for t in range(U)):
+                M.commit("i", f"odone{x}")
+
+    def softmax(x):
+        yield from wait("q", 0)
+        cnt = 0
+        for t in range(U):
+            if not vis(x, t):
+                continue
+            yield from wait(f"sfull{x}", cnt & 1)
+            need((f"S{x}", t) in done, f"softmax {x} read S({t}) before it completed")
+            for tp in range(t):
+                if vis(x, tp):
+                    need((f"PV{x}", tp) in done, f"softmax {x} rescaled O at {t} before PV{x}({tp}) completed")
+            yield None
+            done.add((f"P{x}", t))
+            B[f"full{t % stages}" if x == 0 else "pready1"].arrive()
+            cnt += 1
+        if cnt:
+            yield from wait(f"odone{x}", 0)
+            for tp in range(U):
+                if vis(x, tp):
+                    need((f"PV{x}", tp) in done, f"O{x} read before PV{x}({tp}) completed")
+
+    roles = {"prod": producer(), "mma": issuer(), "sm0": softmax(0)}
+    if has1:
+        roles["sm1"] = softmax(1)
+    return M.run(roles), M.errors
+
+
+def _cases(n):
+    for seed in range(n):
+        r = random.Random(seed * 104729)
+        has1 = r.random() < 0.8
+        U = r.randint(0, 12)
+        union = []
+        for _ in range(U):
+            v0 = r.random() < 0.7
+            v1 = has1 and (not v0 or r.random() < 0.7)
+            union.append((v0, v1 if has1 else False))
+        union = [u for u in union if u[0] or u[1]]
+        yield union, has1, r.choice([2, 4]), seed
+
+
+def test_protocol_has_no_deadlock_or_hazard():
+    for union, has1, stages, seed in _cases(3000):
+        res, errs = run(union, has1, stages, seed)
+        assert res == "ok" and not errs, (union, has1, stages, seed, res, errs[:3])
+
+
+def test_model_finds_an_early_buffer_release():
+    found = [seed for union, has1, stages, seed in _cases(3000)
+             if run(union, has1, stages, seed, early_release=True)[1]]
+    assert found, "the model no longer sees a buffer released before its readers"
