@@ -175,10 +175,24 @@ def _ptr(t):
 def _check_qkv(*ts):
     ref = ts[0]
     for t in ts:
-        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape == ref.shape):
-            raise ValueError("q, k, v, o, dO must be contiguous bf16 CUDA tensors of one shape [B, H, N, d]")
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape == ref.shape
+                and t.device == ref.device):
+            raise ValueError("q, k, v, o, dO must be contiguous bf16 CUDA tensors of one shape [B, H, N, d], "
+                             "on one device")
     if ref.dim() != 4:
         raise ValueError("expected [B, H, N, d]")
+
+
+def _check_aux(name, t, dtype, numel, dev):
+    """An optional buffer the kernels read or write: None, or a contiguous tensor of `dtype` with at
+    least `numel` elements on `dev` (dtype None: any, sized in bytes)."""
+    if t is None:
+        return
+    n = t.numel() * t.element_size() if dtype is None else t.numel()
+    if not ((dtype is None or t.dtype == dtype) and t.is_contiguous() and t.device == dev and n >= numel):
+        kind = "" if dtype is None else f" {dtype}"
+        unit = "bytes" if dtype is None else "elements"
+        raise ValueError(f"{name} must be a contiguous{kind} tensor with at least {numel} {unit} on {dev}")
 
 
 def _check_kv(q, k, v):
@@ -221,6 +235,9 @@ def fwd(q, k, v, *, causal=False, block_mask=None, seqlens_k=None, scale=None, o
     o = torch.empty_like(q) if out is None else out
     _check_qkv(q, o)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_aux("lse", lse, torch.float32, B * H * N, q.device)
+    _check_aux("tile_visits", tile_visits, torch.int32, B * H * ((N + 127) // 128), q.device)
+    _check_aux("status", status, torch.int32, 1, q.device)
     rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, N, d,
                     int(causal), _ptr(block_mask), _ptr(seqlens_k), scale, _ptr(tile_visits), _ptr(status),
                     _stream(stream))
@@ -246,6 +263,9 @@ def bwd(q, k, v, o, lse, do, *, causal=False, block_mask=None, seqlens_k=None, s
     nbytes = fa_bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check_aux("lse", lse, torch.float32, B * H * N, q.device)
+    _check_aux("workspace", workspace, None, nbytes, q.device)
+    _check_aux("status", status, torch.int32, 1, q.device)
     rc = fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, d, int(causal), _ptr(block_mask),
                     _ptr(seqlens_k), scale, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
@@ -300,6 +320,16 @@ def _lse_shape(q, p, packed):
     return (p.H, q.shape[0]) if packed else (p.B, p.H, p.seqlen_q)
 
 
+def _lse_numel(q, p, packed):
+    return math.prod(_lse_shape(q, p, packed))
+
+
+def _same_device(q, *ts):
+    for t in ts:
+        if t is not None and t.device != q.device:
+            raise ValueError(f"every tensor must be on {q.device}")
+
+
 def fwd_varlen(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, *,
                causal=False, scale=None, out=None, lse=None, status=None, stream=None):
     """O, LSE for a fixed-length batch of [B, N, H, d] views (any strides; N_q may differ from
@@ -308,6 +338,9 @@ def fwd_varlen(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
     p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale)
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty(_lse_shape(q, p, packed), dtype=torch.float32, device=q.device) if lse is None else lse
+    _same_device(q, k, v, o)
+    _check_aux("lse", lse, torch.float32, _lse_numel(q, p, packed), q.device)
+    _check_aux("status", status, torch.int32, 1, q.device)
     rc = fa_fwd_varlen(p, q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed), v.data_ptr(),
                        _view(v, packed), o.data_ptr(), _view(o, packed), lse.data_ptr(), _ptr(status), _stream(stream))
     if rc != 0:
@@ -325,6 +358,10 @@ def bwd_varlen(q, k, v, o, lse, do, cu_seqlens_q=None, cu_seqlens_k=None, max_se
     nbytes = fa_bwd_varlen_workspace_bytes(p)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _same_device(q, k, v, o, do, dq, dk, dv)
+    _check_aux("lse", lse, torch.float32, _lse_numel(q, p, packed), q.device)
+    _check_aux("workspace", workspace, None, nbytes, q.device)
+    _check_aux("status", status, torch.int32, 1, q.device)
     rc = fa_bwd_varlen(p, q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed), v.data_ptr(),
                        _view(v, packed), o.data_ptr(), _view(o, packed), do.data_ptr(), _view(do, packed),
                        lse.data_ptr(), dq.data_ptr(), _view(dq, packed), dk.data_ptr(), _view(dk, packed),
@@ -351,6 +388,10 @@ def fwd_splitkv(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None
     nbytes = fa_fwd_splitkv_workspace_bytes(p, num_splits)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _same_device(q, k, v, o)
+    _check_aux("lse", lse, torch.float32, _lse_numel(q, p, packed), q.device)
+    _check_aux("workspace", workspace, None, nbytes, q.device)
+    _check_aux("status", status, torch.int32, 1, q.device)
     rc = fa_fwd_splitkv(p, num_splits, q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed), v.data_ptr(),
                         _view(v, packed), o.data_ptr(), _view(o, packed), lse.data_ptr(), workspace.data_ptr(),
                         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
@@ -367,6 +408,8 @@ def fwd_partial(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None
     """Partial of one key block: (O fp32 [rows, d], LSE fp32 [rows]) in the LSE's row order."""
     p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale)
     rows = int(lib().fa_partial_rows(ctypes.byref(p)))
+    _same_device(q, k, v)
+    _check_aux("status", status, torch.int32, 1, q.device)
     po = torch.empty((rows, p.d), dtype=torch.float32, device=q.device)
     pl = torch.full((rows,), float("-inf"), dtype=torch.float32, device=q.device)
     rc = int(lib().fa_fwd_partial(ctypes.byref(p), q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed),
@@ -381,6 +424,10 @@ def merge_partials(q, k, acc, part, cu_seqlens_q=None, cu_seqlens_k=None, max_se
                    *, stream=None):
     """acc <- merge(acc, part) in place (both from fwd_partial for the same query rows)."""
     p, _ = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, False, None)
+    rows = int(lib().fa_partial_rows(ctypes.byref(p)))
+    for name, (t_o, t_l) in (("acc", acc), ("part", part)):
+        _check_aux(name + " O", t_o, torch.float32, rows * p.d, q.device)
+        _check_aux(name + " LSE", t_l, torch.float32, rows, q.device)
     rc = int(lib().fa_merge_partials(ctypes.byref(p), acc[0].data_ptr(), acc[1].data_ptr(), part[0].data_ptr(),
                                      part[1].data_ptr(), _stream(stream)))
     if rc != 0:
@@ -394,6 +441,11 @@ def finalize_partials(q, k, acc, cu_seqlens_q=None, cu_seqlens_k=None, max_seqle
     p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, False, None)
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty(_lse_shape(q, p, packed), dtype=torch.float32, device=q.device) if lse is None else lse
+    rows = int(lib().fa_partial_rows(ctypes.byref(p)))
+    _same_device(q, o)
+    _check_aux("acc O", acc[0], torch.float32, rows * p.d, q.device)
+    _check_aux("acc LSE", acc[1], torch.float32, rows, q.device)
+    _check_aux("lse", lse, torch.float32, _lse_numel(q, p, packed), q.device)
     rc = int(lib().fa_finalize_partials(ctypes.byref(p), acc[0].data_ptr(), acc[1].data_ptr(), o.data_ptr(),
                                         _view(o, packed), lse.data_ptr(), _stream(stream)))
     if rc != 0:

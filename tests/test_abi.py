@@ -120,6 +120,28 @@ def test_binding_refuses_cpu_tensors(L):
         fa.fwd(q, q, q)
 
 
+def test_binding_checks_optional_buffers(L):
+    """lse, status, tile visits, workspace and partials handed to the kernels: dtype, size,
+    contiguity and device are checked before any call (sizes are minimums)."""
+    import torch
+
+    dev = torch.device("cpu")
+    fa._check_aux("lse", None, torch.float32, 6, dev)
+    fa._check_aux("lse", torch.zeros(6), torch.float32, 6, dev)
+    fa._check_aux("lse", torch.zeros(8), torch.float32, 6, dev)
+    for bad in (torch.zeros(5), torch.zeros(6, dtype=torch.bfloat16), torch.zeros(12)[::2],
+                torch.zeros(6, device="meta")):
+        with pytest.raises(ValueError):
+            fa._check_aux("lse", bad, torch.float32, 6, dev)
+    fa._check_aux("workspace", torch.zeros(64, dtype=torch.uint8), None, 64, dev)
+    fa._check_aux("workspace", torch.zeros(16), None, 64, dev)  # sized in bytes
+    with pytest.raises(ValueError):
+        fa._check_aux("workspace", torch.zeros(64, dtype=torch.uint8), None, 65, dev)
+    fa._same_device(torch.zeros(1), torch.zeros(2), None)
+    with pytest.raises(ValueError):
+        fa._same_device(torch.zeros(1), torch.zeros(1, device="meta"))
+
+
 def varlen_rc(bwd=False, problem=None, **kw):
     p = fa.VarlenProblem(2, 4, 2, 64, 100, 120, None, None, 0, 0, 1, 0.125) if problem is None else problem
     for name, val in kw.items():
