@@ -42,8 +42,12 @@ class Bar:
 
 
 class Machine:
-    def __init__(self, seed):
+    def __init__(self, seed, abort_p=0.0):
         self.rnd = random.Random(seed)
+        # Bounded waits: with probability abort_p a blocked wait runs out; from then on (the CTA's
+        # abort flag is set) every wait returns at once, as in the kernels.
+        self.abort_p = abort_p
+        self.aborted = False
         self.B = {}
         self.loads = []  # (barrier, bytes, record)
         self.pipe = {}
@@ -58,8 +62,14 @@ class Machine:
             self.errors.append(msg)
 
     def wait(self, name, parity):
+        """Generator; its return value is True once the phase has completed, False if the wait ran
+        out (or the abort flag was already set)."""
         while not self.B[name].passes(parity):
+            if self.aborted or (self.abort_p and self.rnd.random() < self.abort_p):
+                self.aborted = True
+                return False
             yield (name, parity)
+        return True
 
     def load(self, name, nbytes, record):
         """One arrival with its byte count, and the copy that delivers the bytes."""
@@ -84,8 +94,9 @@ class Machine:
         blocked = {k: None for k in roles}
         alive = set(roles)
         for _ in range(max_ticks):
+            # With bounded waits a blocked role stays schedulable: resumed, its wait may run out.
             cands = [("role", k) for k in sorted(alive)
-                     if blocked[k] is None or self.B[blocked[k][0]].passes(blocked[k][1])]
+                     if blocked[k] is None or self.abort_p or self.B[blocked[k][0]].passes(blocked[k][1])]
             if self.loads:
                 cands.append(("load", None))
             cands += [("pipe", w) for w in sorted(self.pipe) if self.pipe[w]]
