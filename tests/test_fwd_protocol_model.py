@@ -18,12 +18,13 @@ A planted mistake (the buffer's release committed before its last reader is issu
 """
 import random
 
+import pytest
 from mbarrier_model import Machine
 
 
-def run(union, has1, stages, seed, early_release=False):
+def run(union, has1, stages, seed, early_release=False, abort_p=0.0):
     """union: [(v0, v1)] per union key tile (at least one of the two set)."""
-    M = Machine(seed)
+    M = Machine(seed, abort_p)
     B, bar, wait, need, done = M.B, M.bar, M.wait, M.need, M.done
     bar("q", 1)
     bar("k0", 1)
@@ -45,20 +46,22 @@ def run(union, has1, stages, seed, early_release=False):
         for t in range(U):
             b = t % stages
             uses = t // stages + (1 if b == stages - 1 else 0)
+            ok = True
             if uses > 0:
-                yield from wait(f"empty{b}", (uses - 1) & 1)
+                ok = yield from wait(f"empty{b}", (uses - 1) & 1)
                 tv, tk = t - stages, t - stages + 1  # previous V and K of this buffer
                 for x in (0, 1):
                     if tv >= 0 and vis(x, tv):
                         need((f"PV{x}", tv) in done, f"buffer {b} reloaded before PV{x}({tv}) completed")
                     if vis(x, tk):
                         need((f"S{x}", tk) in done, f"buffer {b} reloaded before S{x}({tk}) completed")
-            M.expect(f"full{b}", 2 if t + 1 < U else 1)
-            M.copy(f"full{b}", 1, ("V", t))
-            if t + 1 < U:
-                M.copy(f"full{b}", 1, ("K", t + 1))
-            if not vis(0, t):
-                B[f"full{b}"].arrive()  # stands in for tile 0's softmax
+            if ok:  # the kernel issues the stage only after its wait succeeded
+                M.expect(f"full{b}", 2 if t + 1 < U else 1)
+                M.copy(f"full{b}", 1, ("V", t))
+                if t + 1 < U:
+                    M.copy(f"full{b}", 1, ("K", t + 1))
+                if not vis(0, t):
+                    B[f"full{b}"].arrive()  # stands in for tile 0's softmax
             yield None
 
     def issuer():
@@ -159,3 +162,15 @@ def test_model_finds_an_early_buffer_release():
     found = [seed for union, has1, stages, seed in _cases(3000)
              if run(union, has1, stages, seed, early_release=True)[1]]
     assert found, "the model no longer sees a buffer released before its readers"
+
+
+@pytest.mark.xfail(strict=True, raises=AssertionError, reason=(
+    "after an abort the issuer stops waiting for a stage, so its release can come early: the producer "
+    "can give the stage barrier a second arrive.expect_tx while a copy is in flight, and tile 0's "
+    "softmax can arrive for a later use of the buffer before the current phase completed (pending-"
+    "count underflows the PTX rules leave undefined); both need an abort-flag check"))
+def test_abort_path_terminates():
+    """Waits that run out at random points: every role still leaves its loops."""
+    for union, has1, stages, seed in _cases(1500):
+        res, _ = run(union, has1, stages, seed, abort_p=0.02)
+        assert res == "ok", (union, has1, stages, seed, res)
