@@ -40,13 +40,14 @@ METRIC = "attention TFLOP/s fwd+bwd (bf16, causal N=8192 d=128) and % of BF16 te
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="fa", choices=["fa", "reference"])
     p.add_argument("--workload", default="c4", choices=sorted(workloads.WORKLOADS) + ["dec"],
                    help="dec: decode-shaped forward (informational; its own metric, HBM GB/s)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    p.add_argument("--no-secondary", action="store_true", help="skip the other workloads' figures (profiling runs)")
     p.add_argument("--heads", type=int, default=None, help="override H (smaller profiling cases only)")
     p.add_argument("--flush-l2", action="store_true",
                    help="write 256 MiB before each timed step (outside its events); step time from the events")
@@ -315,6 +316,185 @@ def run_decode(args):
     }), flush=True)
 
 
+def make_device_buffers(w, H, seed, dev):
+    """Seeded inputs of workload `w` on `dev` and the output / workspace buffers of one step."""
+    import exact_io_aware_38_gb300 as fa
+
+    inp = workloads.make_inputs(w, H=H, seed=seed)
+    B, Hq, N, d = inp["q"].shape
+    t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
+    t["bm"] = None if inp["block_mask"] is None else inp["block_mask"].to(dev)
+    t["sl"] = None if inp["seqlens_k"] is None else inp["seqlens_k"].to(dev)
+    t["o"] = torch.empty_like(t["q"])
+    t["lse"] = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    t["dq"], t["dk"], t["dv"] = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["k"])
+    t["ws"] = torch.empty(fa.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+    t["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
+    return inp, t
+
+
+def time_device_steps(w, t, steps, warmup, flush_l2, stream, clocks=None, barrier=lambda: None):
+    """Per-step device times (ms) of fwd, the whole bwd call and its main pass, and the step, from
+    CUDA events on the launching stream; the span over all steps. With flush_l2, 256 MiB are
+    written before each step, outside its events."""
+    import exact_io_aware_38_gb300 as fa
+
+    kw = dict(causal=w.causal, block_mask=t["bm"], seqlens_k=t["sl"], scale=w.scale, status=t["status"])
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(E(), E(), E(), E(), E()) for _ in range(steps)]
+    warm_ev = (E(), E())
+
+    def step(e):
+        fa.fwd(t["q"], t["k"], t["v"], out=t["o"], lse=t["lse"], **kw)
+        if e is not None:
+            e[1].record(stream)
+        fa.bwd(t["q"], t["k"], t["v"], t["o"], t["lse"], t["do"], dq=t["dq"], dk=t["dk"], dv=t["dv"],
+               workspace=t["ws"], main_events=(e[2], e[3]) if e is not None else warm_ev, **kw)
+
+    for _ in range(max(3, warmup)):
+        step(None)
+    torch.cuda.synchronize()
+    assert int(t["status"].item()) == 0, fa.fa_status_string(int(t["status"].item()))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=stream.device) if flush_l2 else None
+    start, end = E(), E()
+    barrier()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+        clocks.mark("t_start")
+    start.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()  # evicts the previous step's data from the 129 MB L2
+        ev[i][0].record(stream)
+        step(ev[i])
+        ev[i][4].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark("t_end")
+    barrier()
+    assert int(t["status"].item()) == 0, fa.fa_status_string(int(t["status"].item()))
+    return {
+        "span_ms": start.elapsed_time(end) / steps,
+        "step": [e[0].elapsed_time(e[4]) for e in ev],
+        "fwd": [e[0].elapsed_time(e[1]) for e in ev],
+        "bwd": [e[1].elapsed_time(e[4]) for e in ev],
+        "main": [e[2].elapsed_time(e[3]) for e in ev],
+    }
+
+
+def run_e2e(w, inp, t, steps, flops_total, dev, pg, world, barrier):
+    """The same step end to end through the public API from pinned host buffers: every step copies
+    its Q, K, V, dO in and its O, LSE, dQ, dK, dV out. Copies run on their own streams: dO's upload
+    overlaps the forward, O/LSE's download the backward, and (two sets of device and host buffers)
+    one step's downloads overlap the next step's uploads and forward."""
+    import exact_io_aware_38_gb300 as fa
+
+    B, H, N, d = inp["q"].shape
+    host_in = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    sets = []
+    for _ in range(2):
+        dv = {n: torch.empty_like(t[n]) for n in ("q", "k", "v", "do", "o", "lse", "dq", "dk", "dv", "ws")}
+        hv = {n: torch.empty(t[n].shape, dtype=t[n].dtype).pin_memory() for n in ("o", "lse", "dq", "dk", "dv")}
+        sets.append((dv, hv))
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in sets[0][1].values())
+    s_c = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    E = lambda: torch.cuda.Event()
+    ev = [{k: E() for k in ("qkv", "do", "fwd", "bwd", "out")} for _ in range(2)]
+    kw = dict(causal=w.causal, block_mask=t["bm"], seqlens_k=t["sl"], scale=w.scale, status=t["status"])
+
+    def e2e_step(i):
+        D, Hh = sets[i % 2]
+        e = ev[i % 2]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(e["bwd"])  # step i - 2 has finished reading this set's inputs
+            for n in ("q", "k", "v"):
+                D[n].copy_(host_in[n], non_blocking=True)
+            e["qkv"].record(s_in)
+            D["do"].copy_(host_in["do"], non_blocking=True)
+            e["do"].record(s_in)
+        s_c.wait_event(e["qkv"])
+        if i >= 2:
+            s_c.wait_event(e["out"])  # step i - 2's results have left this set's output buffers
+        fa.fwd(D["q"], D["k"], D["v"], out=D["o"], lse=D["lse"], stream=s_c, **kw)
+        e["fwd"].record(s_c)
+        s_c.wait_event(e["do"])
+        fa.bwd(D["q"], D["k"], D["v"], D["o"], D["lse"], D["do"], dq=D["dq"], dk=D["dk"], dv=D["dv"],
+               workspace=D["ws"], stream=s_c, **kw)
+        e["bwd"].record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(e["fwd"])
+            Hh["o"].copy_(D["o"], non_blocking=True)
+            Hh["lse"].copy_(D["lse"], non_blocking=True)
+            s_out.wait_event(e["bwd"])
+            for n in ("dq", "dk", "dv"):
+                Hh[n].copy_(D[n], non_blocking=True)
+            e["out"].record(s_out)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for i in range(steps):
+        e2e_step(3 + i)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_c)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    assert int(t["status"].item()) == 0, fa.fa_status_string(int(t["status"].item()))
+    ms = t0.elapsed_time(t1) / steps
+    ms = max_over_ranks(ms, pg, dev)
+    # the last step's results against the device-resident run (same inputs, same kernels)
+    D, Hh = sets[(3 + steps - 1) % 2]
+    assert torch.equal(Hh["o"], t["o"].cpu()) and torch.equal(Hh["dk"], t["dk"].cpu())
+    return {"value": flops_total * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "copies": "pinned host <-> device on two copy streams, double-buffered, overlapping the kernels"}
+
+
+def secondary_figures(names, steps, warmup, dev, peak):
+    """Device step figures of the other workloads (each its own seeded inputs), with the fraction of
+    the same peak; for the L2-resident ones also the figure with L2 flushed before each step."""
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        inp, t = make_device_buffers(w, None, w.seed, dev)
+        B, H, N, d = inp["q"].shape
+        fl = rl.attention_flops(B, H, N, d, causal=w.causal,
+                                block_mask=None if inp["block_mask"] is None else inp["block_mask"].numpy())
+        r = time_device_steps(w, t, steps, warmup, False, stream)
+        step_ms = statistics.median(r["step"])
+        rec = {"workload": workload_label(w, B, H, N, d) + " fwd+bwd", "ms_per_step": step_ms,
+               "value": fl["total"] / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "fwd_ms": statistics.median(r["fwd"]), "bwd_ms": statistics.median(r["bwd"]),
+               "bwd_main_ms": statistics.median(r["main"])}
+        rec["frac"] = rec["value"] / peak
+        in_bytes = sum(t[n].numel() * t[n].element_size() for n in ("q", "k", "v", "do"))
+        if in_bytes <= 129e6:
+            rf = time_device_steps(w, t, steps, warmup, True, stream)
+            ms_f = statistics.median(rf["step"])
+            rec["l2"] = f"inputs {in_bytes / 2**20:.0f} MiB fit in the 129 MB L2: value is L2-warm"
+            rec["l2_flushed"] = {"ms_per_step": ms_f, "value": fl["total"] / (ms_f * 1e-3) / 1e12,
+                                 "frac": fl["total"] / (ms_f * 1e-3) / 1e12 / peak}
+        else:
+            rec["l2"] = f"inputs {in_bytes / 2**20:.0f} MiB > 129 MB L2; no flush"
+        up = useful_padding(w, None if inp["seqlens_k"] is None else inp["seqlens_k"].numpy(), H, N, d, step_ms, 1)
+        if up is not None:
+            rec["useful_padding"] = up
+        out[name] = rec
+        del t
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     if args.workload == "dec":
@@ -338,119 +518,42 @@ def main():
     build.build()
     fa.lib()
 
-    inp = workloads.make_inputs(w, H=args.heads, seed=w.seed + rank)
-    B, H, N, d = w.B, (w.H if args.heads is None else args.heads), w.N, w.d
-    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
-    bm = None if inp["block_mask"] is None else inp["block_mask"].to(dev)
-    sl = None if inp["seqlens_k"] is None else inp["seqlens_k"].to(dev)
-    kw = dict(causal=w.causal, block_mask=bm, seqlens_k=sl, scale=w.scale)
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
-    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    launches_per_step = 4  # fwd kernel; bwd pre, main, post
-
-    def step():
-        fa.fwd(q, k, v, out=o, lse=lse, status=status, **kw)
-        fa.bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, status=status, **kw)
-
     def barrier():
         if pg is not None:
             pg.barrier()
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+    inp, t = make_device_buffers(w, args.heads, w.seed + rank, dev)
+    B, H, N, d = inp["q"].shape
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 4  # fwd kernel; bwd pre, main, post
 
-    # ---- timed region (device-resident inputs; inputs 4 x 64 MiB > L2, so no flush between steps)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
+    # ---- timed region (device-resident inputs; 4 x 64 MiB of inputs > L2, so no flush between steps)
     clocks = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    clocks.mark("t_start")
-    start.record(stream)
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()  # evicts the previous step's data from the 129 MB L2
-        ev[i][0].record(stream)
-        fa.fwd(q, k, v, out=o, lse=lse, status=status, **kw)
-        ev[i][1].record(stream)
-        fa.bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, status=status, **kw)
-        ev[i][2].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark("t_end")
+    r = time_device_steps(w, t, args.steps, args.warmup, args.flush_l2, stream, clocks, barrier)
     clk = clocks.stop()
-    barrier()
-    ms = start.elapsed_time(end) / args.steps
-    if flush is not None:  # the flushes lie between the steps' events
-        ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    step_pct = percentiles([e[0].elapsed_time(e[2]) for e in ev])  # this rank's steps
+    ms = r["span_ms"] if not args.flush_l2 else statistics.mean(r["step"])  # flushes lie between steps
     ms = max_over_ranks(ms, pg, dev)
-    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+    fwd_ms, bwd_ms, main_ms = (statistics.mean(r[k]) for k in ("fwd", "bwd", "main"))
+    step_pct = percentiles(r["step"])  # this rank's steps
 
     flops = rl.attention_flops(B, H, N, d, causal=w.causal,
                                block_mask=None if inp["block_mask"] is None else inp["block_mask"].numpy())
     value = flops["total"] * world / (ms * 1e-3) / 1e12
 
-    # ---- end to end through the public API with pinned host buffers
-    def run_e2e():
-        hq, hk, hv, hdo = (inp[n].pin_memory() for n in ("q", "k", "v", "do"))
-        ho, hdq = (torch.empty_like(hq).pin_memory() for _ in range(2))
-        hdk, hdv = (torch.empty_like(hk).pin_memory() for _ in range(2))
-        hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+    e2e = None if args.no_e2e else run_e2e(w, inp, t, args.steps, flops["total"], dev, pg, world, barrier)
 
-        def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            do.copy_(hdo, non_blocking=True)
-            step()
-            ho.copy_(o, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
-            hdq.copy_(dq, non_blocking=True)
-            hdk.copy_(dk, non_blocking=True)
-            hdv.copy_(dv, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s2.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e2.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = s2.elapsed_time(e2) / args.steps
-        e2e_ms = max_over_ranks(e2e_ms, pg, dev)
-        return {"value": flops["total"] * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
-
-    e2e = None if args.no_e2e else run_e2e()
-
-    in_mib = sum(t.numel() * t.element_size() for t in (q, k, v, do)) / 2**20
+    in_mib = sum(t[n].numel() * t[n].element_size() for n in ("q", "k", "v", "do")) / 2**20
     l2_note = (f"inputs {in_mib:.0f} MiB > 129 MB L2; no flush" if in_mib * 2**20 > 129e6 else
                f"inputs {in_mib:.0f} MiB fit in the 129 MB L2: L2-warm, not a contract number")
-    if flush is not None:
+    if args.flush_l2:
         l2_note = f"inputs {in_mib:.0f} MiB; L2 flushed (256 MiB written) before each step, outside its events"
     peaks = load_peaks()
-    # Dominant launch group: the backward call (pre + main + post in one event span).
-    bwd_tflops = flops["bwd"] / (bwd_ms * 1e-3) / 1e12
+    # The timed region is short (tens of ms at full clock, no power cap), so the burst peak applies.
+    peak = peaks["bf16_tflops"]
+    # Dominant launch: the backward main kernel, timed alone by events around its launch.
+    main_tflops = flops["bwd"] / (main_ms * 1e-3) / 1e12
     fwd_tflops = flops["fwd"] / (fwd_ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    bwd_tflops = flops["bwd"] / (bwd_ms * 1e-3) / 1e12
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -458,13 +561,16 @@ def main():
         "config": {"workload": workload_label(w, B, H, N, d) + " fwd+bwd",
                    "parallelism": f"replicas x{world}", "l2": l2_note},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
-        "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops},
+        "peak_for_pct": f"{peak} TFLOP/s, {peaks['source']} bf16 burst (short timed region at full clock)",
+        "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_main_ms": main_ms, "fwd_tflops": fwd_tflops,
+                    "bwd_tflops": bwd_tflops, "bwd_main_tflops": main_tflops,
+                    "fwd_frac": fwd_tflops / peak, "bwd_frac": bwd_tflops / peak},
         "step_ms_p10_p50_p90": step_pct,
-        "roofline": {"bound": "tensor", "kernel": "bwd_tc_kernel (timed as the fa_bwd span: pre + main + post)",
-                     "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tflops / peak,
+        "roofline": {"bound": "tensor", "kernel": f"bwd_tc_kernel<{d}> (events around its launch)",
+                     "achieved": main_tflops, "peak": peak, "unit": "TFLOP/s", "frac": main_tflops / peak,
                      "traffic": kernel_traffic(f"bwd_tc_kernel<{d}>", w.name, args.heads),
                      "traffic_unit": "DRAM bytes per launch (ncu, profiles/traffic.json)",
-                     "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)"},
+                     "peak_source": f"{peaks['source']} bf16 burst (kernel timed in a short region at full clock)"},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -472,6 +578,8 @@ def main():
     up = useful_padding(w, None if inp["seqlens_k"] is None else inp["seqlens_k"].numpy(), H, N, d, ms, world)
     if up is not None:
         result["useful_padding"] = up
+    if rank == 0 and not args.no_secondary and args.heads is None and args.workload == "c4":
+        result["secondary"] = secondary_figures(["c5", "c3", "c2"], min(args.steps, 20), args.warmup, dev, peak)
     if rank == 0 and not args.no_cpu_baseline:
         heads = [(0, h) for h in range(min(3, H))]  # about 10 s of the oracle on the host cores
         t0 = time.perf_counter()

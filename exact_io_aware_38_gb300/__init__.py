@@ -5,7 +5,8 @@ library's CUDA kernels. PyTorch provides device memory and the current stream. T
 fallback: if the library is missing, every call raises.
 
 Raw C-ABI names (same signatures as ``include/fa.h``, pointers as ints):
-    fa_fwd, fa_bwd, fa_fwd_gqa, fa_bwd_gqa, fa_bwd_workspace_bytes, fa_status_string, fa_bwd_noalloc,
+    fa_fwd, fa_bwd, fa_fwd_gqa, fa_bwd_gqa, fa_bwd_ex (with the BwdExtras struct), fa_bwd_workspace_bytes,
+    fa_status_string, fa_bwd_noalloc,
     fa_fwd_varlen, fa_bwd_varlen, fa_bwd_varlen_workspace_bytes (with the Strides / VarlenProblem structs)
 Tensor helpers (grouped-query attention when k, v have fewer heads than q):
     fwd(q, k, v, ...) -> (o, lse);  bwd(q, k, v, o, lse, do, ...) -> (dq, dk, dv)
@@ -46,6 +47,12 @@ class VarlenProblem(ctypes.Structure):
                 ("scale", ctypes.c_float)]
 
 
+class BwdExtras(ctypes.Structure):
+    """fa_bwd_extras (include/fa.h): optional step-visit counts and events around the main pass."""
+    _fields_ = [("step_visits", ctypes.c_void_p), ("main_begin_event", ctypes.c_void_p),
+                ("main_end_event", ctypes.c_void_p)]
+
+
 _VP = ctypes.POINTER(VarlenProblem)
 _SIGS = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P]),
@@ -55,6 +62,8 @@ _SIGS = {
     "fa_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "fa_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P,
                         ctypes.c_size_t, _P, _P]),
+    "fa_bwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P,
+                       ctypes.c_size_t, ctypes.POINTER(BwdExtras), _P, _P]),
     "fa_fwd_varlen": (_I, [_VP, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, _P]),
     "fa_bwd_varlen_workspace_bytes": (ctypes.c_size_t, [_VP]),
     "fa_bwd_varlen": (_I, [_VP, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, Strides,
@@ -128,6 +137,14 @@ def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block
                workspace_bytes, dev_status, stream) -> int:
     return int(lib().fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k,
                                 scale, workspace, workspace_bytes, dev_status, stream))
+
+
+def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k, scale, workspace,
+              workspace_bytes, extras, dev_status, stream) -> int:
+    """extras: a BwdExtras or None."""
+    x = None if extras is None else ctypes.byref(extras)
+    return int(lib().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k,
+                               scale, workspace, workspace_bytes, x, dev_status, stream))
 
 
 def fa_fwd_varlen(p, q, sq, k, sk, v, sv, o, so, lse, dev_status, stream) -> int:
@@ -247,9 +264,12 @@ def fwd(q, k, v, *, causal=False, block_mask=None, seqlens_k=None, scale=None, o
 
 
 def bwd(q, k, v, o, lse, do, *, causal=False, block_mask=None, seqlens_k=None, scale=None, dq=None, dk=None, dv=None,
-        workspace=None, status=None, stream=None):
+        workspace=None, status=None, stream=None, step_visits=None, main_events=None):
     """dQ, dK, dV of attention on the current CUDA stream (outputs/workspace allocated unless given).
-    k and v may have fewer heads than q (grouped-query attention, fa_bwd_gqa); dk, dv are shaped like k."""
+    k and v may have fewer heads than q (grouped-query attention, fa_bwd_gqa); dk, dv are shaped like k.
+    step_visits: optional int32 [B * Hkv * nb] tensor receiving the query steps the main pass visited per
+    (b, K/V head, key tile); main_events: optional (begin, end) torch.cuda.Event pair recorded around the
+    main pass (fa_bwd_ex)."""
     _check_qkv(q, o, do)
     Hkv = _check_kv(q, k, v)
     B, H, N, d = q.shape
@@ -266,10 +286,19 @@ def bwd(q, k, v, o, lse, do, *, causal=False, block_mask=None, seqlens_k=None, s
     _check_aux("lse", lse, torch.float32, B * H * N, q.device)
     _check_aux("workspace", workspace, None, nbytes, q.device)
     _check_aux("status", status, torch.int32, 1, q.device)
-    rc = fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, d, int(causal), _ptr(block_mask),
-                    _ptr(seqlens_k), scale, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                    _ptr(status), _stream(stream))
+    _check_aux("step_visits", step_visits, torch.int32, B * Hkv * ((N + 127) // 128), q.device)
+    extras = None
+    if step_visits is not None or main_events is not None:
+        if main_events is not None:
+            for e in main_events:
+                if not e.cuda_event:  # torch creates its event at the first record
+                    e.record()
+        ev = (None, None) if main_events is None else tuple(e.cuda_event for e in main_events)
+        extras = BwdExtras(_ptr(step_visits), ev[0], ev[1])
+    rc = fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, d, int(causal), _ptr(block_mask),
+                   _ptr(seqlens_k), scale, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                   extras, _ptr(status), _stream(stream))
     if rc != 0:
         raise FaError(rc)
     return dq, dk, dv

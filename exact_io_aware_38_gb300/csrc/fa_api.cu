@@ -155,13 +155,13 @@ struct BwdTensors {
 };
 
 int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* workspace, size_t workspace_bytes,
-               int* dev_status, void* stream) {
+               int* dev_status, void* stream, const fa_bwd_extras* extras = nullptr) {
   if (!t.q || !t.k || !t.v || !t.o || !t.dout || !t.lse || !t.dq || !t.dk || !t.dv || !workspace)
     return FA_ERR_INVALID_ARG;
   if (workspace_bytes < workspace_for(s)) return FA_ERR_INVALID_ARG;
   if (!aligned(t.q, 16) || !aligned(t.k, 16) || !aligned(t.v, 16) || !aligned(t.o, 16) || !aligned(t.dout, 16) ||
       !aligned(t.dq, 16) || !aligned(t.dk, 16) || !aligned(t.dv, 16) || !aligned(t.lse, 4) ||
-      !aligned(workspace, kAlign) || !aligned(dev_status, 4))
+      !aligned(workspace, kAlign) || !aligned(dev_status, 4) || (extras && !aligned(extras->step_visits, 4)))
     return FA_ERR_MISALIGNED;
   FaBwdArgs a;
   a.q = t.q;
@@ -189,6 +189,9 @@ int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* w
   a.s = s;
   a.scale = scale;
   a.status = dev_status;
+  a.step_visits = extras ? extras->step_visits : nullptr;
+  a.ev_main_begin = extras ? static_cast<cudaEvent_t>(extras->main_begin_event) : nullptr;
+  a.ev_main_end = extras ? static_cast<cudaEvent_t>(extras->main_end_event) : nullptr;
   const cudaError_t e = fa_launch_bwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -282,6 +285,14 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal,
                const uint8_t* block_mask, const int32_t* seqlens_k, float scale, void* workspace,
                size_t workspace_bytes, int* dev_status, void* stream) {
+  return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k, scale,
+                   workspace, workspace_bytes, nullptr, dev_status, stream);
+}
+
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+              void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal,
+              const uint8_t* block_mask, const int32_t* seqlens_k, float scale, void* workspace,
+              size_t workspace_bytes, const fa_bwd_extras* extras, int* dev_status, void* stream) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
   const int rc = check_shape(B, H, N, d, causal, scale);
   if (rc != FA_OK) return rc;
@@ -300,7 +311,7 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
   t.dv = dv;
   t.sq = t.so = t.sdo = t.sdq = contiguous(H, N, d);
   t.sk = t.sv = t.sdk = t.sdv = contiguous(Hkv, N, d);
-  return launch_bwd(s, t, scale, workspace, workspace_bytes, dev_status, stream);
+  return launch_bwd(s, t, scale, workspace, workspace_bytes, dev_status, stream, extras);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,

@@ -308,8 +308,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // four readers of item w have arrived on the slot's empty barrier.
   auto take_tile = [&](int w) -> int {  // one reader thread per role
     int tile = ntiles;  // an abandoned wait ends the loop
-    if (mbar_wait(b_tqfull(w & 1), (w >> 1) & 1, abort_flag, a.status)) tile = tile_q[w & 1];
-    mbar_arrive(b_tqempty(w & 1));
+    if (mbar_wait(b_tqfull(w & 1), (w >> 1) & 1, abort_flag, a.status)) {
+      tile = tile_q[w & 1];
+      mbar_arrive(b_tqempty(w & 1));
+    }
     return tile;
   };
 
@@ -333,7 +335,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int w = 0;; ++w) {
       int tile = ntiles;
       if (lane == 0 && (w < 2 || mbar_wait(b_tqempty(w & 1), ((w - 2) >> 1) & 1, abort_flag, a.status))) {
-        tile = w == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.tile_counter, 1);
+        // After an abort the end marker is published, so every reader leaves its tile loop.
+        tile = *abort_flag ? ntiles : (w == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.tile_counter, 1));
         tile_q[w & 1] = tile;
         mbar_arrive(b_tqfull(w & 1));  // release: the index is visible to every waiter of the phase
       }
@@ -349,6 +352,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_kv = [&]() {  // lane 0
         kv_issued = true;
         if (wt > 0 && !mbar_wait(b_done, (wt - 1) & 1, abort_flag, a.status)) return;
+        if (*abort_flag) return;  // no copy is issued after an abort (see the drain below)
 #ifndef FA_TEST_WITHHOLD_KV  // a test-only build never loads K/V: every wait on them must run out
         mbar_expect_tx(b_kv, 2 * C::kKVBytes);
         for (int c = 0; c < C::kBoxes; ++c) {
@@ -371,7 +375,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // One barrier per stage keeps the parity test unambiguous: its next phase belongs to
           // step i, not loaded yet.
           const int j = (int)i - C::kStages;
-          if (j < 0 || mbar_wait(b_empty(j % C::kStages), (j / C::kStages) & 1, abort_flag, a.status)) {
+          if ((j < 0 || mbar_wait(b_empty(j % C::kStages), (j / C::kStages) & 1, abort_flag, a.status)) &&
+              !*abort_flag) {
             mbar_expect_tx(b_full(st), 2 * C::kQBytes);
             for (int c = 0; c < C::kBoxes; ++c) {
               tma_load_4d(sQs(st) + c * C::kQBox, &tmQ, c * 64, T.seq.q0 + v * BM, T.h0 + gi, T.seq.bb, b_full(st));
@@ -390,7 +395,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0 && !kv_issued) issue_kv();
       ++wt;
     }
-    if (lane == 0 && *abort_flag) {  // let copies still in flight land before the CTA exits
+    // Let copies still in flight land before the CTA exits. A stage is reloaded only after the
+    // gradient issuer released it, which it does only for a step whose copies it saw land (a role
+    // issues and arrives only while all its waits have succeeded), so each barrier has at most one
+    // phase in flight: the last one issued, whose only arrival is the producer's own.
+    if (lane == 0 && *abort_flag) {
       if (kv_any) mbar_wait_drain(b_kv, kv_par);
       for (int k = 0; k < C::kStages; ++k)
         if (issued[k]) mbar_wait_drain(b_full(k), last_par[k]);
@@ -410,6 +419,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t dK0 = desc_kmajor_sw128(sK), dV0 = desc_kmajor_sw128(sV), mK0 = desc_mnmajor_sw128(sK, 16384);
     uint32_t sn = 0;  // global step counter (lane 0)
     int wt = 0;
+    // After its first wait that fails (a timeout, or the CTA's abort flag) the issuer issues no
+    // MMA and no commit: a release it committed for a step it did not see complete would let the
+    // producer reload a stage whose copy is still in flight.
+    bool run = true;
     for (int w = 0;; ++w) {
       int tile = 0;
       if (lane == 0) tile = take_tile(w);
@@ -421,15 +434,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (n == 0) continue;
       if (lane == 0) {
         if (warp == 1) {
-          mbar_wait_spin(b_kv, wt & 1, abort_flag, a.status);
+          if (run) run = mbar_wait_spin(b_kv, wt & 1, abort_flag, a.status);
           fence_after_sync();
-          for (int l = 0; l < n; ++l, ++sn) {
+          for (int l = 0; l < n && run; ++l, ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
-            mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
-            if (sn >= NB) {  // dV of step sn - NB has read P^T from these columns
-              mbar_wait_spin(b_sfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+            run = mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
+            if (run && sn >= NB) {  // dV of step sn - NB has read P^T from these columns
+              run = mbar_wait_spin(b_sfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
             }
+            if (!run) break;
             const uint64_t dq = desc_kmajor_sw128(sQs(st)), ddo = desc_kmajor_sw128(sdOs(st));
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -437,8 +451,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_ss(tmem + tS(buf), desc_add(dK0, okk), desc_add(dq, oq), C::kIdS, kk > 0);
             }
             if (sn >= NB) {  // dQ^T of step sn - NB has been read out of these columns
-              mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+              run = mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
+              if (!run) break;
             }
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -448,14 +463,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(b_sfull(buf));
           }
         } else {
-          if (wt > 0) {  // the previous tile's dK and dV have left tensor memory
-            mbar_wait_spin(b_accfree, (wt - 1) & 1, abort_flag, a.status);
+          if (run && wt > 0) {  // the previous tile's dK and dV have left tensor memory
+            run = mbar_wait_spin(b_accfree, (wt - 1) & 1, abort_flag, a.status);
             fence_after_sync();
           }
-          for (int l = 0; l < n; ++l, ++sn) {
+          for (int l = 0; l < n && run; ++l, ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
-            mbar_wait_spin(b_pready(buf), (sn / NB) & 1, abort_flag, a.status);
+            run = mbar_wait_spin(b_pready(buf), (sn / NB) & 1, abort_flag, a.status);
             fence_after_sync();
+            if (!run) break;
             const uint64_t mq = desc_mnmajor_sw128(sQs(st), C::kQBox), mdo = desc_mnmajor_sw128(sdOs(st), C::kQBox);
             const uint64_t mds = desc_mnmajor_sw128(sDs(buf), 16384);
 #pragma unroll
@@ -473,7 +489,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_ss(tmem + tdQ(buf), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
             mma_commit(b_dqfull(buf));
           }
-          mma_commit(b_done);  // the tile's last MMAs complete after every S^T/dP^T of it
+          if (run) mma_commit(b_done);  // the tile's last MMAs complete after every S^T/dP^T of it
         }
       }
       ++wt;
@@ -493,6 +509,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = a.scale * kLog2e;
     uint32_t it = 0;  // global step counter
     int wt = 0;
+    // After its first wait that fails, a thread makes no more arrivals (its warp keeps the same
+    // control flow, so the warp-collective tensor-memory accesses and named barriers stay whole).
+    bool run = true;
     for (int w = 0;; ++w) {
       // The warpgroup agrees on the tile: its leader reads the queue and shares the index (two
       // slots, so a slot is rewritten only after the next iteration's barrier).
@@ -501,11 +520,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int tile = tile_bc[w & 1];
       if (tile >= ntiles) break;
       const BwdTile T = bwd_tile(s, tile, BM);
-      if (!T.live) continue;
+      int32_t* visits = (a.step_visits != nullptr && threadIdx.x == 128)
+                            ? a.step_visits + ((size_t)T.b * s.Hkv + T.hk) * s.nbk + T.kt
+                            : nullptr;
+      if (!T.live) {
+        if (visits) *visits = 0;
+        continue;
+      }
       const SeqInfo& seq = T.seq;
       const int kt = T.kt;
       const int v_first = bwd_next_v_warp(s, T, 0, BM);
       const bool any_work = v_first < T.nv;
+      const uint32_t it_first = it;
       if (elementwise) {
         // -------------------------------------------------------------- P^T and dS^T
         const int key = kt * 128 + r;
@@ -540,7 +566,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             vn = v_first;
           }
           fetch(gn, vn, next_l, next_d);
-          mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // on the critical path
+          if (run) run = mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // critical path
           fence_after_sync();
           const bool need_mask =
               (s.causal && kt * 128 + 127 > q0 + seq.off) || (kt * 128 + 128 > seq.Lk) || (q0 + BM > seq.Lq);
@@ -598,17 +624,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_st_wait();
           fence_proxy_async_smem();
           fence_before_sync();
-          mbar_arrive(b_pready(buf));
+          if (run) mbar_arrive(b_pready(buf));
           gi = gn;
           v = vn;
         }
+        if (visits) *visits = (int32_t)(it - it_first);  // the steps this warpgroup walked
       } else {
         // -------------------------------------------------------------- dQ into the accumulator
         for (int gi = 0, v = v_first; gi < G && v < T.nv; ++it) {
           const int q0 = v * BM;
           const int buf = it % NB;
           float* dQa = a.dqacc + row_base(s, seq, T.b, T.h0 + gi) * D;
-          mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
+          if (run) run = mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
           fence_after_sync();
           const uint32_t tq = tmem + lane_off + tdQ(buf);
           // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
@@ -618,7 +645,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
           tmem_ld_wait();
           fence_before_sync();
-          mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
+          if (run) mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
           if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
           named_bar_sync(2, 128);
           if (r < D) {
@@ -650,7 +677,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __nv_bfloat16* grow = reinterpret_cast<__nv_bfloat16*>(elementwise ? a.dk : a.dv) +
                             elem_offset(elementwise ? a.sdk : a.sdv, seq.bb, seq.k0 + (store ? key : 0), T.hk);
       if (any_work) {
-        mbar_wait(b_done, wt & 1, abort_flag, a.status);
+        if (run) run = mbar_wait(b_done, wt & 1, abort_flag, a.status);
         fence_after_sync();
       }
       const uint32_t tacc = tmem + lane_off + (elementwise ? C::kTdK : C::kTdV);
@@ -676,7 +703,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (any_work) {  // the accumulators may be overwritten by the next tile's first products
         fence_before_sync();
-        mbar_arrive(b_accfree);
+        if (run) mbar_arrive(b_accfree);
         ++wt;
       }
     }
@@ -715,12 +742,14 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   // Persistent: one CTA per SM (shared memory allows one), key tiles handed out by the counter.
   const long long ntiles = (long long)s.nbk * s.B * s.Hkv;
   if (ntiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (a.ev_main_begin != nullptr && (e = cudaEventRecord(a.ev_main_begin, st)) != cudaSuccess) return e;
   if (ntiles > 0) {
     const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
     bwd_tc_kernel<D><<<grid, kBwdThreads, C::kSmem, st>>>(tq, tk, tv, tdo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  if (a.ev_main_end != nullptr && (e = cudaEventRecord(a.ev_main_end, st)) != cudaSuccess) return e;
   bwd_post_kernel<D><<<grid_ew, 256, 0, st>>>(a);
   return cudaGetLastError();
 }

@@ -164,6 +164,9 @@ struct FaBwdArgs {
   fa::AttnShape s;
   float scale;
   int* status;
+  int32_t* step_visits;       // nullable: query steps visited per (b, K/V head, key tile)
+  cudaEvent_t ev_main_begin;  // nullable (host side): recorded around the main launch
+  cudaEvent_t ev_main_end;
 };
 
 cudaError_t fa_launch_fwd(const FaFwdArgs& a, cudaStream_t st);

@@ -64,6 +64,13 @@ struct FwdSmemCtl {
   uint32_t tmem_base;
   int abort_flag;
   uint32_t vis[2][kVisWords];  // block mask: bit kt of query tile x's word kt / 32 = tile visited
+  // Abort-path drain (read only after an abort): per ring buffer the last stage the producer issued
+  // into it (-1: none) and whether tile 0's softmax arrives on that stage; per row of query tile 0
+  // the last stage its thread arrived on.
+  int last_stage[4];
+  int last_needs_p0[4];
+  int k0_issued;
+  int p0_last[128];
 };
 
 // SPLIT: the CTA covers one split of the key tiles and writes fp32 partials (see FaFwdArgs).
@@ -159,8 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_pready[2] = {smem_u32(&ctl.p_ready[0]), smem_u32(&ctl.p_ready[1])};
   const uint32_t b_odone[2] = {smem_u32(&ctl.o_done[0]), smem_u32(&ctl.o_done[1])};
 
+  if (threadIdx.x < 4) ctl.last_stage[threadIdx.x] = -1;
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
+    ctl.k0_issued = 0;
     mbar_init(b_q, 1);
     mbar_init(b_k0, 1);
     for (int i = 0; i < C::kStages; ++i) {
@@ -205,17 +214,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sQ + x * C::kTileBytes + c * 16384, &tmQ, c * 64, seq.q0 + (x ? qt1 : qt0) * 128, h, seq.bb, b_q);
       // Stage t (the t-th key tile u_t the pair visits) lands V_{u_t} and K_{u_t+1} in buffer
       // t % kStages; the first key tile comes alone, into the K half of the last buffer. A buffer
-      // is reloaded once the MMAs of its previous stage have completed.
-      uint32_t last_par[4];
-      bool issued[4] = {false, false, false, false};
-      bool k0_issued = false;
+      // is reloaded once the MMAs of its previous stage have completed. No copy is issued after an
+      // abort; the copies already issued are drained at the CTA's exit.
       int kt = next_union(kt_lo);
 #ifndef FA_TEST_WITHHOLD_KV
       if (kt < s.nbk) {
         mbar_expect_tx(b_k0, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_4d(sK(C::kStages - 1) + c * 16384, &tmK, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_k0);
-        k0_issued = true;
+        ctl.k0_issued = 1;
       }
 #endif
       for (int t = 0; kt < s.nbk; ++t) {
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // FA_TEST_WITHHOLD_KV (a test-only build) never loads K/V, so every consumer's bounded
         // wait must run out and the kernel must return FA_ERR_DEVICE_TIMEOUT cleanly.
 #ifndef FA_TEST_WITHHOLD_KV
-        if (uses == 0 || mbar_wait(b_empty(b), (uses - 1) & 1, abort_flag, a.status)) {
+        if ((uses == 0 || mbar_wait(b_empty(b), (uses - 1) & 1, abort_flag, a.status)) && !*abort_flag) {
 #else
         if (false) {
 #endif
@@ -235,19 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ktn < s.nbk)
             for (int c = 0; c < C::kBoxes; ++c)
               tma_load_4d(sK(b) + c * 16384, &tmK, c * 64, seq.k0 + ktn * 128, hk, seq.bb, b_full(b));
-          if (!vis(0, kt)) mbar_arrive_cnt(b_full(b), 128);  // tile 0 has no P for this key tile
-          issued[b] = true;
-          last_par[b] = (t / C::kStages) & 1;
+          const bool p0 = vis(0, kt);
+          if (!p0) mbar_arrive_cnt(b_full(b), 128);  // tile 0 has no P for this key tile
+          ctl.last_stage[b] = t;
+          ctl.last_needs_p0[b] = p0;
         }
         kt = ktn;
-      }
-      if (*abort_flag) {  // let copies still in flight land before the CTA exits (bounded)
-        mbar_wait_drain(b_q, 0);
-        if (k0_issued) mbar_wait_drain(b_k0, 0);
-        // A stage barrier also counts tile 0's softmax arrivals, which an aborted CTA may never
-        // make; a copy lands within microseconds, so a short bound suffices.
-        for (int i = 0; i < C::kStages; ++i)
-          if (issued[i]) mbar_wait_drain(b_full(i), last_par[i], kDrainShortNs);
       }
     }
   } else if (warp == 1) {
@@ -279,32 +279,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       // Per key tile two waits: the stage barrier (V_t and K_t+1 landed, P0 written) and P1.
-      mbar_wait_spin(b_q, 0, abort_flag, a.status);
+      // After its first wait that fails (a timeout, or the CTA's abort flag) the issuer issues no
+      // MMA and no commit: a buffer release committed for a stage it did not see land would let
+      // the producer reload the buffer while a copy into it is still in flight.
+      bool run = mbar_wait_spin(b_q, 0, abort_flag, a.status);
       bool v0, v1;  // which query tiles see key tile kt
       int kt = next_union_vis(kt_lo, v0, v1);
-      if (kt < s.nbk) {
-        mbar_wait_spin(b_k0, 0, abort_flag, a.status);
+      if (kt < s.nbk && run) {
+        run = mbar_wait_spin(b_k0, 0, abort_flag, a.status);
         fence_after_sync();
-        if (v0) issue_s(0, sK(C::kStages - 1));
-        if (v1) issue_s(1, sK(C::kStages - 1));
-        any[0] = v0;
-        any[1] = v1;
-        mma_commit(b_empty(C::kStages - 1));
-        for (int t = 0;; ++t) {
+        if (run) {
+          if (v0) issue_s(0, sK(C::kStages - 1));
+          if (v1) issue_s(1, sK(C::kStages - 1));
+          any[0] = v0;
+          any[1] = v1;
+          mma_commit(b_empty(C::kStages - 1));
+        }
+        for (int t = 0; run; ++t) {
           const int b = t % C::kStages;
           bool n0, n1;
           const int ktn = next_union_vis(kt + 1, n0, n1);  // n0 = n1 = false past the last tile
-          mbar_wait_spin(b_full(b), (t / C::kStages) & 1, abort_flag, a.status);
+          run = mbar_wait_spin(b_full(b), (t / C::kStages) & 1, abort_flag, a.status);
           fence_after_sync();
+          if (!run) break;
           if (v0) issue_pv(0, sV(b));
           if (n0) {
             issue_s(0, sK(b));
             any[0] = true;
           }
           if (v1) {
-            mbar_wait_spin(b_pready[1], np[1] & 1, abort_flag, a.status);
+            run = mbar_wait_spin(b_pready[1], np[1] & 1, abort_flag, a.status);
             ++np[1];
             fence_after_sync();
+            if (!run) break;
             issue_pv(1, sV(b));
           }
           if (n1) {
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int x = 0; x < 2; ++x)
-        if (any[x]) mma_commit(b_odone[x]);
+        if (any[x] && run) mma_commit(b_odone[x]);
       mma_commit(smem_u32(&ctl.drain));  // every MMA of this CTA has finished when this arrives
       mbar_wait_drain(smem_u32(&ctl.drain), 0);
     }
@@ -337,13 +344,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale * kLog2e;
     float m = -INFINITY, l = 0.f;
     int cnt = 0;
-    mbar_wait(b_q, 0, abort_flag, a.status);
+    // After its first wait that fails, a thread makes no more arrivals; its warp keeps the same
+    // control flow (the tensor-memory accesses are warp-collective). Tile 0's threads record the
+    // last stage they arrived on, for the producer's drain at exit.
+    bool run = mbar_wait(b_q, 0, abort_flag, a.status);
+    if (x == 0) ctl.p0_last[r] = -1;
     if (active) {
       int t = -1;  // union index of the key tile (tile 0 reports P on stage t's barrier)
       for (int kt = next_union(kt_lo); kt < s.nbk; kt = next_union(kt + 1)) {
         ++t;
         if (!vis(x, kt)) continue;
-        mbar_wait(b_sfull[x], cnt & 1, abort_flag, a.status);
+        if (run) run = mbar_wait(b_sfull[x], cnt & 1, abort_flag, a.status);
         fence_after_sync();
         const int k0 = kt * 128;
         const bool masked = (s.causal && k0 + 127 > qt * 128 + seq.off) || k0 + 128 > seq.Lk;
@@ -421,12 +432,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         l += sum;
         fence_before_sync();
-        mbar_arrive(x == 0 ? b_full(t % C::kStages) : b_pready[1]);
+        if (run) {
+          mbar_arrive(x == 0 ? b_full(t % C::kStages) : b_pready[1]);
+          if (x == 0) ctl.p0_last[r] = t;
+        }
         ++cnt;
       }
       // ---------------------------------------------------------------- epilogue
       if (cnt > 0) {
-        mbar_wait(b_odone[x], 0, abort_flag, a.status);
+        if (run) run = mbar_wait(b_odone[x], 0, abort_flag, a.status);
         fence_after_sync();
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -510,6 +524,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     fence_after_sync();
     tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag) {
+    // Every role has finished, so no arrival is still to come: let the copies still in flight
+    // land before the CTA exits. A buffer is reloaded only after the issuer released it, which it
+    // does only for a stage it saw complete (a role issues and arrives only while all its waits
+    // have succeeded), so each stage barrier has at most one phase in flight, the last one issued.
+    // That phase also counts tile 0's 128 softmax arrivals: the ones that will never come are made
+    // here (a thread arrived on stage t iff its last arrival was on a stage >= t, since threads
+    // arrive in stage order and stop at their first failed wait), then the copies' bytes
+    // complete the phase.
+    mbar_wait_drain(b_q, 0);
+    if (ctl.k0_issued) mbar_wait_drain(b_k0, 0);
+    for (int b = 0; b < C::kStages; ++b) {
+      const int t = ctl.last_stage[b];
+      if (t < 0) continue;
+      const uint32_t par = (t / C::kStages) & 1;
+      if (mbar_test(b_full(b), par)) continue;
+      if (ctl.last_needs_p0[b]) {
+        int arrived = 0;
+        for (int i = 0; i < 128; ++i) arrived += ctl.p0_last[i] >= t;
+        if (arrived < 128) mbar_arrive_cnt(b_full(b), 128 - arrived);
+      }
+      mbar_wait_drain(b_full(b), par);
+    }
   }
 }
 

@@ -129,6 +129,33 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
 /*
+ * The backward pass of fa_bwd_gqa with optional extras, for verification and measurement. Every
+ * argument but `extras` is as for fa_bwd_gqa; extras == NULL is fa_bwd_gqa.
+ *   step_visits       nullable, device int32 [B * Hkv * nb]: receives, per (b, K/V head, 128-key
+ *                     tile) in that order, the number of 64-row query steps the main pass visited
+ *                     for the key tile, summed over the group's query heads. A step (query rows
+ *                     64 v .. 64 v + 63) is visited iff its 128-row query tile and the key tile hold
+ *                     at least one valid pair (the skip rule of fa_fwd's tile_visits); written for
+ *                     every key tile, 0 where none is visited.
+ *   main_begin_event  nullable cudaEvent_t, recorded on `stream` right before the main pass
+ *   main_end_event    nullable cudaEvent_t, recorded on `stream` right after it (the pair times
+ *                     the main pass alone, without the pre- and post-passes)
+ * Errors as for fa_bwd_gqa; an event record that fails returns FA_ERR_CUDA.
+ */
+typedef struct {
+  int32_t* step_visits;
+  void* main_begin_event;
+  void* main_end_event;
+} fa_bwd_extras;
+
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+              const float* lse, void* dq, void* dk, void* dv,
+              int B, int H, int Hkv, int N, int d, int causal,
+              const uint8_t* block_mask, const int32_t* seqlens_k, float scale,
+              void* workspace, size_t workspace_bytes, const fa_bwd_extras* extras,
+              int* dev_status, void* stream);
+
+/*
  * Variable-length and strided batches.
  * The pages fix no tensor layout; frameworks hand attention either padded [B, N, H, d] / [B, H, N, d]
  * tensors or packed sequences (the rows of all sequences concatenated, located by cumulative

@@ -89,11 +89,17 @@ class Machine:
     def commit(self, who, name):
         self.pipe.setdefault(who, []).append(("commit", name))
 
-    def run(self, roles, max_ticks=400000):
-        """'ok', 'deadlock' (nothing can move while a role is unfinished) or 'timeout'."""
+    def run(self, roles, max_ticks=400000, final=None):
+        """'ok', 'deadlock' (nothing can move while a role is unfinished) or 'timeout'.
+        final: a generator function started as one more role once every other role has finished
+        (code after a CTA-wide barrier, e.g. an exit drain), while copies may still be in flight."""
+        roles = dict(roles)
         blocked = {k: None for k in roles}
         alive = set(roles)
         for _ in range(max_ticks):
+            if not alive and final is not None:
+                roles["exit"], blocked["exit"], final = final(), None, None
+                alive.add("exit")
             # With bounded waits a blocked role stays schedulable: resumed, its wait may run out.
             cands = [("role", k) for k in sorted(alive)
                      if blocked[k] is None or self.abort_p or self.B[blocked[k][0]].passes(blocked[k][1])]

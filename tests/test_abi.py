@@ -206,3 +206,16 @@ def test_splitkv_host_rules(L):
     for ns, ws, nbytes, rc in ((0, A, 1 << 30, -1), (257, A, 1 << 30, -1), (4, None, 1 << 30, -1), (4, A, 16, -1),
                                (4, A + 16, 1 << 30, -3)):
         assert fa.fa_fwd_splitkv(p, ns, A, st, A, sk, A, sk, A, st, A, ws, nbytes, None, None) == rc
+
+
+def test_bwd_ex_validation(L):
+    """fa_bwd_ex checks its extras on the host too: a misaligned step-visit array is rejected
+    before any launch, and every fa_bwd check still applies."""
+    base = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, B=1, H=2, Hkv=1, N=128, d=64, causal=0,
+                block_mask=None, seqlens_k=None, scale=0.125, workspace=A, workspace_bytes=1 << 30, dev_status=None,
+                stream=None)
+    bad = fa.BwdExtras(A + 2, None, None)
+    assert fa.fa_bwd_ex(**base, extras=bad) == -3
+    assert fa.fa_bwd_ex(**dict(base, q=None), extras=fa.BwdExtras(A, None, None)) == -1
+    assert fa.fa_bwd_ex(**dict(base, Hkv=3), extras=None) == -1
+    assert fa.fa_bwd_ex(**dict(base, d=96), extras=None) == -2

@@ -23,9 +23,16 @@ from mbarrier_model import Machine
 KST, NB = 3, 2
 
 
-def run(tiles, seed, release="stage", abort_p=0.0):
+def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
+    """unguarded: the earlier abort handling, where the issuers and the warpgroups carried on
+    issuing, committing and arriving after a failed wait and the producer did not check the abort
+    flag before a copy."""
     M = Machine(seed, abort_p)
-    B, bar, wait, need, done, mma, commit = M.B, M.bar, M.wait, M.need, M.done, M.mma, M.commit
+    B, bar, need, done, mma, commit = M.B, M.bar, M.need, M.done, M.mma, M.commit
+
+    def wait(name, parity):
+        ok = yield from M.wait(name, parity)
+        return ok or unguarded
 
     bar("kv", 1)
     for i in range(KST):
@@ -48,25 +55,40 @@ def run(tiles, seed, release="stage", abort_p=0.0):
     counter = [0]
     grid = 1
     def take_tile(w):
-        ok = yield from wait(f"tqfull{w & 1}", (w >> 1) & 1)
-        t = tile_q[w & 1] if ok else ntiles  # a wait that ran out ends the role's tile loop
+        ok = yield from M.wait(f"tqfull{w & 1}", (w >> 1) & 1)
+        if not ok:
+            return ntiles  # a wait that ran out ends the role's tile loop
         B[f"tqempty{w & 1}"].arrive()
-        return t
+        return tile_q[w & 1]
 
     # step -> work-tile index, filled by the producer (all roles walk the same sequence)
     step_tile = {}
 
+    last_par = {}  # stage (or "kv") -> parity of the last phase the producer issued copies for
+
+    def drain():
+        """At exit, wait (ignoring the abort flag) for the last phase of every barrier that got
+        copies: with at most one phase in flight per barrier, no copy is then still in flight."""
+        for name, par in last_par.items():
+            while not B[name].passes(par):
+                yield (name, par)
+        need(not M.loads, "the CTA exits with copies in flight")
+
     def producer():
+        yield from producer_loop()
+        yield from drain()
+
+    def producer_loop():
         i, wt, w = 0, 0, 0
         while True:
             if w >= 2:
-                ok = yield from wait(f"tqempty{w & 1}", ((w - 2) >> 1) & 1)
+                ok = yield from M.wait(f"tqempty{w & 1}", ((w - 2) >> 1) & 1)
                 if not ok:
                     return  # the producer stops taking tiles; the readers' waits run out too
             t = w if w == 0 else grid + counter[0]
             if w > 0:
                 counter[0] += 1
-            t = min(t, ntiles)
+            t = ntiles if M.aborted and not unguarded else min(t, ntiles)  # after an abort: the end marker
             tile_q[w & 1] = t
             B[f"tqfull{w & 1}"].arrive()
             w += 1
@@ -80,13 +102,17 @@ def run(tiles, seed, release="stage", abort_p=0.0):
 
             def issue_kv():
                 if wt > 0:
-                    if not (yield from wait("done", (wt - 1) & 1)):
+                    if not (yield from M.wait("done", (wt - 1) & 1)):
                         return  # the kernel skips the copy after a wait that ran out
+                if M.aborted and not unguarded:
+                    return  # no copy is issued after an abort
+                if wt > 0:
                     # every MMA of the previous work tile has completed (K and V are read by them)
                     for s in [s for s, tt in step_tile.items() if tt == wt - 1]:
                         for k in ("S", "dP", "dQ"):
                             need((k, s) in done, f"K/V of work tile {wt} loaded before {k}{s} completed")
                 M.load("kv", 2, ("kv", wt))
+                last_par["kv"] = wt & 1
 
             if wt == 0:
                 yield from issue_kv()
@@ -99,14 +125,16 @@ def run(tiles, seed, release="stage", abort_p=0.0):
                 ok = True
                 if j >= 0:
                     if release == "stage":  # the kernel: one release barrier per stage
-                        ok = yield from wait(f"empty{j % KST}", (j // KST) & 1)
+                        ok = yield from M.wait(f"empty{j % KST}", (j // KST) & 1)
                     else:  # an earlier form: the NB-deep dq_full barriers of the TMEM buffers
-                        ok = yield from wait(f"dqfull{j % NB}", (j // NB) & 1)
-                    for k in ("S", "dP", "dV", "dK"):
-                        need((k, j) in done, f"stage {st} reloaded for step {i} before {k}{j} completed")
+                        ok = yield from M.wait(f"dqfull{j % NB}", (j // NB) & 1)
                 step_tile[i] = wt
-                if ok:  # the kernel issues the copies only after the wait succeeded
+                if ok and (unguarded or not M.aborted):  # after a successful wait, never after an abort
+                    if j >= 0:
+                        for k in ("S", "dP", "dV", "dK"):
+                            need((k, j) in done, f"stage {st} reloaded for step {i} before {k}{j} completed")
                     M.load(f"full{st}", 1, ("qdo", i))
+                    last_par[f"full{st}"] = (i // KST) & 1
                 i += 1
                 yield None
             if not kv_issued:
@@ -114,7 +142,8 @@ def run(tiles, seed, release="stage", abort_p=0.0):
             wt += 1
 
     def issuer1():
-        sn, wt, w = 0, 0, 0
+        # After its first wait that fails the issuer issues no MMA and no commit.
+        sn, wt, w, run = 0, 0, 0, True
         while True:
             t = yield from take_tile(w)
             w += 1
@@ -123,29 +152,36 @@ def run(tiles, seed, release="stage", abort_p=0.0):
             n = tiles[t]
             if n == 0:
                 continue
-            yield from wait("kv", wt & 1)
-            need(("kv", wt) in done, f"S issuer saw K/V of work tile {wt} before they landed")
+            if run:
+                run = yield from wait("kv", wt & 1)
+                if run:
+                    need(("kv", wt) in done, f"S issuer saw K/V of work tile {wt} before they landed")
             for _ in range(n):
                 st, buf = sn % KST, sn % NB
-                yield from wait(f"full{st}", (sn // KST) & 1)
-                need(("qdo", sn) in done, f"S^T{sn} issued before its Q/dO landed")
-                if sn >= NB:
-                    yield from wait(f"sfree{buf}", ((sn - NB) // NB) & 1)
-                    need(("dV", sn - NB) in done, f"S^T{sn} over P^T before dV{sn - NB} completed")
-                mma(1, ("S", sn))
-                if sn >= NB:
-                    yield from wait(f"dqfree{buf}", ((sn - NB) // NB) & 1)
-                    for k in ("dK", "dQ", "rdQ"):
-                        need((k, sn - NB) in done, f"dP^T{sn} over dS^T/dQ^T before {k}{sn - NB}")
-                mma(1, ("dP", sn))
-                commit(1, f"sfull{buf}")
+                if run:
+                    run = yield from wait(f"full{st}", (sn // KST) & 1)
+                if run and sn >= NB:
+                    run = yield from wait(f"sfree{buf}", ((sn - NB) // NB) & 1)
+                if run:
+                    need(("qdo", sn) in done, f"S^T{sn} issued before its Q/dO landed")
+                    if sn >= NB:
+                        need(("dV", sn - NB) in done, f"S^T{sn} over P^T before dV{sn - NB} completed")
+                    mma(1, ("S", sn))
+                if run and sn >= NB:
+                    run = yield from wait(f"dqfree{buf}", ((sn - NB) // NB) & 1)
+                    if run:
+                        for k in ("dK", "dQ", "rdQ"):
+                            need((k, sn - NB) in done, f"dP^T{sn} over dS^T/dQ^T before {k}{sn - NB}")
+                if run:
+                    mma(1, ("dP", sn))
+                    commit(1, f"sfull{buf}")
                 sn += 1
                 yield None
             wt += 1
         commit(1, "drain")
 
     def issuer2():
-        g, wt, w = 0, 0, 0
+        g, wt, w, run = 0, 0, 0, True
         while True:
             t = yield from take_tile(w)
             w += 1
@@ -154,28 +190,34 @@ def run(tiles, seed, release="stage", abort_p=0.0):
             n = tiles[t]
             if n == 0:
                 continue
-            if wt > 0:
-                yield from wait("accfree", (wt - 1) & 1)
-                need(("acc_ew", wt - 1) in done and ("acc_dq", wt - 1) in done,
-                     f"accumulators of work tile {wt - 1} overwritten before their read-out")
+            if run and wt > 0:
+                run = yield from wait("accfree", (wt - 1) & 1)
+                if run:
+                    need(("acc_ew", wt - 1) in done and ("acc_dq", wt - 1) in done,
+                         f"accumulators of work tile {wt - 1} overwritten before their read-out")
             for _ in range(n):
                 st, buf = g % KST, g % NB
-                yield from wait(f"pready{buf}", (g // NB) & 1)
-                need(("P", g) in done, f"dV{g} issued before P/dS of step {g} were written")
-                mma(2, ("dV", g))
-                commit(2, f"sfree{buf}")
-                mma(2, ("dK", g))
-                commit(2, f"empty{st}")
-                mma(2, ("dQ", g))
-                commit(2, f"dqfull{buf}")
+                if run:
+                    run = yield from wait(f"pready{buf}", (g // NB) & 1)
+                if run:
+                    need(("P", g) in done, f"dV{g} issued before P/dS of step {g} were written")
+                    mma(2, ("dV", g))
+                    commit(2, f"sfree{buf}")
+                    mma(2, ("dK", g))
+                    commit(2, f"empty{st}")
+                    mma(2, ("dQ", g))
+                    commit(2, f"dqfull{buf}")
                 g += 1
                 yield None
-            commit(2, "done")
+            if run:
+                commit(2, "done")
             wt += 1
         commit(2, "drain")
 
     def group(kind):
-        it, wt, w = 0, 0, 0
+        # After its first wait that fails the warpgroup makes no more arrivals (its data may then
+        # be stale, which is allowed once the call has failed).
+        it, wt, w, run = 0, 0, 0, True
         while True:
             t = yield from take_tile(w)
             w += 1
@@ -185,27 +227,34 @@ def run(tiles, seed, release="stage", abort_p=0.0):
             for _ in range(n):
                 buf = it % NB
                 if kind == "ew":
-                    yield from wait(f"sfull{buf}", (it // NB) & 1)
-                    need(("S", it) in done and ("dP", it) in done, f"P/dS of step {it} before S/dP completed")
-                    if it >= NB:  # dS^T into the shared-memory tile read by dQ of step it - NB
-                        need(("dQ", it - NB) in done, f"dS^T{it} written before dQ{it - NB} completed")
-                    done.add(("P", it))
-                    B[f"pready{buf}"].arrive()
+                    if run:
+                        run = yield from wait(f"sfull{buf}", (it // NB) & 1)
+                    if run:
+                        need(("S", it) in done and ("dP", it) in done, f"P/dS of step {it} before S/dP completed")
+                        if it >= NB:  # dS^T into the shared-memory tile read by dQ of step it - NB
+                            need(("dQ", it - NB) in done, f"dS^T{it} written before dQ{it - NB} completed")
+                        done.add(("P", it))
+                        B[f"pready{buf}"].arrive()
                 else:
-                    yield from wait(f"dqfull{buf}", (it // NB) & 1)
-                    need(("dQ", it) in done, f"dQ^T{it} read before it completed")
-                    done.add(("rdQ", it))
-                    B[f"dqfree{buf}"].arrive()
+                    if run:
+                        run = yield from wait(f"dqfull{buf}", (it // NB) & 1)
+                    if run:
+                        need(("dQ", it) in done, f"dQ^T{it} read before it completed")
+                        done.add(("rdQ", it))
+                        B[f"dqfree{buf}"].arrive()
                 it += 1
                 yield None
             if n > 0:
-                yield from wait("done", wt & 1)
-                last = [s for s, tt in step_tile.items() if tt == wt]
-                for s in last:
-                    need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
+                if run:
+                    run = yield from wait("done", wt & 1)
+                if run:
+                    last = [s for s, tt in step_tile.items() if tt == wt]
+                    for s in last:
+                        need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
                 yield None
-                done.add(("acc_" + kind, wt))
-                B["accfree"].arrive()
+                if run:
+                    done.add(("acc_" + kind, wt))
+                    B["accfree"].arrive()
                 wt += 1
 
     roles = {"prod": producer(), "i1": issuer1(), "i2": issuer2(), "ew": group("ew"), "dr": group("dq")}
@@ -229,15 +278,24 @@ def test_model_finds_the_earlier_release_race():
     assert hangs, "the model no longer sees the aliasing deadlock of the earlier release"
 
 
-@pytest.mark.xfail(strict=True, raises=AssertionError, reason=(
-    "after an abort the issuers stop waiting for a stage's copies, so its release can come early and "
-    "the producer can give the stage barrier a second arrive.expect_tx while the previous copy is "
-    "in flight (a pending-count underflow the PTX rules leave undefined); the producer needs an "
-    "abort-flag check before each copy"))
 def test_abort_path_terminates():
     """Waits that run out at random points: every role still leaves its loops (the kernel's
     abort flag makes every later wait return at once; a tile-queue read that fails ends the role's
-    tile loop), even when the roles no longer agree on how many tiles they saw."""
+    tile loop), even when the roles no longer agree on how many tiles they saw. No barrier gets a
+    second arrive.expect_tx while a copy of its previous phase is in flight (the mbarrier model
+    raises on an arrival beyond the count), no hazard is issued, and the producer's drain leaves
+    no copy in flight when the CTA exits."""
     for tiles, seed in _cases(1500):
-        res, _ = run(tiles, seed, abort_p=0.02)
-        assert res == "ok", (tiles, seed, res)
+        res, errs = run(tiles, seed, abort_p=0.02)
+        assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
+
+
+def test_abort_path_model_sees_the_unguarded_release():
+    """The same model with the earlier abort handling (issuers that ignore a failed wait and still
+    issue and commit) must hit the double arrive.expect_tx: the model can see that fault."""
+    for tiles, seed in _cases(1500):
+        try:
+            run(tiles, seed, abort_p=0.02, unguarded=True)
+        except AssertionError:
+            return
+    raise AssertionError("the model no longer sees the unguarded abort path")

@@ -22,10 +22,16 @@ import pytest
 from mbarrier_model import Machine
 
 
-def run(union, has1, stages, seed, early_release=False, abort_p=0.0):
-    """union: [(v0, v1)] per union key tile (at least one of the two set)."""
+def run(union, has1, stages, seed, early_release=False, abort_p=0.0, unguarded=False):
+    """union: [(v0, v1)] per union key tile (at least one of the two set).
+    unguarded: the earlier abort handling (the issuer and the softmax warpgroups carried on after a
+    failed wait, and the producer did not check the abort flag before a copy)."""
     M = Machine(seed, abort_p)
-    B, bar, wait, need, done = M.B, M.bar, M.wait, M.need, M.done
+    B, bar, need, done = M.B, M.bar, M.need, M.done
+
+    def wait(name, parity):
+        ok = yield from M.wait(name, parity)
+        return ok or unguarded
     bar("q", 1)
     bar("k0", 1)
     for i in range(stages):
@@ -38,6 +44,9 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0):
     U = len(union)
     vis = lambda x, t: t < U and bool(union[t][x])
 
+    last_stage = {}  # buffer -> (last stage issued into it, whether tile 0's softmax arrives on it)
+    p0_last = [-1]   # the last stage tile 0's softmax arrived on
+
     def producer():
         M.load("q", 1, ("Q",))
         if U == 0:
@@ -48,21 +57,42 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0):
             uses = t // stages + (1 if b == stages - 1 else 0)
             ok = True
             if uses > 0:
-                ok = yield from wait(f"empty{b}", (uses - 1) & 1)
+                ok = yield from M.wait(f"empty{b}", (uses - 1) & 1)
+            if ok and (unguarded or not M.aborted):  # after a successful wait, never after an abort
                 tv, tk = t - stages, t - stages + 1  # previous V and K of this buffer
                 for x in (0, 1):
-                    if tv >= 0 and vis(x, tv):
+                    if uses > 0 and tv >= 0 and vis(x, tv):
                         need((f"PV{x}", tv) in done, f"buffer {b} reloaded before PV{x}({tv}) completed")
-                    if vis(x, tk):
+                    if uses > 0 and vis(x, tk):
                         need((f"S{x}", tk) in done, f"buffer {b} reloaded before S{x}({tk}) completed")
-            if ok:  # the kernel issues the stage only after its wait succeeded
                 M.expect(f"full{b}", 2 if t + 1 < U else 1)
                 M.copy(f"full{b}", 1, ("V", t))
                 if t + 1 < U:
                     M.copy(f"full{b}", 1, ("K", t + 1))
                 if not vis(0, t):
                     B[f"full{b}"].arrive()  # stands in for tile 0's softmax
+                last_stage[b] = (t, vis(0, t))
             yield None
+
+    def exit_drain():
+        """After the CTA-wide barrier at exit, when the CTA has aborted: every stage barrier has at
+        most one phase in flight (the last issued); tile 0's softmax arrival on it is made up if it
+        never came, then the phase completes once the copies have landed."""
+        if not M.aborted:
+            return
+        for name in ("q", "k0") if U > 0 else ("q",):  # K0 is loaded only when a key tile is visited
+            while not B[name].passes(0):
+                yield (name, 0)
+        for b, (t, needs_p0) in last_stage.items():
+            par = (t // stages) & 1
+            if B[f"full{b}"].passes(par):
+                continue
+            if needs_p0 and p0_last[0] < t:
+                B[f"full{b}"].arrive()
+            while not B[f"full{b}"].passes(par):
+                yield (f"full{b}", par)
+        need(not M.loads, "the CTA exits with copies in flight")
+        yield None
 
     def issuer():
         last_p = {0: None, 1: None}  # the latest tile whose P_x the issuer has consumed
@@ -80,18 +110,25 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0):
             M.mma("i", (f"PV{x}", t))
             last_p[x] = t
 
-        yield from wait("q", 0)
+        # After its first wait that fails the issuer issues no MMA and no commit.
+        run = yield from wait("q", 0)
         if U == 0:
             return
-        yield from wait("k0", 0)
-        for x in (0, 1):
-            if vis(x, 0):
-                issue_s(x, 0)
-        M.commit("i", f"empty{stages - 1}")
+        if run:
+            run = yield from wait("k0", 0)
+        if run:
+            for x in (0, 1):
+                if vis(x, 0):
+                    issue_s(x, 0)
+            M.commit("i", f"empty{stages - 1}")
         np1 = 0
         for t in range(U):
+            if not run:
+                break
             b = t % stages
-            yield from wait(f"full{b}", (t // stages) & 1)
+            run = yield from wait(f"full{b}", (t // stages) & 1)
+            if not run:
+                break
             if early_release:
                 M.commit("i", f"empty{b}")
             if vis(0, t):
@@ -99,8 +136,10 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0):
             if vis(0, t + 1):
                 issue_s(0, t + 1)
             if vis(1, t):
-                yield from wait("pready1", np1 & 1)
+                run = yield from wait("pready1", np1 & 1)
                 np1 += 1
+                if not run:
+                    break
                 issue_pv(1, t)
             if vis(1, t + 1):
                 issue_s(1, t + 1)
@@ -108,34 +147,41 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0):
                 M.commit("i", f"empty{b}")
             yield None
         for x in (0, 1):
-            if any(vis(x, t) for t in range(U)):
+            if run and any(vis(x, t) for t in range(U)):
                 M.commit("i", f"odone{x}")
 
     def softmax(x):
-        yield from wait("q", 0)
+        # After its first wait that fails the warpgroup makes no more arrivals.
+        run = yield from wait("q", 0)
         cnt = 0
         for t in range(U):
             if not vis(x, t):
                 continue
-            yield from wait(f"sfull{x}", cnt & 1)
-            need((f"S{x}", t) in done, f"softmax {x} read S({t}) before it completed")
-            for tp in range(t):
-                if vis(x, tp):
-                    need((f"PV{x}", tp) in done, f"softmax {x} rescaled O at {t} before PV{x}({tp}) completed")
+            if run:
+                run = yield from wait(f"sfull{x}", cnt & 1)
+            if run:
+                need((f"S{x}", t) in done, f"softmax {x} read S({t}) before it completed")
+                for tp in range(t):
+                    if vis(x, tp):
+                        need((f"PV{x}", tp) in done, f"softmax {x} rescaled O at {t} before PV{x}({tp}) completed")
             yield None
-            done.add((f"P{x}", t))
-            B[f"full{t % stages}" if x == 0 else "pready1"].arrive()
+            if run:
+                done.add((f"P{x}", t))
+                B[f"full{t % stages}" if x == 0 else "pready1"].arrive()
+                if x == 0:
+                    p0_last[0] = t
             cnt += 1
-        if cnt:
-            yield from wait(f"odone{x}", 0)
-            for tp in range(U):
-                if vis(x, tp):
-                    need((f"PV{x}", tp) in done, f"O{x} read before PV{x}({tp}) completed")
+        if cnt and run:
+            run = yield from wait(f"odone{x}", 0)
+            if run:
+                for tp in range(U):
+                    if vis(x, tp):
+                        need((f"PV{x}", tp) in done, f"O{x} read before PV{x}({tp}) completed")
 
     roles = {"prod": producer(), "mma": issuer(), "sm0": softmax(0)}
     if has1:
         roles["sm1"] = softmax(1)
-    return M.run(roles), M.errors
+    return M.run(roles, final=exit_drain), M.errors
 
 
 def _cases(n):
@@ -164,13 +210,22 @@ def test_model_finds_an_early_buffer_release():
     assert found, "the model no longer sees a buffer released before its readers"
 
 
-@pytest.mark.xfail(strict=True, raises=AssertionError, reason=(
-    "after an abort the issuer stops waiting for a stage, so its release can come early: the producer "
-    "can give the stage barrier a second arrive.expect_tx while a copy is in flight, and tile 0's "
-    "softmax can arrive for a later use of the buffer before the current phase completed (pending-"
-    "count underflows the PTX rules leave undefined); both need an abort-flag check"))
 def test_abort_path_terminates():
-    """Waits that run out at random points: every role still leaves its loops."""
+    """Waits that run out at random points: every role still leaves its loops, no stage barrier
+    gets an arrival beyond its count (a second arrive.expect_tx, or tile 0's softmax arriving for a
+    later use of the buffer, while a phase is in flight), no hazard is issued, and the exit drain
+    leaves no copy in flight."""
     for union, has1, stages, seed in _cases(1500):
-        res, _ = run(union, has1, stages, seed, abort_p=0.02)
-        assert res == "ok", (union, has1, stages, seed, res)
+        res, errs = run(union, has1, stages, seed, abort_p=0.02)
+        assert res == "ok" and not errs, (union, has1, stages, seed, res, errs[:3])
+
+
+def test_abort_path_model_sees_the_unguarded_release():
+    """With the earlier abort handling the model must hit an arrival beyond a stage barrier's
+    count (the undefined pending-count underflow): the model can see that fault."""
+    for union, has1, stages, seed in _cases(1500):
+        try:
+            run(union, has1, stages, seed, abort_p=0.02, unguarded=True)
+        except AssertionError:
+            return
+    raise AssertionError("the model no longer sees the unguarded abort path")

@@ -2,8 +2,9 @@
 
 Tolerances (bf16 inputs/outputs, fp32 accumulation): O max-abs <= 2e-2 and mean-abs <= 2e-3;
 LSE max-abs <= 1e-3 (and -inf exactly where a row has no valid key); dQ, dK, dV relative
-Frobenius error <= 2e-2 each. Tile-skip decisions are compared bit-exactly with the oracle's
-"block holds a valid pair" grid.
+Frobenius error <= 2e-2 each. Tile-skip decisions of both passes are compared bit-exactly with the
+oracle's "block holds a valid pair" grid: the forward's key tiles per query tile, and the backward's
+64-row query steps per key tile.
 """
 
 import numpy as np
@@ -35,16 +36,20 @@ def run_gpu(inp, backward=True, visits=False):
     sl = None if inp.get("seqlens_k") is None else inp["seqlens_k"].to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     tv = torch.full((B * H * nb,), -1, dtype=torch.int32, device=dev) if visits else None
+    Hkv = k.shape[1]
+    sv = torch.full((B * Hkv * nb,), -1, dtype=torch.int32, device=dev) if visits and backward else None
     kw = dict(causal=inp["causal"], block_mask=bm, seqlens_k=sl, scale=inp["scale"], status=status)
     o, lse = fa.fwd(q, k, v, tile_visits=tv, **kw)
     out = {"o": o, "lse": lse}
     if backward:
-        out["dq"], out["dk"], out["dv"] = fa.bwd(q, k, v, o, lse, do, **kw)
+        out["dq"], out["dk"], out["dv"] = fa.bwd(q, k, v, o, lse, do, step_visits=sv, **kw)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
     res = {n: t.cpu() for n, t in out.items()}
     if visits:
         res["visits"] = tv.cpu().view(B, H, nb)
+    if sv is not None:
+        res["step_visits"] = sv.cpu().view(B, Hkv, nb)
     return res
 
 
@@ -91,18 +96,30 @@ def full_check(inp, backward=True):
                                       **oracle_args(inp))
         for name, ref in zip(("dq", "dk", "dv"), g):
             rel_fro(got[name], ref)
-    check_visits(got["visits"], inp)
+    check_visits(got, inp)
     return got
 
 
-def check_visits(visits, inp):
+def check_visits(got, inp):
+    """Forward: key tiles visited per (b, h, query tile) = row sums of the oracle's grid. Backward:
+    64-row query steps visited per (b, K/V head, key tile) = the steps of the query tiles in the
+    grid's column (a tile of rows 128 I .. has the steps 2 I and, if row 64 (2 I + 1) exists,
+    2 I + 1), times the query heads sharing the K/V head."""
     B, H, N, _ = inp["q"].shape
+    Hkv = inp["k"].shape[1]
     a = oracle_args(inp)
+    nb = (N + 127) // 128
+    steps_in = np.array([1 + int((2 * i + 1) * 64 < N) for i in range(nb)])
     for b in range(B):
         L = None if a["seqlens_k"] is None else int(a["seqlens_k"][b])
-        want = oracle.tile_grid(N, a["causal"], a["block_mask"], L).sum(axis=1)
+        grid = oracle.tile_grid(N, a["causal"], a["block_mask"], L)
+        want = grid.sum(axis=1)
         for h in range(H):
-            assert (visits[b, h].numpy() == want).all(), (b, h)
+            assert (got["visits"][b, h].numpy() == want).all(), (b, h)
+        if "step_visits" in got:
+            want_b = (H // Hkv) * (grid * steps_in[:, None]).sum(axis=0)
+            for hk in range(Hkv):
+                assert (got["step_visits"][b, hk].numpy() == want_b).all(), (b, hk)
 
 
 def small_inputs(B, H, N, d, kind, seed):
@@ -145,7 +162,7 @@ def test_all_tiles_masked():
     inp = workloads.random_inputs(1, 2, 256, 128, 5)
     inp.update(causal=False, block_mask=torch.zeros((2, 2), dtype=torch.uint8), seqlens_k=None, scale=0.1)
     got = full_check(inp)
-    assert (got["visits"] == 0).all()
+    assert (got["visits"] == 0).all() and (got["step_visits"] == 0).all()
 
 
 def test_repeatable():
@@ -186,15 +203,24 @@ def test_config_full(name):
     full_check(workloads.make_inputs(w), backward=w.backward)
 
 
-def sampled_check(inp, heads, n_rows, n_cols, seed):
-    """Full-size launch; the oracle evaluates sampled K/V heads (b, hk), and for each the query
-    heads that share it, on sampled rows and key columns one by one."""
+def sampled_check(inp, heads, n_rows, n_cols, seed, fwd_rows=128):
+    """Full-size launch; the oracle evaluates O and LSE on `fwd_rows` sampled rows of every head,
+    and sampled K/V heads (b, hk), with the query heads that share each, on sampled rows and key
+    columns one by one for the gradients."""
     got = run_gpu(inp, backward=True, visits=True)
     B, H, N, d = inp["q"].shape
     Hkv = inp["k"].shape[1]
     a = oracle_args(inp)
     c = inp["scale"]
     rng = np.random.default_rng(seed)
+    for b in range(B):
+        L = None if a["seqlens_k"] is None else int(a["seqlens_k"][b])
+        for h in range(H):
+            hk = oracle.kv_head(h, H, Hkv)
+            rows = np.sort(rng.choice(N, fwd_rows, replace=False))
+            om, lm = oracle.head_forward(f64(inp["q"][b, h]), f64(inp["k"][b, hk]), f64(inp["v"][b, hk]), c,
+                                         a["causal"], a["block_mask"], L, rows=rows)
+            check_o_lse(got["o"][b, h][rows], got["lse"][b, h][rows], om, lm)
     for (b, hk) in heads:
         k, v = (f64(inp[n][b, hk]) for n in ("k", "v"))
         L = None if a["seqlens_k"] is None else int(a["seqlens_k"][b])
@@ -220,7 +246,7 @@ def sampled_check(inp, heads, n_rows, n_cols, seed):
     dk = got["dk"].double()
     colsum = dk.sum(dim=2).norm(dim=-1)
     assert (colsum <= 0.05 * dk.norm(dim=(2, 3)) + 1e-3).all()
-    check_visits(got["visits"], inp)
+    check_visits(got, inp)
 
 
 def test_config_c4_sampled():
