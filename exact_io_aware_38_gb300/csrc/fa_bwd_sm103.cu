@@ -308,10 +308,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // four readers of item w have arrived on the slot's empty barrier.
   auto take_tile = [&](int w) -> int {  // one reader thread per role
     int tile = ntiles;  // an abandoned wait ends the loop
-    if (mbar_wait(b_tqfull(w & 1), (w >> 1) & 1, abort_flag, a.status)) {
-      tile = tile_q[w & 1];
-      mbar_arrive(b_tqempty(w & 1));
-    }
+    if (mbar_wait(b_tqfull(w & 1), (w >> 1) & 1, abort_flag, a.status)) tile = tile_q[w & 1];
+    mbar_arrive(b_tqempty(w & 1));
     return tile;
   };
 
@@ -329,7 +327,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t last_par[kMaxStages];
     bool issued[kMaxStages] = {};
     bool kv_any = false;
-    uint32_t kv_par = 0;
+    uint32_t kv_par = 1;  // parity of the last K/V phase issued (flips before each issue)
     uint32_t i = 0;  // Q/dO ring position, continued across key tiles
     int wt = 0;      // key tiles with work so far
     for (int w = 0;; ++w) {
@@ -352,7 +350,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_kv = [&]() {  // lane 0
         kv_issued = true;
         if (wt > 0 && !mbar_wait(b_done, (wt - 1) & 1, abort_flag, a.status)) return;
-        if (*abort_flag) return;  // no copy is issued after an abort (see the drain below)
+        // The previous K/V copy has landed (only the producer arrives on this barrier, so the
+        // parity test cannot alias), and no copy is issued after an abort.
+        if ((kv_any && !mbar_wait(b_kv, kv_par, abort_flag, a.status)) || *abort_flag) return;
 #ifndef FA_TEST_WITHHOLD_KV  // a test-only build never loads K/V: every wait on them must run out
         mbar_expect_tx(b_kv, 2 * C::kKVBytes);
         for (int c = 0; c < C::kBoxes; ++c) {
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_4d(sV + c * 16384, &tmV, c * 64, T.seq.k0 + T.kt * 128, T.hk, T.seq.bb, b_kv);
         }
         kv_any = true;
-        kv_par = wt & 1;
+        kv_par = kv_par ^ 1u;
 #endif
       };
       if (lane == 0 && wt == 0) issue_kv();
@@ -373,9 +373,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // The stage is free once dV and dK of step j = i - kStages have read it (its S^T/dP^T
           // finished before them), which the gradient issuer commits to the stage's own barrier.
           // One barrier per stage keeps the parity test unambiguous: its next phase belongs to
-          // step i, not loaded yet.
+          // step i, not loaded yet. The producer also checks that step j's own copy has landed (in
+          // the normal path long since; after an abort the issuers' releases no longer prove it),
+          // so a stage barrier never gets a second arrive.expect_tx while a phase is open, and it
+          // issues no copy after an abort.
           const int j = (int)i - C::kStages;
-          if ((j < 0 || mbar_wait(b_empty(j % C::kStages), (j / C::kStages) & 1, abort_flag, a.status)) &&
+          if ((j < 0 || (mbar_wait(b_empty(j % C::kStages), (j / C::kStages) & 1, abort_flag, a.status) &&
+                         mbar_wait(b_full(j % C::kStages), (j / C::kStages) & 1, abort_flag, a.status))) &&
               !*abort_flag) {
             mbar_expect_tx(b_full(st), 2 * C::kQBytes);
             for (int c = 0; c < C::kBoxes; ++c) {
@@ -395,9 +399,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0 && !kv_issued) issue_kv();
       ++wt;
     }
-    // Let copies still in flight land before the CTA exits. A stage is reloaded only after the
-    // gradient issuer released it, which it does only for a step whose copies it saw land (a role
-    // issues and arrives only while all its waits have succeeded), so each barrier has at most one
+    // Let copies still in flight land before the CTA exits. A stage (and the K/V buffer) is
+    // reloaded only once its previous copy has landed, so each of these barriers has at most one
     // phase in flight: the last one issued, whose only arrival is the producer's own.
     if (lane == 0 && *abort_flag) {
       if (kv_any) mbar_wait_drain(b_kv, kv_par);
@@ -419,10 +422,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t dK0 = desc_kmajor_sw128(sK), dV0 = desc_kmajor_sw128(sV), mK0 = desc_mnmajor_sw128(sK, 16384);
     uint32_t sn = 0;  // global step counter (lane 0)
     int wt = 0;
-    // After its first wait that fails (a timeout, or the CTA's abort flag) the issuer issues no
-    // MMA and no commit: a release it committed for a step it did not see complete would let the
-    // producer reload a stage whose copy is still in flight.
-    bool run = true;
     for (int w = 0;; ++w) {
       int tile = 0;
       if (lane == 0) tile = take_tile(w);
@@ -434,16 +433,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (n == 0) continue;
       if (lane == 0) {
         if (warp == 1) {
-          if (run) run = mbar_wait_spin(b_kv, wt & 1, abort_flag, a.status);
+          mbar_wait_spin(b_kv, wt & 1, abort_flag, a.status);
           fence_after_sync();
-          for (int l = 0; l < n && run; ++l, ++sn) {
+          for (int l = 0; l < n; ++l, ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
-            run = mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
-            if (run && sn >= NB) {  // dV of step sn - NB has read P^T from these columns
-              run = mbar_wait_spin(b_sfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+            mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
+            if (sn >= NB) {  // dV of step sn - NB has read P^T from these columns
+              mbar_wait_spin(b_sfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
             }
-            if (!run) break;
             const uint64_t dq = desc_kmajor_sw128(sQs(st)), ddo = desc_kmajor_sw128(sdOs(st));
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -451,9 +449,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_ss(tmem + tS(buf), desc_add(dK0, okk), desc_add(dq, oq), C::kIdS, kk > 0);
             }
             if (sn >= NB) {  // dQ^T of step sn - NB has been read out of these columns
-              run = mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
+              mbar_wait_spin(b_dqfree(buf), ((sn - NB) / NB) & 1, abort_flag, a.status);
               fence_after_sync();
-              if (!run) break;
             }
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -463,15 +460,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(b_sfull(buf));
           }
         } else {
-          if (run && wt > 0) {  // the previous tile's dK and dV have left tensor memory
-            run = mbar_wait_spin(b_accfree, (wt - 1) & 1, abort_flag, a.status);
+          if (wt > 0) {  // the previous tile's dK and dV have left tensor memory
+            mbar_wait_spin(b_accfree, (wt - 1) & 1, abort_flag, a.status);
             fence_after_sync();
           }
-          for (int l = 0; l < n && run; ++l, ++sn) {
+          for (int l = 0; l < n; ++l, ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
-            run = mbar_wait_spin(b_pready(buf), (sn / NB) & 1, abort_flag, a.status);
+            mbar_wait_spin(b_pready(buf), (sn / NB) & 1, abort_flag, a.status);
             fence_after_sync();
-            if (!run) break;
             const uint64_t mq = desc_mnmajor_sw128(sQs(st), C::kQBox), mdo = desc_mnmajor_sw128(sdOs(st), C::kQBox);
             const uint64_t mds = desc_mnmajor_sw128(sDs(buf), 16384);
 #pragma unroll
@@ -489,7 +485,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_ss(tmem + tdQ(buf), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
             mma_commit(b_dqfull(buf));
           }
-          if (run) mma_commit(b_done);  // the tile's last MMAs complete after every S^T/dP^T of it
+          mma_commit(b_done);  // the tile's last MMAs complete after every S^T/dP^T of it
         }
       }
       ++wt;
@@ -509,9 +505,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = a.scale * kLog2e;
     uint32_t it = 0;  // global step counter
     int wt = 0;
-    // After its first wait that fails, a thread makes no more arrivals (its warp keeps the same
-    // control flow, so the warp-collective tensor-memory accesses and named barriers stay whole).
-    bool run = true;
     for (int w = 0;; ++w) {
       // The warpgroup agrees on the tile: its leader reads the queue and shares the index (two
       // slots, so a slot is rewritten only after the next iteration's barrier).
@@ -566,7 +559,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             vn = v_first;
           }
           fetch(gn, vn, next_l, next_d);
-          if (run) run = mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // critical path
+          mbar_wait_spin(b_sfull(buf), (it / NB) & 1, abort_flag, a.status);  // on the critical path
           fence_after_sync();
           const bool need_mask =
               (s.causal && kt * 128 + 127 > q0 + seq.off) || (kt * 128 + 128 > seq.Lk) || (q0 + BM > seq.Lq);
@@ -624,7 +617,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_st_wait();
           fence_proxy_async_smem();
           fence_before_sync();
-          if (run) mbar_arrive(b_pready(buf));
+          mbar_arrive(b_pready(buf));
           gi = gn;
           v = vn;
         }
@@ -635,7 +628,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int q0 = v * BM;
           const int buf = it % NB;
           float* dQa = a.dqacc + row_base(s, seq, T.b, T.h0 + gi) * D;
-          if (run) run = mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
+          mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
           fence_after_sync();
           const uint32_t tq = tmem + lane_off + tdQ(buf);
           // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
@@ -645,7 +638,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
           tmem_ld_wait();
           fence_before_sync();
-          if (run) mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
+          mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
           if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
           named_bar_sync(2, 128);
           if (r < D) {
@@ -677,7 +670,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __nv_bfloat16* grow = reinterpret_cast<__nv_bfloat16*>(elementwise ? a.dk : a.dv) +
                             elem_offset(elementwise ? a.sdk : a.sdv, seq.bb, seq.k0 + (store ? key : 0), T.hk);
       if (any_work) {
-        if (run) run = mbar_wait(b_done, wt & 1, abort_flag, a.status);
+        mbar_wait(b_done, wt & 1, abort_flag, a.status);
         fence_after_sync();
       }
       const uint32_t tacc = tmem + lane_off + (elementwise ? C::kTdK : C::kTdV);
@@ -703,7 +696,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (any_work) {  // the accumulators may be overwritten by the next tile's first products
         fence_before_sync();
-        if (run) mbar_arrive(b_accfree);
+        mbar_arrive(b_accfree);
         ++wt;
       }
     }

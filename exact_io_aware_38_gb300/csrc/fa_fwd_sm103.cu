@@ -232,7 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // FA_TEST_WITHHOLD_KV (a test-only build) never loads K/V, so every consumer's bounded
         // wait must run out and the kernel must return FA_ERR_DEVICE_TIMEOUT cleanly.
 #ifndef FA_TEST_WITHHOLD_KV
-        if ((uses == 0 || mbar_wait(b_empty(b), (uses - 1) & 1, abort_flag, a.status)) && !*abort_flag) {
+        // Besides the release, the buffer's previous stage barrier phase must have completed (in the
+        // normal path long since: the issuer waited for it before releasing the buffer), so a stage
+        // barrier never gets a second arrive.expect_tx while a phase is open.
+        if ((uses == 0 || mbar_wait(b_empty(b), (uses - 1) & 1, abort_flag, a.status)) &&
+            (t < C::kStages || mbar_wait(b_full(b), ((t - C::kStages) / C::kStages) & 1, abort_flag, a.status)) &&
+            !*abort_flag) {
 #else
         if (false) {
 #endif

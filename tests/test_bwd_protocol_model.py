@@ -14,6 +14,14 @@ rewritten, the dK/dV accumulators overwritten before their read-out).
 The same model with the earlier producer release (waiting on the two dq_full barriers for step
 i - 3) must deadlock on some interleaving: that aliasing hang is what the per-stage release fixes,
 and finding it shows the model can see that class of error.
+
+Abort path: waits that run out at random. After the CTA's abort flag is set every role keeps its
+loops (a failed wait returns false at once; the issuers and warpgroups carry on with stale data,
+which only spoils the outputs of a call that has already failed, so hazards after the abort are not
+errors). What must hold: no barrier gets an arrival beyond its count (a second arrive.expect_tx on
+an open phase), every role ends, and no copy is in flight when the producer has drained at exit.
+The producer guarantees the first on its own: before reloading a stage (or K/V) it checks that the
+stage's previous copy has landed, and it issues nothing once the abort flag is set.
 """
 import random
 
@@ -24,15 +32,14 @@ KST, NB = 3, 2
 
 
 def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
-    """unguarded: the earlier abort handling, where the issuers and the warpgroups carried on
-    issuing, committing and arriving after a failed wait and the producer did not check the abort
-    flag before a copy."""
+    """unguarded: the earlier producer, which reloaded a stage once its release arrived, without
+    checking its own previous copy or the abort flag."""
     M = Machine(seed, abort_p)
-    B, bar, need, done, mma, commit = M.B, M.bar, M.need, M.done, M.mma, M.commit
+    B, bar, wait, done, mma, commit = M.B, M.bar, M.wait, M.done, M.mma, M.commit
 
-    def wait(name, parity):
-        ok = yield from M.wait(name, parity)
-        return ok or unguarded
+    def need(cond, msg):  # a hazard matters only before the abort (afterwards the outputs are void)
+        if not M.aborted:
+            M.need(cond, msg)
 
     bar("kv", 1)
     for i in range(KST):
@@ -55,24 +62,31 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
     counter = [0]
     grid = 1
     def take_tile(w):
-        ok = yield from M.wait(f"tqfull{w & 1}", (w >> 1) & 1)
-        if not ok:
-            return ntiles  # a wait that ran out ends the role's tile loop
+        ok = yield from wait(f"tqfull{w & 1}", (w >> 1) & 1)
+        t = tile_q[w & 1] if ok else ntiles  # a wait that ran out ends the role's tile loop
         B[f"tqempty{w & 1}"].arrive()
-        return tile_q[w & 1]
+        return t
 
     # step -> work-tile index, filled by the producer (all roles walk the same sequence)
     step_tile = {}
 
-    last_par = {}  # stage (or "kv") -> parity of the last phase the producer issued copies for
+    last_par = {}  # "kv" or stage -> parity of the last phase the producer issued copies for
 
     def drain():
-        """At exit, wait (ignoring the abort flag) for the last phase of every barrier that got
-        copies: with at most one phase in flight per barrier, no copy is then still in flight."""
+        """At exit, after an abort: wait (ignoring the abort flag) for the last phase of every
+        barrier that got copies; with at most one phase in flight each, no copy is left."""
+        if not M.aborted:
+            return
         for name, par in last_par.items():
             while not B[name].passes(par):
                 yield (name, par)
-        need(not M.loads, "the CTA exits with copies in flight")
+        M.need(not M.loads, "the CTA exits with copies in flight")
+
+    def landed(name):
+        """The producer's own previous copy into this barrier has landed (only it arrives there)."""
+        if unguarded or name not in last_par:
+            return True
+        return (yield from wait(name, last_par[name]))
 
     def producer():
         yield from producer_loop()
@@ -82,7 +96,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
         i, wt, w = 0, 0, 0
         while True:
             if w >= 2:
-                ok = yield from M.wait(f"tqempty{w & 1}", ((w - 2) >> 1) & 1)
+                ok = yield from wait(f"tqempty{w & 1}", ((w - 2) >> 1) & 1)
                 if not ok:
                     return  # the producer stops taking tiles; the readers' waits run out too
             t = w if w == 0 else grid + counter[0]
@@ -102,10 +116,10 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
 
             def issue_kv():
                 if wt > 0:
-                    if not (yield from M.wait("done", (wt - 1) & 1)):
+                    if not (yield from wait("done", (wt - 1) & 1)):
                         return  # the kernel skips the copy after a wait that ran out
-                if M.aborted and not unguarded:
-                    return  # no copy is issued after an abort
+                if not (yield from landed("kv")) or (M.aborted and not unguarded):
+                    return
                 if wt > 0:
                     # every MMA of the previous work tile has completed (K and V are read by them)
                     for s in [s for s, tt in step_tile.items() if tt == wt - 1]:
@@ -125,11 +139,12 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
                 ok = True
                 if j >= 0:
                     if release == "stage":  # the kernel: one release barrier per stage
-                        ok = yield from M.wait(f"empty{j % KST}", (j // KST) & 1)
+                        ok = yield from wait(f"empty{j % KST}", (j // KST) & 1)
                     else:  # an earlier form: the NB-deep dq_full barriers of the TMEM buffers
-                        ok = yield from M.wait(f"dqfull{j % NB}", (j // NB) & 1)
+                        ok = yield from wait(f"dqfull{j % NB}", (j // NB) & 1)
+                    ok = ok and (yield from landed(f"full{st}"))
                 step_tile[i] = wt
-                if ok and (unguarded or not M.aborted):  # after a successful wait, never after an abort
+                if ok and (unguarded or not M.aborted):  # after its waits succeeded, never after an abort
                     if j >= 0:
                         for k in ("S", "dP", "dV", "dK"):
                             need((k, j) in done, f"stage {st} reloaded for step {i} before {k}{j} completed")
@@ -142,8 +157,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
             wt += 1
 
     def issuer1():
-        # After its first wait that fails the issuer issues no MMA and no commit.
-        sn, wt, w, run = 0, 0, 0, True
+        sn, wt, w = 0, 0, 0
         while True:
             t = yield from take_tile(w)
             w += 1
@@ -152,36 +166,29 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
             n = tiles[t]
             if n == 0:
                 continue
-            if run:
-                run = yield from wait("kv", wt & 1)
-                if run:
-                    need(("kv", wt) in done, f"S issuer saw K/V of work tile {wt} before they landed")
+            yield from wait("kv", wt & 1)
+            need(("kv", wt) in done, f"S issuer saw K/V of work tile {wt} before they landed")
             for _ in range(n):
                 st, buf = sn % KST, sn % NB
-                if run:
-                    run = yield from wait(f"full{st}", (sn // KST) & 1)
-                if run and sn >= NB:
-                    run = yield from wait(f"sfree{buf}", ((sn - NB) // NB) & 1)
-                if run:
-                    need(("qdo", sn) in done, f"S^T{sn} issued before its Q/dO landed")
-                    if sn >= NB:
-                        need(("dV", sn - NB) in done, f"S^T{sn} over P^T before dV{sn - NB} completed")
-                    mma(1, ("S", sn))
-                if run and sn >= NB:
-                    run = yield from wait(f"dqfree{buf}", ((sn - NB) // NB) & 1)
-                    if run:
-                        for k in ("dK", "dQ", "rdQ"):
-                            need((k, sn - NB) in done, f"dP^T{sn} over dS^T/dQ^T before {k}{sn - NB}")
-                if run:
-                    mma(1, ("dP", sn))
-                    commit(1, f"sfull{buf}")
+                yield from wait(f"full{st}", (sn // KST) & 1)
+                need(("qdo", sn) in done, f"S^T{sn} issued before its Q/dO landed")
+                if sn >= NB:
+                    yield from wait(f"sfree{buf}", ((sn - NB) // NB) & 1)
+                    need(("dV", sn - NB) in done, f"S^T{sn} over P^T before dV{sn - NB} completed")
+                mma(1, ("S", sn))
+                if sn >= NB:
+                    yield from wait(f"dqfree{buf}", ((sn - NB) // NB) & 1)
+                    for k in ("dK", "dQ", "rdQ"):
+                        need((k, sn - NB) in done, f"dP^T{sn} over dS^T/dQ^T before {k}{sn - NB}")
+                mma(1, ("dP", sn))
+                commit(1, f"sfull{buf}")
                 sn += 1
                 yield None
             wt += 1
         commit(1, "drain")
 
     def issuer2():
-        g, wt, w, run = 0, 0, 0, True
+        g, wt, w = 0, 0, 0
         while True:
             t = yield from take_tile(w)
             w += 1
@@ -190,34 +197,28 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
             n = tiles[t]
             if n == 0:
                 continue
-            if run and wt > 0:
-                run = yield from wait("accfree", (wt - 1) & 1)
-                if run:
-                    need(("acc_ew", wt - 1) in done and ("acc_dq", wt - 1) in done,
-                         f"accumulators of work tile {wt - 1} overwritten before their read-out")
+            if wt > 0:
+                yield from wait("accfree", (wt - 1) & 1)
+                need(("acc_ew", wt - 1) in done and ("acc_dq", wt - 1) in done,
+                     f"accumulators of work tile {wt - 1} overwritten before their read-out")
             for _ in range(n):
                 st, buf = g % KST, g % NB
-                if run:
-                    run = yield from wait(f"pready{buf}", (g // NB) & 1)
-                if run:
-                    need(("P", g) in done, f"dV{g} issued before P/dS of step {g} were written")
-                    mma(2, ("dV", g))
-                    commit(2, f"sfree{buf}")
-                    mma(2, ("dK", g))
-                    commit(2, f"empty{st}")
-                    mma(2, ("dQ", g))
-                    commit(2, f"dqfull{buf}")
+                yield from wait(f"pready{buf}", (g // NB) & 1)
+                need(("P", g) in done, f"dV{g} issued before P/dS of step {g} were written")
+                mma(2, ("dV", g))
+                commit(2, f"sfree{buf}")
+                mma(2, ("dK", g))
+                commit(2, f"empty{st}")
+                mma(2, ("dQ", g))
+                commit(2, f"dqfull{buf}")
                 g += 1
                 yield None
-            if run:
-                commit(2, "done")
+            commit(2, "done")
             wt += 1
         commit(2, "drain")
 
     def group(kind):
-        # After its first wait that fails the warpgroup makes no more arrivals (its data may then
-        # be stale, which is allowed once the call has failed).
-        it, wt, w, run = 0, 0, 0, True
+        it, wt, w = 0, 0, 0
         while True:
             t = yield from take_tile(w)
             w += 1
@@ -227,34 +228,27 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
             for _ in range(n):
                 buf = it % NB
                 if kind == "ew":
-                    if run:
-                        run = yield from wait(f"sfull{buf}", (it // NB) & 1)
-                    if run:
-                        need(("S", it) in done and ("dP", it) in done, f"P/dS of step {it} before S/dP completed")
-                        if it >= NB:  # dS^T into the shared-memory tile read by dQ of step it - NB
-                            need(("dQ", it - NB) in done, f"dS^T{it} written before dQ{it - NB} completed")
-                        done.add(("P", it))
-                        B[f"pready{buf}"].arrive()
+                    yield from wait(f"sfull{buf}", (it // NB) & 1)
+                    need(("S", it) in done and ("dP", it) in done, f"P/dS of step {it} before S/dP completed")
+                    if it >= NB:  # dS^T into the shared-memory tile read by dQ of step it - NB
+                        need(("dQ", it - NB) in done, f"dS^T{it} written before dQ{it - NB} completed")
+                    done.add(("P", it))
+                    B[f"pready{buf}"].arrive()
                 else:
-                    if run:
-                        run = yield from wait(f"dqfull{buf}", (it // NB) & 1)
-                    if run:
-                        need(("dQ", it) in done, f"dQ^T{it} read before it completed")
-                        done.add(("rdQ", it))
-                        B[f"dqfree{buf}"].arrive()
+                    yield from wait(f"dqfull{buf}", (it // NB) & 1)
+                    need(("dQ", it) in done, f"dQ^T{it} read before it completed")
+                    done.add(("rdQ", it))
+                    B[f"dqfree{buf}"].arrive()
                 it += 1
                 yield None
             if n > 0:
-                if run:
-                    run = yield from wait("done", wt & 1)
-                if run:
-                    last = [s for s, tt in step_tile.items() if tt == wt]
-                    for s in last:
-                        need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
+                yield from wait("done", wt & 1)
+                last = [s for s, tt in step_tile.items() if tt == wt]
+                for s in last:
+                    need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
                 yield None
-                if run:
-                    done.add(("acc_" + kind, wt))
-                    B["accfree"].arrive()
+                done.add(("acc_" + kind, wt))
+                B["accfree"].arrive()
                 wt += 1
 
     roles = {"prod": producer(), "i1": issuer1(), "i2": issuer2(), "ew": group("ew"), "dr": group("dq")}
@@ -279,23 +273,21 @@ def test_model_finds_the_earlier_release_race():
 
 
 def test_abort_path_terminates():
-    """Waits that run out at random points: every role still leaves its loops (the kernel's
-    abort flag makes every later wait return at once; a tile-queue read that fails ends the role's
-    tile loop), even when the roles no longer agree on how many tiles they saw. No barrier gets a
-    second arrive.expect_tx while a copy of its previous phase is in flight (the mbarrier model
-    raises on an arrival beyond the count), no hazard is issued, and the producer's drain leaves
-    no copy in flight when the CTA exits."""
+    """Waits that run out at random points: every role still leaves its loops (the kernel's abort
+    flag makes every later wait return at once; a tile-queue read that fails ends the role's tile
+    loop), even when the roles no longer agree on how many tiles they saw; no barrier gets an
+    arrival beyond its count (the mbarrier model raises); the drain leaves no copy in flight."""
     for tiles, seed in _cases(1500):
         res, errs = run(tiles, seed, abort_p=0.02)
         assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
 
 
-def test_abort_path_model_sees_the_unguarded_release():
-    """The same model with the earlier abort handling (issuers that ignore a failed wait and still
-    issue and commit) must hit the double arrive.expect_tx: the model can see that fault."""
+def test_abort_path_model_sees_the_unguarded_producer():
+    """The earlier producer (reloading a stage on its release alone) must hit the second
+    arrive.expect_tx on an open phase: the model can see that fault."""
     for tiles, seed in _cases(1500):
         try:
             run(tiles, seed, abort_p=0.02, unguarded=True)
         except AssertionError:
             return
-    raise AssertionError("the model no longer sees the unguarded abort path")
+    raise AssertionError("the model no longer sees the unguarded producer")

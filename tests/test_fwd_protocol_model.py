@@ -58,6 +58,8 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0, unguarded=F
             ok = True
             if uses > 0:
                 ok = yield from M.wait(f"empty{b}", (uses - 1) & 1)
+            if ok and t >= stages and not unguarded:  # the buffer's previous stage phase has completed
+                ok = yield from M.wait(f"full{b}", ((t - stages) // stages) & 1)
             if ok and (unguarded or not M.aborted):  # after a successful wait, never after an abort
                 tv, tk = t - stages, t - stages + 1  # previous V and K of this buffer
                 for x in (0, 1):
