@@ -495,6 +495,41 @@ def secondary_figures(names, steps, warmup, dev, peak):
     return out
 
 
+def fp8_forward_figure(steps, warmup, dev, peak_bf16):
+    """The FP8 forward (e4m3 Q, K, V^T with per-head descales) on the long-context causal shape,
+    CUDA events on the launching stream; FLOPs as the bf16 forward; the peak is the measured bf16
+    burst figure times the nominal FP8 / BF16 ratio of 2."""
+    import exact_io_aware_38_gb300 as fa
+
+    w = workloads.WORKLOADS["c4"]
+    inp = workloads.make_fp8_inputs(w)
+    q8, k8, vt8 = (inp[n].to(dev) for n in ("q8", "k8", "vt8"))
+    qs, ks, vs = (inp[n].to(dev) for n in ("q_descale", "k_descale", "v_descale"))
+    B, H, N, d = q8.shape
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    run = lambda: fa.fwd_fp8(q8, k8, vt8, qs, ks, vs, causal=True, out=o, lse=lse, status=status)
+    for _ in range(max(3, warmup)):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e in ev:
+        e[0].record(stream)
+        run()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+    ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    fl = rl.attention_flops(B, H, N, d, causal=True)["fwd"]
+    tf = fl / (ms * 1e-3) / 1e12
+    peak = 2.0 * peak_bf16
+    return {"workload": workload_label(w, B, H, N, d) + " forward, e4m3 inputs", "ms": ms, "value": tf,
+            "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
+            "peak_source": "measured bf16 burst x 2 (nominal FP8 / BF16 dense ratio)"}
+
+
 def main():
     args = parse()
     if args.workload == "dec":
@@ -580,6 +615,7 @@ def main():
         result["useful_padding"] = up
     if rank == 0 and not args.no_secondary and args.heads is None and args.workload == "c4":
         result["secondary"] = secondary_figures(["c5", "c3", "c2"], min(args.steps, 20), args.warmup, dev, peak)
+        result["secondary"]["fp8_fwd"] = fp8_forward_figure(min(args.steps, 20), args.warmup, dev, peak)
     if rank == 0 and not args.no_cpu_baseline:
         heads = [(0, h) for h in range(min(3, H))]  # about 10 s of the oracle on the host cores
         t0 = time.perf_counter()

@@ -10,6 +10,7 @@ Raw C-ABI names (same signatures as ``include/fa.h``, pointers as ints):
     fa_fwd_varlen, fa_bwd_varlen, fa_bwd_varlen_workspace_bytes (with the Strides / VarlenProblem structs)
 Tensor helpers (grouped-query attention when k, v have fewer heads than q):
     fwd(q, k, v, ...) -> (o, lse);  bwd(q, k, v, o, lse, do, ...) -> (dq, dk, dv)
+    fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, ...) -> (o, lse): e4m3 inputs (fa_fwd_fp8)
     fwd_varlen(q, k, v, ...), bwd_varlen(...): [B, N, H, d] views with any strides, or packed
     [rows, H, d] sequences located by cu_seqlens; query and key lengths may differ.
     fwd_splitkv(q, k, v, ..., num_splits=None): the forward split over keys (decode shapes).
@@ -57,6 +58,7 @@ _VP = ctypes.POINTER(VarlenProblem)
 _SIGS = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P,
                     ctypes.c_size_t, _P, _P]),
     "fa_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _P]),
@@ -137,6 +139,12 @@ def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block
                workspace_bytes, dev_status, stream) -> int:
     return int(lib().fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k,
                                 scale, workspace, workspace_bytes, dev_status, stream))
+
+
+def fa_fwd_fp8(q, k, vt, o, lse, B, H, Hkv, N, d, causal, block_mask, seqlens_k, q_descale, k_descale, v_descale,
+               scale, tile_visits, dev_status, stream) -> int:
+    return int(lib().fa_fwd_fp8(q, k, vt, o, lse, B, H, Hkv, N, d, causal, block_mask, seqlens_k, q_descale, k_descale,
+                                v_descale, scale, tile_visits, dev_status, stream))
 
 
 def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, block_mask, seqlens_k, scale, workspace,
@@ -258,6 +266,42 @@ def fwd(q, k, v, *, causal=False, block_mask=None, seqlens_k=None, scale=None, o
     rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, N, d,
                     int(causal), _ptr(block_mask), _ptr(seqlens_k), scale, _ptr(tile_visits), _ptr(status),
                     _stream(stream))
+    if rc != 0:
+        raise FaError(rc)
+    return o, lse
+
+
+def fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, *, causal=False, block_mask=None, seqlens_k=None, scale=None,
+            out=None, lse=None, tile_visits=None, status=None, stream=None):
+    """O (bf16), LSE of attention over e4m3 inputs (fa_fwd_fp8): q8 [B, H, N, d], k8 [B, Hkv, N, d] and
+    vt8 = V^T [B, Hkv, d, N] as torch.float8_e4m3fn tensors, with fp32 per-head descales q_descale
+    [B, H], k_descale and v_descale [B, Hkv] (the inputs are descale * values). d = 128."""
+    f8 = torch.float8_e4m3fn
+    for name, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):
+        if not (t.is_cuda and t.dtype == f8 and t.is_contiguous() and t.dim() == 4 and t.device == q8.device):
+            raise ValueError(f"{name} must be a contiguous 4-D float8_e4m3fn CUDA tensor on {q8.device}")
+    B, H, N, d = q8.shape
+    Hkv = k8.shape[1]
+    if k8.shape != (B, Hkv, N, d) or vt8.shape != (B, Hkv, d, N) or H % Hkv != 0:
+        raise ValueError("k8 must be [B, Hkv, N, d] and vt8 [B, Hkv, d, N] with Hkv dividing H")
+    _masks(block_mask, seqlens_k, N, B, q8.device)
+    for name, t, n in (("q_descale", q_descale, B * H), ("k_descale", k_descale, B * Hkv),
+                       ("v_descale", v_descale, B * Hkv)):
+        if t is None:
+            raise ValueError(f"{name} is required")
+        _check_aux(name, t, torch.float32, n, q8.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    _check_qkv(o)
+    if o.shape != (B, H, N, d) or o.device != q8.device:
+        raise ValueError("out must be a bf16 [B, H, N, d] tensor on the inputs' device")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _check_aux("lse", lse, torch.float32, B * H * N, q8.device)
+    _check_aux("tile_visits", tile_visits, torch.int32, B * H * ((N + 127) // 128), q8.device)
+    _check_aux("status", status, torch.int32, 1, q8.device)
+    rc = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, N, d,
+                    int(causal), _ptr(block_mask), _ptr(seqlens_k), q_descale.data_ptr(), k_descale.data_ptr(),
+                    v_descale.data_ptr(), scale, _ptr(tile_visits), _ptr(status), _stream(stream))
     if rc != 0:
         raise FaError(rc)
     return o, lse

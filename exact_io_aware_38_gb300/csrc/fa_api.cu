@@ -119,7 +119,7 @@ int launch_fwd(const fa::AttnShape& s, const void* q, FaStrides sq, const void* 
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       !aligned(tile_visits, 4) || !aligned(dev_status, 4))
     return FA_ERR_MISALIGNED;
-  FaFwdArgs a;
+  FaFwdArgs a{};
   a.q = q;
   a.k = k;
   a.v = v;
@@ -163,7 +163,7 @@ int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* w
       !aligned(t.dq, 16) || !aligned(t.dk, 16) || !aligned(t.dv, 16) || !aligned(t.lse, 4) ||
       !aligned(workspace, kAlign) || !aligned(dev_status, 4) || (extras && !aligned(extras->step_visits, 4)))
     return FA_ERR_MISALIGNED;
-  FaBwdArgs a;
+  FaBwdArgs a{};
   a.q = t.q;
   a.k = t.k;
   a.v = t.v;
@@ -214,7 +214,7 @@ int launch_partial(const fa::AttnShape& s, const fa_varlen_problem* p, int split
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       !aligned(part_o, 16) || !aligned(part_lse, 4) || !aligned(dev_status, 4))
     return FA_ERR_MISALIGNED;
-  FaFwdArgs a;
+  FaFwdArgs a{};
   a.q = q;
   a.k = k;
   a.v = v;
@@ -274,6 +274,40 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            void* stream) {
   return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, block_mask, seqlens_k, scale, tile_visits, dev_status,
                     stream);
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+               int causal, const uint8_t* block_mask, const int32_t* seqlens_k, const float* q_descale,
+               const float* k_descale, const float* v_descale, float scale, int32_t* tile_visits, int* dev_status,
+               void* stream) {
+  if (!q || !k || !vt || !o || !lse || !q_descale || !k_descale || !v_descale) return FA_ERR_INVALID_ARG;
+  const int rc = check_shape(B, H, N, d, causal, scale);
+  if (rc != FA_OK) return rc;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (d != 128 || N % 16 != 0) return FA_ERR_UNSUPPORTED;  // 128-byte operand rows; V^T rows on 16-byte boundaries
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(vt, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(q_descale, 4) || !aligned(k_descale, 4) || !aligned(v_descale, 4) || !aligned(seqlens_k, 4) ||
+      !aligned(tile_visits, 4) || !aligned(dev_status, 4))
+    return FA_ERR_MISALIGNED;
+  FaFwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = vt;
+  a.o = o;
+  a.lse = lse;
+  a.so = contiguous(H, N, d);
+  a.s = fixed_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
+  a.scale = scale;
+  a.tile_visits = tile_visits;
+  a.status = dev_status;
+  a.splits = 1;
+  a.kt_chunk = a.s.nbk;
+  a.fp8 = 1;
+  a.q_descale = q_descale;
+  a.k_descale = k_descale;
+  a.v_descale = v_descale;
+  const cudaError_t e = fa_launch_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -151,6 +151,10 @@ struct FaFwdArgs {
   int splits, kt_chunk;
   float *part_o, *part_lse;
   size_t part_rows;
+  // e4m3 operands (fp8 != 0): q, k are [B][H or Hkv][N][d] bytes, v is V^T [B][Hkv][d][N] bytes, and
+  // the true inputs are q_descale[b * H + h] * q (k, v likewise with [b * Hkv + hk]).
+  int fp8;
+  const float *q_descale, *k_descale, *v_descale;
 };
 
 struct FaBwdArgs {

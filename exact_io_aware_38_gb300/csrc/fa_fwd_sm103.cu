@@ -39,17 +39,27 @@ using namespace tc;
 
 constexpr int kThreads = 320;
 constexpr int kVisWords = 64;  // key tiles covered by the per-CTA visibility bitmap: 2048
-constexpr float kRescaleLog2 = 8.0f;
 
-template <int D>
+// F8: e4m3 operands (Q, K and V^T with per-head descales; d = 128), the two products as
+// kind::f8f6f4 MMAs and P rounded to e4m3 as 2^8 P; otherwise bf16 operands (kind::f16).
+template <int D, bool F8 = false>
 struct FwdCfg {
-  static constexpr int kBoxes = D / 64;                 // 64-column (128-byte) TMA boxes per row
-  static constexpr int kTileBytes = 128 * D * 2;        // one 128-row bf16 tile
-  static constexpr int kStages = D == 128 ? 2 : 4;      // K/V ring: stage t holds V_t and K_t+1
-  static constexpr int kSmem = (2 + 2 * kStages) * kTileBytes + 1024;
-  static constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-  static constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+  static constexpr int kBoxCols = F8 ? 128 : 64;        // columns of one 128-byte TMA box
+  static constexpr int kBoxes = D / kBoxCols;           // boxes per operand row
+  static constexpr int kOBoxes = D / 64;                // boxes per bf16 output row
+  static constexpr int kTileBytes = 128 * D * (F8 ? 1 : 2);  // one 128-row operand tile (Q, K, V or V^T)
+  static constexpr int kQSlot = 128 * D * 2;            // a query tile's slot: Q, later its bf16 O staging
+  static constexpr int kStages = (D == 128 && !F8) ? 2 : 4;  // K/V ring: stage t holds V_t and K_t+1
+  static constexpr int kSmem = 2 * kQSlot + 2 * kStages * kTileBytes + 1024;
+  static constexpr int kSSteps = D / (F8 ? 32 : 16);    // MMAs of one S = Q K^T (K = 16 bf16 / 32 e4m3 each)
+  static constexpr int kPVSteps = 128 / (F8 ? 32 : 16);  // MMAs of one O += P V
+  static constexpr uint32_t kIdS = F8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
+  static constexpr uint32_t kIdPV = F8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
   static constexpr uint32_t kTmemS0 = 0, kTmemO0 = 256;
+  // O is rescaled only when a row max grows by more than 2^kRescale (lazy; exact since l and O share
+  // the stale max). The e4m3 P is 2^8 exp2(s - m) <= 256 only with the exact running max.
+  static constexpr float kRescale = F8 ? 0.0f : 8.0f;
+  static constexpr float kPExp = F8 ? 8.0f : 0.0f;      // P is computed as 2^kPExp exp2(s - m)
 };
 
 struct FwdSmemCtl {
@@ -75,16 +85,17 @@ struct FwdSmemCtl {
 
 // SPLIT: the CTA covers one split of the key tiles and writes fp32 partials (see FaFwdArgs).
 // MASKED: a block mask is given (never with SPLIT); without one, visibility is in closed form.
-template <int D, bool SPLIT, bool MASKED>
+// F8: e4m3 operands (see FwdCfg; never with SPLIT).
+template <int D, bool SPLIT, bool MASKED, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FaFwdArgs a) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sQ = smem_u32(smem);                       // Q0, Q1 (later O staging)
-  const uint32_t sKV = sQ + 2 * C::kTileBytes;              // ring: stage buffer b = V then K
+  const uint32_t sQ = smem_u32(smem);                       // Q0, Q1 (later O staging), kQSlot each
+  const uint32_t sKV = sQ + 2 * C::kQSlot;                  // ring: stage buffer b = V (V^T) then K
   volatile int* abort_flag = &ctl.abort_flag;
 
   const AttnShape& s = a.s;
@@ -211,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(b_q, (has1 ? 2 : 1) * C::kTileBytes);
       for (int x = 0; x < (has1 ? 2 : 1); ++x)
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_4d(sQ + x * C::kTileBytes + c * 16384, &tmQ, c * 64, seq.q0 + (x ? qt1 : qt0) * 128, h, seq.bb, b_q);
+          tma_load_4d(sQ + x * C::kQSlot + c * 16384, &tmQ, c * C::kBoxCols, seq.q0 + (x ? qt1 : qt0) * 128, h,
+                      seq.bb, b_q);
       // Stage t (the t-th key tile u_t the pair visits) lands V_{u_t} and K_{u_t+1} in buffer
       // t % kStages; the first key tile comes alone, into the K half of the last buffer. A buffer
       // is reloaded once the MMAs of its previous stage have completed. No copy is issued after an
@@ -221,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kt < s.nbk) {
         mbar_expect_tx(b_k0, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_4d(sK(C::kStages - 1) + c * 16384, &tmK, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_k0);
+          tma_load_4d(sK(C::kStages - 1) + c * 16384, &tmK, c * C::kBoxCols, seq.k0 + kt * 128, hk, seq.bb, b_k0);
         ctl.k0_issued = 1;
       }
 #endif
@@ -242,11 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (false) {
 #endif
           mbar_expect_tx(b_full(b), (ktn < s.nbk ? 2 : 1) * C::kTileBytes);
-          for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_4d(sV(b) + c * 16384, &tmV, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_full(b));
+          if constexpr (F8) {  // V^T: rows are the d dimensions, keys along the row
+            tma_load_4d(sV(b), &tmV, kt * 128, 0, hk, seq.bb, b_full(b));
+          } else {
+            for (int c = 0; c < C::kBoxes; ++c)
+              tma_load_4d(sV(b) + c * 16384, &tmV, c * 64, seq.k0 + kt * 128, hk, seq.bb, b_full(b));
+          }
           if (ktn < s.nbk)
             for (int c = 0; c < C::kBoxes; ++c)
-              tma_load_4d(sK(b) + c * 16384, &tmK, c * 64, seq.k0 + ktn * 128, hk, seq.bb, b_full(b));
+              tma_load_4d(sK(b) + c * 16384, &tmK, c * C::kBoxCols, seq.k0 + ktn * 128, hk, seq.bb, b_full(b));
           const bool p0 = vis(0, kt);
           if (!p0) mbar_arrive_cnt(b_full(b), 128);  // tile 0 has no P for this key tile
           ctl.last_stage[b] = t;
@@ -264,22 +280,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // No abort-flag reads on the issue path (see mbar_wait): after an abort the remaining MMAs
       // run on stale data and complete normally.
       // Descriptors are built once per operand tile and advanced by constant byte offsets per k-step.
-      const uint64_t dQ[2] = {desc_kmajor_sw128(sQ), desc_kmajor_sw128(sQ + C::kTileBytes)};
+      const uint64_t dQ[2] = {desc_kmajor_sw128(sQ), desc_kmajor_sw128(sQ + C::kQSlot)};
+      // Each K step is 32 bytes of the 128-byte rows (16 bf16 or 32 e4m3 elements).
       auto issue_s = [&](int x, uint32_t ka) {
         const uint64_t dq = dQ[x], dk = desc_kmajor_sw128(ka);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::kSSteps; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kTmemS0 + x * 128, desc_add(dq, off), desc_add(dk, off), C::kIdS, kk > 0);
+          if constexpr (F8)
+            mma_ss_f8(tmem + C::kTmemS0 + x * 128, desc_add(dq, off), desc_add(dk, off), C::kIdS, kk > 0);
+          else
+            mma_ss(tmem + C::kTmemS0 + x * 128, desc_add(dq, off), desc_add(dk, off), C::kIdS, kk > 0);
         }
         mma_commit(b_sfull[x]);
       };
+      // P (8 tensor-memory columns per K step) times V: bf16 V is MN-major (d contiguous); e4m3 V^T
+      // is K-major (keys contiguous).
       auto issue_pv = [&](int x, uint32_t va) {
-        const uint64_t dv = desc_mnmajor_sw128(va, 16384);
+        const uint64_t dv = F8 ? desc_kmajor_sw128(va) : desc_mnmajor_sw128(va, 16384);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kTmemO0 + x * D, tmem + C::kTmemS0 + x * 128 + kk * 8, desc_add(dv, kk * 2048), C::kIdPV,
-                 (first[x] && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < C::kPVSteps; ++kk) {
+          if constexpr (F8)
+            mma_ts_f8(tmem + C::kTmemO0 + x * D, tmem + C::kTmemS0 + x * 128 + kk * 8, desc_add(dv, kk * 32),
+                      C::kIdPV, (first[x] && kk == 0) ? 0u : 1u);
+          else
+            mma_ts(tmem + C::kTmemO0 + x * D, tmem + C::kTmemS0 + x * 128 + kk * 8, desc_add(dv, kk * 2048),
+                   C::kIdPV, (first[x] && kk == 0) ? 0u : 1u);
+        }
         first[x] = false;
       };
 
@@ -346,8 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::kTmemS0 + x * 128;
     const uint32_t tO = tmem + lane_off + C::kTmemO0 + x * D;
-    const float sl2 = a.scale * kLog2e;
-    float m = -INFINITY, l = 0.f;
+    // e4m3 operands: the per-head descales of Q and K enter the scores, V's the output.
+    const float qk_descale = F8 ? a.q_descale[(size_t)b * s.H + h] * a.k_descale[(size_t)b * s.Hkv + hk] : 1.f;
+    const float sl2 = a.scale * kLog2e * qk_descale;
+    float m = -INFINITY, l = 0.f;  // l: row sum of 2^kPExp exp2(s - m)
     int cnt = 0;
     // After its first wait that fails, a thread makes no more arrivals; its warp keeps the same
     // control flow (the tensor-memory accesses are warp-collective). Tile 0's threads record the
@@ -389,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mc = mx * sl2;
         if (cnt == 0) {
           m = mc;
-        } else if (__any_sync(0xffffffffu, mc > m + kRescaleLog2)) {
+        } else if (__any_sync(0xffffffffu, mc > m + C::kRescale)) {
           const float mn = fmaxf(m, mc);
           const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m - mn);
 #pragma unroll
@@ -405,11 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mn;
         }
         const float mu = (m == -INFINITY) ? 0.f : m;
-        // Pass 2: P = exp2(c log2(e) s - m) in bf16 over the first 64 columns of S (each chunk is
-        // written only over columns already read), and the row sum of P.
+        // Pass 2: P = exp2(c log2(e) s - m) over the first columns of S (bf16: 64 columns; e4m3,
+        // as 2^8 P: 32 columns; each chunk is written only over columns already read), and the
+        // row sum of P.
         auto exp_pass = [&](auto mask_tag) -> float {
           constexpr bool MASK = decltype(mask_tag)::value;
-          const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-mu, -mu);
+          const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(C::kPExp - mu, C::kPExp - mu);
           float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -427,9 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p1 = (c * 32 + 2 * i + 1 < lim) ? p1 : 0.f;
               }
               ps[i & 1] = add2(ps[i & 1], make_float2(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
+              if constexpr (F8) {  // four e4m3 values per column, key 4w + j in byte j of column w
+                const uint32_t pair = pack_e4m3x2(p0, p1);
+                pk[i >> 1] = (i & 1) ? (pk[i >> 1] | (pair << 16)) : pair;
+              } else {
+                pk[i] = pack_bf16x2(p0, p1);
+              }
             }
-            tmem_st16(tS + c * 16, pk);
+            if constexpr (F8) {
+              tmem_st8(tS + c * 8, *reinterpret_cast<const uint32_t(*)[8]>(pk));
+            } else {
+              tmem_st16(tS + c * 16, pk);
+            }
           }
           return (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
         };
@@ -448,7 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (run) run = mbar_wait(b_odone[x], 0, abort_flag, a.status);
         fence_after_sync();
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // l sums 2^kPExp exp2(s - m); with e4m3 operands V's descale scales the output.
+      const float inv = l > 0.f ? (F8 ? a.v_descale[(size_t)b * s.Hkv + hk] : 1.f) / l : 0.f;
+      const float lse2 = l > 0.f ? m + log2f(l) - C::kPExp : -INFINITY;  // log2-domain LSE
       if constexpr (SPLIT) {  // split over keys: normalised fp32 partials for the merge pass
         // The tensor-memory loads are warp-collective: every lane loads, only valid rows store.
         const bool live = row < seq.Lq;
@@ -472,9 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                               __uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
           }
         }
-        if (live) a.part_lse[R] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (live) a.part_lse[R] = lse2 * kLn2;
       } else {
-        const uint32_t stg = sQ + x * C::kTileBytes;
+        const uint32_t stg = sQ + x * C::kQSlot;
         // A packed sequence's last tile is stored row by row: a tile-wide copy would write the next
         // sequence's rows.
         const bool direct = s.cu_q != nullptr && qt * 128 + 128 > seq.Lq;
@@ -510,12 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "memory");
           }
         }
-        if (row < seq.Lq) a.lse[row_base(s, seq, b, h) + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (row < seq.Lq) a.lse[row_base(s, seq, b, h) + row] = lse2 * kLn2;
         fence_proxy_async_smem();
         named_bar_sync(1 + x, 128);
         if (warp == 2 + 4 * x && lane == 0) {
           if (!direct)
-            for (int c = 0; c < C::kBoxes; ++c) tma_store_4d(&tmO, stg + c * 16384, c * 64, seq.q0 + qt * 128, h, seq.bb);
+            for (int c = 0; c < C::kOBoxes; ++c) tma_store_4d(&tmO, stg + c * 16384, c * 64, seq.q0 + qt * 128, h, seq.bb);
           tma_store_commit();
           tma_store_wait_read0();  // the staging is read; the writes land before the grid completes
           if (a.tile_visits != nullptr) a.tile_visits[(size_t)bh * s.nbq + qt] = cnt;
@@ -583,10 +624,33 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// e4m3 operands (d = 128, fixed-length [B, H, N, d] Q and K, [B, Hkv, d, N] V^T, no split).
+cudaError_t launch_f8(const FaFwdArgs& a, cudaStream_t st) {
+  constexpr int D = 128;
+  using C = FwdCfg<D, true>;
+  const AttnShape& s = a.s;
+  if (s.cu_q != nullptr || a.part_o != nullptr || s.d != D) return cudaErrorInvalidValue;
+  CUtensorMap tq, tk, tv, to;
+  const long long nq = s.Nq, nk = s.Nk;
+  if (!fa_make_tmap_u8(&tq, a.q, D, s.Nq, s.H, s.B, D, nq * D, (long long)s.H * nq * D, 128, 128) ||
+      !fa_make_tmap_u8(&tk, a.k, D, s.Nk, s.Hkv, s.B, D, nk * D, (long long)s.Hkv * nk * D, 128, 128) ||
+      !fa_make_tmap_u8(&tv, a.v, s.Nk, D, s.Hkv, s.B, nk, nk * D, (long long)s.Hkv * nk * D, 128, 128) ||
+      !fa_make_tmap_bf16(&to, a.o, D, s.Nq, s.H, s.B, a.so.row, a.so.head, a.so.batch))
+    return cudaErrorInvalidValue;
+  auto kern = s.block_mask != nullptr ? fwd_tc_kernel<D, false, true, true> : fwd_tc_kernel<D, false, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)((s.nbq + 1) / 2) * s.B * s.H;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, to, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 }  // namespace fa
 
 cudaError_t fa_launch_fwd(const FaFwdArgs& a, cudaStream_t st) {
+  if (a.fp8) return fa::launch_f8(a, st);
   return a.s.d == 64 ? fa::launch<64>(a, st) : fa::launch<128>(a, st);
 }
 

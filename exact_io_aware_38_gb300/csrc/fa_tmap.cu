@@ -32,3 +32,16 @@ bool fa_make_tmap_bf16(CUtensorMap* m, const void* ptr, int D, int rows, int hea
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+bool fa_make_tmap_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int heads, int batches, long long row_stride,
+                     long long head_stride, long long batch_stride, int box_inner, int box_rows) {
+  auto enc = get_encode();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batches};
+  cuuint64_t strides[3] = {(cuuint64_t)row_stride, (cuuint64_t)head_stride, (cuuint64_t)batch_stride};
+  cuuint32_t box[4] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}

@@ -7,3 +7,7 @@
 
 bool fa_make_tmap_bf16(CUtensorMap* m, const void* ptr, int D, int rows, int heads, int batches, long long row_stride,
                        long long head_stride, long long batch_stride, int box_rows = 128);
+// The same for 8-bit elements (e4m3 operands) with a box of box_inner elements (bytes) x box_rows;
+// strides in bytes. box_inner * 1 byte must not exceed the 128-byte swizzle span.
+bool fa_make_tmap_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int heads, int batches, long long row_stride,
+                     long long head_stride, long long batch_stride, int box_inner, int box_rows);

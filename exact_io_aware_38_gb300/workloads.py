@@ -84,11 +84,12 @@ def band_random_block_mask(nb: int, gen: torch.Generator, p: float = 0.08) -> to
 
 
 def make_inputs(w: Workload, *, B: int | None = None, H: int | None = None, N: int | None = None,
-                seed: int | None = None) -> dict:
+                seed: int | None = None, _keep_fp32: bool = False) -> dict:
     """Host (CPU) tensors for workload ``w``; B, H, N and seed may be overridden (smaller tests).
 
     Returns dict with q, do (bf16 [B,H,N,d]), k, v (bf16 [B,Hkv,N,d]), seqlens_k (int32 [B] or
     None), block_mask (uint8 [nb, nb] or None), causal, scale. An H override keeps H / Hkv.
+    (_keep_fp32 also returns the fp32 draws as _f32_q, _f32_k, _f32_v, _f32_do.)
     """
     G = w.H // w.kv_heads
     B = w.B if B is None else B
@@ -98,13 +99,18 @@ def make_inputs(w: Workload, *, B: int | None = None, H: int | None = None, N: i
         raise ValueError(f"H={H} is not a multiple of the workload's group size {G}")
     g = torch.Generator("cpu").manual_seed(w.seed if seed is None else seed)
 
-    def draw(std, heads):
-        return (torch.randn((B, heads, N, w.d), generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+    f32 = {}
 
-    q = draw(w.qk_std, H)
-    k = draw(w.qk_std, H // G)
-    v = draw(1.0, H // G)
-    do = draw(1.0, H)
+    def draw(name, std, heads):
+        x = torch.randn((B, heads, N, w.d), generator=g, dtype=torch.float32) * std
+        if _keep_fp32:
+            f32["_f32_" + name] = x
+        return x.to(torch.bfloat16)
+
+    q = draw("q", w.qk_std, H)
+    k = draw("k", w.qk_std, H // G)
+    v = draw("v", 1.0, H // G)
+    do = draw("do", 1.0, H)
     seqlens = None
     mask = None
     if w.key_padding:
@@ -112,7 +118,7 @@ def make_inputs(w: Workload, *, B: int | None = None, H: int | None = None, N: i
         seqlens = torch.randint(lo, N + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
     if w.block_sparse:
         mask = band_random_block_mask((N + TILE - 1) // TILE, g)
-    return dict(q=q, k=k, v=v, do=do, seqlens_k=seqlens, block_mask=mask, causal=w.causal, scale=w.scale)
+    return dict(q=q, k=k, v=v, do=do, seqlens_k=seqlens, block_mask=mask, causal=w.causal, scale=w.scale, **f32)
 
 
 def random_inputs(B, H, N, d, seed, *, std=1.0, dtype=torch.bfloat16) -> dict:
@@ -122,4 +128,23 @@ def random_inputs(B, H, N, d, seed, *, std=1.0, dtype=torch.bfloat16) -> dict:
     out = {}
     for name in ("q", "k", "v", "do"):
         out[name] = (torch.randn(shape, generator=g, dtype=torch.float32) * std).to(dtype)
+    return out
+
+
+def make_fp8_inputs(w: Workload, H: int | None = None, seed: int | None = None) -> dict:
+    """e4m3 inputs for the FP8 forward with the workload's shape, masks and seed: Q, K, V are drawn
+    exactly as in ``make_inputs`` (fp32 N(0,1) times the workload's std, same generator order), then
+    each (b, head) slice is divided by its descale factor max|x| / 448 and converted to e4m3
+    (torch's float8_e4m3fn: nearest, ties to even; nothing exceeds 448). V is returned transposed,
+    [B, Hkv, d, N]. Returns q8, k8, vt8, the fp32 descales [B, H] / [B, Hkv] and the masks."""
+    base = make_inputs(w, H=H, seed=seed, _keep_fp32=True)
+    out = {n: base[n] for n in ("block_mask", "seqlens_k", "causal", "scale")}
+    for n in ("q", "k", "v"):
+        x = base["_f32_" + n]
+        amax = x.abs().amax(dim=(2, 3)).clamp_min(1e-30)
+        desc = (amax / 448.0).to(torch.float32)
+        x8 = (x / desc[:, :, None, None]).to(torch.float8_e4m3fn)
+        out[n + "_descale"] = desc
+        out[n + "8"] = x8 if n != "v" else x8.transpose(-1, -2).contiguous()
+    out["vt8"] = out.pop("v8")
     return out

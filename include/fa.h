@@ -76,6 +76,29 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            const uint8_t* block_mask, const int32_t* seqlens_k, float scale,
            int32_t* tile_visits, int* dev_status, void* stream);
 
+/*
+ * FP8 forward pass: O and LSE from e4m3 Q, K, V with per-head descale factors.
+ * "FlashAttention." (Vol. XVI Kernels and Efficiency, plate 4), "Never write the scores", names FP8
+ * as the direction FlashAttention-3 took and fixes no scheme; the reading adopted:
+ *   inputs    q  e4m3 [B, H, N, d];  k  e4m3 [B, Hkv, N, d];  vt  e4m3 V^T [B, Hkv, d, N] (V with
+ *             the keys contiguous, the layout of the second product's operand); the attention
+ *             inputs are q_descale[b*H + h] * q, k_descale[b*Hkv + hk] * k and
+ *             v_descale[b*Hkv + hk] * v (fp32 device arrays [B*H], [B*Hkv], [B*Hkv])
+ *   computes  exact attention over those inputs, as fa_fwd_gqa does for bf16 ones (same masks,
+ *             scale, causal reading, grouped K/V heads, LSE and tile_visits), up to rounding: the
+ *             scores are exact e4m3 products summed in fp32; the probabilities are rounded to e4m3
+ *             as 2^8 P (an exact running maximum keeps 2^8 P <= 256) for the P V product, whose
+ *             error is at most sum_j max(2^-4 P_ij, 2^-18) |v_jk| per output element
+ *   outputs   o bf16 [B, H, N, d]; lse fp32 [B, H, N] (natural log of the scaled scores)
+ * Supported: d = 128 and N a multiple of 16 (else FA_ERR_UNSUPPORTED). Errors, stream and
+ * ownership as for fa_fwd.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse,
+               int B, int H, int Hkv, int N, int d, int causal,
+               const uint8_t* block_mask, const int32_t* seqlens_k,
+               const float* q_descale, const float* k_descale, const float* v_descale,
+               float scale, int32_t* tile_visits, int* dev_status, void* stream);
+
 /* Bytes of device workspace fa_bwd needs: D (fp32 [B,H,N]) and the fp32 dQ accumulator
  * ([B,H,N,d]), each rounded up to 256 bytes, then 256 bytes for the main pass's key-tile counter.
  * Returns 0 for invalid sizes. */

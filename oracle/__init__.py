@@ -1,5 +1,6 @@
 """fp64 CPU oracle (test infrastructure; see ``oracle.attention``)."""
 
+from . import fp8  # noqa: F401
 from .attention import (  # noqa: F401
     attention_backward,
     attention_backward_block,

@@ -219,3 +219,19 @@ def test_bwd_ex_validation(L):
     assert fa.fa_bwd_ex(**dict(base, q=None), extras=fa.BwdExtras(A, None, None)) == -1
     assert fa.fa_bwd_ex(**dict(base, Hkv=3), extras=None) == -1
     assert fa.fa_bwd_ex(**dict(base, d=96), extras=None) == -2
+
+
+def test_fwd_fp8_validation(L):
+    """fa_fwd_fp8 checks its arguments on the host: d must be 128 and N a multiple of 16 (the V^T rows
+    start on 16-byte boundaries), every descale array is required and 4-byte aligned."""
+    base = dict(q=A, k=A, vt=A, o=A, lse=A, B=1, H=2, Hkv=1, N=256, d=128, causal=1, block_mask=None,
+                seqlens_k=None, q_descale=A, k_descale=A, v_descale=A, scale=0.088, tile_visits=None,
+                dev_status=None, stream=None)
+    assert fa.fa_fwd_fp8(**dict(base, d=64)) == -2
+    assert fa.fa_fwd_fp8(**dict(base, N=100)) == -2
+    assert fa.fa_fwd_fp8(**dict(base, q_descale=None)) == -1
+    assert fa.fa_fwd_fp8(**dict(base, vt=None)) == -1
+    assert fa.fa_fwd_fp8(**dict(base, Hkv=3)) == -1
+    assert fa.fa_fwd_fp8(**dict(base, vt=A + 8)) == -3
+    assert fa.fa_fwd_fp8(**dict(base, k_descale=A + 2)) == -3
+    assert fa.fa_fwd_fp8(**dict(base, scale=0.0)) == -1
