@@ -7,7 +7,8 @@ fallback: if the library is missing, every call raises.
 Raw C-ABI names (same signatures as ``include/fa.h``, pointers as ints):
     fa_fwd, fa_bwd, fa_fwd_gqa, fa_bwd_gqa, fa_bwd_ex (with the BwdExtras struct), fa_bwd_workspace_bytes,
     fa_status_string, fa_bwd_noalloc,
-    fa_fwd_varlen, fa_bwd_varlen, fa_bwd_varlen_workspace_bytes (with the Strides / VarlenProblem structs)
+    fa_fwd_varlen, fa_bwd_varlen, fa_bwd_varlen_accumulate, fa_bwd_varlen_workspace_bytes (with the Strides /
+    VarlenProblem structs)
 Tensor helpers (grouped-query attention when k, v have fewer heads than q):
     fwd(q, k, v, ...) -> (o, lse);  bwd(q, k, v, o, lse, do, ...) -> (dq, dk, dv)
     fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, ...) -> (o, lse): e4m3 inputs (fa_fwd_fp8)
@@ -70,6 +71,8 @@ _SIGS = {
     "fa_bwd_varlen_workspace_bytes": (ctypes.c_size_t, [_VP]),
     "fa_bwd_varlen": (_I, [_VP, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, Strides,
                            _P, Strides, _P, Strides, _P, ctypes.c_size_t, _P, _P]),
+    "fa_bwd_varlen_accumulate": (_I, [_VP, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P,
+                                      Strides, _P, Strides, _P, Strides, _P, ctypes.c_size_t, _P, _P]),
     "fa_fwd_splitkv_splits": (_I, [_VP, _I]),
     "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_VP, _I]),
     "fa_fwd_splitkv": (_I, [_VP, _I, _P, Strides, _P, Strides, _P, Strides, _P, Strides, _P, _P, ctypes.c_size_t, _P,
@@ -443,6 +446,46 @@ def bwd_varlen(q, k, v, o, lse, do, cu_seqlens_q=None, cu_seqlens_k=None, max_se
     if rc != 0:
         raise FaError(rc)
     return dq, dk, dv
+
+
+def _view_f32(t, packed):
+    """Strides of an fp32 accumulator laid out like a bf16 tensor view (d contiguous)."""
+    if not (t.is_cuda and t.dtype == torch.float32 and t.stride(-1) == 1):
+        raise ValueError("accumulators must be fp32 CUDA tensors with a contiguous last (head) dimension")
+    if packed:
+        if t.dim() != 3:
+            raise ValueError("packed accumulators are [rows, heads, d]")
+        return Strides(t.stride(0), t.stride(1), 0)
+    if t.dim() != 4:
+        raise ValueError("fixed-length accumulators are [B, N, H, d] views")
+    return Strides(t.stride(1), t.stride(2), t.stride(0))
+
+
+def bwd_varlen_accumulate(q, k, v, o, lse, do, dq_acc, dk_acc, dv_acc, cu_seqlens_q=None, cu_seqlens_k=None,
+                          max_seqlen_q=None, max_seqlen_k=None, *, causal=False, scale=None, workspace=None,
+                          status=None, stream=None):
+    """bwd_varlen whose fp32 dQ, dK, dV shares are added into dq_acc, dk_acc, dv_acc (fp32 tensors
+    shaped like q, k, v) in place (fa_bwd_varlen_accumulate)."""
+    p, packed = _problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale)
+    for name, acc, ref in (("dq_acc", dq_acc, q), ("dk_acc", dk_acc, k), ("dv_acc", dv_acc, v)):
+        if acc.shape != ref.shape:
+            raise ValueError(f"{name} must have the shape of its tensor {tuple(ref.shape)}")
+    nbytes = fa_bwd_varlen_workspace_bytes(p)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _same_device(q, k, v, o, do, dq_acc, dk_acc, dv_acc)
+    _check_aux("lse", lse, torch.float32, _lse_numel(q, p, packed), q.device)
+    _check_aux("workspace", workspace, None, nbytes, q.device)
+    _check_aux("status", status, torch.int32, 1, q.device)
+    rc = int(lib().fa_bwd_varlen_accumulate(
+        ctypes.byref(p), q.data_ptr(), _view(q, packed), k.data_ptr(), _view(k, packed), v.data_ptr(),
+        _view(v, packed), o.data_ptr(), _view(o, packed), do.data_ptr(), _view(do, packed), lse.data_ptr(),
+        dq_acc.data_ptr(), _view_f32(dq_acc, packed), dk_acc.data_ptr(), _view_f32(dk_acc, packed),
+        dv_acc.data_ptr(), _view_f32(dv_acc, packed), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+    if rc != 0:
+        raise FaError(rc)
+    return dq_acc, dk_acc, dv_acc
 
 
 def fwd_splitkv(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, *,

@@ -150,8 +150,9 @@ size_t splitkv_bytes(const fa::AttnShape& s, int splits) {
 struct BwdTensors {
   const void *q, *k, *v, *o, *dout;
   const float* lse;
-  void *dq, *dk, *dv;
+  void *dq, *dk, *dv;  // bf16 outputs, or (accumulate) the fp32 accumulators
   FaStrides sq, sk, sv, so, sdo, sdq, sdk, sdv;
+  bool accumulate = false;
 };
 
 int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* workspace, size_t workspace_bytes,
@@ -189,6 +190,11 @@ int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* w
   a.s = s;
   a.scale = scale;
   a.status = dev_status;
+  if (t.accumulate) {
+    a.dq_acc = static_cast<float*>(t.dq);
+    a.dk_acc = static_cast<float*>(t.dk);
+    a.dv_acc = static_cast<float*>(t.dv);
+  }
   a.step_visits = extras ? extras->step_visits : nullptr;
   a.ev_main_begin = extras ? static_cast<cudaEvent_t>(extras->main_begin_event) : nullptr;
   a.ev_main_end = extras ? static_cast<cudaEvent_t>(extras->main_end_event) : nullptr;
@@ -475,10 +481,34 @@ size_t fa_bwd_varlen_workspace_bytes(const fa_varlen_problem* p) {
   return workspace_for(s);
 }
 
+static int bwd_varlen_impl(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                           const void* v, fa_strides sv, const void* o, fa_strides so, const void* dout,
+                           fa_strides sdo, const float* lse, void* dq, fa_strides sdq, void* dk, fa_strides sdk,
+                           void* dv, fa_strides sdv, void* workspace, size_t workspace_bytes, int* dev_status,
+                           void* stream, bool accumulate);
+
 int fa_bwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
                   const void* v, fa_strides sv, const void* o, fa_strides so, const void* dout, fa_strides sdo,
                   const float* lse, void* dq, fa_strides sdq, void* dk, fa_strides sdk, void* dv, fa_strides sdv,
                   void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+  return bwd_varlen_impl(p, q, sq, k, sk, v, sv, o, so, dout, sdo, lse, dq, sdq, dk, sdk, dv, sdv, workspace,
+                         workspace_bytes, dev_status, stream, false);
+}
+
+int fa_bwd_varlen_accumulate(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                             const void* v, fa_strides sv, const void* o, fa_strides so, const void* dout,
+                             fa_strides sdo, const float* lse, float* dq_acc, fa_strides sdq, float* dk_acc,
+                             fa_strides sdk, float* dv_acc, fa_strides sdv, void* workspace, size_t workspace_bytes,
+                             int* dev_status, void* stream) {
+  return bwd_varlen_impl(p, q, sq, k, sk, v, sv, o, so, dout, sdo, lse, dq_acc, sdq, dk_acc, sdk, dv_acc, sdv,
+                         workspace, workspace_bytes, dev_status, stream, true);
+}
+
+static int bwd_varlen_impl(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                           const void* v, fa_strides sv, const void* o, fa_strides so, const void* dout,
+                           fa_strides sdo, const float* lse, void* dq, fa_strides sdq, void* dk, fa_strides sdk,
+                           void* dv, fa_strides sdv, void* workspace, size_t workspace_bytes, int* dev_status,
+                           void* stream, bool accumulate) {
   fa::AttnShape s;
   int rc = varlen_shape(p, &s);
   if (rc != FA_OK) return rc;
@@ -494,6 +524,7 @@ int fa_bwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, cons
   t.dq = dq;
   t.dk = dk;
   t.dv = dv;
+  t.accumulate = accumulate;
   if ((rc = take_strides(sq, packed, s.B, rq, s.H, &t.sq)) != FA_OK ||
       (rc = take_strides(sk, packed, s.B, rk, s.Hkv, &t.sk)) != FA_OK ||
       (rc = take_strides(sv, packed, s.B, rk, s.Hkv, &t.sv)) != FA_OK ||

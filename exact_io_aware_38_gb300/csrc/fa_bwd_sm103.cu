@@ -147,8 +147,14 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const FaBwdArgs a) {
   for (size_t r = warp0; r < rows; r += nwarps) {
     int b, row, h;
     row_coords(a.s, r, b, row, h);
-    __nv_bfloat16* out = dq + elem_offset(a.sdq, b, row, h) + lane * PER;
     const float* acc = a.dqacc + r * D + lane * PER;
+    if (a.dq_acc != nullptr) {  // accumulate: the caller's fp32 dQ += scale * this call's sum
+      float* dst = a.dq_acc + elem_offset(a.sdq, b, row, h) + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) dst[e] += acc[e] * a.scale;
+      continue;
+    }
+    __nv_bfloat16* out = dq + elem_offset(a.sdq, b, row, h) + lane * PER;
     if constexpr (PER == 2) {
       const float2 x = *reinterpret_cast<const float2*>(acc);
       *reinterpret_cast<uint32_t*>(out) = pack_bf16x2(x.x * a.scale, x.y * a.scale);
@@ -224,7 +230,9 @@ __device__ __forceinline__ int bwd_count_steps(const AttnShape& s, const BwdTile
   return n;
 }
 
-template <int D>
+// ACC: accumulate mode (dK and dV added in fp32 into the caller's accumulators); a separate
+// instantiation keeps the bf16-output kernel's code as it is.
+template <int D, bool ACC = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -684,6 +692,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) vv[i] = 0u;
         }
+        if constexpr (ACC) {  // fp32 shares added into the caller's accumulators (this CTA owns the rows)
+          if (store) {
+            float4* arow = reinterpret_cast<float4*>((elementwise ? a.dk_acc : a.dv_acc) +
+                                                     elem_offset(elementwise ? a.sdk : a.sdv, seq.bb, seq.k0 + key, T.hk)) +
+                           c * 8;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float4 x = arow[j];
+              x.x += __uint_as_float(vv[4 * j]) * mul;
+              x.y += __uint_as_float(vv[4 * j + 1]) * mul;
+              x.z += __uint_as_float(vv[4 * j + 2]) * mul;
+              x.w += __uint_as_float(vv[4 * j + 3]) * mul;
+              arow[j] = x;
+            }
+          }
+        } else {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -692,6 +716,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             *reinterpret_cast<uint4*>(grow + c * 32 + j * 8) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
         }
       }
       if (any_work) {  // the accumulators may be overwritten by the next tile's first products
@@ -730,7 +755,8 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   bwd_pre_kernel<D><<<grid_ew, 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  auto main_kernel = a.dk_acc != nullptr ? bwd_tc_kernel<D, true> : bwd_tc_kernel<D, false>;
+  e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   // Persistent: one CTA per SM (shared memory allows one), key tiles handed out by the counter.
   const long long ntiles = (long long)s.nbk * s.B * s.Hkv;
@@ -738,7 +764,7 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   if (a.ev_main_begin != nullptr && (e = cudaEventRecord(a.ev_main_begin, st)) != cudaSuccess) return e;
   if (ntiles > 0) {
     const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
-    bwd_tc_kernel<D><<<grid, kBwdThreads, C::kSmem, st>>>(tq, tk, tv, tdo, a);
+    main_kernel<<<grid, kBwdThreads, C::kSmem, st>>>(tq, tk, tv, tdo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -168,6 +168,9 @@ struct FaBwdArgs {
   fa::AttnShape s;
   float scale;
   int* status;
+  // Accumulate mode (all three set): fp32 dQ, dK, dV shares are added into these caller tensors
+  // (element strides sdq, sdk, sdv) instead of writing bf16 dq, dk, dv.
+  float *dq_acc, *dk_acc, *dv_acc;
   int32_t* step_visits;       // nullable: query steps visited per (b, K/V head, key tile)
   cudaEvent_t ev_main_begin;  // nullable (host side): recorded around the main launch
   cudaEvent_t ev_main_end;

@@ -14,9 +14,10 @@ The backward pass follows the same schedule. With each query row's final O and l
 all keys, one (query block, key block) pair's share of the gradients is exactly what the fused
 backward kernel computes for that pair: P = exp(c S - LSE) is the row's softmax restricted to the
 block and D = rowsum(dO * O) is the whole row's. So each step runs fa_bwd_varlen on the block it
-holds; dQ accumulates on the rank, and the fp32 dK, dV accumulators travel with their K/V block.
-After the last step a rank holds block rank + 1 and its accumulators, so one more rotation delivers
-every block's dK, dV to its owner.
+holds; the library adds each share in fp32 into the rank's dQ accumulator and the dK, dV
+accumulators that travel with the K/V block (fa_bwd_varlen_accumulate), so no share is rounded to
+bf16 before it is summed. After the last step a rank holds block rank + 1 and its accumulators, so
+one more rotation delivers every block's dK, dV to its owner.
 
 Out of scope: load balancing of the causal case (e.g. zig-zag block orders), overlap of the
 rotation with the compute.
@@ -81,10 +82,11 @@ def ring_forward(q, k, v, *, causal=False, scale=None, group=None, partial=None,
 def ring_backward(q, k, v, o, lse, do, *, causal=False, scale=None, group=None, partial_bwd=None, rotate_fn=None):
     """dQ, dK, dV of this rank's blocks ([B, N_block, H, d] views, as for ring_forward; o and lse
     are ring_forward's results for this rank's queries, do the gradient of o). `partial_bwd`
-    (q, k_blk, v_blk, o, lse, do, causal) -> (dq, dk, dv) shares and `rotate_fn` default to the
-    library's backward kernel and torch.distributed point-to-point copies."""
-    partial_bwd = partial_bwd or (lambda q_, k_, v_, o_, l_, do_, c_: fa.bwd_varlen(q_, k_, v_, o_, l_, do_,
-                                                                                   causal=c_, scale=scale))
+    (q, k_blk, v_blk, o, lse, do, causal, dq_acc, dk_acc, dv_acc) adds one block pair's shares into
+    the accumulators in place; it and `rotate_fn` default to the library's accumulating backward
+    kernel and torch.distributed point-to-point copies."""
+    partial_bwd = partial_bwd or (lambda q_, k_, v_, o_, l_, do_, c_, aq, ak, av: fa.bwd_varlen_accumulate(
+        q_, k_, v_, o_, l_, do_, aq, ak, av, causal=c_, scale=scale))
     rotate_fn = rotate_fn or rotate
     world = dist.get_world_size(group)
     rank = dist.get_rank(group)
@@ -94,10 +96,7 @@ def ring_backward(q, k, v, o, lse, do, *, causal=False, scale=None, group=None, 
     dkv = [torch.zeros(k.shape, dtype=acc, device=k.device), torch.zeros(v.shape, dtype=acc, device=v.device)]
     for step, _src, c in ring_schedule(rank, world, causal):
         if c is not None:
-            gq, gk, gv = partial_bwd(q, kv[0], kv[1], o, lse, do, c)
-            dq += gq.to(acc)
-            dkv[0] += gk.to(acc)
-            dkv[1] += gv.to(acc)
+            partial_bwd(q, kv[0], kv[1], o, lse, do, c, dq, dkv[0], dkv[1])
         if step + 1 < world:
             moved = rotate_fn(kv + dkv, group)  # the block and its accumulators travel together
             kv, dkv = moved[:2], moved[2:]

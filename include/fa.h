@@ -226,6 +226,23 @@ int fa_bwd_varlen(const fa_varlen_problem* p, const void* q, fa_strides sq, cons
                   void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
 /*
+ * fa_bwd_varlen adding fp32 shares into caller accumulators instead of writing bf16 gradients:
+ * dq_acc += c dS K, dk_acc += c dS^T Q and dv_acc += P^T dO for this call's problem (sequence-sharded
+ * ring attention sums one such share per (query block, key block) pair, and rounding each share to
+ * bf16 before the sum would lose precision the kernels hold in fp32). dq_acc, dk_acc and dv_acc are
+ * fp32 device tensors in the [batch][row][head][d] views of dq, dk, dv (element strides sdq, sdk, sdv,
+ * multiples of 8, 16-byte aligned base); every other argument, the workspace and the errors are as for
+ * fa_bwd_varlen. Rows outside every sequence are left as they are. Calls on one stream accumulate in
+ * order; dK and dV rows are each owned by one CTA and the dQ rows by one warp of the post-pass, so a
+ * call has no races of its own, but calls that overlap on the GPU and share accumulators race.
+ */
+int fa_bwd_varlen_accumulate(const fa_varlen_problem* p, const void* q, fa_strides sq, const void* k, fa_strides sk,
+                             const void* v, fa_strides sv, const void* o, fa_strides so, const void* dout,
+                             fa_strides sdo, const float* lse, float* dq_acc, fa_strides sdq, float* dk_acc,
+                             fa_strides sdk, float* dv_acc, fa_strides sdv, void* workspace,
+                             size_t workspace_bytes, int* dev_status, void* stream);
+
+/*
  * Forward split over keys, for decode-shaped problems (few query rows, long keys), where one CTA
  * per pair of 128-row query tiles would leave most SMs idle. The pages name no decode path; the
  * method is the same online softmax, with the key tiles of each query tile split into

@@ -43,9 +43,10 @@ def rel_fro(x, ref):
     nr = np.linalg.norm(ref)
     if nr == 0:
         assert np.abs(x).max() <= 1e-3
-        return
+        return 0.0
     r = np.linalg.norm(x - ref) / nr
     assert r <= REL_FRO, r
+    return r
 
 
 def run_status(fn):
@@ -268,6 +269,7 @@ def test_ring_backward_simulated_on_one_gpu(causal, d):
     dq = torch.zeros((B, W * blk, H, d), dtype=torch.float32, device="cuda")
     dk = torch.zeros((B, W * blk, Hkv, d), dtype=torch.float32, device="cuda")
     dv = torch.zeros_like(dk)
+    dq16, dk16, dv16 = torch.zeros_like(dq), torch.zeros_like(dk), torch.zeros_like(dv)  # bf16 shares summed
     for rank in range(W):
         qb, dob = block(qc, rank), block(doc, rank)
         acc = None
@@ -280,10 +282,64 @@ def test_ring_backward_simulated_on_one_gpu(causal, d):
         for _, src, c in ring.ring_schedule(rank, W, causal):
             if c is None:
                 continue
+            # fp32 shares added in place into the accumulators' blocks (views of the full tensors)
+            fa.bwd_varlen_accumulate(qb, block(kc, src), block(vc, src), ob, lb, dob, dq[:, rank * blk:(rank + 1) * blk],
+                                     dk[:, src * blk:(src + 1) * blk], dv[:, src * blk:(src + 1) * blk], causal=c,
+                                     scale=scale)
             gq, gk, gv = fa.bwd_varlen(qb, block(kc, src), block(vc, src), ob, lb, dob, causal=c, scale=scale)
-            dq[:, rank * blk:(rank + 1) * blk] += gq.float()
-            dk[:, src * blk:(src + 1) * blk] += gk.float()
-            dv[:, src * blk:(src + 1) * blk] += gv.float()
+            dq16[:, rank * blk:(rank + 1) * blk] += gq.float()
+            dk16[:, src * blk:(src + 1) * blk] += gk.float()
+            dv16[:, src * blk:(src + 1) * blk] += gv.float()
     torch.cuda.synchronize()
-    for got, want in ((dq, rq), (dk, rk), (dv, rv)):
-        rel_fro(f64(got).transpose(0, 2, 1, 3), want)
+    errs, errs16 = [], []
+    for got, got16, want in ((dq, dq16, rq), (dk, dk16, rk), (dv, dv16, rv)):
+        errs.append(rel_fro(f64(got).transpose(0, 2, 1, 3), want))
+        errs16.append(rel_fro(f64(got16).transpose(0, 2, 1, 3), want))
+    # Summing fp32 shares is at least as accurate as summing bf16-rounded ones, and clearly more
+    # accurate for dK, dV, the sums over the ring's key blocks (the dQ share of a row block is
+    # rounded only once in both: its post-pass output).
+    print(f"ring backward rel. Frobenius error, fp32 shares {errs}, bf16 shares {errs16}")
+    assert all(e <= e16 * 1.02 for e, e16 in zip(errs, errs16)), (errs, errs16)
+    assert errs[1] < errs16[1] and errs[2] < errs16[2], (errs, errs16)
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_backward_accumulate_adds_fp32_shares(packed):
+    """fa_bwd_varlen_accumulate adds its fp32 dQ, dK, dV into the caller's accumulators: starting
+    from random contents, the difference after one call matches the oracle gradients, a second call
+    adds the same again, and rows outside every sequence are left as they were."""
+    g = torch.Generator().manual_seed(77)
+    d, H, Hkv, scale = 128, 4, 2, 0.09
+    if packed:
+        lens = [130, 0, 257]
+        cu = torch.tensor([0, 130, 130, 387], dtype=torch.int32)
+        rows = 400  # 13 spare rows
+        q, do = bf16((rows, H, d), g), bf16((rows, H, d), g)
+        k, v = bf16((rows, Hkv, d), g), bf16((rows, Hkv, d), g)
+        kw = dict(cu_seqlens_q=cu.cuda(), cu_seqlens_k=cu.cuda(), max_seqlen_q=max(lens), max_seqlen_k=max(lens))
+    else:
+        q, do = bf16((2, 300, H, d), g), bf16((2, 300, H, d), g)
+        k, v = bf16((2, 300, Hkv, d), g), bf16((2, 300, Hkv, d), g)
+        kw = {}
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.fwd_varlen(qc, kc, vc, causal=True, scale=scale, **kw)
+    acc0 = [torch.randn(t.shape, generator=g).cuda() for t in (q, k, v)]
+    acc = [a.clone() for a in acc0]
+    fa.bwd_varlen_accumulate(qc, kc, vc, o, lse, doc, *acc, causal=True, scale=scale, **kw)
+    torch.cuda.synchronize()
+    one = [a - a0 for a, a0 in zip(acc, acc0)]
+    if packed:
+        rq, rk, rv = oracle.attention_backward_varlen(f64(q), f64(k), f64(v), f64(do), cu.numpy(), cu.numpy(), scale,
+                                                      causal=True)
+        for got, want in zip(one, (rq, rk, rv)):
+            rel_fro(f64(got)[:387], want[:387])
+            assert (got[387:] == 0).all()  # spare rows untouched
+    else:
+        t4 = lambda x: f64(x).transpose(0, 2, 1, 3)
+        rq, rk, rv = oracle.attention_backward(t4(q), t4(k), t4(v), t4(do), scale, causal=True)
+        for got, want in zip(one, (rq, rk, rv)):
+            rel_fro(f64(got).transpose(0, 2, 1, 3), want)
+    fa.bwd_varlen_accumulate(qc, kc, vc, o, lse, doc, *acc, causal=True, scale=scale, **kw)
+    torch.cuda.synchronize()
+    for a, a0, x in zip(acc, acc0, one):  # a second call adds the same shares again
+        assert torch.allclose(a - a0, 2 * x, atol=1e-4, rtol=1e-4)

@@ -146,10 +146,12 @@ def _ring_bwd_worker(rank, world, port, causal, q):
         qb, kb, vb, dob = (t[:, sl].contiguous() for t in (qf, kf, vf, dof))
         ob, lb = back(of)[:, sl].contiguous(), torch.from_numpy(lf[:, :, sl].copy())
 
-        def partial_bwd(q_, k_, v_, o_, l_, do_, c_):
+        def partial_bwd(q_, k_, v_, o_, l_, do_, c_, aq, ak, av):
             gq, gk, gv = oracle.attention_backward_block(t4(q_), t4(k_), t4(v_), t4(o_), l_.numpy(), t4(do_), c,
                                                          causal=c_)
-            return back(gq), back(gk), back(gv)
+            aq += back(gq)
+            ak += back(gk)
+            av += back(gv)
 
         dq, dk, dv = ring.ring_backward(qb, kb, vb, ob, lb, dob, causal=causal, partial_bwd=partial_bwd)
         rq, rk, rv = (back(x)[:, sl] for x in oracle.attention_backward(t4(qf), t4(kf), t4(vf), t4(dof), c,
