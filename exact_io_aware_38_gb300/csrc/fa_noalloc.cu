@@ -11,11 +11,13 @@
 // The array is a file-scope __device__ object of FA_NOALLOC_SCRATCH_BYTES bytes. Every GPU on
 // which the library is loaded holds it until the process exits. Host code cannot use the
 // array's name as a device address, so the first call on each device looks the address up with
-// cudaGetSymbolAddress (with that device current) and caches it; make that first call before
-// any stream capture. All calls share the one array and it keeps the previous call's contents;
+// cudaGetSymbolAddress (with that device current) and caches it with the context it belongs to;
+// after a device reset the next call looks it up again in the new context. Make the first call on
+// a device (and the first after a reset) before any stream capture. All calls share the one array and it keeps the previous call's contents;
 // the backward kernels overwrite D and clear the dQ accumulator themselves on every call, so no
 // extra clearing is needed. Two calls whose work overlaps on the GPU (e.g. on two streams) race
 // on the array.
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include <mutex>
@@ -29,6 +31,25 @@ static __device__ __align__(256) unsigned char g_fa_scratch[FA_NOALLOC_SCRATCH_B
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices];  // device address of g_fa_scratch per device ordinal
+CUcontext g_scratch_ctx[kMaxDevices];  // the context that address belongs to
+
+// The current context (through the driver entry point; null if it cannot be queried). A device
+// reset gives the device a new primary context, in which the array has a new address.
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  }
+  CUcontext c = nullptr;
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 // Same shape rules as fa_bwd, checked before any CUDA call.
 int check_shape_noalloc(int B, int H, int N, int d, int causal, float scale) {
@@ -44,10 +65,12 @@ int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  const CUcontext ctx = current_context();
+  if (g_scratch_addr[dev] == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_fa_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = current_context();  // the runtime has made the primary context current by now
   }
   *out = g_scratch_addr[dev];
   return FA_OK;

@@ -299,8 +299,9 @@ int fa_finalize_partials(const fa_varlen_problem* p, const float* acc_o, const f
  * FA_NOALLOC_SCRATCH_BYTES array of its own device image instead (held on every GPU where the
  * library is loaded, until the process exits). Problems whose fa_bwd_workspace_bytes exceed it
  * return FA_ERR_SCRATCH_LIMIT before anything is launched; e.g. d = 128 fits up to about 65 000
- * rows B*H*N. The first call on a device looks up the array's device address (call it once
- * before any stream capture). Calls share the array: two calls whose work overlaps on the GPU
+ * rows B*H*N. The first call on a device looks up the array's device address, and so does the
+ * first call after a device reset (the address belongs to the device's context); make those calls
+ * before any stream capture. Calls share the array: two calls whose work overlaps on the GPU
  * (e.g. on different streams) race. Calls in sequence are safe; every call re-initialises what
  * it reads.
  */

@@ -4,11 +4,15 @@ framework owns the device memory pool). It must give the same gradients as fa_bw
 caller-supplied workspace, call after call, although its fixed scratch array keeps the previous
 call's contents. This file is collected last on purpose."""
 
+import os
+import re
+
 import numpy as np
 import pytest
 import torch
 
 import exact_io_aware_38_gb300 as fa
+import oracle
 from exact_io_aware_38_gb300 import build, workloads
 
 REL_FRO = 2e-2  # the gradient tolerance of the parity tests
@@ -41,6 +45,8 @@ def _noalloc(t, kw, shape, o, lse, status):
 
 @pytest.mark.gpu
 def test_noalloc_matches_fa_bwd_on_consecutive_calls():
+    """Two calls in a row, with different problems, each against fa_bwd with a workspace (the scratch
+    keeps the previous call's contents) and the first also against the fp64 oracle."""
     build.build()
     fa.lib()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -54,6 +60,21 @@ def test_noalloc_matches_fa_bwd_on_consecutive_calls():
         for name, a, b in zip(("dq", "dk", "dv"), got, ref):
             assert torch.isfinite(a.float()).all(), name
             assert _rel(a, b) <= REL_FRO, (seed, name, _rel(a, b))
+        if seed == 21:
+            f = lambda x: x.double().cpu().numpy()
+            want = oracle.attention_backward(f(t["q"]), f(t["k"]), f(t["v"]), f(t["do"]), kw["scale"], causal=causal)
+            for name, a, w in zip(("dq", "dk", "dv"), got, want):
+                r = float(np.linalg.norm(f(a) - w) / np.linalg.norm(w))
+                assert r <= REL_FRO, (name, r)
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    """The binding's constant is the header's FA_NOALLOC_SCRATCH_BYTES."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = open(os.path.join(root, "include", "fa.h")).read()
+    m = re.search(r"#define\s+FA_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "FA_NOALLOC_SCRATCH_BYTES not found"
+    assert fa.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
