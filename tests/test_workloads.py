@@ -69,3 +69,26 @@ def test_c5_mask_band_and_density():
     kept = float(off.sum())
     assert abs(kept - 0.08 * n) < 5 * math.sqrt(0.08 * 0.92 * n), (kept, n)
     assert bool((m.sum(dim=1) > 0).all())
+
+
+def test_fp8_recipe_matches_the_oracle_quantiser():
+    """make_fp8_inputs draws Q, K, V as make_inputs does, divides each (b, head) by max|x| / 448 and
+    rounds to e4m3: the same values as the oracle's own quantiser gives, none saturated, and V
+    comes back transposed."""
+    import numpy as np
+
+    from oracle import fp8
+
+    w = W.WORKLOADS["c4"]
+    inp = W.make_fp8_inputs(w, H=2)
+    base = W.make_inputs(w, H=2, _keep_fp32=True)
+    for n in ("q", "k", "v"):
+        desc = inp[n + "_descale"]
+        x = (base["_f32_" + n] / desc[:, :, None, None]).double().numpy()
+        want = fp8.e4m3_quantize(x)
+        got = inp[n + "8"] if n != "v" else inp["vt8"].transpose(-1, -2)
+        got = got.double().numpy()
+        assert np.array_equal(got, want), n
+        assert np.abs(got).max() <= 448.0 and np.isclose(np.abs(got).max(), 448.0)
+    a = W.make_inputs(w, H=2)
+    assert all(torch.equal(a[n], base[n]) for n in ("q", "k", "v", "do"))  # the fp32 option changes no draw
