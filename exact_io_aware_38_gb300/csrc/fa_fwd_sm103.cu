@@ -37,25 +37,29 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;        // pair mode: producer, issuer, two softmax warpgroups
+constexpr int kThreadsSingle = 192;  // single mode: producer, issuer, one softmax warpgroup
 constexpr int kVisWords = 64;  // key tiles covered by the per-CTA visibility bitmap: 2048
 
 // F8: e4m3 operands (Q, K and V^T with per-head descales; d = 128), the two products as
 // kind::f8f6f4 MMAs and P rounded to e4m3 as 2^8 P; otherwise bf16 operands (kind::f16).
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, bool SINGLE = false>
 struct FwdCfg {
   static constexpr int kBoxCols = F8 ? 128 : 64;        // columns of one 128-byte TMA box
   static constexpr int kBoxes = D / kBoxCols;           // boxes per operand row
   static constexpr int kOBoxes = D / 64;                // boxes per bf16 output row
   static constexpr int kTileBytes = 128 * D * (F8 ? 1 : 2);  // one 128-row operand tile (Q, K, V or V^T)
   static constexpr int kQSlot = 128 * D * 2;            // a query tile's slot: Q, later its bf16 O staging
-  static constexpr int kStages = (D == 128 && !F8) ? 2 : 4;  // K/V ring: stage t holds V_t and K_t+1
-  static constexpr int kSmem = 2 * kQSlot + 2 * kStages * kTileBytes + 1024;
+  static constexpr int kTiles = SINGLE ? 1 : 2;         // query tiles per CTA
+  static constexpr int kStages = (SINGLE || (D == 128 && !F8)) ? 2 : 4;  // K/V ring: stage t holds V_t, K_t+1
+  static constexpr int kSmem = kTiles * kQSlot + 2 * kStages * kTileBytes + 1024;
+  static constexpr int kThreadsCta = SINGLE ? kThreadsSingle : kThreads;
+  static constexpr uint32_t kTmemCols = SINGLE ? 256 : 512;
   static constexpr int kSSteps = D / (F8 ? 32 : 16);    // MMAs of one S = Q K^T (K = 16 bf16 / 32 e4m3 each)
   static constexpr int kPVSteps = 128 / (F8 ? 32 : 16);  // MMAs of one O += P V
   static constexpr uint32_t kIdS = F8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
   static constexpr uint32_t kIdPV = F8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
-  static constexpr uint32_t kTmemS0 = 0, kTmemO0 = 256;
+  static constexpr uint32_t kTmemS0 = 0, kTmemO0 = SINGLE ? 128 : 256;
   // O is rescaled only when a row max grows by more than 2^kRescale (lazy; exact since l and O share
   // the stale max). The e4m3 P is 2^8 exp2(s - m) <= 256 only with the exact running max.
   static constexpr float kRescale = F8 ? 0.0f : 8.0f;
@@ -86,21 +90,24 @@ struct FwdSmemCtl {
 // SPLIT: the CTA covers one split of the key tiles and writes fp32 partials (see FaFwdArgs).
 // MASKED: a block mask is given (never with SPLIT); without one, visibility is in closed form.
 // F8: e4m3 operands (see FwdCfg; never with SPLIT).
-template <int D, bool SPLIT, bool MASKED, bool F8 = false>
-__global__ void __launch_bounds__(kThreads, 1)
+// SINGLE: one query tile per CTA (d = 64), small enough that two CTAs share an SM: one CTA's
+// softmax runs while the other's products do. A pair of query tiles instead walks the union of
+// their key tiles, and under a block mask one tile's softmax is then often idle.
+template <int D, bool SPLIT, bool MASKED, bool F8 = false, bool SINGLE = false>
+__global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2 : 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FaFwdArgs a) {
-  using C = FwdCfg<D, F8>;
+  using C = FwdCfg<D, F8, SINGLE>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);                       // Q0, Q1 (later O staging), kQSlot each
-  const uint32_t sKV = sQ + 2 * C::kQSlot;                  // ring: stage buffer b = V (V^T) then K
+  const uint32_t sKV = sQ + C::kTiles * C::kQSlot;         // ring: stage buffer b = V (V^T) then K
   volatile int* abort_flag = &ctl.abort_flag;
 
   const AttnShape& s = a.s;
   const int BH = s.B * s.H;
-  const int npairs = (s.nbq + 1) >> 1;
+  const int npairs = (s.nbq + C::kTiles - 1) / C::kTiles;  // CTAs per head (pairs of query tiles, or tiles)
   const int split = SPLIT ? (int)(blockIdx.x / (npairs * BH)) : 0;  // key range [kt_lo, kt_hi) of this CTA
   const int pidx = (blockIdx.x % (npairs * BH)) / BH;
   const int bh = blockIdx.x % BH;
@@ -109,9 +116,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / s.H, h = bh % s.H;
   const int hk = h / (s.H / s.Hkv);  // K/V head of this query head
   const SeqInfo seq = seq_info(s, b);
-  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+  const int qt0 = C::kTiles * pair, qt1 = qt0 + 1;
   if (qt0 * 128 >= seq.Lq) return;  // a packed sequence shorter than the grid's maximum
-  const bool has1 = qt1 * 128 < seq.Lq;
+  const bool has1 = !SINGLE && qt1 * 128 < seq.Lq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // Without a block mask a query tile sees exactly the key tiles 0 .. last_kt (the predicate of
@@ -196,12 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl.tmem_base), 512);
+    tmem_alloc(smem_u32(&ctl.tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
   if (MASKED && bitmap) {  // one vote per 32 key tiles of a query tile; only [kt_lo, kt_end) is ever read
     const int words = (kt_end + 31) >> 5;
-    for (int idx = warp; idx < 2 * words; idx += kThreads / 32) {
+    for (int idx = warp; idx < 2 * words; idx += C::kThreadsCta / 32) {
       const int x = idx & 1, wd = idx >> 1, kt = wd * 32 + lane;
       const bool bit = kt >= kt_lo && kt < kt_end && (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt);
       const uint32_t m = __ballot_sync(0xffffffffu, bit);
@@ -569,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     fence_after_sync();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) {
     // Every role has finished, so no arrival is still to come: let the copies still in flight
@@ -614,6 +621,23 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
   const int BH = s.B * s.H;
   const bool split = a.part_o != nullptr;
   if (split && s.block_mask != nullptr) return cudaErrorInvalidValue;  // no split path takes a mask
+  // d = 64 without a split: one query tile per CTA, two CTAs per SM (measured faster than the pair
+  // of query tiles on block-sparse and causal problems, equal on the rest).
+  if constexpr (D == 64) {
+    if (!split) {
+      using CS = FwdCfg<D, false, true>;
+      auto ks = s.block_mask != nullptr ? fwd_tc_kernel<D, false, true, false, true>
+                                        : fwd_tc_kernel<D, false, false, false, true>;
+      cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::kSmem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(ks, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return e;
+      const long long grid = (long long)s.nbq * BH;
+      if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      ks<<<(unsigned)grid, CS::kThreadsCta, CS::kSmem, st>>>(tq, tk, tv, to, a);
+      return cudaGetLastError();
+    }
+  }
   auto kern = split ? fwd_tc_kernel<D, true, false>
                     : (s.block_mask != nullptr ? fwd_tc_kernel<D, false, true> : fwd_tc_kernel<D, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
