@@ -96,71 +96,90 @@ __device__ __forceinline__ float* dvec_row(BwdSmemCtl& c, int buf) {
   return c.dvec + buf * BwdCfg<D>::BM;
 }
 
-// D = rowsum(dO * O) per query row (one warp per row) and a cleared dQ accumulator.
+// The pre and post passes walk the per-row arrays (D, the fp32 dQ accumulator) in their LSE order:
+// runs of rows, one per (b, h) for fixed-length batches or per h for packed ones. A CTA takes 64
+// rows of one run, so a row's tensor coordinates need no division, and moves 16 bytes per thread.
+constexpr int kRowTile = 64;
+struct RowTile {
+  int b, h, row0, rows;  // rows [row0, row0 + rows) of run (b, h)
+  size_t r0;             // LSE-order index of the run's row 0
+};
+__device__ __forceinline__ RowTile row_tile(const AttnShape& s) {
+  const bool packed = s.cu_q != nullptr;
+  const int nrows = packed ? s.rows_q : s.Nq;
+  const int tiles = (nrows + kRowTile - 1) / kRowTile;
+  const int run = blockIdx.x / tiles;
+  RowTile t;
+  t.b = packed ? 0 : run / s.H;
+  t.h = packed ? run : run % s.H;
+  t.row0 = (blockIdx.x % tiles) * kRowTile;
+  t.rows = min(kRowTile, nrows - t.row0);
+  t.r0 = (size_t)run * nrows;
+  return t;
+}
+__host__ inline long long row_tile_grid(const AttnShape& s) {
+  const bool packed = s.cu_q != nullptr;
+  const long long nrows = packed ? s.rows_q : s.Nq;
+  return (packed ? (long long)s.H : (long long)s.B * s.H) * ((nrows + kRowTile - 1) / kRowTile);
+}
+
+// D = rowsum(dO * O) per query row and a cleared dQ accumulator. A row of O (d bf16) is read by
+// d / 8 lanes, 16 bytes each, and summed over them with shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
-  constexpr int PER = D / 32;
-  const size_t rows = per_row_count(a.s);
-  const int lane = threadIdx.x & 31;
-  const size_t warp0 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
+  constexpr int LPR = D / 8, RPW = 32 / LPR;  // lanes per row, rows per warp
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.tile_counter = 0;  // the main kernel's key-tile counter
+  if ((a.s.cu_q != nullptr ? a.s.rows_q : a.s.Nq) <= 0) return;   // (then a one-CTA launch)
+  const RowTile T = row_tile(a.s);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, part = lane % LPR;
   const __nv_bfloat16* O = reinterpret_cast<const __nv_bfloat16*>(a.o);
   const __nv_bfloat16* dO = reinterpret_cast<const __nv_bfloat16*>(a.dout);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *a.tile_counter = 0;  // the main kernel's key-tile counter
-  for (size_t r = warp0; r < rows; r += nwarps) {
-    int b, row, h;
-    row_coords(a.s, r, b, row, h);
-    const __nv_bfloat16* op = O + elem_offset(a.so, b, row, h) + lane * PER;
-    const __nv_bfloat16* gp = dO + elem_offset(a.sdo, b, row, h) + lane * PER;
-    float* acc_row = a.dqacc + r * D + lane * PER;
+#pragma unroll
+  for (int i = warp * RPW + lane / LPR; i < kRowTile; i += 8 * RPW) {
+    const bool live = i < T.rows;
     float acc = 0.f;
-    if constexpr (PER == 2) {
-      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(op);
-      const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(gp);
-      acc = __bfloat162float(x.x) * __bfloat162float(y.x) + __bfloat162float(x.y) * __bfloat162float(y.y);
-      *reinterpret_cast<float2*>(acc_row) = make_float2(0.f, 0.f);
-    } else {
-      const uint2 xs = *reinterpret_cast<const uint2*>(op);
-      const uint2 ys = *reinterpret_cast<const uint2*>(gp);
+    if (live) {
+      const int row = T.row0 + i;
+      const uint4 xs = *reinterpret_cast<const uint4*>(O + elem_offset(a.so, T.b, row, T.h) + part * 8);
+      const uint4 ys = *reinterpret_cast<const uint4*>(dO + elem_offset(a.sdo, T.b, row, T.h) + part * 8);
       const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&xs);
       const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&ys);
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-        acc += __bfloat162float(x[i].x) * __bfloat162float(y[i].x) + __bfloat162float(x[i].y) * __bfloat162float(y[i].y);
-      *reinterpret_cast<float4*>(acc_row) = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < 4; ++e)
+        acc += __bfloat162float(x[e].x) * __bfloat162float(y[e].x) + __bfloat162float(x[e].y) * __bfloat162float(y[e].y);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) a.dvec[r] = acc;
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && part == 0) a.dvec[T.r0 + T.row0 + i] = acc;
   }
+  float4* z = reinterpret_cast<float4*>(a.dqacc + (T.r0 + T.row0) * D);
+  const int n4 = T.rows * (D / 4);
+  for (int i = threadIdx.x; i < n4; i += 256) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// dQ = scale * accumulator in bf16, one warp per query row (one coordinate lookup per row).
+// dQ = scale * accumulator in bf16 (or, accumulating, the caller's fp32 dQ += scale * accumulator).
+// A row of the accumulator (d fp32) is read by d / 4 lanes, 16 bytes each.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const FaBwdArgs a) {
-  constexpr int PER = D / 32;
-  const size_t rows = per_row_count(a.s);
-  const int lane = threadIdx.x & 31;
-  const size_t warp0 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
+  constexpr int LPR = D / 4, RPW = 32 / LPR;
+  const RowTile T = row_tile(a.s);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, part = lane % LPR;
   __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
-  for (size_t r = warp0; r < rows; r += nwarps) {
-    int b, row, h;
-    row_coords(a.s, r, b, row, h);
-    const float* acc = a.dqacc + r * D + lane * PER;
-    if (a.dq_acc != nullptr) {  // accumulate: the caller's fp32 dQ += scale * this call's sum
-      float* dst = a.dq_acc + elem_offset(a.sdq, b, row, h) + lane * PER;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) dst[e] += acc[e] * a.scale;
-      continue;
-    }
-    __nv_bfloat16* out = dq + elem_offset(a.sdq, b, row, h) + lane * PER;
-    if constexpr (PER == 2) {
-      const float2 x = *reinterpret_cast<const float2*>(acc);
-      *reinterpret_cast<uint32_t*>(out) = pack_bf16x2(x.x * a.scale, x.y * a.scale);
+  for (int i = warp * RPW + lane / LPR; i < kRowTile; i += 8 * RPW) {
+    if (i >= T.rows) continue;
+    const int row = T.row0 + i;
+    const float4 x = *reinterpret_cast<const float4*>(a.dqacc + (T.r0 + row) * D + part * 4);
+    if (a.dq_acc != nullptr) {
+      float4* dst = reinterpret_cast<float4*>(a.dq_acc + elem_offset(a.sdq, T.b, row, T.h) + part * 4);
+      float4 y = *dst;
+      y.x += x.x * a.scale;
+      y.y += x.y * a.scale;
+      y.z += x.z * a.scale;
+      y.w += x.w * a.scale;
+      *dst = y;
     } else {
-      const float4 x = *reinterpret_cast<const float4*>(acc);
-      *reinterpret_cast<uint2*>(out) =
+      *reinterpret_cast<uint2*>(dq + elem_offset(a.sdq, T.b, row, T.h) + part * 4) =
           make_uint2(pack_bf16x2(x.x * a.scale, x.y * a.scale), pack_bf16x2(x.z * a.scale, x.w * a.scale));
     }
   }
@@ -742,7 +761,8 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid_ew = sms * 8;
+  const long long grid_rows = row_tile_grid(a.s);
+  if (grid_rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const AttnShape& s = a.s;
   const bool packed = s.cu_q != nullptr;
   const int rq = packed ? s.rows_q : s.Nq, rk = packed ? s.rows_k : s.Nk, nbatch = packed ? 1 : s.B;
@@ -752,7 +772,7 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
       !fa_make_tmap_bf16(&tv, a.v, D, rk, s.Hkv, nbatch, a.sv.row, a.sv.head, a.sv.batch) ||
       !fa_make_tmap_bf16(&tdo, a.dout, D, rq, s.H, nbatch, a.sdo.row, a.sdo.head, a.sdo.batch, C::BM))
     return cudaErrorInvalidValue;
-  bwd_pre_kernel<D><<<grid_ew, 256, 0, st>>>(a);
+  bwd_pre_kernel<D><<<(unsigned)(grid_rows > 0 ? grid_rows : 1), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto main_kernel = a.dk_acc != nullptr ? bwd_tc_kernel<D, true> : bwd_tc_kernel<D, false>;
@@ -769,7 +789,7 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   if (a.ev_main_end != nullptr && (e = cudaEventRecord(a.ev_main_end, st)) != cudaSuccess) return e;
-  bwd_post_kernel<D><<<grid_ew, 256, 0, st>>>(a);
+  if (grid_rows > 0) bwd_post_kernel<D><<<(unsigned)grid_rows, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
