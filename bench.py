@@ -333,10 +333,11 @@ def make_device_buffers(w, H, seed, dev):
     return inp, t
 
 
-def time_device_steps(w, t, steps, warmup, flush_l2, stream, clocks=None, barrier=lambda: None):
+def time_device_steps(w, t, steps, warmup, flush_l2, stream, clocks=None, barrier=lambda: None, breakdown=True):
     """Per-step device times (ms) of fwd, the whole bwd call and its main pass, and the step, from
     CUDA events on the launching stream; the span over all steps. With flush_l2, 256 MiB are
-    written before each step, outside its events."""
+    written before each step, outside its events. Without breakdown only the span is taken, with
+    no event recorded between the launches it times."""
     import exact_io_aware_38_gb300 as fa
 
     kw = dict(causal=w.causal, block_mask=t["bm"], seqlens_k=t["sl"], scale=w.scale, status=t["status"])
@@ -367,15 +368,20 @@ def time_device_steps(w, t, steps, warmup, flush_l2, stream, clocks=None, barrie
     for i in range(steps):
         if flush is not None:
             flush.zero_()  # evicts the previous step's data from the 129 MB L2
-        ev[i][0].record(stream)
-        step(ev[i])
-        ev[i][4].record(stream)
+        if breakdown or flush is not None:
+            ev[i][0].record(stream)
+            step(ev[i])
+            ev[i][4].record(stream)
+        else:
+            step(None)
     end.record(stream)
     torch.cuda.synchronize()
     if clocks is not None:
         clocks.mark("t_end")
     barrier()
     assert int(t["status"].item()) == 0, fa.fa_status_string(int(t["status"].item()))
+    if not (breakdown or flush is not None):
+        return {"span_ms": start.elapsed_time(end) / steps}
     return {
         "span_ms": start.elapsed_time(end) / steps,
         "step": [e[0].elapsed_time(e[4]) for e in ev],
@@ -470,8 +476,8 @@ def secondary_figures(names, steps, warmup, dev, peak):
         B, H, N, d = inp["q"].shape
         fl = rl.attention_flops(B, H, N, d, causal=w.causal,
                                 block_mask=None if inp["block_mask"] is None else inp["block_mask"].numpy())
-        r = time_device_steps(w, t, steps, warmup, False, stream)
-        step_ms = statistics.median(r["step"])
+        step_ms = time_device_steps(w, t, steps, warmup, False, stream, breakdown=False)["span_ms"]
+        r = time_device_steps(w, t, steps, 0, False, stream)  # per-kernel figures (events between launches)
         rec = {"workload": workload_label(w, B, H, N, d) + " fwd+bwd", "ms_per_step": step_ms,
                "value": fl["total"] / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "fwd_ms": statistics.median(r["fwd"]), "bwd_ms": statistics.median(r["bwd"]),
@@ -564,12 +570,15 @@ def main():
 
     # ---- timed region (device-resident inputs; 4 x 64 MiB of inputs > L2, so no flush between steps)
     clocks = ClockSampler(local)
-    r = time_device_steps(w, t, args.steps, args.warmup, args.flush_l2, stream, clocks, barrier)
+    r = time_device_steps(w, t, args.steps, args.warmup, args.flush_l2, stream, clocks, barrier, breakdown=False)
     clk = clocks.stop()
     ms = r["span_ms"] if not args.flush_l2 else statistics.mean(r["step"])  # flushes lie between steps
     ms = max_over_ranks(ms, pg, dev)
-    fwd_ms, bwd_ms, main_ms = (statistics.mean(r[k]) for k in ("fwd", "bwd", "main"))
-    step_pct = percentiles(r["step"])  # this rank's steps
+    # The per-kernel figures and the step percentiles come from a second pass of the same steps
+    # with events around each launch.
+    rb = time_device_steps(w, t, args.steps, 0, args.flush_l2, stream, None, barrier, breakdown=True)
+    fwd_ms, bwd_ms, main_ms = (statistics.mean(rb[k]) for k in ("fwd", "bwd", "main"))
+    step_pct = percentiles(rb["step"])  # this rank's steps (events between launches)
 
     flops = rl.attention_flops(B, H, N, d, causal=w.causal,
                                block_mask=None if inp["block_mask"] is None else inp["block_mask"].numpy())

@@ -90,6 +90,109 @@ struct FwdSmemCtl {
   int p0_last[128];
 };
 
+// One key tile of the online softmax for the query row this thread owns (its tensor-memory
+// lane): S is read at tS, O (at tO) is rescaled when the row max grows by more than 2^kRescale,
+// P is written over the first columns of S and m, l are updated. With `masked`, the keys at
+// columns >= lim are excluded. first: the row's first key tile. Called by whole warps.
+template <int D, bool F8, bool SINGLE>
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool masked, int lim, float sl2, bool first,
+                                             float& m, float& l) {
+  using C = FwdCfg<D, F8, SINGLE>;
+  // Columns [32c, 32c + 32) of the row of S: the loads of kLdBatch chunks share one wait.
+  uint32_t sr[C::kLdBatch * 32];
+  auto chunk = [&](int c, uint32_t(&rr)[32]) {
+    constexpr int NB = C::kLdBatch;
+    if (c % NB == 0) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j) tmem_ld32(tS + (c + j) * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + j * 32));
+      tmem_ld_wait();
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) rr[i] = sr[(c % NB) * 32 + i];
+  };
+  // Pass 1: row max of the (masked) scores, 32 columns at a time.
+  auto row_max = [&](auto mask_tag) -> float {
+    constexpr bool MASK = decltype(mask_tag)::value;
+    float pm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t rr[32];
+      chunk(c, rr);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float v0 = __uint_as_float(rr[i]), v1 = __uint_as_float(rr[i + 1]);
+        if constexpr (MASK) {
+          v0 = (c * 32 + i < lim) ? v0 : -INFINITY;
+          v1 = (c * 32 + i + 1 < lim) ? v1 : -INFINITY;
+        }
+        pm[(i >> 1) & 3] = fmax3(pm[(i >> 1) & 3], v0, v1);
+      }
+    }
+    return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+  };
+  const float mx = masked ? row_max(std::true_type{}) : row_max(std::false_type{});
+  const float mc = mx * sl2;
+  if (first) {
+    m = mc;
+  } else if (__any_sync(0xffffffffu, mc > m + C::kRescale)) {
+    const float mn = fmaxf(m, mc);
+    const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m - mn);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t rr[32];
+      tmem_ld32(tO + c * 32, rr);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+      tmem_st32(tO + c * 32, rr);
+    }
+    l *= alpha;
+    m = mn;
+  }
+  const float mu = (m == -INFINITY) ? 0.f : m;
+  // Pass 2: P = exp2(c log2(e) s - m) over the first columns of S (bf16: 64 columns; e4m3,
+  // as 2^8 P: 32 columns; each chunk is written only over columns already read), and the
+  // row sum of P.
+  auto exp_pass = [&](auto mask_tag) -> float {
+    constexpr bool MASK = decltype(mask_tag)::value;
+    const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(C::kPExp - mu, C::kPExp - mu);
+    float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t rr[32];
+      chunk(c, rr);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 x = fma2(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sc2, nm2);
+        float p0 = ex2_approx(x.x);
+        float p1 = ex2_approx(x.y);
+        if constexpr (MASK) {
+          p0 = (c * 32 + 2 * i < lim) ? p0 : 0.f;
+          p1 = (c * 32 + 2 * i + 1 < lim) ? p1 : 0.f;
+        }
+        ps[i & 1] = add2(ps[i & 1], make_float2(p0, p1));
+        if constexpr (F8) {  // four e4m3 values per column, key 4w + j in byte j of column w
+          const uint32_t pair = pack_e4m3x2(p0, p1);
+          pk[i >> 1] = (i & 1) ? (pk[i >> 1] | (pair << 16)) : pair;
+        } else {
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+      }
+      if constexpr (F8) {
+        tmem_st8(tS + c * 8, *reinterpret_cast<const uint32_t(*)[8]>(pk));
+      } else {
+        tmem_st16(tS + c * 16, pk);
+      }
+    }
+    return (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
+  };
+  const float sum = masked ? exp_pass(std::true_type{}) : exp_pass(std::false_type{});
+  tmem_st_wait();
+  tmem_st_wait();
+  l += sum;
+}
+
 // SPLIT: the CTA covers one split of the key tiles and writes fp32 partials (see FaFwdArgs).
 // MASKED: a block mask is given (never with SPLIT); without one, visibility is in closed form.
 // F8: e4m3 operands (see FwdCfg; never with SPLIT).
@@ -187,6 +290,28 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
   const uint32_t b_pready[2] = {smem_u32(&ctl.p_ready[0]), smem_u32(&ctl.p_ready[1])};
   const uint32_t b_odone[2] = {smem_u32(&ctl.o_done[0]), smem_u32(&ctl.o_done[1])};
 
+  // The producer's first copies: Q0, Q1 and the first key tile alone, into the K half of the last
+  // buffer. Without a block mask the first key tile is known before the CTA-wide barrier, so they
+  // are issued right after the barrier set-up and their latency overlaps the rest of the prologue.
+  auto first_loads = [&]() {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    mbar_expect_tx(b_q, (has1 ? 2 : 1) * C::kTileBytes);
+    for (int x = 0; x < (has1 ? 2 : 1); ++x)
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_load_4d(sQ + x * C::kQSlot + c * 16384, &tmQ, c * C::kBoxCols, seq.q0 + (x ? qt1 : qt0) * 128, h, seq.bb,
+                    b_q);
+    const int kt = next_union(kt_lo);
+#ifndef FA_TEST_WITHHOLD_KV
+    if (kt < s.nbk) {
+      mbar_expect_tx(b_k0, C::kTileBytes);
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_load_4d(sK(C::kStages - 1) + c * 16384, &tmK, c * C::kBoxCols, seq.k0 + kt * 128, hk, seq.bb, b_k0);
+      ctl.k0_issued = 1;
+    }
+#endif
+  };
   if (threadIdx.x < 4) ctl.last_stage[threadIdx.x] = -1;
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
@@ -204,6 +329,7 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
     }
     mbar_init(smem_u32(&ctl.drain), 1);
     fence_mbar_init();
+    if constexpr (!MASKED) first_loads();  // thread 0 is the producer
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl.tmem_base), C::kTmemCols);
@@ -226,27 +352,11 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      mbar_expect_tx(b_q, (has1 ? 2 : 1) * C::kTileBytes);
-      for (int x = 0; x < (has1 ? 2 : 1); ++x)
-        for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_4d(sQ + x * C::kQSlot + c * 16384, &tmQ, c * C::kBoxCols, seq.q0 + (x ? qt1 : qt0) * 128, h,
-                      seq.bb, b_q);
+      if constexpr (MASKED) first_loads();
       // Stage t (the t-th key tile u_t the pair visits) lands V_{u_t} and K_{u_t+1} in buffer
-      // t % kStages; the first key tile comes alone, into the K half of the last buffer. A buffer
-      // is reloaded once the MMAs of its previous stage have completed. No copy is issued after an
-      // abort; the copies already issued are drained at the CTA's exit.
+      // t % kStages. A buffer is reloaded once the MMAs of its previous stage have completed. No
+      // copy is issued after an abort; the copies already issued are drained at the CTA's exit.
       int kt = next_union(kt_lo);
-#ifndef FA_TEST_WITHHOLD_KV
-      if (kt < s.nbk) {
-        mbar_expect_tx(b_k0, C::kTileBytes);
-        for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_4d(sK(C::kStages - 1) + c * 16384, &tmK, c * C::kBoxCols, seq.k0 + kt * 128, hk, seq.bb, b_k0);
-        ctl.k0_issued = 1;
-      }
-#endif
       for (int t = 0; kt < s.nbk; ++t) {
         const int b = t % C::kStages;
         const int ktn = next_union(kt + 1);
@@ -403,98 +513,7 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
         const int k0 = kt * 128;
         const bool masked = (s.causal && k0 + 127 > qt * 128 + seq.off) || k0 + 128 > seq.Lk;
         const int lim = min(seq.Lk - k0, s.causal ? row + seq.off - k0 + 1 : 128);  // keys [k0, k0 + lim) valid
-        // Columns [32c, 32c + 32) of the row of S: the loads of kLdBatch chunks share one wait.
-        uint32_t sr[C::kLdBatch * 32];
-        auto chunk = [&](int c, uint32_t(&rr)[32]) {
-          constexpr int NB = C::kLdBatch;
-          if (c % NB == 0) {
-#pragma unroll
-            for (int j = 0; j < NB; ++j) tmem_ld32(tS + (c + j) * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + j * 32));
-            tmem_ld_wait();
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = sr[(c % NB) * 32 + i];
-        };
-        // Pass 1: row max of the (masked) scores, 32 columns at a time.
-        auto row_max = [&](auto mask_tag) -> float {
-          constexpr bool MASK = decltype(mask_tag)::value;
-          float pm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t rr[32];
-            chunk(c, rr);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float v0 = __uint_as_float(rr[i]), v1 = __uint_as_float(rr[i + 1]);
-              if constexpr (MASK) {
-                v0 = (c * 32 + i < lim) ? v0 : -INFINITY;
-                v1 = (c * 32 + i + 1 < lim) ? v1 : -INFINITY;
-              }
-              pm[(i >> 1) & 3] = fmax3(pm[(i >> 1) & 3], v0, v1);
-            }
-          }
-          return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
-        };
-        const float mx = masked ? row_max(std::true_type{}) : row_max(std::false_type{});
-        const float mc = mx * sl2;
-        if (cnt == 0) {
-          m = mc;
-        } else if (__any_sync(0xffffffffu, mc > m + C::kRescale)) {
-          const float mn = fmaxf(m, mc);
-          const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m - mn);
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(tO + c * 32, rr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            tmem_st32(tO + c * 32, rr);
-          }
-          l *= alpha;
-          m = mn;
-        }
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        // Pass 2: P = exp2(c log2(e) s - m) over the first columns of S (bf16: 64 columns; e4m3,
-        // as 2^8 P: 32 columns; each chunk is written only over columns already read), and the
-        // row sum of P.
-        auto exp_pass = [&](auto mask_tag) -> float {
-          constexpr bool MASK = decltype(mask_tag)::value;
-          const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(C::kPExp - mu, C::kPExp - mu);
-          float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t rr[32];
-            chunk(c, rr);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 x = fma2(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sc2, nm2);
-              float p0 = ex2_approx(x.x);
-              float p1 = ex2_approx(x.y);
-              if constexpr (MASK) {
-                p0 = (c * 32 + 2 * i < lim) ? p0 : 0.f;
-                p1 = (c * 32 + 2 * i + 1 < lim) ? p1 : 0.f;
-              }
-              ps[i & 1] = add2(ps[i & 1], make_float2(p0, p1));
-              if constexpr (F8) {  // four e4m3 values per column, key 4w + j in byte j of column w
-                const uint32_t pair = pack_e4m3x2(p0, p1);
-                pk[i >> 1] = (i & 1) ? (pk[i >> 1] | (pair << 16)) : pair;
-              } else {
-                pk[i] = pack_bf16x2(p0, p1);
-              }
-            }
-            if constexpr (F8) {
-              tmem_st8(tS + c * 8, *reinterpret_cast<const uint32_t(*)[8]>(pk));
-            } else {
-              tmem_st16(tS + c * 16, pk);
-            }
-          }
-          return (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
-        };
-        const float sum = masked ? exp_pass(std::true_type{}) : exp_pass(std::false_type{});
-        tmem_st_wait();
-        l += sum;
+        softmax_tile<D, F8, SINGLE>(tS, tO, masked, lim, sl2, cnt == 0, m, l);
         fence_before_sync();
         if (run) {
           mbar_arrive(x == 0 ? b_full(t % C::kStages) : b_pready[1]);
@@ -616,6 +635,7 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
     }
   }
 }
+
 
 template <int D>
 cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
