@@ -112,9 +112,31 @@ size_t workspace_for(const fa::AttnShape& s) {
   return round_up(rows * sizeof(float)) + round_up(rows * s.d * sizeof(float)) + kAlign;
 }
 
-int launch_fwd(const fa::AttnShape& s, const void* q, FaStrides sq, const void* k, FaStrides sk, const void* v,
+// Decode with grouped K/V heads: one query row per head (fixed length, no block mask). The G query
+// heads of a K/V head are viewed as G query rows of one head: the head stride becomes the row stride
+// (the row stride is unused with one row), so one query tile carries all G and each K/V tile is
+// streamed once for them instead of G times. A single query row sees every key under the
+// bottom-right causal reading, so the view is non-causal. Its LSE and per-row order, [B][Hkv][G],
+// is the problem's [B][H] for one row, so outputs, partials and merges are unchanged.
+bool decode_view(fa::AttnShape& s, FaStrides* sq, FaStrides* so) {
+  if (s.cu_q != nullptr || s.Nq != 1 || s.H == s.Hkv || s.block_mask != nullptr) return false;
+  const int G = s.H / s.Hkv;
+  for (FaStrides* t : {sq, so})
+    if (t != nullptr) {
+      t->row = t->head;
+      t->head *= G;
+    }
+  s.H = s.Hkv;
+  s.Nq = G;
+  s.nbq = (G + fa::kTile - 1) / fa::kTile;
+  s.causal = 0;
+  return true;
+}
+
+int launch_fwd(fa::AttnShape s, const void* q, FaStrides sq, const void* k, FaStrides sk, const void* v,
                FaStrides sv, void* o, FaStrides so, float* lse, float scale, int32_t* tile_visits, int* dev_status,
                void* stream) {
+  if (tile_visits == nullptr) decode_view(s, &sq, &so);  // (tile visits are recorded per query head)
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       !aligned(tile_visits, 4) || !aligned(dev_status, 4))
@@ -220,6 +242,8 @@ int launch_partial(const fa::AttnShape& s, const fa_varlen_problem* p, int split
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       !aligned(part_o, 16) || !aligned(part_lse, 4) || !aligned(dev_status, 4))
     return FA_ERR_MISALIGNED;
+  fa::AttnShape sv_ = s;
+  decode_view(sv_, &tq, merge ? &to : nullptr);
   FaFwdArgs a{};
   a.q = q;
   a.k = k;
@@ -230,13 +254,13 @@ int launch_partial(const fa::AttnShape& s, const fa_varlen_problem* p, int split
   a.sk = tk;
   a.sv = tv;
   a.so = to;
-  a.s = s;
+  a.s = sv_;
   a.scale = p->scale;
   a.tile_visits = nullptr;
   a.status = dev_status;
   a.splits = splits;
-  a.kt_chunk = (s.nbk + splits - 1) / splits;
-  a.part_rows = per_row(s);
+  a.kt_chunk = (sv_.nbk + splits - 1) / splits;
+  a.part_rows = per_row(sv_);
   a.part_o = part_o;
   a.part_lse = part_lse;
   cudaError_t e = fa_launch_fwd(a, st);
@@ -365,20 +389,21 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 int fa_fwd_splitkv_splits(const fa_varlen_problem* p, int num_sms) {
   fa::AttnShape s;
   if (varlen_shape(p, &s) != FA_OK || num_sms < 1) return 1;
-  // No split once the CTAs without one cover the SMs (measured: the merge then costs more than
-  // the balance gains). Otherwise the count, with at least four key tiles per split, whose CTAs
-  // fill their waves best (the fraction of SM slots used; ties to fewer splits).
+  decode_view(s, nullptr, nullptr);  // the shape the kernels run
+  // The count with the least estimated time, in key-tile units: the CTAs' waves times (a CTA's
+  // fixed cost, measured at about 6 key tiles: start-up, pipeline fill and drain, epilogue, plus
+  // its key tiles), and for a split the merge pass (about 3). At least four key tiles per split.
+  constexpr long long kFixedTiles = 6, kMergeTiles = 3;
   const long long units = (long long)s.B * s.H * ((s.nbq + 1) / 2);  // CTAs without a split
-  if (units >= num_sms) return 1;
   long long cap = s.nbk / 4;
   if (cap > kMaxSplits) cap = kMaxSplits;
   int best = 1;
-  double best_eff = 0.0;
-  for (long long n = 1; n <= cap; ++n) {
-    const long long ctas = n * units;
-    const double eff = (double)ctas / ((double)((ctas + num_sms - 1) / num_sms) * num_sms);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
+  long long best_cost = -1;
+  for (long long n = 1; n <= (cap < 1 ? 1 : cap); ++n) {
+    const long long waves = (n * units + num_sms - 1) / num_sms;
+    const long long cost = waves * (kFixedTiles + (s.nbk + n - 1) / n) + (n > 1 ? kMergeTiles : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
       best = (int)n;
     }
   }

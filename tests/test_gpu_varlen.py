@@ -200,6 +200,27 @@ def test_splitkv_decode_shapes(Nq, Nk, splits, d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,Hkv", [(12, 3), (32, 1)])
+def test_decode_grouped_heads_equal_repeated_kv(H, Hkv, d, causal):
+    """One query row per head with grouped K/V heads runs as G rows of each K/V head (one query
+    tile per K/V head). Its O and LSE must equal, bit for bit, the same problem with the K/V heads
+    repeated, which runs one query row per head; and match the oracle."""
+    g = torch.Generator().manual_seed(H * 7 + d)
+    B, Nk = 3, 1000
+    q = bf16((B, 1, H, d), g)
+    k, v = bf16((B, Nk, Hkv, d), g), bf16((B, Nk, Hkv, d), g)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = run_status(lambda st: fa.fwd_varlen(qc, kc, vc, causal=causal, status=st))
+    kr, vr = (x.repeat_interleave(H // Hkv, dim=2).contiguous() for x in (kc, vc))
+    o2, l2 = run_status(lambda st: fa.fwd_varlen(qc, kr, vr, causal=causal, status=st))
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    t4 = lambda x: f64(x).transpose(0, 2, 1, 3)
+    ro, rl = oracle.attention_forward(t4(q), t4(k), t4(v), 1.0 / np.sqrt(d), causal=causal)
+    check_o_lse(t4(o1), f64(l1), ro, rl)
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_splitkv_packed(causal):
     lq, lk = [1, 4, 0, 1, 130], [5000, 900, 7, 1, 2000]
     g = torch.Generator().manual_seed(77)
