@@ -112,6 +112,24 @@ size_t workspace_for(const fa::AttnShape& s) {
   return round_up(rows * sizeof(float)) + round_up(rows * s.d * sizeof(float)) + kAlign;
 }
 
+// The masks and sequence arrays are read by the kernels, so they must be device-accessible
+// (device, managed, or mapped host memory). A plain host array would fault the kernel; it is
+// rejected here instead, after every other check, with FA_ERR_INVALID_ARG.
+bool device_accessible(const void* p) {
+  if (p == nullptr) return true;
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged ||
+         (attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr);
+}
+bool aux_on_device(const fa::AttnShape& s) {
+  return device_accessible(s.block_mask) && device_accessible(s.seqlens_k) && device_accessible(s.cu_q) &&
+         device_accessible(s.cu_k);
+}
+
 // Decode with grouped K/V heads: one query row per head (fixed length, no block mask). The G query
 // heads of a K/V head are viewed as G query rows of one head: the head stride becomes the row stride
 // (the row stride is unused with one row), so one query tile carries all G and each K/V tile is
@@ -141,6 +159,7 @@ int launch_fwd(fa::AttnShape s, const void* q, FaStrides sq, const void* k, FaSt
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       !aligned(tile_visits, 4) || !aligned(dev_status, 4))
     return FA_ERR_MISALIGNED;
+  if (!aux_on_device(s)) return FA_ERR_INVALID_ARG;
   FaFwdArgs a{};
   a.q = q;
   a.k = k;
@@ -186,6 +205,7 @@ int launch_bwd(const fa::AttnShape& s, const BwdTensors& t, float scale, void* w
       !aligned(t.dq, 16) || !aligned(t.dk, 16) || !aligned(t.dv, 16) || !aligned(t.lse, 4) ||
       !aligned(workspace, kAlign) || !aligned(dev_status, 4) || (extras && !aligned(extras->step_visits, 4)))
     return FA_ERR_MISALIGNED;
+  if (!aux_on_device(s)) return FA_ERR_INVALID_ARG;
   FaBwdArgs a{};
   a.q = t.q;
   a.k = t.k;
@@ -242,6 +262,7 @@ int launch_partial(const fa::AttnShape& s, const fa_varlen_problem* p, int split
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       !aligned(part_o, 16) || !aligned(part_lse, 4) || !aligned(dev_status, 4))
     return FA_ERR_MISALIGNED;
+  if (!aux_on_device(s)) return FA_ERR_INVALID_ARG;
   fa::AttnShape sv_ = s;
   decode_view(sv_, &tq, merge ? &to : nullptr);
   FaFwdArgs a{};
@@ -320,13 +341,14 @@ int fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse
       !aligned(tile_visits, 4) || !aligned(dev_status, 4))
     return FA_ERR_MISALIGNED;
   FaFwdArgs a{};
+  a.s = fixed_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
+  if (!aux_on_device(a.s)) return FA_ERR_INVALID_ARG;
   a.q = q;
   a.k = k;
   a.v = vt;
   a.o = o;
   a.lse = lse;
   a.so = contiguous(H, N, d);
-  a.s = fixed_shape(B, H, Hkv, N, d, causal, block_mask, seqlens_k);
   a.scale = scale;
   a.tile_visits = tile_visits;
   a.status = dev_status;
@@ -471,6 +493,7 @@ int fa_finalize_partials(const fa_varlen_problem* p, const float* acc_o, const f
   if ((rc = take_strides(so, packed, s.B, packed ? s.rows_q : s.Nq, s.H, &to)) != FA_OK) return rc;
   if (!acc_o || !acc_lse || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(acc_o, 16) || !aligned(o, 16) || !aligned(acc_lse, 4) || !aligned(lse, 4)) return FA_ERR_MISALIGNED;
+  if (!aux_on_device(s)) return FA_ERR_INVALID_ARG;
   FaFwdArgs a{};
   a.o = o;
   a.lse = lse;

@@ -65,6 +65,10 @@ typedef enum {
  *   block_mask  nullable, device uint8 [nb * nb], row-major (query tile, key tile), nonzero = keep
  *   seqlens_k   nullable, device int32 [B], each in [0, N]; keys j >= seqlens_k[b] are masked for
  *               every query row of sequence b (a value outside [0, N] is clamped into it)
+ *               Both arrays are read by the kernels, so they live in device memory (or managed or
+ *               mapped host memory), not in a host array: the library copies nothing. A pointer to
+ *               plain host memory is detected before any launch and returns FA_ERR_INVALID_ARG
+ *               (the same holds for the cu_seqlens arrays of fa_varlen_problem).
  *   scale       softmax scale c, finite and > 0 (callers normally pass 1/sqrt(d))
  *   tile_visits nullable, device int32 [B * H * nb]: receives, per (b, h, query tile), the number
  *               of 128 x 128 key tiles the kernel visited (tiles with no valid pair are skipped)

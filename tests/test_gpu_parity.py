@@ -158,6 +158,25 @@ def test_degenerate_masks():
     assert torch.isneginf(got["lse"][:, :, 128:256]).all()
 
 
+def test_host_mask_arrays_are_rejected():
+    """A block mask or key lengths in plain host memory would fault the kernel: the library checks
+    where they live before any launch and returns FA_ERR_INVALID_ARG; a device copy runs."""
+    B, H, N, d = 1, 2, 256, 64
+    g = torch.Generator().manual_seed(1)
+    q, k, v = (torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).cuda() for _ in range(3))
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    host_mask = np.ones(4, dtype=np.uint8)
+    host_len = np.array([100], dtype=np.int32)
+    stream = torch.cuda.current_stream().cuda_stream
+    call = lambda bm, sl: fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                                    0, bm, sl, 0.125, None, None, stream)
+    assert call(host_mask.ctypes.data, None) == -1
+    assert call(None, host_len.ctypes.data) == -1
+    dev_mask = torch.from_numpy(host_mask).cuda()
+    assert call(dev_mask.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+
+
 def test_all_tiles_masked():
     inp = workloads.random_inputs(1, 2, 256, 128, 5)
     inp.update(causal=False, block_mask=torch.zeros((2, 2), dtype=torch.uint8), seqlens_k=None, scale=0.1)
