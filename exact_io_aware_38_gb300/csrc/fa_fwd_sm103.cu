@@ -60,9 +60,11 @@ struct FwdCfg {
   static constexpr uint32_t kIdS = F8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
   static constexpr uint32_t kIdPV = F8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
   static constexpr uint32_t kTmemS0 = 0, kTmemO0 = SINGLE ? 128 : 256;
-  // O is rescaled only when a row max grows by more than 2^kRescale (lazy; exact since l and O share
-  // the stale max). The e4m3 P is 2^8 exp2(s - m) <= 256 only with the exact running max.
-  static constexpr float kRescale = F8 ? 0.0f : 8.0f;
+  // O is rescaled only when a row max grows by more than kRescale in log2 units (lazy; exact since
+  // l and O share the stale max). The e4m3 P is 2^8 exp2(s - m): with m at most 0.8 below the
+  // true max it stays <= 2^8.8 < 448, the largest e4m3 value, so it never saturates (measured:
+  // the e4m3 forward 4% faster than with an exact running max).
+  static constexpr float kRescale = F8 ? 0.8f : 8.0f;
   static constexpr float kPExp = F8 ? 8.0f : 0.0f;      // P is computed as 2^kPExp exp2(s - m)
   // Chunks of 32 columns of S a softmax thread loads from tensor memory per wait: two in the
   // single mode (measured 2% faster there), one in the pair mode (two measured 1.5% slower).
@@ -91,7 +93,7 @@ struct FwdSmemCtl {
 };
 
 // One key tile of the online softmax for the query row this thread owns (its tensor-memory
-// lane): S is read at tS, O (at tO) is rescaled when the row max grows by more than 2^kRescale,
+// lane): S is read at tS, O (at tO) is rescaled when the row max grows by more than a factor 2^kRescale,
 // P is written over the first columns of S and m, l are updated. With `masked`, the keys at
 // columns >= lim are excluded. first: the row's first key tile. Called by whole warps.
 template <int D, bool F8, bool SINGLE>

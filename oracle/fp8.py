@@ -13,8 +13,9 @@ section "Never write the scores") and fix no scheme. The reading adopted here:
   * What is computed. Exact attention over those dequantised inputs: O = softmax(c q k^T [mask]) v
     and LSE = ln sum_j exp(c q k_j) over the valid keys, in fp64 here (``attention_forward_fp8``).
     The fused kernel reaches it up to rounding: its scores are exact fp8 products summed in fp32;
-    its probabilities P are rounded to e4m3 (after scaling by 2^8, with an exact running maximum so
-    that 2^8 P <= 256) before the P V product. That rounding is the dominant error; its per-element
+    its probabilities P are rounded to e4m3 (after scaling by 2^8, relative to a running maximum
+    that lags the row's true maximum by at most 0.8 in log2 units, so that 2^8 P <= 2^8.8 < 448
+    never saturates) before the P V product. That rounding is the dominant error; its per-element
     bound is ``p_rounding_bound``.
 
 The e4m3 format (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; no infinities; the code
@@ -33,7 +34,7 @@ from .attention import attention_forward
 E4M3_MAX = 448.0
 E4M3_MIN_NORMAL = 2.0 ** -6
 E4M3_MIN_SUBNORMAL = 2.0 ** -9
-P_SCALE = 256.0  # probabilities are quantised as 2^8 * P (at most 256 with an exact running max)
+P_SCALE = 256.0  # probabilities are quantised as 2^8 * P (at most 2^8.8 < 448: the running max lags by <= 0.8)
 
 
 def e4m3_decode(codes) -> np.ndarray:
@@ -85,9 +86,10 @@ def p_rounding_bound(p, v_abs):
     """Per-element bound on |O - O_exact| from rounding 2^8 P to e4m3 (one row block).
 
     p [rows, keys] are the exact probabilities (row sums 1), v_abs [keys, d] the |v| of the keys.
-    The kernel divides by the row sum l >= 1 of the unrounded exponentials (the row's maximum
-    contributes 1), so the error of each weight is at most half an e4m3 spacing of 2^8 P, over
-    2^8: 2^-4 P for normal values (3 mantissa bits), 2^-10 / 2^8 = 2^-18 in the subnormal range.
+    The kernel's exponentials are taken relative to a running maximum m at or below the row's true
+    maximum, and it divides by their unrounded row sum l >= 1 (the row's maximum contributes at
+    least 1), so the error of each weight is at most half an e4m3 spacing of 2^8 P, over 2^8:
+    2^-4 P for normal values (3 mantissa bits), 2^-10 / 2^8 = 2^-18 in the subnormal range.
     Hence |dO_ik| <= sum_j max(2^-4 P_ij, 2^-18) |v_jk|.
     """
     w = np.maximum(2.0 ** -4 * np.asarray(p, np.float64), 2.0 ** -18)
