@@ -191,7 +191,6 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool mask
   };
   const float sum = masked ? exp_pass(std::true_type{}) : exp_pass(std::false_type{});
   tmem_st_wait();
-  tmem_st_wait();
   l += sum;
 }
 
