@@ -177,6 +177,32 @@ def test_host_mask_arrays_are_rejected():
     torch.cuda.synchronize()
 
 
+def test_block_mask_rows_longer_than_the_bitmap():
+    """Block-sparse rows of 2051 key tiles, more than the 2048 the forward's per-CTA bitmap covers
+    (the rest are looked up tile by tile), and as many query tiles: O and LSE on sampled rows
+    against the oracle, and every skip decision of both passes bit-exactly. With no causal mask, no
+    key padding and whole tiles, the oracle's visit grid is the block mask itself (pinned against
+    oracle.tile_grid on small sizes in test_io_model); its brute force is too slow at this size."""
+    nb = 2051
+    B, H, N, d = 1, 1, nb * 128, 64
+    inp = workloads.random_inputs(B, H, N, d, 11)
+    rng = np.random.default_rng(12)
+    bm = (rng.random((nb, nb)) < 0.01).astype(np.uint8)
+    np.fill_diagonal(bm, 1)
+    bm[:, nb - 3:] = 1  # every row also sees the key tiles past the bitmap's reach
+    inp.update(causal=False, block_mask=torch.from_numpy(bm), seqlens_k=None, scale=0.125)
+    got = run_gpu(inp, backward=True, visits=True)
+    rows = np.sort(rng.choice(N, 64, replace=False))
+    om, lm = oracle.head_forward(f64(inp["q"][0, 0]), f64(inp["k"][0, 0]), f64(inp["v"][0, 0]), 0.125, False, bm,
+                                 None, rows=rows)
+    check_o_lse(got["o"][0, 0][rows], got["lse"][0, 0][rows], om, lm)
+    grid = bm != 0
+    assert (got["visits"][0, 0].numpy() == grid.sum(axis=1)).all()
+    assert (got["step_visits"][0, 0].numpy() == 2 * grid.sum(axis=0)).all()  # two 64-row steps per tile
+    for n in ("o", "dq", "dk", "dv"):
+        assert torch.isfinite(got[n].float()).all(), n
+
+
 def test_all_tiles_masked():
     inp = workloads.random_inputs(1, 2, 256, 128, 5)
     inp.update(causal=False, block_mask=torch.zeros((2, 2), dtype=torch.uint8), seqlens_k=None, scale=0.1)

@@ -75,3 +75,5 @@ def test_tile_grid_matches_oracle():
                     a = rl.tile_visit_grid(N, causal, mask, L)
                     b = oracle.tile_grid(N, causal, mask, L)
                     assert (a == b).all(), (N, causal, L)
+        if N % 128 == 0:  # whole tiles, no causal mask, no key padding: the grid is the block mask
+            assert (oracle.tile_grid(N, False, bm, None) == (bm != 0)).all(), N
