@@ -22,6 +22,9 @@ errors). What must hold: no barrier gets an arrival beyond its count (a second a
 an open phase), every role ends, and no copy is in flight when the producer has drained at exit.
 The producer guarantees the first on its own: before reloading a stage (or K/V) it checks that the
 stage's previous copy has landed, and it issues nothing once the abort flag is set.
+
+kvbufs: the K/V buffers (1 at d = 128; 2 at d = 64, where work tile t uses buffer t % 2, each buffer
+with its own K/V and done barriers, and a tile's K/V load waits for the done of tile t - 2 only).
 """
 import random
 
@@ -31,7 +34,7 @@ from mbarrier_model import Machine
 KST, NB = 3, 2
 
 
-def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
+def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1):
     """unguarded: the earlier producer, which reloaded a stage once its release arrived, without
     checking its own previous copy or the abort flag."""
     M = Machine(seed, abort_p)
@@ -41,7 +44,9 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
         if not M.aborted:
             M.need(cond, msg)
 
-    bar("kv", 1)
+    for kb in range(kvbufs):
+        bar(f"kv{kb}", 1)
+        bar(f"done{kb}", 1)
     for i in range(KST):
         bar(f"full{i}", 1)
         bar(f"empty{i}", 1)
@@ -53,7 +58,6 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
     for i in range(2):
         bar(f"tqfull{i}", 1)
         bar(f"tqempty{i}", 4)
-    bar("done", 1)
     bar("accfree", 2)  # the two warpgroups
     bar("drain", 2)
 
@@ -114,21 +118,23 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
                 continue
             kv_issued = False
 
+            kb = wt % kvbufs
+
             def issue_kv():
-                if wt > 0:
-                    if not (yield from wait("done", (wt - 1) & 1)):
+                if wt >= kvbufs:
+                    if not (yield from wait(f"done{kb}", ((wt // kvbufs) - 1) & 1)):
                         return  # the kernel skips the copy after a wait that ran out
-                if not (yield from landed("kv")) or (M.aborted and not unguarded):
+                if not (yield from landed(f"kv{kb}")) or (M.aborted and not unguarded):
                     return
-                if wt > 0:
-                    # every MMA of the previous work tile has completed (K and V are read by them)
-                    for s in [s for s, tt in step_tile.items() if tt == wt - 1]:
+                if wt >= kvbufs:
+                    # every MMA of the buffer's previous work tile has completed (they read K and V)
+                    for s in [s for s, tt in step_tile.items() if tt == wt - kvbufs]:
                         for k in ("S", "dP", "dQ"):
                             need((k, s) in done, f"K/V of work tile {wt} loaded before {k}{s} completed")
-                M.load("kv", 2, ("kv", wt))
-                last_par["kv"] = wt & 1
+                M.load(f"kv{kb}", 2, ("kv", wt))
+                last_par[f"kv{kb}"] = (wt // kvbufs) & 1
 
-            if wt == 0:
+            if wt == 0 or kvbufs > 1:
                 yield from issue_kv()
                 kv_issued = True
             for l in range(n):
@@ -166,7 +172,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
             n = tiles[t]
             if n == 0:
                 continue
-            yield from wait("kv", wt & 1)
+            yield from wait(f"kv{wt % kvbufs}", (wt // kvbufs) & 1)
             need(("kv", wt) in done, f"S issuer saw K/V of work tile {wt} before they landed")
             for _ in range(n):
                 st, buf = sn % KST, sn % NB
@@ -213,7 +219,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
                 commit(2, f"dqfull{buf}")
                 g += 1
                 yield None
-            commit(2, "done")
+            commit(2, f"done{wt % kvbufs}")
             wt += 1
         commit(2, "drain")
 
@@ -242,7 +248,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False):
                 it += 1
                 yield None
             if n > 0:
-                yield from wait("done", wt & 1)
+                yield from wait(f"done{wt % kvbufs}", (wt // kvbufs) & 1)
                 last = [s for s, tt in step_tile.items() if tt == wt]
                 for s in last:
                     need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
@@ -261,9 +267,10 @@ def _cases(n):
         yield [r.choice([0, 0, 1, 1, 2, 3, 4, 5, 7]) for _ in range(r.randint(1, 10))], seed
 
 
-def test_protocol_has_no_deadlock_or_hazard():
+@pytest.mark.parametrize("kvbufs", [1, 2])
+def test_protocol_has_no_deadlock_or_hazard(kvbufs):
     for tiles, seed in _cases(3000):
-        res, errs = run(tiles, seed)
+        res, errs = run(tiles, seed, kvbufs=kvbufs)
         assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
 
 
@@ -272,13 +279,14 @@ def test_model_finds_the_earlier_release_race():
     assert hangs, "the model no longer sees the aliasing deadlock of the earlier release"
 
 
-def test_abort_path_terminates():
+@pytest.mark.parametrize("kvbufs", [1, 2])
+def test_abort_path_terminates(kvbufs):
     """Waits that run out at random points: every role still leaves its loops (the kernel's abort
     flag makes every later wait return at once; a tile-queue read that fails ends the role's tile
     loop), even when the roles no longer agree on how many tiles they saw; no barrier gets an
     arrival beyond its count (the mbarrier model raises); the drain leaves no copy in flight."""
     for tiles, seed in _cases(1500):
-        res, errs = run(tiles, seed, abort_p=0.02)
+        res, errs = run(tiles, seed, abort_p=0.02, kvbufs=kvbufs)
         assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
 
 
