@@ -536,6 +536,68 @@ def fp8_forward_figure(steps, warmup, dev, peak_bf16):
             "peak_source": "measured bf16 burst x 2 (nominal FP8 / BF16 dense ratio)"}
 
 
+def ring_figure(steps, warmup, dev, peak, world=4):
+    """Ring attention's per-rank schedule on the long-context causal shape, the W ranks run one
+    after another on one GPU: the compute of a W-way sequence-sharded fwd + bwd step, without its
+    K/V rotation. Per rank: the partial forwards of its query block over the key blocks it sees
+    (the diagonal one causal), their log-sum-exp merges and the finalize; then the accumulating
+    backward shares into fp32 dQ, dK, dV (zeroed each step). The FLOPs are the fused step's (the
+    ring visits the same tiles), so the figure compares directly with it."""
+    import exact_io_aware_38_gb300 as fa
+    from exact_io_aware_38_gb300 import ring
+
+    w = workloads.WORKLOADS["c4"]
+    inp = workloads.make_inputs(w)
+    t = {n: inp[n].permute(0, 2, 1, 3).contiguous() for n in ("q", "k", "v", "do")}  # [B, N, H, d]
+    B, N, H, d = t["q"].shape
+    Hkv = t["k"].shape[2]
+    blk = N // world
+    # each rank's own blocks (a rank holds its query, key, value and gradient blocks)
+    blocks = {n: [t[n][:, r * blk:(r + 1) * blk].contiguous().to(dev) for r in range(world)] for n in t}
+    dq = torch.zeros((B, N, H, d), dtype=torch.float32, device=dev)
+    dk = torch.zeros((B, N, Hkv, d), dtype=torch.float32, device=dev)
+    dv = torch.zeros_like(dk)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sched = [ring.ring_schedule(r, world, True) for r in range(world)]
+
+    def run():
+        dq.zero_()
+        dk.zero_()
+        dv.zero_()
+        for r in range(world):
+            qb, dob = blocks["q"][r], blocks["do"][r]
+            acc = None
+            for _, src, c in sched[r]:
+                if c is None:
+                    continue
+                part = fa.fwd_partial(qb, blocks["k"][src], blocks["v"][src], causal=c, scale=w.scale, status=status)
+                acc = part if acc is None else fa.merge_partials(qb, blocks["k"][src], acc, part)
+            o, lse = fa.finalize_partials(qb, blocks["k"][r], acc)
+            for _, src, c in sched[r]:
+                if c is None:
+                    continue
+                fa.bwd_varlen_accumulate(qb, blocks["k"][src], blocks["v"][src], o, lse, dob,
+                                         dq[:, r * blk:(r + 1) * blk], dk[:, src * blk:(src + 1) * blk],
+                                         dv[:, src * blk:(src + 1) * blk], causal=c, scale=w.scale, status=status)
+
+    for _ in range(max(3, warmup)):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+    ms = a.elapsed_time(b) / steps
+    tf = rl.attention_flops(B, H, N, d, causal=True)["total"] / (ms * 1e-3) / 1e12
+    return {"workload": workload_label(w, B, H, N, d) + f" fwd+bwd as a {world}-rank ring, ranks in sequence",
+            "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "frac": tf / peak,
+            "note": "compute only (no K/V rotation); same FLOPs as the fused step"}
+
+
 def main():
     args = parse()
     if args.workload == "dec":
@@ -625,6 +687,7 @@ def main():
     if rank == 0 and not args.no_secondary and args.heads is None and args.workload == "c4":
         result["secondary"] = secondary_figures(["c5", "c3", "c2"], min(args.steps, 20), args.warmup, dev, peak)
         result["secondary"]["fp8_fwd"] = fp8_forward_figure(min(args.steps, 20), args.warmup, dev, peak)
+        result["secondary"]["ring"] = ring_figure(min(args.steps, 10), args.warmup, dev, peak)
     if rank == 0 and not args.no_cpu_baseline:
         heads = [(0, h) for h in range(min(3, H))]  # about 10 s of the oracle on the host cores
         t0 = time.perf_counter()
