@@ -43,27 +43,33 @@ using namespace tc;
 
 constexpr int kBwdThreads = 384;
 
-template <int D>
+// SINGLE (d = 64): one [S^T | dP^T] buffer, a 2-stage Q/dO ring and one K/V pair (97 KB of shared
+// memory, 256 tensor-memory columns), 192 threads (producer, one issuer, one warpgroup), so two
+// CTAs share an SM and one CTA's step chain runs while the other's waits.
+template <int D, bool SINGLE = false>
 struct BwdCfg {
   // Steps of 64 queries through two [S^T | dP^T] tensor-memory buffers; dQ^T = K^T dS^T (lanes =
   // head dimension) accumulates over its buffer's dP^T columns. At d = 64 that product keeps
   // M = 128: its upper 64 rows read the next shared-memory tile and are never read out (half of
   // one small product wasted for the known 128-lane layout and the double buffering).
   static constexpr int BM = 64;                      // query rows per step
-  static constexpr int kBufs = 2;                    // tensor-memory [S^T | dP^T] buffers
+  static constexpr int kBufs = SINGLE ? 1 : 2;       // tensor-memory [S^T | dP^T] buffers
   static constexpr int kBoxes = D / 64;              // 64-column boxes per row
   static constexpr int kKVBytes = 128 * D * 2;       // K or V tile (128 rows)
   // K/V buffers: at d = 64 two, so the next key tile's K and V load while the current tile's
   // products still read its own (d = 128 has no room for a second pair).
-  static constexpr int kKVBufs = D == 64 ? 2 : 1;
+  static constexpr int kKVBufs = (D == 64 && !SINGLE) ? 2 : 1;
   static constexpr int kQBox = BM * 128;             // one 64-column box of a Q or dO tile
   static constexpr int kQBytes = BM * D * 2;         // Q or dO tile (BM rows)
-  static constexpr int kStages = 3;                  // Q/dO ring depth
+  static constexpr int kStages = SINGLE ? 2 : 3;     // Q/dO ring depth
   // dS^T tile [128 keys][BM queries] per buffer, in 128-byte-swizzled rows of 64 queries (a step
   // of 32 queries uses the first half of each row).
   static constexpr int kDsBytes = 128 * BM * 2;
   static constexpr int kDqBytes = BM * D * 4;        // fp32 dQ staging for the bulk add
   static constexpr int kSmem = kKVBufs * 2 * kKVBytes + kStages * 2 * kQBytes + kBufs * kDsBytes + kDqBytes + 1024;
+  static constexpr int kThreadsCta = SINGLE ? 192 : kBwdThreads;
+  static constexpr uint32_t kTmemCols = SINGLE ? 256 : 512;
+  static_assert(!SINGLE || D == 64, "the single mode fits tensor memory at d = 64");
   static constexpr uint32_t kTdK = 0, kTdV = D;
   static constexpr uint32_t kTS0 = 2 * D;            // S^T of buffer b at kTS0 + b * 2 * BM
   static constexpr uint32_t kIdS = idesc_bf16(128, BM, false, false);
@@ -254,12 +260,12 @@ __device__ __forceinline__ int bwd_count_steps(const AttnShape& s, const BwdTile
 
 // ACC: accumulate mode (dK and dV added in fp32 into the caller's accumulators); a separate
 // instantiation keeps the bf16-output kernel's code as it is.
-template <int D, bool ACC = false>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+template <int D, bool ACC = false, bool SINGLE = false>
+__global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const FaBwdArgs a) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, SINGLE>;
   constexpr int BM = C::BM;
   constexpr int NB = C::kBufs;
   extern __shared__ uint8_t smem_raw[];
@@ -320,14 +326,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_tqfull(i), 1);
-      mbar_init(b_tqempty(i), 4);  // the two issuers and the leaders of the two warpgroups
+      mbar_init(b_tqempty(i), SINGLE ? 2 : 4);  // the issuers and the warpgroups' leaders
     }
-    mbar_init(b_accfree, 256);  // every thread of the two warpgroups, after reading dK or dV
-    mbar_init(b_drain, 2);      // one commit per MMA issuer
+    mbar_init(b_accfree, SINGLE ? 128 : 256);  // every warpgroup thread, after reading dK or dV
+    mbar_init(b_drain, SINGLE ? 1 : 2);        // one commit per MMA issuer
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl.tmem_base), 512);
+    tmem_alloc(smem_u32(&ctl.tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
   fence_before_sync();
@@ -444,7 +450,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int k = 0; k < C::kStages; ++k)
         if (issued[k]) mbar_wait_drain(b_full(k), last_par[k]);
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if (SINGLE ? warp == 1 : (warp == 1 || warp == 2)) {
     // ------------------------------------------------------------------ MMA issuers
     // Two issuing threads, one per dependency chain: a thread issuing tcgen05 MMAs blocks while
     // the tensor core's queue is full, so one issuer could not react to the other chain.
@@ -472,7 +478,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (n == 0) continue;
       const int kb = wt % C::kKVBufs;
       const uint64_t dK0 = dKb[kb], dV0 = dVb[kb], mK0 = mKb[kb];
-      if (lane == 0) {
+      if (lane == 0 && SINGLE) {
+        // One issuer, one buffer: per step S^T and dP^T, then (after the warpgroup's P^T, dS^T)
+        // dV, dK and dQ^T. S^T of the next step follows dQ^T in the same in-order queue, so it
+        // overwrites P^T only after dV has read it; dP^T waits for the read-out of dQ^T, which
+        // accumulates over the dP^T columns.
+        mbar_wait_spin(b_kv(kb), (wt / C::kKVBufs) & 1, abort_flag, a.status);
+        fence_after_sync();
+        for (int l = 0; l < n; ++l, ++sn) {
+          const int st = sn % C::kStages;
+          mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
+          fence_after_sync();
+          const uint64_t dq = desc_kmajor_sw128(sQs(st)), ddo = desc_kmajor_sw128(sdOs(st));
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+            mma_ss(tmem + tS(0), desc_add(dK0, okk), desc_add(dq, oq), C::kIdS, kk > 0);
+          }
+          if (sn > 0) {  // dQ^T of the previous step has been read out of the dP^T columns
+            mbar_wait_spin(b_dqfree(0), (sn - 1) & 1, abort_flag, a.status);
+            fence_after_sync();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
+            mma_ss(tmem + tdP(0), desc_add(dV0, okk), desc_add(ddo, oq), C::kIdS, kk > 0);
+          }
+          mma_commit(b_sfull(0));
+          if (l == 0 && wt > 0) {  // the previous tile's dK and dV have left tensor memory
+            mbar_wait_spin(b_accfree, (wt - 1) & 1, abort_flag, a.status);
+            fence_after_sync();
+          }
+          mbar_wait_spin(b_pready(0), sn & 1, abort_flag, a.status);
+          fence_after_sync();
+          const uint64_t mq = desc_mnmajor_sw128(sQs(st), C::kQBox), mdo = desc_mnmajor_sw128(sdOs(st), C::kQBox);
+          const uint64_t mds = desc_mnmajor_sw128(sDs(0), 16384);
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            mma_ts(tmem + C::kTdV, tmem + tS(0) + kk * 8, desc_add(mdo, kk * 2048), C::kIdG, (l > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            mma_ts(tmem + C::kTdK, tmem + tdP(0) + kk * 8, desc_add(mq, kk * 2048), C::kIdG, (l > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(b_empty(st));  // dV and dK have read the step's Q/dO stage
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + tdQ(0), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
+          mma_commit(b_dqfull(0));
+        }
+        mma_commit(b_done(kb));  // the tile's last MMAs complete after every product of it
+      } else if (lane == 0) {
         if (warp == 1) {
           mbar_wait_spin(b_kv(kb), (wt / C::kKVBufs) & 1, abort_flag, a.status);
           fence_after_sync();
@@ -535,13 +589,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(b_drain);
       mbar_wait_drain(b_drain, 0);
     }
-  } else if (warp >= 4) {
+  } else if (SINGLE ? warp >= 2 : warp >= 4) {
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // tensor-memory lane: key row (and head dimension of dQ^T)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const bool elementwise = warp < 8;
-    const int grp_bar = elementwise ? 1 : 2;             // the warpgroup's named barrier
-    const int leader = elementwise ? 128 : 256;          // its reader of the tile queue
+    // SINGLE: one warpgroup (warps 2-5) does the elementwise step, the dQ read-out and both dK, dV.
+    const bool elementwise = SINGLE || warp < 8;
+    const int grp_bar = elementwise ? 1 : 2;                     // the warpgroup's named barrier
+    const int leader = SINGLE ? 64 : (elementwise ? 128 : 256);  // its reader of the tile queue
+    const int dq_leader = SINGLE ? 64 : 256;                     // issues the dQ bulk adds
     volatile int* tile_bc = ctl.tile_bc[elementwise ? 0 : 1];
     const float sl2 = a.scale * kLog2e;
     uint32_t it = 0;  // global step counter
@@ -554,7 +610,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int tile = tile_bc[w & 1];
       if (tile >= ntiles) break;
       const BwdTile T = bwd_tile(s, tile, BM);
-      int32_t* visits = (a.step_visits != nullptr && threadIdx.x == 128)
+      int32_t* visits = (a.step_visits != nullptr && threadIdx.x == (SINGLE ? 64 : 128))
                             ? a.step_visits + ((size_t)T.b * s.Hkv + T.hk) * s.nbk + T.kt
                             : nullptr;
       if (!T.live) {
@@ -566,6 +622,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int v_first = bwd_next_v_warp(s, T, 0, BM);
       const bool any_work = v_first < T.nv;
       const uint32_t it_first = it;
+      // dQ^T of step it_ (query head gi_, rows q0_..): read out of tensor memory, staged row-major
+      // and added into the fp32 accumulator by one bulk reduce-add.
+      auto dq_out = [&](uint32_t it_, int gi_, int q0_) {
+        const int buf = it_ % NB;
+        float* dQa = a.dqacc + row_base(s, seq, T.b, T.h0 + gi_) * D;
+        mbar_wait(b_dqfull(buf), (it_ / NB) & 1, abort_flag, a.status);
+        fence_after_sync();
+        const uint32_t tq = tmem + lane_off + tdQ(buf);
+        // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
+        // unused rows of the d = 64 product).
+        uint32_t vals[BM];
+#pragma unroll
+        for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
+        tmem_ld_wait();
+        fence_before_sync();
+        mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it_ + NB
+        if (threadIdx.x == dq_leader) tma_store_wait_read0();  // the previous bulk add has read the staging
+        named_bar_sync(2, 128);
+        if (r < D) {
+#pragma unroll
+          for (int qq = 0; qq < BM; ++qq)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (threadIdx.x == dq_leader && !*abort_flag) {
+          const int rows = min(BM, seq.Lq - q0_);
+          bulk_reduce_add_f32(dQa + (size_t)q0_ * D, sDq, (uint32_t)(rows * D * 4));
+          tma_store_commit();
+        }
+      };
       if (elementwise) {
         // -------------------------------------------------------------- P^T and dS^T
         const int key = kt * 128 + r;
@@ -584,11 +671,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int gi = 0, v = v_first; gi < G && v < T.nv; ++it) {
           const int q0 = v * BM;
           const int buf = it % NB;
-          float* lrow = lse_row<D>(ctl, buf);
-          float* drow = dvec_row<D>(ctl, buf);
+          float* lrow = lse_row<D>(ctl, it & 1);
+          float* drow = dvec_row<D>(ctl, it & 1);
           // With two row buffers, every thread finished reading this one (step it - 2) before the
           // barrier of step it - 1, so only one barrier per step is needed.
-          static_assert(NB == 2, "row buffers");
           if (r < BM) {
             lrow[r] = next_l * kLog2e;
             drow[r] = next_d;
@@ -659,6 +745,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fence_proxy_async_smem();
           fence_before_sync();
           mbar_arrive(b_pready(buf));
+          if constexpr (SINGLE) dq_out(it, gi, q0);  // the same warpgroup reads out the step's dQ
           gi = gn;
           v = vn;
         }
@@ -666,34 +753,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       } else {
         // -------------------------------------------------------------- dQ into the accumulator
         for (int gi = 0, v = v_first; gi < G && v < T.nv; ++it) {
-          const int q0 = v * BM;
-          const int buf = it % NB;
-          float* dQa = a.dqacc + row_base(s, seq, T.b, T.h0 + gi) * D;
-          mbar_wait(b_dqfull(buf), (it / NB) & 1, abort_flag, a.status);
-          fence_after_sync();
-          const uint32_t tq = tmem + lane_off + tdQ(buf);
-          // dQ^T: lane r = head dimension, columns = the step's BM queries (lanes r >= d hold the
-          // unused rows of the d = 64 product).
-          uint32_t vals[BM];
-#pragma unroll
-          for (int c = 0; c < BM / 32; ++c) tmem_ld32(tq + c * 32, *reinterpret_cast<uint32_t(*)[32]>(vals + c * 32));
-          tmem_ld_wait();
-          fence_before_sync();
-          mbar_arrive(b_dqfree(buf));  // tensor-memory columns free for step it + NB
-          if (threadIdx.x == 256) tma_store_wait_read0();  // the previous bulk add has read the staging
-          named_bar_sync(2, 128);
-          if (r < D) {
-#pragma unroll
-            for (int qq = 0; qq < BM; ++qq)
-              asm volatile("st.shared.b32 [%0], %1;" ::"r"(sDq + (uint32_t)(qq * D + r) * 4u), "r"(vals[qq]) : "memory");
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(2, 128);
-          if (threadIdx.x == 256 && !*abort_flag) {
-            const int rows = min(BM, seq.Lq - q0);
-            bulk_reduce_add_f32(dQa + (size_t)q0 * D, sDq, (uint32_t)(rows * D * 4));
-            tma_store_commit();
-          }
+          dq_out(it, gi, v * BM);
           v = bwd_next_v_warp(s, T, v + 1, BM);
           if (v >= T.nv) {
             ++gi;
@@ -705,16 +765,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // -------------------------------------------------------------- dK (warps 4-7), dV (8-11)
       // Read out of tensor memory, released for the next tile's first products, then stored
       // straight from registers (no shared-memory staging competes with the next tile's loads).
-      const float mul = elementwise ? a.scale : 1.f;
+      // SINGLE: the one warpgroup writes dK, then dV.
       const int key = kt * 128 + r;
       const bool store = key < seq.krows;
-      __nv_bfloat16* grow = reinterpret_cast<__nv_bfloat16*>(elementwise ? a.dk : a.dv) +
-                            elem_offset(elementwise ? a.sdk : a.sdv, seq.bb, seq.k0 + (store ? key : 0), T.hk);
       if (any_work) {
         mbar_wait(b_done(wt % C::kKVBufs), (wt / C::kKVBufs) & 1, abort_flag, a.status);
         fence_after_sync();
       }
-      const uint32_t tacc = tmem + lane_off + (elementwise ? C::kTdK : C::kTdV);
+#pragma unroll 1
+      for (int pass = 0; pass < (SINGLE ? 2 : 1); ++pass) {
+      const bool is_dk = SINGLE ? pass == 0 : elementwise;
+      const float mul = is_dk ? a.scale : 1.f;
+      __nv_bfloat16* grow = reinterpret_cast<__nv_bfloat16*>(is_dk ? a.dk : a.dv) +
+                            elem_offset(is_dk ? a.sdk : a.sdv, seq.bb, seq.k0 + (store ? key : 0), T.hk);
+      const uint32_t tacc = tmem + lane_off + (is_dk ? C::kTdK : C::kTdV);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t vv[32];
@@ -727,8 +791,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if constexpr (ACC) {  // fp32 shares added into the caller's accumulators (this CTA owns the rows)
           if (store) {
-            float4* arow = reinterpret_cast<float4*>((elementwise ? a.dk_acc : a.dv_acc) +
-                                                     elem_offset(elementwise ? a.sdk : a.sdv, seq.bb, seq.k0 + key, T.hk)) +
+            float4* arow = reinterpret_cast<float4*>((is_dk ? a.dk_acc : a.dv_acc) +
+                                                     elem_offset(is_dk ? a.sdk : a.sdv, seq.bb, seq.k0 + key, T.hk)) +
                            c * 8;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -752,26 +816,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         }
       }
+      }
       if (any_work) {  // the accumulators may be overwritten by the next tile's first products
         fence_before_sync();
         mbar_arrive(b_accfree);
         ++wt;
       }
     }
-    if (threadIdx.x == 256) tma_store_wait_read0();  // the staging is read before the CTA exits
+    if (threadIdx.x == dq_leader) tma_store_wait_read0();  // the staging is read before the CTA exits
   }
 
   fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     fence_after_sync();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
 template <int D>
 cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
-  using C = BwdCfg<D>;
+  // d = 64 runs the single mode: two CTAs per SM, so one CTA's step chain runs while the other's
+  // waits on its softmax or dQ read-out.
+  constexpr bool SG = D == 64;
+  using C = BwdCfg<D, SG>;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -789,16 +857,19 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   bwd_pre_kernel<D><<<(unsigned)(grid_rows > 0 ? grid_rows : 1), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto main_kernel = a.dk_acc != nullptr ? bwd_tc_kernel<D, true> : bwd_tc_kernel<D, false>;
+  auto main_kernel = a.dk_acc != nullptr ? bwd_tc_kernel<D, true, SG> : bwd_tc_kernel<D, false, SG>;
   e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  // Persistent: one CTA per SM (shared memory allows one), key tiles handed out by the counter.
+  if (SG && (e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess)
+    return e;
+  // Persistent: one CTA per SM (two in the single mode), key tiles handed out by the counter.
   const long long ntiles = (long long)s.nbk * s.B * s.Hkv;
   if (ntiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (a.ev_main_begin != nullptr && (e = cudaEventRecord(a.ev_main_begin, st)) != cudaSuccess) return e;
   if (ntiles > 0) {
-    const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
-    main_kernel<<<grid, kBwdThreads, C::kSmem, st>>>(tq, tk, tv, tdo, a);
+    const long long slots = (long long)sms * (SG ? 2 : 1);
+    const unsigned grid = (unsigned)(ntiles < slots ? ntiles : slots);
+    main_kernel<<<grid, C::kThreadsCta, C::kSmem, st>>>(tq, tk, tv, tdo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -23,8 +23,15 @@ an open phase), every role ends, and no copy is in flight when the producer has 
 The producer guarantees the first on its own: before reloading a stage (or K/V) it checks that the
 stage's previous copy has landed, and it issues nothing once the abort flag is set.
 
-kvbufs: the K/V buffers (1 at d = 128; 2 at d = 64, where work tile t uses buffer t % 2, each buffer
-with its own K/V and done barriers, and a tile's K/V load waits for the done of tile t - 2 only).
+kvbufs: the K/V buffers (1 at d = 128; 2 in the two-buffer form at d = 64, where work tile t uses
+buffer t % 2, each buffer with its own K/V and done barriers, and a tile's K/V load waits for the
+done of tile t - 2 only).
+
+single: the single mode that d = 64 runs (two CTAs per SM): one tensor-memory buffer, a two-deep
+Q/dO ring, one K/V buffer, one issuer for the whole step chain and one warpgroup that writes P^T
+and dS^T, reads out dQ^T and both accumulators. Overwrites that the in-order MMA queue orders (S^T
+of step s over the P^T that dV of step s - 1 reads, dQ^T over the dS^T that dK reads) are checked
+as "issued earlier in the same queue".
 """
 import random
 
@@ -34,9 +41,12 @@ from mbarrier_model import Machine
 KST, NB = 3, 2
 
 
-def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1):
+def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, single=False):
     """unguarded: the earlier producer, which reloaded a stage once its release arrived, without
     checking its own previous copy or the abort flag."""
+    KST, NB = (2, 1) if single else (3, 2)
+    if single:
+        kvbufs = 1
     M = Machine(seed, abort_p)
     B, bar, wait, done, mma, commit = M.B, M.bar, M.wait, M.done, M.mma, M.commit
 
@@ -57,9 +67,9 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1):
         bar(f"dqfree{i}", 1)  # 128 dQ threads
     for i in range(2):
         bar(f"tqfull{i}", 1)
-        bar(f"tqempty{i}", 4)
-    bar("accfree", 2)  # the two warpgroups
-    bar("drain", 2)
+        bar(f"tqempty{i}", 2 if single else 4)  # the issuers and the warpgroups' leaders
+    bar("accfree", 1 if single else 2)  # the warpgroups
+    bar("drain", 1 if single else 2)
 
     ntiles = len(tiles)
     tile_q = [None, None]
@@ -223,6 +233,88 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1):
             wt += 1
         commit(2, "drain")
 
+    def issuer_single():
+        sn, wt, w = 0, 0, 0
+        queued = set()  # operations already in this thread's in-order queue
+
+        def mma1(rec):
+            mma(1, rec)
+            queued.add(rec)
+
+        while True:
+            t = yield from take_tile(w)
+            w += 1
+            if t >= ntiles:
+                break
+            n = tiles[t]
+            if n == 0:
+                continue
+            yield from wait("kv0", wt & 1)
+            need(("kv", wt) in done, f"issuer saw K/V of work tile {wt} before they landed")
+            for l in range(n):
+                st = sn % KST
+                yield from wait(f"full{st}", (sn // KST) & 1)
+                need(("qdo", sn) in done, f"S^T{sn} issued before its Q/dO landed")
+                if sn >= 1:
+                    need(("dV", sn - 1) in queued, f"S^T{sn} over P^T ahead of dV{sn - 1} in the queue")
+                mma1(("S", sn))
+                if sn >= 1:
+                    yield from wait("dqfree0", (sn - 1) & 1)
+                    need(("rdQ", sn - 1) in done, f"dP^T{sn} over dQ^T{sn - 1} before its read-out")
+                    need(("dK", sn - 1) in queued and ("dQ", sn - 1) in queued,
+                         f"dP^T{sn} over dS^T ahead of dK/dQ{sn - 1} in the queue")
+                mma1(("dP", sn))
+                commit(1, "sfull0")
+                if l == 0 and wt > 0:
+                    yield from wait("accfree", (wt - 1) & 1)
+                    need(("acc_ew", wt - 1) in done and ("acc_dq", wt - 1) in done,
+                         f"accumulators of work tile {wt - 1} overwritten before their read-out")
+                yield from wait("pready0", sn & 1)
+                need(("P", sn) in done, f"dV{sn} issued before P/dS of step {sn} were written")
+                mma1(("dV", sn))
+                mma1(("dK", sn))
+                commit(1, f"empty{st}")
+                need(("dK", sn) in queued, f"dQ^T{sn} over dS^T ahead of dK{sn} in the queue")
+                mma1(("dQ", sn))
+                commit(1, "dqfull0")
+                sn += 1
+                yield None
+            commit(1, "done0")
+            wt += 1
+        commit(1, "drain")
+
+    def group_single():
+        it, wt, w = 0, 0, 0
+        while True:
+            t = yield from take_tile(w)
+            w += 1
+            if t >= ntiles:
+                break
+            n = tiles[t]
+            for _ in range(n):
+                yield from wait("sfull0", it & 1)
+                need(("S", it) in done and ("dP", it) in done, f"P/dS of step {it} before S/dP completed")
+                if it >= 1:  # dS^T into the shared-memory tile read by dQ of step it - 1
+                    need(("dQ", it - 1) in done, f"dS^T{it} written before dQ{it - 1} completed")
+                done.add(("P", it))
+                B["pready0"].arrive()
+                yield None
+                yield from wait("dqfull0", it & 1)
+                need(("dQ", it) in done, f"dQ^T{it} read before it completed")
+                done.add(("rdQ", it))
+                B["dqfree0"].arrive()
+                it += 1
+                yield None
+            if n > 0:
+                yield from wait("done0", wt & 1)
+                for s in [s for s, tt in step_tile.items() if tt == wt]:
+                    need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
+                yield None
+                done.add(("acc_ew", wt))
+                done.add(("acc_dq", wt))
+                B["accfree"].arrive()
+                wt += 1
+
     def group(kind):
         it, wt, w = 0, 0, 0
         while True:
@@ -257,7 +349,10 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1):
                 B["accfree"].arrive()
                 wt += 1
 
-    roles = {"prod": producer(), "i1": issuer1(), "i2": issuer2(), "ew": group("ew"), "dr": group("dq")}
+    if single:
+        roles = {"prod": producer(), "i": issuer_single(), "g": group_single()}
+    else:
+        roles = {"prod": producer(), "i1": issuer1(), "i2": issuer2(), "ew": group("ew"), "dr": group("dq")}
     return M.run(roles), M.errors
 
 
@@ -267,10 +362,10 @@ def _cases(n):
         yield [r.choice([0, 0, 1, 1, 2, 3, 4, 5, 7]) for _ in range(r.randint(1, 10))], seed
 
 
-@pytest.mark.parametrize("kvbufs", [1, 2])
-def test_protocol_has_no_deadlock_or_hazard(kvbufs):
+@pytest.mark.parametrize("kvbufs,single", [(1, False), (2, False), (1, True)])
+def test_protocol_has_no_deadlock_or_hazard(kvbufs, single):
     for tiles, seed in _cases(3000):
-        res, errs = run(tiles, seed, kvbufs=kvbufs)
+        res, errs = run(tiles, seed, kvbufs=kvbufs, single=single)
         assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
 
 
@@ -279,14 +374,14 @@ def test_model_finds_the_earlier_release_race():
     assert hangs, "the model no longer sees the aliasing deadlock of the earlier release"
 
 
-@pytest.mark.parametrize("kvbufs", [1, 2])
-def test_abort_path_terminates(kvbufs):
+@pytest.mark.parametrize("kvbufs,single", [(1, False), (2, False), (1, True)])
+def test_abort_path_terminates(kvbufs, single):
     """Waits that run out at random points: every role still leaves its loops (the kernel's abort
     flag makes every later wait return at once; a tile-queue read that fails ends the role's tile
     loop), even when the roles no longer agree on how many tiles they saw; no barrier gets an
     arrival beyond its count (the mbarrier model raises); the drain leaves no copy in flight."""
     for tiles, seed in _cases(1500):
-        res, errs = run(tiles, seed, abort_p=0.02, kvbufs=kvbufs)
+        res, errs = run(tiles, seed, abort_p=0.02, kvbufs=kvbufs, single=single)
         assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
 
 
