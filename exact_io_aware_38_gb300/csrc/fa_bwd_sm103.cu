@@ -24,6 +24,8 @@
 // has read dS^T there, so S^T of step i+2 waits only for dV of step i and dP^T for the read-out
 // of step i's dQ^T.
 //
+// d = 64 runs a single mode (192 threads, two CTAs per SM): one tensor-memory buffer, one issuer
+// for the whole step chain, and one warpgroup for the elementwise step, the dQ read-out and dK, dV.
 // CTA layout (384 threads): warp 0 TMA producer; warp 1 S^T/dP^T MMA issuer and tensor-memory owner;
 // warp 2 gradient MMA issuer;
 // warps 4-7 elementwise warpgroup (thread = key row; lane quadrant = warp % 4), which also writes
@@ -56,9 +58,6 @@ struct BwdCfg {
   static constexpr int kBufs = SINGLE ? 1 : 2;       // tensor-memory [S^T | dP^T] buffers
   static constexpr int kBoxes = D / 64;              // 64-column boxes per row
   static constexpr int kKVBytes = 128 * D * 2;       // K or V tile (128 rows)
-  // K/V buffers: at d = 64 two, so the next key tile's K and V load while the current tile's
-  // products still read its own (d = 128 has no room for a second pair).
-  static constexpr int kKVBufs = (D == 64 && !SINGLE) ? 2 : 1;
   static constexpr int kQBox = BM * 128;             // one 64-column box of a Q or dO tile
   static constexpr int kQBytes = BM * D * 2;         // Q or dO tile (BM rows)
   static constexpr int kStages = SINGLE ? 2 : 3;     // Q/dO ring depth
@@ -66,7 +65,7 @@ struct BwdCfg {
   // of 32 queries uses the first half of each row).
   static constexpr int kDsBytes = 128 * BM * 2;
   static constexpr int kDqBytes = BM * D * 4;        // fp32 dQ staging for the bulk add
-  static constexpr int kSmem = kKVBufs * 2 * kKVBytes + kStages * 2 * kQBytes + kBufs * kDsBytes + kDqBytes + 1024;
+  static constexpr int kSmem = 2 * kKVBytes + kStages * 2 * kQBytes + kBufs * kDsBytes + kDqBytes + 1024;
   static constexpr int kThreadsCta = SINGLE ? 192 : kBwdThreads;
   static constexpr uint32_t kTmemCols = SINGLE ? 256 : 512;
   static_assert(!SINGLE || D == 64, "the single mode fits tensor memory at d = 64");
@@ -83,10 +82,10 @@ constexpr int kMaxStages = 4;
 constexpr int kMaxBufs = 4;
 
 struct alignas(16) BwdSmemCtl {
-  uint64_t kv_full[2];  // per K/V buffer
+  uint64_t kv_full;
   uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t s_full[kMaxBufs], p_ready[kMaxBufs], dq_full[kMaxBufs], dq_free[kMaxBufs], s_free[kMaxBufs];
-  uint64_t done[2], acc_free, drain;  // done: per K/V buffer
+  uint64_t done, acc_free, drain;
   uint64_t tq_full[2], tq_empty[2];  // key-tile queue
   uint32_t tmem_base;
   int abort_flag;
@@ -271,10 +270,8 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // K/V buffer kb: K at +2kb, V at +2kb+1 (kKVBytes each); a work tile uses buffer (its index) % kKVBufs.
-  auto sK = [&](int kb) { return smem_u32(smem) + (2 * kb) * C::kKVBytes; };
-  auto sV = [&](int kb) { return smem_u32(smem) + (2 * kb + 1) * C::kKVBytes; };
-  const uint32_t sStage0 = smem_u32(smem) + 2 * C::kKVBufs * C::kKVBytes;  // stage s: Q at +2s, dO at +2s+1
+  const uint32_t sK = smem_u32(smem), sV = sK + C::kKVBytes;  // the key tile's K and V
+  const uint32_t sStage0 = sV + C::kKVBytes;                    // stage s: Q at +2s, dO at +2s+1
   const uint32_t sDs0 = sStage0 + C::kStages * 2 * C::kQBytes;
   const uint32_t sDq = sDs0 + NB * C::kDsBytes;
   volatile int* abort_flag = &ctl.abort_flag;
@@ -294,7 +291,7 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
   // so the next S^T into the buffer waits only for dV's read of P^T.
   auto tdQ = [&](int buf) { return tdP(buf); };
 
-  auto b_kv = [&](int kb) { return smem_u32(&ctl.kv_full[kb]); };
+  const uint32_t b_kv = smem_u32(&ctl.kv_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
   auto b_empty = [&](int i) { return smem_u32(&ctl.empty[i]); };
   auto b_sfull = [&](int i) { return smem_u32(&ctl.s_full[i]); };
@@ -304,15 +301,13 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
   auto b_sfree = [&](int i) { return smem_u32(&ctl.s_free[i]); };
   auto b_tqfull = [&](int i) { return smem_u32(&ctl.tq_full[i]); };
   auto b_tqempty = [&](int i) { return smem_u32(&ctl.tq_empty[i]); };
-  auto b_done = [&](int kb) { return smem_u32(&ctl.done[kb]); };
+  const uint32_t b_done = smem_u32(&ctl.done);
   const uint32_t b_accfree = smem_u32(&ctl.acc_free), b_drain = smem_u32(&ctl.drain);
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
-    for (int kb = 0; kb < 2; ++kb) {
-      mbar_init(b_kv(kb), 1);
-      mbar_init(b_done(kb), 1);
-    }
+    mbar_init(b_kv, 1);
+    mbar_init(b_done, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(b_full(i), 1);
       mbar_init(b_empty(i), 1);
@@ -366,8 +361,8 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
     }
     uint32_t last_par[kMaxStages];
     bool issued[kMaxStages] = {};
-    bool kv_any[2] = {false, false};
-    uint32_t kv_par[2] = {1, 1};  // per buffer: parity of the last K/V phase issued (flips before each issue)
+    bool kv_any = false;
+    uint32_t kv_par = 1;  // parity of the last K/V phase issued (flips before each issue)
     uint32_t i = 0;  // Q/dO ring position, continued across key tiles
     int wt = 0;      // key tiles with work so far
     for (int w = 0;; ++w) {
@@ -383,29 +378,27 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
       const BwdTile T = bwd_tile(s, tile, BM);
       const int v_first = T.live ? bwd_next_v_warp(s, T, 0, BM) : T.nv;
       if (v_first >= T.nv) continue;
-      // K and V of this tile go into buffer wt % kKVBufs once every MMA of the buffer's previous
-      // tile (wt - kKVBufs) has completed (its done commit). With one buffer that is the previous
-      // tile, so the first two Q/dO steps are requested before that wait (their stages are
-      // released earlier); with two, the wait has long been met and the copy goes out at once.
-      const int kb = wt % C::kKVBufs;
+      // K and V of this tile load once every MMA of the previous tile has completed (its done
+      // commit), so the first two Q/dO steps are requested before that wait (their stages are
+      // released earlier).
       bool kv_issued = false;
       auto issue_kv = [&]() {  // lane 0
         kv_issued = true;
-        if (wt >= C::kKVBufs && !mbar_wait(b_done(kb), ((wt / C::kKVBufs) - 1) & 1, abort_flag, a.status)) return;
-        // The buffer's previous K/V copy has landed (only the producer arrives on this barrier,
-        // so the parity test cannot alias), and no copy is issued after an abort.
-        if ((kv_any[kb] && !mbar_wait(b_kv(kb), kv_par[kb], abort_flag, a.status)) || *abort_flag) return;
+        if (wt > 0 && !mbar_wait(b_done, (wt - 1) & 1, abort_flag, a.status)) return;
+        // The previous K/V copy has landed (only the producer arrives on this barrier, so the
+        // parity test cannot alias), and no copy is issued after an abort.
+        if ((kv_any && !mbar_wait(b_kv, kv_par, abort_flag, a.status)) || *abort_flag) return;
 #ifndef FA_TEST_WITHHOLD_KV  // a test-only build never loads K/V: every wait on them must run out
-        mbar_expect_tx(b_kv(kb), 2 * C::kKVBytes);
+        mbar_expect_tx(b_kv, 2 * C::kKVBytes);
         for (int c = 0; c < C::kBoxes; ++c) {
-          tma_load_4d(sK(kb) + c * 16384, &tmK, c * 64, T.seq.k0 + T.kt * 128, T.hk, T.seq.bb, b_kv(kb));
-          tma_load_4d(sV(kb) + c * 16384, &tmV, c * 64, T.seq.k0 + T.kt * 128, T.hk, T.seq.bb, b_kv(kb));
+          tma_load_4d(sK + c * 16384, &tmK, c * 64, T.seq.k0 + T.kt * 128, T.hk, T.seq.bb, b_kv);
+          tma_load_4d(sV + c * 16384, &tmV, c * 64, T.seq.k0 + T.kt * 128, T.hk, T.seq.bb, b_kv);
         }
-        kv_any[kb] = true;
-        kv_par[kb] = kv_par[kb] ^ 1u;
+        kv_any = true;
+        kv_par ^= 1u;
 #endif
       };
-      if (lane == 0 && (wt == 0 || C::kKVBufs > 1)) issue_kv();
+      if (lane == 0 && wt == 0) issue_kv();
       int l = 0;
       for (int gi = 0, v = v_first; walk && gi < G && v < T.nv; ++i, ++l) {
         if (lane == 0) {
@@ -445,8 +438,7 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
     // reloaded only once its previous copy has landed, so each of these barriers has at most one
     // phase in flight: the last one issued, whose only arrival is the producer's own.
     if (lane == 0 && *abort_flag) {
-      for (int kb = 0; kb < C::kKVBufs; ++kb)
-        if (kv_any[kb]) mbar_wait_drain(b_kv(kb), kv_par[kb]);
+      if (kv_any) mbar_wait_drain(b_kv, kv_par);
       for (int k = 0; k < C::kStages; ++k)
         if (issued[k]) mbar_wait_drain(b_full(k), last_par[k]);
     }
@@ -462,9 +454,7 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
     //           accumulators) once the previous tile's dK and dV have been read out.
     // Step counters run on across key tiles, so the ring and the buffers never drain between them.
     // Descriptors of the resident K and V tiles, advanced by constant byte offsets per k-step.
-    const uint64_t dKb[2] = {desc_kmajor_sw128(sK(0)), desc_kmajor_sw128(sK(C::kKVBufs - 1))};
-    const uint64_t dVb[2] = {desc_kmajor_sw128(sV(0)), desc_kmajor_sw128(sV(C::kKVBufs - 1))};
-    const uint64_t mKb[2] = {desc_mnmajor_sw128(sK(0), 16384), desc_mnmajor_sw128(sK(C::kKVBufs - 1), 16384)};
+    const uint64_t dK0 = desc_kmajor_sw128(sK), dV0 = desc_kmajor_sw128(sV), mK0 = desc_mnmajor_sw128(sK, 16384);
     uint32_t sn = 0;  // global step counter (lane 0)
     int wt = 0;
     for (int w = 0;; ++w) {
@@ -476,14 +466,12 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
       if (!T.live) continue;
       const int n = bwd_count_steps(s, T, BM) * G;
       if (n == 0) continue;
-      const int kb = wt % C::kKVBufs;
-      const uint64_t dK0 = dKb[kb], dV0 = dVb[kb], mK0 = mKb[kb];
       if (lane == 0 && SINGLE) {
         // One issuer, one buffer: per step S^T and dP^T, then (after the warpgroup's P^T, dS^T)
         // dV, dK and dQ^T. S^T of the next step follows dQ^T in the same in-order queue, so it
         // overwrites P^T only after dV has read it; dP^T waits for the read-out of dQ^T, which
         // accumulates over the dP^T columns.
-        mbar_wait_spin(b_kv(kb), (wt / C::kKVBufs) & 1, abort_flag, a.status);
+        mbar_wait_spin(b_kv, wt & 1, abort_flag, a.status);
         fence_after_sync();
         for (int l = 0; l < n; ++l, ++sn) {
           const int st = sn % C::kStages;
@@ -525,10 +513,10 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
             mma_ss(tmem + tdQ(0), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
           mma_commit(b_dqfull(0));
         }
-        mma_commit(b_done(kb));  // the tile's last MMAs complete after every product of it
+        mma_commit(b_done);  // the tile's last MMAs complete after every product of it
       } else if (lane == 0) {
         if (warp == 1) {
-          mbar_wait_spin(b_kv(kb), (wt / C::kKVBufs) & 1, abort_flag, a.status);
+          mbar_wait_spin(b_kv, wt & 1, abort_flag, a.status);
           fence_after_sync();
           for (int l = 0; l < n; ++l, ++sn) {
             const int st = sn % C::kStages, buf = sn % NB;
@@ -580,7 +568,7 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
               mma_ss(tmem + tdQ(buf), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
             mma_commit(b_dqfull(buf));
           }
-          mma_commit(b_done(kb));  // the tile's last MMAs complete after every S^T/dP^T of it
+          mma_commit(b_done);  // the tile's last MMAs complete after every S^T/dP^T of it
         }
       }
       ++wt;
@@ -769,7 +757,7 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
       const int key = kt * 128 + r;
       const bool store = key < seq.krows;
       if (any_work) {
-        mbar_wait(b_done(wt % C::kKVBufs), (wt / C::kKVBufs) & 1, abort_flag, a.status);
+        mbar_wait(b_done, wt & 1, abort_flag, a.status);
         fence_after_sync();
       }
 #pragma unroll 1

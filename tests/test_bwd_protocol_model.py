@@ -23,10 +23,6 @@ an open phase), every role ends, and no copy is in flight when the producer has 
 The producer guarantees the first on its own: before reloading a stage (or K/V) it checks that the
 stage's previous copy has landed, and it issues nothing once the abort flag is set.
 
-kvbufs: the K/V buffers (1 at d = 128; 2 in the two-buffer form at d = 64, where work tile t uses
-buffer t % 2, each buffer with its own K/V and done barriers, and a tile's K/V load waits for the
-done of tile t - 2 only).
-
 single: the single mode that d = 64 runs (two CTAs per SM): one tensor-memory buffer, a two-deep
 Q/dO ring, one K/V buffer, one issuer for the whole step chain and one warpgroup that writes P^T
 and dS^T, reads out dQ^T and both accumulators. Overwrites that the in-order MMA queue orders (S^T
@@ -41,12 +37,10 @@ from mbarrier_model import Machine
 KST, NB = 3, 2
 
 
-def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, single=False):
+def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, single=False):
     """unguarded: the earlier producer, which reloaded a stage once its release arrived, without
     checking its own previous copy or the abort flag."""
     KST, NB = (2, 1) if single else (3, 2)
-    if single:
-        kvbufs = 1
     M = Machine(seed, abort_p)
     B, bar, wait, done, mma, commit = M.B, M.bar, M.wait, M.done, M.mma, M.commit
 
@@ -54,9 +48,8 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, si
         if not M.aborted:
             M.need(cond, msg)
 
-    for kb in range(kvbufs):
-        bar(f"kv{kb}", 1)
-        bar(f"done{kb}", 1)
+    bar("kv", 1)
+    bar("done", 1)
     for i in range(KST):
         bar(f"full{i}", 1)
         bar(f"empty{i}", 1)
@@ -128,23 +121,21 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, si
                 continue
             kv_issued = False
 
-            kb = wt % kvbufs
-
             def issue_kv():
-                if wt >= kvbufs:
-                    if not (yield from wait(f"done{kb}", ((wt // kvbufs) - 1) & 1)):
+                if wt >= 1:
+                    if not (yield from wait("done", (wt - 1) & 1)):
                         return  # the kernel skips the copy after a wait that ran out
-                if not (yield from landed(f"kv{kb}")) or (M.aborted and not unguarded):
+                if not (yield from landed("kv")) or (M.aborted and not unguarded):
                     return
-                if wt >= kvbufs:
-                    # every MMA of the buffer's previous work tile has completed (they read K and V)
-                    for s in [s for s, tt in step_tile.items() if tt == wt - kvbufs]:
+                if wt >= 1:
+                    # every MMA of the previous work tile has completed (they read K and V)
+                    for s in [s for s, tt in step_tile.items() if tt == wt - 1]:
                         for k in ("S", "dP", "dQ"):
                             need((k, s) in done, f"K/V of work tile {wt} loaded before {k}{s} completed")
-                M.load(f"kv{kb}", 2, ("kv", wt))
-                last_par[f"kv{kb}"] = (wt // kvbufs) & 1
+                M.load("kv", 2, ("kv", wt))
+                last_par["kv"] = wt & 1
 
-            if wt == 0 or kvbufs > 1:
+            if wt == 0:
                 yield from issue_kv()
                 kv_issued = True
             for l in range(n):
@@ -182,7 +173,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, si
             n = tiles[t]
             if n == 0:
                 continue
-            yield from wait(f"kv{wt % kvbufs}", (wt // kvbufs) & 1)
+            yield from wait("kv", wt & 1)
             need(("kv", wt) in done, f"S issuer saw K/V of work tile {wt} before they landed")
             for _ in range(n):
                 st, buf = sn % KST, sn % NB
@@ -229,7 +220,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, si
                 commit(2, f"dqfull{buf}")
                 g += 1
                 yield None
-            commit(2, f"done{wt % kvbufs}")
+            commit(2, "done")
             wt += 1
         commit(2, "drain")
 
@@ -249,7 +240,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, si
             n = tiles[t]
             if n == 0:
                 continue
-            yield from wait("kv0", wt & 1)
+            yield from wait("kv", wt & 1)
             need(("kv", wt) in done, f"issuer saw K/V of work tile {wt} before they landed")
             for l in range(n):
                 st = sn % KST
@@ -279,7 +270,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, si
                 commit(1, "dqfull0")
                 sn += 1
                 yield None
-            commit(1, "done0")
+            commit(1, "done")
             wt += 1
         commit(1, "drain")
 
@@ -306,7 +297,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, si
                 it += 1
                 yield None
             if n > 0:
-                yield from wait("done0", wt & 1)
+                yield from wait("done", wt & 1)
                 for s in [s for s, tt in step_tile.items() if tt == wt]:
                     need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
                 yield None
@@ -340,7 +331,7 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, kvbufs=1, si
                 it += 1
                 yield None
             if n > 0:
-                yield from wait(f"done{wt % kvbufs}", (wt // kvbufs) & 1)
+                yield from wait("done", wt & 1)
                 last = [s for s, tt in step_tile.items() if tt == wt]
                 for s in last:
                     need(("dV", s) in done and ("dK", s) in done, f"read-out of work tile {wt} before dV/dK{s}")
@@ -362,10 +353,10 @@ def _cases(n):
         yield [r.choice([0, 0, 1, 1, 2, 3, 4, 5, 7]) for _ in range(r.randint(1, 10))], seed
 
 
-@pytest.mark.parametrize("kvbufs,single", [(1, False), (2, False), (1, True)])
-def test_protocol_has_no_deadlock_or_hazard(kvbufs, single):
+@pytest.mark.parametrize("single", [False, True])
+def test_protocol_has_no_deadlock_or_hazard(single):
     for tiles, seed in _cases(3000):
-        res, errs = run(tiles, seed, kvbufs=kvbufs, single=single)
+        res, errs = run(tiles, seed, single=single)
         assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
 
 
@@ -374,14 +365,14 @@ def test_model_finds_the_earlier_release_race():
     assert hangs, "the model no longer sees the aliasing deadlock of the earlier release"
 
 
-@pytest.mark.parametrize("kvbufs,single", [(1, False), (2, False), (1, True)])
-def test_abort_path_terminates(kvbufs, single):
+@pytest.mark.parametrize("single", [False, True])
+def test_abort_path_terminates(single):
     """Waits that run out at random points: every role still leaves its loops (the kernel's abort
     flag makes every later wait return at once; a tile-queue read that fails ends the role's tile
     loop), even when the roles no longer agree on how many tiles they saw; no barrier gets an
     arrival beyond its count (the mbarrier model raises); the drain leaves no copy in flight."""
     for tiles, seed in _cases(1500):
-        res, errs = run(tiles, seed, abort_p=0.02, kvbufs=kvbufs, single=single)
+        res, errs = run(tiles, seed, abort_p=0.02, single=single)
         assert res == "ok" and not errs, (tiles, seed, res, errs[:3])
 
 
