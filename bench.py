@@ -536,6 +536,53 @@ def fp8_forward_figure(steps, warmup, dev, peak_bf16):
             "peak_source": "measured bf16 burst x 2 (nominal FP8 / BF16 dense ratio)"}
 
 
+def varlen_figure(steps, warmup, dev, peak):
+    """The packed-sequence path on the key-padding workload's sequences: queries as in c2 (N rows
+    per sequence), keys and values packed to each sequence's L_b rows (cu_seqlens, N_q != N_k),
+    fwd_varlen + bwd_varlen per step. FLOPs are the useful count 4 H d N sum_b L_b per forward
+    (x3.5 with the backward), the count of c2's useful_padding figure."""
+    import exact_io_aware_38_gb300 as fa
+
+    w = workloads.WORKLOADS["c2"]
+    inp = workloads.make_inputs(w)
+    B, H, N, d = inp["q"].shape
+    lens = [int(x) for x in inp["seqlens_k"].tolist()]
+    rows = lambda x: x.permute(0, 2, 1, 3).reshape(B * N, x.shape[1], d)  # [B*N, heads, d]
+    q, do = (rows(inp[n]).contiguous().to(dev) for n in ("q", "do"))
+    k, v = (torch.cat([inp[n][b, :, :lens[b]].permute(1, 0, 2) for b in range(B)]).contiguous().to(dev)
+            for n in ("k", "v"))
+    cu_q = torch.arange(0, (B + 1) * N, N, dtype=torch.int32, device=dev)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+    kw = dict(cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=N, max_seqlen_k=N, causal=False, scale=w.scale)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o, lse = fa.fwd_varlen(q, k, v, **kw, status=status)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p, _ = fa._problem(q, k, cu_q, cu_k, N, N, False, w.scale)
+    ws = torch.empty(fa.fa_bwd_varlen_workspace_bytes(p), dtype=torch.uint8, device=dev)
+
+    def run():
+        fa.fwd_varlen(q, k, v, **kw, out=o, lse=lse, status=status)
+        fa.bwd_varlen(q, k, v, o, lse, do, **kw, dq=dq, dk=dk, dv=dv, workspace=ws, status=status)
+
+    for _ in range(max(3, warmup)):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, fa.fa_status_string(int(status.item()))
+    ms = a.elapsed_time(b) / steps
+    tf = 3.5 * rl.useful_padding_flops(H, N, d, np.asarray(lens)) / (ms * 1e-3) / 1e12
+    return {"workload": f"c2 sequences packed: B{B} H{H} N_q{N} per sequence, N_k = L_b (sum {sum(lens)}) d{d} "
+            "fwd+bwd (fwd_varlen, bwd_varlen)", "ms_per_step": ms, "value": tf, "unit": "TFLOP/s",
+            "frac": tf / peak, "count": "4 H d N sum_b L_b per forward, x3.5 with the backward",
+            "l2": "inputs fit in the 129 MB L2: value is L2-warm"}
+
+
 def ring_figure(steps, warmup, dev, peak, world=4):
     """Ring attention's per-rank schedule on the long-context causal shape, the W ranks run one
     after another on one GPU: the compute of a W-way sequence-sharded fwd + bwd step, without its
@@ -688,6 +735,7 @@ def main():
         result["secondary"] = secondary_figures(["c5", "c3", "c2"], min(args.steps, 20), args.warmup, dev, peak)
         result["secondary"]["fp8_fwd"] = fp8_forward_figure(min(args.steps, 20), args.warmup, dev, peak)
         result["secondary"]["ring"] = ring_figure(min(args.steps, 10), args.warmup, dev, peak)
+        result["secondary"]["varlen_packed"] = varlen_figure(min(args.steps, 20), args.warmup, dev, peak)
     if rank == 0 and not args.no_cpu_baseline:
         heads = [(0, h) for h in range(min(3, H))]  # about 10 s of the oracle on the host cores
         t0 = time.perf_counter()
