@@ -6,6 +6,8 @@ its tensor memory and return, and the GPU must stay usable for a normal call.
 
 Each case runs in a child process of its own, so whatever happens there cannot reach the CUDA
 context of the test session; the child also checks a normal call against the oracle afterwards.
+Both head dimensions run, so each kernel layout is covered: the forward's pair mode (d = 128) and
+single mode (d = 64), the backward's two-buffer layout (d = 128) and single mode (d = 64).
 """
 
 import os
@@ -35,7 +37,7 @@ f = lambda t: t.double().numpy()
 if CASE == "fwd":
     L.fa_fwd.restype = I
     L.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, ctypes.c_float, P, P, P]
-    B, H, N, d = 1, 2, 256, 128
+    B, H, N, d = 1, 2, 256, D
     inp = workloads.random_inputs(B, H, N, d, seed=3)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
     o = torch.empty_like(q)
@@ -60,7 +62,7 @@ else:
     L.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
     # 512 key tiles on the persistent grid: after its abort each CTA still takes tiles through the
     # queue, the per-tile done / accumulator waits and the step barriers.
-    B, H, N, d, scale = 1, 64, 1024, 64, 0.125
+    B, H, N, d, scale = 1, 64, 1024, D, 0.125
     g = torch.Generator("cuda").manual_seed(11)
     q, k, v, o, do = (torch.randn((B, H, N, d), generator=g, device="cuda").to(torch.bfloat16) for _ in range(5))
     lse = torch.randn((B, H, N), generator=g, device="cuda")
@@ -89,18 +91,20 @@ print("CHILD_OK")
 '''
 
 
-def _run_child(case):
-    code = f"ROOT = {ROOT!r}\nCASE = {case!r}\n" + _CHILD
+def _run_child(case, d):
+    code = f"ROOT = {ROOT!r}\nCASE = {case!r}\nD = {d}\n" + _CHILD
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0 and "CHILD_OK" in r.stdout, (r.returncode, r.stdout[-2000:], r.stderr[-4000:])
 
 
-def test_forward_bounded_wait_reports_timeout_and_gpu_stays_usable():
-    _run_child("fwd")
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_bounded_wait_reports_timeout_and_gpu_stays_usable(d):
+    _run_child("fwd", d)
 
 
-def test_backward_bounded_wait_reports_timeout_and_gpu_stays_usable():
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_bounded_wait_reports_timeout_and_gpu_stays_usable(d):
     """The persistent backward under the same test build: its key-tile queue, the per-tile done and
     accumulator-release waits and the step barriers all give up, every role leaves its tile loop,
     and the next normal call on the context is correct."""
-    _run_child("bwd")
+    _run_child("bwd", d)
