@@ -415,14 +415,16 @@ int fa_fwd_splitkv_splits(const fa_varlen_problem* p, int num_sms) {
   // The count with the least estimated time, in key-tile units: the CTAs' waves times (a CTA's
   // fixed cost, measured at about 6 key tiles: start-up, pipeline fill and drain, epilogue, plus
   // its key tiles), and for a split the merge pass (about 3). At least four key tiles per split.
+  // With one query tile per (batch, head) a split runs two CTAs per SM (the single mode).
   constexpr long long kFixedTiles = 6, kMergeTiles = 3;
   const long long units = (long long)s.B * s.H * ((s.nbq + 1) / 2);  // CTAs without a split
+  const long long slots = (long long)num_sms * (s.nbq == 1 ? 2 : 1);
   long long cap = s.nbk / 4;
   if (cap > kMaxSplits) cap = kMaxSplits;
   int best = 1;
   long long best_cost = -1;
   for (long long n = 1; n <= (cap < 1 ? 1 : cap); ++n) {
-    const long long waves = (n * units + num_sms - 1) / num_sms;
+    const long long waves = (n * units + (n > 1 ? slots : num_sms) - 1) / (n > 1 ? slots : num_sms);
     const long long cost = waves * (kFixedTiles + (s.nbk + n - 1) / n) + (n > 1 ? kMergeTiles : 0);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;

@@ -51,7 +51,9 @@ struct FwdCfg {
   static constexpr int kTileBytes = 128 * D * (F8 ? 1 : 2);  // one 128-row operand tile (Q, K, V or V^T)
   static constexpr int kQSlot = 128 * D * 2;            // a query tile's slot: Q, later its bf16 O staging
   static constexpr int kTiles = SINGLE ? 1 : 2;         // query tiles per CTA
-  static constexpr int kStages = (SINGLE || (D == 128 && !F8)) ? 2 : 4;  // K/V ring: stage t holds V_t, K_t+1
+  // K/V ring: stage t holds V_t, K_t+1. The bf16 single mode at d = 128 (one query tile: decode
+  // shapes) keeps one stage, so two CTAs fit an SM and each hides the other's loads.
+  static constexpr int kStages = SINGLE ? ((D == 128 && !F8) ? 1 : 2) : ((D == 128 && !F8) ? 2 : 4);
   static constexpr int kSmem = kTiles * kQSlot + 2 * kStages * kTileBytes + 1024;
   static constexpr int kThreadsCta = SINGLE ? kThreadsSingle : kThreads;
   static constexpr uint32_t kTmemCols = SINGLE ? 256 : 512;
@@ -655,6 +657,22 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
   const int BH = s.B * s.H;
   const bool split = a.part_o != nullptr;
   if (split && s.block_mask != nullptr) return cudaErrorInvalidValue;  // no split path takes a mask
+  // A split over keys with one query tile per (batch, head) (decode shapes): the single mode, two
+  // CTAs per SM, instead of a pair whose second tile would be empty (measured on the decode shape:
+  // 4.73 TB/s of K/V read at 4 splits against 4.42 at the pair's best count; without a split the
+  // pair's two-stage ring stays ahead, and so it does for one split: 64 CTAs, 2.7 against 2.2).
+  if (split && s.nbq == 1 && a.splits > 1) {
+    using CS = FwdCfg<D, false, true>;
+    auto ks = fwd_tc_kernel<D, true, false, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(ks, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    const long long grid = (long long)BH * a.splits;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    ks<<<(unsigned)grid, CS::kThreadsCta, CS::kSmem, st>>>(tq, tk, tv, to, a);
+    return cudaGetLastError();
+  }
   // d = 64 without a split: one query tile per CTA, two CTAs per SM (measured faster than the pair
   // of query tiles on block-sparse and causal problems, equal on the rest).
   if constexpr (D == 64) {

@@ -190,18 +190,19 @@ def test_splitkv_host_rules(L):
     r256 = lambda x: (x + 255) // 256 * 256
     p = fa.VarlenProblem(1, 8, 2, 128, 1, 8192, None, None, 0, 0, 1, 0.1)
     # Estimated cost in key-tile units: waves x (6 fixed + key tiles per split), + 3 for a merge.
-    # One query row with grouped heads runs as G rows of each K/V head (one CTA per K/V head).
+    # One query row with grouped heads runs as G rows of each K/V head (one CTA per K/V head); a
+    # split with one query tile per (batch, head) runs two CTAs per SM.
     assert fa.fa_fwd_splitkv_splits(p, 152) == 16        # 2 CTAs: 16 splits (cap 64/4), one wave
     p2 = fa.VarlenProblem(4, 32, 32, 128, 4096, 4096, None, None, 0, 0, 1, 0.1)
     assert fa.fa_fwd_splitkv_splits(p2, 152) == 1        # 2048 CTAs: a split only adds waves
     p3 = fa.VarlenProblem(1, 1, 1, 64, 1, 300, None, None, 0, 0, 0, 0.1)
     assert fa.fa_fwd_splitkv_splits(p3, 152) == 1        # 3 key tiles: fewer than four per split
     p4 = fa.VarlenProblem(8, 32, 8, 128, 1, 8192, None, None, 0, 0, 1, 0.1)
-    assert fa.fa_fwd_splitkv_splits(p4, 152) == 2        # decode at batch 8: 64 CTAs; 2 splits, one wave
+    assert fa.fa_fwd_splitkv_splits(p4, 152) == 4        # decode at batch 8: 64 CTAs; 4 splits, one wave of 2/SM
     p5 = fa.VarlenProblem(1, 32, 8, 128, 1, 8192, None, None, 0, 0, 1, 0.1)
     assert fa.fa_fwd_splitkv_splits(p5, 152) == 16       # 8 CTAs: 16 splits, one wave
     p6 = fa.VarlenProblem(1, 32, 32, 128, 1, 8192, None, None, 0, 0, 1, 0.1)
-    assert fa.fa_fwd_splitkv_splits(p6, 152) == 4        # 32 CTAs (no grouping): 4 splits, one wave
+    assert fa.fa_fwd_splitkv_splits(p6, 152) == 8        # 32 CTAs (no grouping): 8 splits, one wave of 2/SM
     rows = 8 * 1
     assert fa.fa_fwd_splitkv_workspace_bytes(p, 5) == r256(5 * rows * 4) + r256(5 * rows * 128 * 4)
     assert fa.fa_fwd_splitkv_workspace_bytes(p, 0) == 0 and fa.fa_fwd_splitkv_workspace_bytes(p, 257) == 0

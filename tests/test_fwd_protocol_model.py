@@ -197,7 +197,7 @@ def _cases(n):
             v1 = has1 and (not v0 or r.random() < 0.7)
             union.append((v0, v1 if has1 else False))
         union = [u for u in union if u[0] or u[1]]
-        yield union, has1, r.choice([2, 4]), seed
+        yield union, has1, r.choice([1, 2, 4]), seed
 
 
 def test_protocol_has_no_deadlock_or_hazard():
