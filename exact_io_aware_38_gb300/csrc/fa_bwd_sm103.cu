@@ -135,6 +135,7 @@ __host__ inline long long row_tile_grid(const AttnShape& s) {
 // d / 8 lanes, 16 bytes each, and summed over them with shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
+  grid_dependency_wait();
   constexpr int LPR = D / 8, RPW = 32 / LPR;  // lanes per row, rows per warp
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.tile_counter = 0;  // the main kernel's key-tile counter
   if ((a.s.cu_q != nullptr ? a.s.rows_q : a.s.Nq) <= 0) return;   // (then a one-CTA launch)
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
 // A row of the accumulator (d fp32) is read by d / 4 lanes, 16 bytes each.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const FaBwdArgs a) {
+  grid_dependency_wait();
   constexpr int LPR = D / 4, RPW = 32 / LPR;
   const RowTile T = row_tile(a.s);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, part = lane % LPR;
@@ -265,6 +267,7 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const FaBwdArgs a) {
   using C = BwdCfg<D, SINGLE>;
+  grid_dependency_wait();
   constexpr int BM = C::BM;
   constexpr int NB = C::kBufs;
   extern __shared__ uint8_t smem_raw[];
@@ -842,8 +845,7 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
       !fa_make_tmap_bf16(&tv, a.v, D, rk, s.Hkv, nbatch, a.sv.row, a.sv.head, a.sv.batch) ||
       !fa_make_tmap_bf16(&tdo, a.dout, D, rq, s.H, nbatch, a.sdo.row, a.sdo.head, a.sdo.batch, C::BM))
     return cudaErrorInvalidValue;
-  bwd_pre_kernel<D><<<(unsigned)(grid_rows > 0 ? grid_rows : 1), 256, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(bwd_pre_kernel<D>, dim3((unsigned)(grid_rows > 0 ? grid_rows : 1)), dim3(256), 0, st, a);
   if (e != cudaSuccess) return e;
   auto main_kernel = a.dk_acc != nullptr ? bwd_tc_kernel<D, true, SG> : bwd_tc_kernel<D, false, SG>;
   e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
@@ -857,13 +859,12 @@ cudaError_t launch(const FaBwdArgs& a, cudaStream_t st) {
   if (ntiles > 0) {
     const long long slots = (long long)sms * (SG ? 2 : 1);
     const unsigned grid = (unsigned)(ntiles < slots ? ntiles : slots);
-    main_kernel<<<grid, C::kThreadsCta, C::kSmem, st>>>(tq, tk, tv, tdo, a);
-    e = cudaGetLastError();
+    e = launch_dependent(main_kernel, dim3(grid), dim3(C::kThreadsCta), C::kSmem, st, tq, tk, tv, tdo, a);
     if (e != cudaSuccess) return e;
   }
   if (a.ev_main_end != nullptr && (e = cudaEventRecord(a.ev_main_end, st)) != cudaSuccess) return e;
-  if (grid_rows > 0) bwd_post_kernel<D><<<(unsigned)grid_rows, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  if (grid_rows > 0) return launch_dependent(bwd_post_kernel<D>, dim3((unsigned)grid_rows), dim3(256), 0, st, a);
+  return cudaSuccess;
 }
 
 }  // namespace

@@ -177,6 +177,24 @@ struct FaBwdArgs {
 };
 
 cudaError_t fa_launch_fwd(const FaFwdArgs& a, cudaStream_t st);
+// A launch that may begin while the previous kernel on the stream finishes: the kernel waits on
+// the grid dependency (griddepcontrol.wait) before its first global-memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 cudaError_t fa_launch_splitkv_merge(const FaFwdArgs& a, cudaStream_t st);
 cudaError_t fa_launch_merge_two(float* acc_o, float* acc_lse, const float* part_o, const float* part_lse, size_t rows,
                                 int d, cudaStream_t st);

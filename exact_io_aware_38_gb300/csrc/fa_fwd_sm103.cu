@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FaFwdArgs a) {
   using C = FwdCfg<D, F8, SINGLE>;
+  grid_dependency_wait();
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -688,8 +689,7 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
       if (e != cudaSuccess) return e;
       const long long grid = (long long)s.nbq * BH;
       if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-      ks<<<(unsigned)grid, CS::kThreadsCta, CS::kSmem, st>>>(tq, tk, tv, to, a);
-      return cudaGetLastError();
+      return launch_dependent(ks, dim3((unsigned)grid), dim3(CS::kThreadsCta), CS::kSmem, st, tq, tk, tv, to, a);
     }
   }
   auto kern = split ? fwd_tc_kernel<D, true, false>
@@ -698,8 +698,7 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long grid = (long long)((s.nbq + 1) / 2) * BH * (split ? a.splits : 1);
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, to, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3((unsigned)grid), dim3(kThreads), C::kSmem, st, tq, tk, tv, to, a);
 }
 
 // e4m3 operands (d = 128, fixed-length [B, H, N, d] Q and K, [B, Hkv, d, N] V^T, no split). The
