@@ -1,6 +1,7 @@
 // Backward attention on the 5th-generation tensor cores (sm_103a).
 //
-// Three launches on the caller's stream:
+// Three launches on the caller's stream, each a programmatic dependent of the kernel before it
+// (its launch overlaps that kernel's tail; it waits on the grid dependency before touching memory):
 //   pre   D_i = sum_k dO_ik O_ik (fp32, from the stored bf16 O), a cleared fp32 dQ accumulator and
 //         a cleared key-tile counter;
 //   main  persistent, one CTA per SM, taking (128-key tile j, K/V head) pairs from the counter,
@@ -135,7 +136,7 @@ __host__ inline long long row_tile_grid(const AttnShape& s) {
 // d / 8 lanes, 16 bytes each, and summed over them with shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
-  grid_dependency_wait();
+  grid_dependency_wait();  // a programmatic dependent of the previous kernel on the stream
   constexpr int LPR = D / 8, RPW = 32 / LPR;  // lanes per row, rows per warp
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.tile_counter = 0;  // the main kernel's key-tile counter
   if ((a.s.cu_q != nullptr ? a.s.rows_q : a.s.Nq) <= 0) return;   // (then a one-CTA launch)
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const FaBwdArgs a) {
 // A row of the accumulator (d fp32) is read by d / 4 lanes, 16 bytes each.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const FaBwdArgs a) {
-  grid_dependency_wait();
+  grid_dependency_wait();  // the main pass has completed
   constexpr int LPR = D / 4, RPW = 32 / LPR;
   const RowTile T = row_tile(a.s);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, part = lane % LPR;
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const FaBwdArgs a) {
   using C = BwdCfg<D, SINGLE>;
-  grid_dependency_wait();
+  grid_dependency_wait();  // the pre pass has completed (D, the cleared accumulator, the counter)
   constexpr int BM = C::BM;
   constexpr int NB = C::kBufs;
   extern __shared__ uint8_t smem_raw[];

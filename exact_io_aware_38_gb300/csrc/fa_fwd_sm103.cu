@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FaFwdArgs a) {
   using C = FwdCfg<D, F8, SINGLE>;
-  grid_dependency_wait();
+  grid_dependency_wait();  // launched as a programmatic dependent of the previous kernel
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
