@@ -673,8 +673,7 @@ cudaError_t launch(const FaFwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const long long grid = (long long)BH * a.splits;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    ks<<<(unsigned)grid, CS::kThreadsCta, CS::kSmem, st>>>(tq, tk, tv, to, a);
-    return cudaGetLastError();
+    return launch_dependent(ks, dim3((unsigned)grid), dim3(CS::kThreadsCta), CS::kSmem, st, tq, tk, tv, to, a);
   }
   // d = 64 without a split: one query tile per CTA, two CTAs per SM (measured faster than the pair
   // of query tiles on block-sparse and causal problems, equal on the rest).
@@ -724,8 +723,7 @@ cudaError_t launch_f8(const FaFwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long grid = (long long)s.nbq * s.B * s.H;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)grid, C::kThreadsCta, C::kSmem, st>>>(tq, tk, tv, to, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3((unsigned)grid), dim3(C::kThreadsCta), C::kSmem, st, tq, tk, tv, to, a);
 }
 
 }  // namespace
