@@ -220,6 +220,38 @@ def test_repeatable():
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_back_to_back_calls_reuse_buffers(d):
+    """The kernels run as programmatic dependents of the kernel before them on the stream. Calls
+    queued back to back, with no host synchronisation, that reuse the same O, LSE, gradient and
+    workspace buffers (each call's pre pass clears the accumulator the previous call's post pass
+    reads; each forward overwrites the O and LSE the previous backward read) must give the results
+    of the same calls made one at a time."""
+    dev = "cuda"
+    inputs = [small_inputs(2, 4, 640, d, "causal", 11), small_inputs(2, 4, 640, d, "causal", 12)]
+    dev_in = [{n: inp[n].to(dev) for n in ("q", "k", "v", "do")} for inp in inputs]
+    shape = dev_in[0]["q"]
+    o, lse = torch.empty_like(shape), torch.empty((2, 4, 640), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(shape), torch.empty_like(shape), torch.empty_like(shape)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(2, 4, 640, d), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    snaps = []
+    for t in (dev_in[0], dev_in[1], dev_in[0], dev_in[1]):
+        fa.fwd(t["q"], t["k"], t["v"], causal=True, out=o, lse=lse, status=status)
+        fa.bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=True, dq=dq, dk=dk, dv=dv, workspace=ws, status=status)
+        snaps.append([x.clone() for x in (o, lse, dq, dk, dv)])  # stream-ordered copies, no host sync
+    snaps = [[x.cpu() for x in snap] for snap in snaps]
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i, inp in enumerate(inputs):
+        ref = run_gpu(inp)  # the same call alone, fresh buffers
+        for got in (snaps[i], snaps[i + 2]):
+            for n, x in zip(("o", "lse", "dk", "dv"), (got[0], got[1], got[3], got[4])):
+                assert torch.equal(x, ref[n]), n
+            # dQ is summed with fp32 reduce-adds in no fixed order
+            assert (got[2].float() - ref["dq"].float()).abs().max() <= 1e-2
+
+
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("H,Hkv", [(4, 2), (8, 1), (6, 3), (4, 4)])
 @pytest.mark.parametrize("N,kind", [(129, "dense"), (300, "causal"), (384, "causal+pad+block")])
 def test_gqa_parity(H, Hkv, N, kind, d):
