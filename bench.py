@@ -732,7 +732,7 @@ def main():
     if up is not None:
         result["useful_padding"] = up
     if rank == 0 and not args.no_secondary and args.heads is None and args.workload == "c4":
-        result["secondary"] = secondary_figures(["c5", "c3", "c2"], min(args.steps, 20), args.warmup, dev, peak)
+        result["secondary"] = secondary_figures(["c5", "c3", "c2", "c4g"], min(args.steps, 20), args.warmup, dev, peak)
         result["secondary"]["fp8_fwd"] = fp8_forward_figure(min(args.steps, 20), args.warmup, dev, peak)
         result["secondary"]["ring"] = ring_figure(min(args.steps, 10), args.warmup, dev, peak)
         result["secondary"]["varlen_packed"] = varlen_figure(min(args.steps, 20), args.warmup, dev, peak)
