@@ -94,6 +94,10 @@ struct alignas(16) BwdSmemCtl {
   int tile_bc[2][2];  // the tile index shared within each warpgroup, two slots each
   alignas(16) float lse2[128];  // LSE * log2(e) per query of the step: [buffer][BM]
   alignas(16) float dvec[128];  // D per query of the step: [buffer][BM]
+  // Single mode: the queue item's visited steps per query head and first step, and the first step
+  // as shared within the warpgroup (after the fields above, which keep their places).
+  int tile_n[2], tile_vf[2];
+  int tile_bcv[2];
 };
 
 template <int D>
@@ -241,21 +245,40 @@ __device__ __forceinline__ int bwd_next_v_warp(const AttnShape& s, const BwdTile
   return t.nv;
 }
 
-// Visited steps of the tile for one query head, counted by a whole warp: every step from v_lo on
-// without a block mask; with one, eight block-mask loads per lane are in flight before the votes.
-__device__ __forceinline__ int bwd_count_steps(const AttnShape& s, const BwdTile& t, int BM) {
-  if (s.block_mask == nullptr) return t.nv > t.v_lo ? t.nv - t.v_lo : 0;
+// Visited steps of the tile for one query head and the first of them (nv if none), found by a
+// whole warp: every step from v_lo on without a block mask; with one, each lane first loads its
+// eight mask bytes unconditionally (the candidate is clamped to the last step, whose 128-row tile
+// is inside the mask), so the eight loads are in flight together, and only then applies the
+// bounds and the causal test. With the tests guarding each load, the loads went out one after
+// another (~12,600 cycles per key tile on a 128 x 128 mask).
+__device__ __forceinline__ int bwd_scan_steps(const AttnShape& s, const BwdTile& t, int BM, int& v_first) {
+  if (!t.live) {
+    v_first = t.nv;
+    return 0;
+  }
+  if (s.block_mask == nullptr) {
+    v_first = min(t.v_lo, t.nv);
+    return t.nv - v_first;
+  }
   const int lane_id = threadIdx.x & 31;
   int n = 0;
+  v_first = t.nv;
   for (int v0 = t.v_lo; v0 < t.nv; v0 += 8 * 32) {
-    bool hit[8];
+    uint32_t m[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int v = min(v0 + u * 32 + lane_id, t.nv - 1);
+      m[u] = __ldg(s.block_mask + (size_t)((v * BM) / 128) * s.nbk + t.kt);
+    }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int v = v0 + u * 32 + lane_id;
-      hit[u] = v < t.nv && tile_visited(s, t.seq, (v * BM) / 128, t.kt);
+      const int qt = (v * BM) / 128;
+      const unsigned hit = __ballot_sync(
+          0xffffffffu, v < t.nv && m[u] != 0 && !(s.causal && t.kt * 128 > qt * 128 + 127 + t.seq.off));
+      if (v_first == t.nv && hit) v_first = v0 + u * 32 + __ffs(hit) - 1;
+      n += __popc(hit);
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) n += __popc(__ballot_sync(0xffffffffu, hit[u]));
   }
   return n;
 }
@@ -342,12 +365,30 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
 
   // Key tiles come from a counter shared by all CTAs (the first one is the CTA's own index), in
   // the heavy-first order of the tile index. The producer takes each one and publishes it through
-  // a two-slot queue; every other role reads the same sequence from there. Item w's phase of a
+  // a two-slot queue; every other role reads the same sequence from there. In the single mode the
+  // producer also counts the tile's visited steps and finds the first before publishing, so the
+  // issuer and the warpgroup scan nothing at a tile's start, where two CTAs with short key tiles
+  // (d = 64) wait on it. With one CTA per SM (d = 128) each role scans for itself: the published
+  // form measured 2-6% slower there, with identical outputs. Item w's phase of a
   // slot's full barrier cannot be confused with item w + 2's: that one is published only after all
   // four readers of item w have arrived on the slot's empty barrier.
   auto take_tile = [&](int w) -> int {  // one reader thread per role
     int tile = ntiles;  // an abandoned wait ends the loop
     if (mbar_wait(b_tqfull(w & 1), (w >> 1) & 1, abort_flag, a.status)) tile = tile_q[w & 1];
+    mbar_arrive(b_tqempty(w & 1));
+    return tile;
+  };
+  // Single mode: the same, also returning the item's step count and first step (read before the
+  // arrival that lets the producer rewrite the slot).
+  auto take_item = [&](int w, int& nsteps, int& v_first) -> int {
+    int tile = ntiles;
+    nsteps = 0;
+    v_first = 0;
+    if (mbar_wait(b_tqfull(w & 1), (w >> 1) & 1, abort_flag, a.status)) {
+      tile = tile_q[w & 1];
+      nsteps = ((volatile int*)ctl.tile_n)[w & 1];
+      v_first = ((volatile int*)ctl.tile_vf)[w & 1];
+    }
     mbar_arrive(b_tqempty(w & 1));
     return tile;
   };
@@ -371,16 +412,37 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
     int wt = 0;      // key tiles with work so far
     for (int w = 0;; ++w) {
       int tile = ntiles;
+      bool publish = false;
       if (lane == 0 && (w < 2 || mbar_wait(b_tqempty(w & 1), ((w - 2) >> 1) & 1, abort_flag, a.status))) {
         // After an abort the end marker is published, so every reader leaves its tile loop.
         tile = *abort_flag ? ntiles : (w == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.tile_counter, 1));
-        tile_q[w & 1] = tile;
-        mbar_arrive(b_tqfull(w & 1));  // release: the index is visible to every waiter of the phase
+        if constexpr (!SINGLE) {
+          tile_q[w & 1] = tile;
+          mbar_arrive(b_tqfull(w & 1));  // release: the index is visible to every waiter of the phase
+        }
+        publish = true;
       }
       tile = __shfl_sync(0xffffffffu, tile, 0);
-      if (tile >= ntiles) break;
-      const BwdTile T = bwd_tile(s, tile, BM);
-      const int v_first = T.live ? bwd_next_v_warp(s, T, 0, BM) : T.nv;
+      int v_first = 0;
+      BwdTile T;
+      if constexpr (SINGLE) {  // scan first, then publish the item (the whole warp scans)
+        int nsteps = 0;
+        if (tile < ntiles) {
+          T = bwd_tile(s, tile, BM);
+          nsteps = bwd_scan_steps(s, T, BM, v_first);
+        }
+        if (publish) {
+          tile_q[w & 1] = tile;
+          ctl.tile_n[w & 1] = nsteps;
+          ctl.tile_vf[w & 1] = v_first;
+          mbar_arrive(b_tqfull(w & 1));  // release: the item is visible to every waiter of the phase
+        }
+        if (tile >= ntiles) break;
+      } else {
+        if (tile >= ntiles) break;
+        T = bwd_tile(s, tile, BM);
+        v_first = T.live ? bwd_next_v_warp(s, T, 0, BM) : T.nv;
+      }
       if (v_first >= T.nv) continue;
       // K and V of this tile load once every MMA of the previous tile has completed (its done
       // commit), so the first two Q/dO steps are requested before that wait (their stages are
@@ -462,13 +524,22 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
     uint32_t sn = 0;  // global step counter (lane 0)
     int wt = 0;
     for (int w = 0;; ++w) {
-      int tile = 0;
-      if (lane == 0) tile = take_tile(w);
-      tile = __shfl_sync(0xffffffffu, tile, 0);
-      if (tile >= ntiles) break;
-      const BwdTile T = bwd_tile(s, tile, BM);
-      if (!T.live) continue;
-      const int n = bwd_count_steps(s, T, BM) * G;
+      int tile = 0, n = 0;
+      if constexpr (SINGLE) {  // the producer's count
+        int vf_unused;
+        if (lane == 0) tile = take_item(w, n, vf_unused);
+        tile = __shfl_sync(0xffffffffu, tile, 0);
+        if (tile >= ntiles) break;
+        n = __shfl_sync(0xffffffffu, n, 0) * G;
+      } else {
+        if (lane == 0) tile = take_tile(w);
+        tile = __shfl_sync(0xffffffffu, tile, 0);
+        if (tile >= ntiles) break;
+        const BwdTile T = bwd_tile(s, tile, BM);
+        if (!T.live) continue;
+        int vf_unused;
+        n = bwd_scan_steps(s, T, BM, vf_unused) * G;
+      }
       if (n == 0) continue;
       if (lane == 0 && SINGLE) {
         // One issuer, one buffer: per step S^T and dP^T, then (after the warpgroup's P^T, dS^T)
@@ -595,9 +666,18 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
     uint32_t it = 0;  // global step counter
     int wt = 0;
     for (int w = 0;; ++w) {
-      // The warpgroup agrees on the tile: its leader reads the queue and shares the index (two
-      // slots, so a slot is rewritten only after the next iteration's barrier).
-      if (threadIdx.x == leader) tile_bc[w & 1] = take_tile(w);
+      // The warpgroup agrees on the tile: its leader reads the queue and shares the index (and in
+      // the single mode the first visited step; two slots, so a slot is rewritten only after the
+      // next iteration's barrier).
+      if (threadIdx.x == leader) {
+        if constexpr (SINGLE) {
+          int n_unused, vf;
+          tile_bc[w & 1] = take_item(w, n_unused, vf);
+          ctl.tile_bcv[w & 1] = vf;
+        } else {
+          tile_bc[w & 1] = take_tile(w);
+        }
+      }
       named_bar_sync(grp_bar, 128);
       const int tile = tile_bc[w & 1];
       if (tile >= ntiles) break;
@@ -611,7 +691,12 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
       }
       const SeqInfo& seq = T.seq;
       const int kt = T.kt;
-      const int v_first = bwd_next_v_warp(s, T, 0, BM);
+      int v_first;
+      if constexpr (SINGLE) {
+        v_first = ((volatile int*)ctl.tile_bcv)[w & 1];  // the producer's scan
+      } else {
+        v_first = bwd_next_v_warp(s, T, 0, BM);
+      }
       const bool any_work = v_first < T.nv;
       const uint32_t it_first = it;
       // dQ^T of step it_ (query head gi_, rows q0_..): read out of tensor memory, staged row-major
