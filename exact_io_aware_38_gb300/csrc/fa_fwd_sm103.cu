@@ -297,7 +297,9 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
   // The producer's first copies: Q0, Q1 and the first key tile alone, into the K half of the last
   // buffer. Without a block mask the first key tile is known before the CTA-wide barrier, so they
   // are issued right after the barrier set-up and their latency overlaps the rest of the prologue.
-  auto first_loads = [&]() {
+  // The query tiles' copy does not depend on the mask: with one it is issued before the bitmap is
+  // built, and only the first K copy waits for the bitmap.
+  auto load_q = [&]() {
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
@@ -306,6 +308,8 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
       for (int c = 0; c < C::kBoxes; ++c)
         tma_load_4d(sQ + x * C::kQSlot + c * 16384, &tmQ, c * C::kBoxCols, seq.q0 + (x ? qt1 : qt0) * 128, h, seq.bb,
                     b_q);
+  };
+  auto load_k0 = [&]() {
     const int kt = next_union(kt_lo);
 #ifndef FA_TEST_WITHHOLD_KV
     if (kt < s.nbk) {
@@ -333,17 +337,24 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
     }
     mbar_init(smem_u32(&ctl.drain), 1);
     fence_mbar_init();
-    if constexpr (!MASKED) first_loads();  // thread 0 is the producer
+    load_q();  // thread 0 is the producer
+    if constexpr (!MASKED) load_k0();
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl.tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
   if (MASKED && bitmap) {  // one vote per 32 key tiles of a query tile; only [kt_lo, kt_end) is ever read
+    // Items (query tile x, word wd) are dealt to the warps; without a second query tile its row is
+    // all zeros and takes no warp's turn, so no warp waits on two mask loads in a row.
     const int words = (kt_end + 31) >> 5;
-    for (int idx = warp; idx < 2 * words; idx += C::kThreadsCta / 32) {
-      const int x = idx & 1, wd = idx >> 1, kt = wd * 32 + lane;
-      const bool bit = kt >= kt_lo && kt < kt_end && (x == 0 || has1) && tile_visited(s, seq, x ? qt1 : qt0, kt);
+    const int nx = has1 ? 2 : 1;
+    if (!has1 && warp == 0) {
+      for (int wd = lane; wd < words; wd += 32) ctl.vis[1][wd] = 0u;
+    }
+    for (int idx = warp; idx < nx * words; idx += C::kThreadsCta / 32) {
+      const int x = idx % nx, wd = idx / nx, kt = wd * 32 + lane;
+      const bool bit = kt >= kt_lo && kt < kt_end && tile_visited(s, seq, x ? qt1 : qt0, kt);
       const uint32_t m = __ballot_sync(0xffffffffu, bit);
       if (lane == 0) ctl.vis[x][wd] = m;
     }
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(SINGLE ? kThreadsSingle : kThreads, SINGLE ? 2
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      if constexpr (MASKED) first_loads();
+      if constexpr (MASKED) load_k0();
       // Stage t (the t-th key tile u_t the pair visits) lands V_{u_t} and K_{u_t+1} in buffer
       // t % kStages. A buffer is reloaded once the MMAs of its previous stage have completed. No
       // copy is issued after an abort; the copies already issued are drained at the CTA's exit.
