@@ -842,12 +842,76 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
       // -------------------------------------------------------------- dK (warps 4-7), dV (8-11)
       // Read out of tensor memory, released for the next tile's first products, then stored
       // straight from registers (no shared-memory staging competes with the next tile's loads).
-      // SINGLE: the one warpgroup writes dK, then dV.
+      // SINGLE: the one warpgroup writes both, staged through shared memory (below); with ACC
+      // it adds dK, then dV, into the caller's fp32 accumulators.
       const int key = kt * 128 + r;
       const bool store = key < seq.krows;
       if (any_work) {
         mbar_wait(b_done, wt & 1, abort_flag, a.status);
         fence_after_sync();
+      }
+      if constexpr (SINGLE && !ACC) {
+        // Both accumulators are read out first (the next tile's first products may then start),
+        // staged as bf16 rows in 128-byte-swizzled shared memory (dK in the dS^T tile, which the
+        // tile's last dQ^T product has finished reading, dV in the dQ staging once its last bulk
+        // add has read it), and copied out eight threads per 128-byte row: a warp's store covers
+        // four rows instead of 32 (the row-per-thread stores took ~3,200 cycles per key tile).
+        uint32_t pk[2][D / 2];
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          const float mul = pass == 0 ? a.scale : 1.f;
+          const uint32_t tacc = tmem + lane_off + (pass == 0 ? C::kTdK : C::kTdV);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t vv[32];
+            if (any_work) {
+              tmem_ld32(tacc + c * 32, vv);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) vv[i] = 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[pass][c * 16 + i] = pack_bf16x2(__uint_as_float(vv[2 * i]) * mul, __uint_as_float(vv[2 * i + 1]) * mul);
+          }
+        }
+        if (any_work) {  // the accumulators may be overwritten by the next tile's first products
+          fence_before_sync();
+          mbar_arrive(b_accfree);
+          ++wt;
+        }
+        if (threadIdx.x == dq_leader) tma_store_wait_read0();  // the last dQ bulk add has read its staging
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          const uint32_t row = (pass == 0 ? sDs(0) : sDq) + (uint32_t)r * 128u;
+#pragma unroll
+          for (int j = 0; j < D / 8; ++j)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((j ^ (r & 7)) << 4)),
+                         "r"(pk[pass][4 * j]), "r"(pk[pass][4 * j + 1]), "r"(pk[pass][4 * j + 2]), "r"(pk[pass][4 * j + 3])
+                         : "memory");
+        }
+        named_bar_sync(1, 128);
+        const int t = threadIdx.x - 64;  // 0..127 within the warpgroup
+#pragma unroll 4
+        for (int k = 0; k < 2 * 128 * (D / 8) / 128; ++k) {
+          const int idx = k * 128 + t;
+          const int pass = idx / (128 * (D / 8));
+          const int rr = (idx / (D / 8)) % 128, chunk = idx % (D / 8);
+          uint4 x;
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                       : "r"((pass == 0 ? sDs(0) : sDq) + (uint32_t)rr * 128u + ((chunk ^ (rr & 7)) << 4))
+                       : "memory");
+          const int krow = kt * 128 + rr;
+          if (krow < seq.krows)
+            *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pass == 0 ? a.dk : a.dv) +
+                                      elem_offset(pass == 0 ? a.sdk : a.sdv, seq.bb, seq.k0 + krow, T.hk) +
+                                      chunk * 8) = x;
+        }
+        // The staging buffers are next written after the next tile's first barrier.
+        continue;
       }
 #pragma unroll 1
       for (int pass = 0; pass < (SINGLE ? 2 : 1); ++pass) {
