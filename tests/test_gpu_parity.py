@@ -203,11 +203,35 @@ def test_block_mask_rows_longer_than_the_bitmap():
         assert torch.isfinite(got[n].float()).all(), n
 
 
-def test_all_tiles_masked():
-    inp = workloads.random_inputs(1, 2, 256, 128, 5)
+@pytest.mark.parametrize("d", [64, 128])
+def test_all_tiles_masked(d):
+    """Every key tile has no visited step: each is taken from the queue, skipped by the issuers,
+    and its dK/dV rows are written as zeros."""
+    inp = workloads.random_inputs(1, 2, 256, d, 5)
     inp.update(causal=False, block_mask=torch.zeros((2, 2), dtype=torch.uint8), seqlens_k=None, scale=0.1)
     got = full_check(inp)
     assert (got["visits"] == 0).all() and (got["step_visits"] == 0).all()
+    assert (got["dk"] == 0).all() and (got["dv"] == 0).all()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_empty_key_tile_columns(d):
+    """Key tiles whose block-mask column is empty (no query tile sees them) between ones that are
+    seen, with a causal mask and a short last tile: the empty tiles' dK/dV are zero, the rest match
+    the oracle, and every skip decision matches bit-exactly."""
+    B, H, N = 2, 2, 5 * 128 + 40
+    inp = workloads.random_inputs(B, H, N, d, 91)
+    nb = (N + 127) // 128
+    bm = torch.ones((nb, nb), dtype=torch.uint8)
+    bm[:, 1] = 0
+    bm[:, 3] = 0
+    bm[0, 3] = 1  # column 3 is seen only by query tile 0, which the causal mask then hides
+    inp.update(causal=True, block_mask=bm, seqlens_k=None, scale=1.0 / np.sqrt(d))
+    got = full_check(inp)
+    for kt in (1, 3):
+        assert (got["dk"][:, :, kt * 128:(kt + 1) * 128] == 0).all(), kt
+        assert (got["dv"][:, :, kt * 128:(kt + 1) * 128] == 0).all(), kt
+        assert (got["step_visits"][:, :, kt] == 0).all(), kt
 
 
 def test_repeatable():
