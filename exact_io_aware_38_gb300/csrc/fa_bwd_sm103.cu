@@ -27,6 +27,8 @@
 //
 // d = 64 runs a single mode (192 threads, two CTAs per SM): one tensor-memory buffer, one issuer
 // for the whole step chain, and one warpgroup for the elementwise step, the dQ read-out and dK, dV.
+// There dQ^T accumulates over the S^T columns instead (free once dV has read P^T) and is issued
+// before dK, so the step's dQ^T completes earlier and the next dP^T runs during its read-out.
 // CTA layout (384 threads): warp 0 TMA producer; warp 1 S^T/dP^T MMA issuer and tensor-memory owner;
 // warp 2 gradient MMA issuer;
 // warps 4-7 elementwise warpgroup (thread = key row; lane quadrant = warp % 4), which also writes
@@ -315,8 +317,9 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
   auto tS = [&](int buf) { return C::kTS0 + buf * 2 * BM; };
   auto tdP = [&](int buf) { return C::kTS0 + buf * 2 * BM + BM; };
   // dQ^T of a step accumulates over its buffer's dP^T columns (free once dK has read dS^T there),
-  // so the next S^T into the buffer waits only for dV's read of P^T.
-  auto tdQ = [&](int buf) { return tdP(buf); };
+  // so the next S^T into the buffer waits only for dV's read of P^T. The single mode puts it over
+  // the S^T columns (free once dV has read P^T), issued ahead of dK (see the issuer).
+  auto tdQ = [&](int buf) { return SINGLE ? tS(buf) : tdP(buf); };
 
   const uint32_t b_kv = smem_u32(&ctl.kv_full);
   auto b_full = [&](int i) { return smem_u32(&ctl.full[i]); };
@@ -542,10 +545,13 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
       }
       if (n == 0) continue;
       if (lane == 0 && SINGLE) {
-        // One issuer, one buffer: per step S^T and dP^T, then (after the warpgroup's P^T, dS^T)
-        // dV, dK and dQ^T. S^T of the next step follows dQ^T in the same in-order queue, so it
-        // overwrites P^T only after dV has read it; dP^T waits for the read-out of dQ^T, which
-        // accumulates over the dP^T columns.
+        // One issuer, one buffer: per step dP^T and S^T, then (after the warpgroup's P^T, dS^T)
+        // dV, dQ^T and dK. In the one in-order queue dQ^T overwrites P^T only after dV has read
+        // it, and the next step's dP^T overwrites dS^T only after dK has read it, so dP^T issues
+        // at once; the next S^T waits for the read-out of dQ^T, held in the S^T columns. With dK
+        // after dQ^T the read-out starts one product earlier, and the next dP^T runs during it
+        // (block-sparse d = 64 backward 0.4585 -> 0.4366 ms side by side, against dV, dK, dQ^T
+        // over the dP^T columns).
         mbar_wait_spin(b_kv, wt & 1, abort_flag, a.status);
         fence_after_sync();
         for (int l = 0; l < n; ++l, ++sn) {
@@ -553,19 +559,21 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
           mbar_wait_spin(b_full(st), (sn / C::kStages) & 1, abort_flag, a.status);
           fence_after_sync();
           const uint64_t dq = desc_kmajor_sw128(sQs(st)), ddo = desc_kmajor_sw128(sdOs(st));
+          // dP^T first: its columns are free once the previous step's dK has read dS^T (earlier in
+          // this queue); S^T waits for the read-out of the previous dQ^T, held in its columns.
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
-            mma_ss(tmem + tS(0), desc_add(dK0, okk), desc_add(dq, oq), C::kIdS, kk > 0);
+            mma_ss(tmem + tdP(0), desc_add(dV0, okk), desc_add(ddo, oq), C::kIdS, kk > 0);
           }
-          if (sn > 0) {  // dQ^T of the previous step has been read out of the dP^T columns
+          if (sn > 0) {  // dQ^T of the previous step has been read out of the S^T columns
             mbar_wait_spin(b_dqfree(0), (sn - 1) & 1, abort_flag, a.status);
             fence_after_sync();
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t okk = (kk >> 2) * 16384 + (kk & 3) * 32, oq = (kk >> 2) * C::kQBox + (kk & 3) * 32;
-            mma_ss(tmem + tdP(0), desc_add(dV0, okk), desc_add(ddo, oq), C::kIdS, kk > 0);
+            mma_ss(tmem + tS(0), desc_add(dK0, okk), desc_add(dq, oq), C::kIdS, kk > 0);
           }
           mma_commit(b_sfull(0));
           if (l == 0 && wt > 0) {  // the previous tile's dK and dV have left tensor memory
@@ -579,14 +587,15 @@ __global__ void __launch_bounds__(SINGLE ? 192 : kBwdThreads, SINGLE ? 2 : 1)
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
             mma_ts(tmem + C::kTdV, tmem + tS(0) + kk * 8, desc_add(mdo, kk * 2048), C::kIdG, (l > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ts(tmem + C::kTdK, tmem + tdP(0) + kk * 8, desc_add(mq, kk * 2048), C::kIdG, (l > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(b_empty(st));  // dV and dK have read the step's Q/dO stage
+          // dQ^T over the S^T columns (after dV has read P^T there), ahead of dK.
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + tdQ(0), desc_add(mK0, kk * 2048), desc_add(mds, kk * 2048), C::kIdQ, kk > 0);
           mma_commit(b_dqfull(0));
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            mma_ts(tmem + C::kTdK, tmem + tdP(0) + kk * 8, desc_add(mq, kk * 2048), C::kIdG, (l > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(b_empty(st));  // dV and dK have read the step's Q/dO stage
         }
         mma_commit(b_done);  // the tile's last MMAs complete after every product of it
       } else if (lane == 0) {

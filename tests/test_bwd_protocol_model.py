@@ -25,9 +25,10 @@ stage's previous copy has landed, and it issues nothing once the abort flag is s
 
 single: the single mode that d = 64 runs (two CTAs per SM): one tensor-memory buffer, a two-deep
 Q/dO ring, one K/V buffer, one issuer for the whole step chain and one warpgroup that writes P^T
-and dS^T, reads out dQ^T and both accumulators. Overwrites that the in-order MMA queue orders (S^T
-of step s over the P^T that dV of step s - 1 reads, dQ^T over the dS^T that dK reads) are checked
-as "issued earlier in the same queue".
+and dS^T, reads out dQ^T and both accumulators. Its issue order per step is dP^T, S^T (after the
+previous dQ^T's read-out: dQ^T accumulates over the S^T columns), then dV, dQ^T, dK. Overwrites that
+the in-order MMA queue orders (dQ^T of step s over the P^T that dV of step s reads, dP^T of step s
+over the dS^T that dK of step s - 1 reads) are checked as "issued earlier in the same queue".
 """
 import random
 
@@ -247,14 +248,12 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, single=False
                 yield from wait(f"full{st}", (sn // KST) & 1)
                 need(("qdo", sn) in done, f"S^T{sn} issued before its Q/dO landed")
                 if sn >= 1:
-                    need(("dV", sn - 1) in queued, f"S^T{sn} over P^T ahead of dV{sn - 1} in the queue")
-                mma1(("S", sn))
+                    need(("dK", sn - 1) in queued, f"dP^T{sn} over dS^T ahead of dK{sn - 1} in the queue")
+                mma1(("dP", sn))
                 if sn >= 1:
                     yield from wait("dqfree0", (sn - 1) & 1)
-                    need(("rdQ", sn - 1) in done, f"dP^T{sn} over dQ^T{sn - 1} before its read-out")
-                    need(("dK", sn - 1) in queued and ("dQ", sn - 1) in queued,
-                         f"dP^T{sn} over dS^T ahead of dK/dQ{sn - 1} in the queue")
-                mma1(("dP", sn))
+                    need(("rdQ", sn - 1) in done, f"S^T{sn} over dQ^T{sn - 1} before its read-out")
+                mma1(("S", sn))
                 commit(1, "sfull0")
                 if l == 0 and wt > 0:
                     yield from wait("accfree", (wt - 1) & 1)
@@ -263,11 +262,11 @@ def run(tiles, seed, release="stage", abort_p=0.0, unguarded=False, single=False
                 yield from wait("pready0", sn & 1)
                 need(("P", sn) in done, f"dV{sn} issued before P/dS of step {sn} were written")
                 mma1(("dV", sn))
-                mma1(("dK", sn))
-                commit(1, f"empty{st}")
-                need(("dK", sn) in queued, f"dQ^T{sn} over dS^T ahead of dK{sn} in the queue")
+                need(("dV", sn) in queued, f"dQ^T{sn} over P^T ahead of dV{sn} in the queue")
                 mma1(("dQ", sn))
                 commit(1, "dqfull0")
+                mma1(("dK", sn))
+                commit(1, f"empty{st}")
                 sn += 1
                 yield None
             commit(1, "done")
