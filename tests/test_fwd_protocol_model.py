@@ -15,6 +15,11 @@ Checked: no deadlock, and no hazard: a buffer reloaded before the MMAs that read
 completed; an MMA issued before its operands landed or its P was written; S_x overwritten before
 its P_x was written; O_x rescaled while an earlier PV_x is unfinished; O read before all PV_x.
 A planted mistake (the buffer's release committed before its last reader is issued) must be found.
+
+sepp: the single mode at d = 64 (one query tile), where P has columns of its own: per tile the
+issuer issues S(t+1) first (the softmax has read S(t) once P(t) is written), then PV(t) and a
+commit on pv_done; the softmax waits for pv_done of the previous tile before it rescales O or
+writes P. Checked as above, and a softmax that skips that wait must be found.
 """
 import random
 
@@ -22,7 +27,8 @@ import pytest
 from mbarrier_model import Machine
 
 
-def run(union, has1, stages, seed, early_release=False, abort_p=0.0, unguarded=False):
+def run(union, has1, stages, seed, early_release=False, abort_p=0.0, unguarded=False, sepp=False,
+        skip_pv_wait=False):
     """union: [(v0, v1)] per union key tile (at least one of the two set).
     unguarded: the earlier abort handling (the issuer and the softmax warpgroups carried on after a
     failed wait, and the producer did not check the abort flag before a copy)."""
@@ -41,6 +47,7 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0, unguarded=F
         bar(f"sfull{x}", 1)
         bar(f"odone{x}", 1)
     bar("pready1", 1)  # 128 softmax threads of tile 1, modelled as one arrival
+    bar("pvdone", 1)   # sepp: the issuer's commit after each PV
     U = len(union)
     vis = lambda x, t: t < U and bool(union[t][x])
 
@@ -101,6 +108,8 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0, unguarded=F
 
         def issue_s(x, t):
             need(("K", t) in done, f"S{x}({t}) issued before K({t}) landed")
+            if sepp and t > 0:
+                need((f"P{x}", t - 1) in done, f"S{x}({t}) over S{x} before the softmax read S{x}({t - 1})")
             if last_p[x] is not None:
                 need((f"P{x}", last_p[x]) in done, f"S{x}({t}) over S{x} before P{x}({last_p[x]}) was written")
             M.mma("i", (f"S{x}", t))
@@ -133,10 +142,17 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0, unguarded=F
                 break
             if early_release:
                 M.commit("i", f"empty{b}")
-            if vis(0, t):
-                issue_pv(0, t)
-            if vis(0, t + 1):
-                issue_s(0, t + 1)
+            if sepp:
+                if vis(0, t + 1):
+                    issue_s(0, t + 1)
+                if vis(0, t):
+                    issue_pv(0, t)
+                    M.commit("i", "pvdone")
+            else:
+                if vis(0, t):
+                    issue_pv(0, t)
+                if vis(0, t + 1):
+                    issue_s(0, t + 1)
             if vis(1, t):
                 run = yield from wait("pready1", np1 & 1)
                 np1 += 1
@@ -163,6 +179,9 @@ def run(union, has1, stages, seed, early_release=False, abort_p=0.0, unguarded=F
                 run = yield from wait(f"sfull{x}", cnt & 1)
             if run:
                 need((f"S{x}", t) in done, f"softmax {x} read S({t}) before it completed")
+            if run and sepp and cnt > 0 and not skip_pv_wait:  # before the rescale and the P write
+                run = yield from wait("pvdone", (cnt - 1) & 1)
+            if run:
                 for tp in range(t):
                     if vis(x, tp):
                         need((f"PV{x}", tp) in done, f"softmax {x} rescaled O at {t} before PV{x}({tp}) completed")
@@ -198,6 +217,27 @@ def _cases(n):
             union.append((v0, v1 if has1 else False))
         union = [u for u in union if u[0] or u[1]]
         yield union, has1, r.choice([1, 2, 4]), seed
+
+
+def _sepp_cases(n):
+    for union, _, stages, seed in _cases(n):
+        union = [(True, False) for u in union if u[0]]
+        yield union, stages, seed
+
+
+def test_single_mode_separate_p_has_no_deadlock_or_hazard():
+    for union, stages, seed in _sepp_cases(3000):
+        res, errs = run(union, False, stages, seed, sepp=True)
+        assert res == "ok" and not errs, (union, stages, seed, res, errs[:3])
+    for union, stages, seed in _sepp_cases(1500):
+        res, errs = run(union, False, stages, seed, abort_p=0.02, sepp=True)
+        assert res == "ok" and not errs, (union, stages, seed, res, errs[:3])
+
+
+def test_model_finds_a_missing_pv_wait():
+    found = [seed for union, stages, seed in _sepp_cases(3000)
+             if run(union, False, stages, seed, sepp=True, skip_pv_wait=True)[1]]
+    assert found, "the model no longer sees P or O written before the previous PV completed"
 
 
 def test_protocol_has_no_deadlock_or_hazard():
